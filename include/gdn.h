@@ -1,0 +1,131 @@
+/*
+ * gdn.h - C ABI of libgdn.so, the GB300 (sm_103a) Gated DeltaNet prefill
+ * recurrence and its gated RMSNorm output.
+ *
+ * Pages this interface follows (cited by title and section):
+ *   [P413]  "#413 prefill: DeltaNet recurrence with the three value heads of a key
+ *           head in one thread" - section "What changes" (the recurrence, the key
+ *           head shared by value heads qh, qh+16, qh+32, the FP32 recurrence
+ *           output y and its FP16 normed copy y_h) and section "Exactness" (the
+ *           state after the chunk is part of the result; parity is checked from
+ *           a non-zero starting state).
+ *   [P1372] "#1372 DeltaNet recurrence: STRATA_GDN_CHUNKED=1 - the prompt's
+ *           recurrence in 32-token chunks" - section "What it does" (the 32-token
+ *           WY form, 2048-token super-blocks, the per-device scratch kept between
+ *           calls).
+ *
+ * Layout (all tensors dense, row-major, contiguous, FP32 unless stated):
+ *   q, k        [T][n_kh][d]      query / key rows per key head
+ *   v, out      [T][n_vh][d]      value rows / recurrence output o per value head
+ *   g, beta     [T][n_vh]         log-decay gate (g <= 0) and delta-rule strength
+ *   state_inout [n_vh][d][d]      S[h][i][j]: i = key dim (row), j = value dim
+ *   z           [T][n_vh][d]      output gate
+ *   w           [d]               norm weight, shared by all value heads
+ *   y_fp16      [T][n_vh][d]      IEEE binary16 bits
+ * Value head h reads key head h % n_kh.
+ *
+ * Ownership: every pointer is a DEVICE pointer owned by the caller, on the
+ * current CUDA device.  The library allocates only (a) a 4-byte status word per
+ * device and (b) the chunked mode's per-device scratch (one 2048-token
+ * super-block of prep results, about 25.9 MB), both on first use and kept until
+ * gdn_release_scratch() or process exit.
+ *
+ * Asynchrony: every compute call only validates its arguments on the host and
+ * enqueues kernels on `cuda_stream` (a cudaStream_t; NULL = the legacy default
+ * stream).  Nothing synchronises the host except the one-time allocations above.
+ * Inputs and outputs must not overlap (out, state_inout and y_fp16 are written
+ * while q, k, v, g, beta, z, w are read).
+ *
+ * Errors: no call throws.  Each returns a gdn_status; on a non-OK status
+ * gdn_last_error() returns a message for the calling thread.  A kernel that
+ * gives up a bounded wait records GDN_ERR_TIMEOUT in the device status word,
+ * which gdn_device_status() reads.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gdn_mode {
+    GDN_SEQUENTIAL = 0, /* one token at a time; bit-identical across reruns and T splits */
+    GDN_CHUNKED = 1     /* 32-token WY chunks in 2048-token super-blocks */
+} gdn_mode;
+
+typedef enum gdn_status {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = -1, /* null pointer, T < 0, n_vh % n_kh != 0, bad mode, eps < 0 */
+    GDN_ERR_UNSUPPORTED = -2, /* shapes this build has no kernel for (d != 128, n_vh != 3 n_kh) */
+    GDN_ERR_ALLOC = -3,       /* the per-device scratch or status word could not be allocated */
+    GDN_ERR_CUDA = -4,        /* a CUDA runtime call or a launch failed */
+    GDN_ERR_TIMEOUT = -5      /* a kernel gave up a bounded wait (gdn_device_status only) */
+} gdn_status;
+
+/*
+ * gdn_recurrence - the gated delta-rule recurrence over T tokens ([P413] "What
+ * changes"; [P1372] "What it does" for mode GDN_CHUNKED).  Per value head h,
+ * key head kh = h % n_kh, and token t:
+ *     S <- exp(g[t][h]) S
+ *     delta = beta[t][h] (v[t][h] - S^T k[t][kh])
+ *     S <- S + k[t][kh] delta^T
+ *     out[t][h] = S^T q[t][kh]
+ * state_inout is read as the starting state and overwritten with the state
+ * after token T-1, so consecutive calls continue one sequence.  In
+ * GDN_SEQUENTIAL mode a sequence split over several calls gives the same bits
+ * as one call.  GDN_CHUNKED evaluates the same recurrence in 32-token WY
+ * chunks (other FP32 rounding; within 2e-6 of the FP64 result, relative to
+ * the largest magnitude).
+ *
+ * Supported shapes: d == 128 and n_vh == 3 * n_kh (n_kh >= 1).  T == 0 is a
+ * no-op returning GDN_OK.  The first GDN_CHUNKED call on a device allocates the
+ * scratch (GDN_ERR_ALLOC if that fails; nothing is launched then).
+ */
+int gdn_recurrence(const float* q, const float* k, const float* v,
+                   const float* g, const float* beta,
+                   float* state_inout, float* out,
+                   int64_t T, int n_kh, int n_vh, int d, int mode,
+                   void* cuda_stream);
+
+/*
+ * gdn_out_norm - gated RMSNorm of the recurrence output to FP16 ([P413] "What
+ * changes": gdn_out_norm_kernel writes the FP16 copy y_h).  Per (t, h) row:
+ *     r = 1 / sqrt(mean_j out[t][h][j]^2 + eps)
+ *     y_fp16[t][h][j] = fp16_rn( out[t][h][j] * r * w[j] * silu(z[t][h][j]) )
+ * computed in FP32 with one round-to-nearest-even to binary16 at the end.
+ * Supported: d == 128, any n_vh >= 1, eps >= 0.  T == 0 is a no-op.
+ */
+int gdn_out_norm(const float* out, const float* z, const float* w, float eps,
+                 uint16_t* y_fp16, int64_t T, int n_vh, int d, void* cuda_stream);
+
+/* Message for the calling thread's last non-OK status ("" if none). */
+const char* gdn_last_error(void);
+
+/*
+ * Synchronises `cuda_stream`, then reads and clears the current device's
+ * status word: GDN_OK, or GDN_ERR_TIMEOUT if a kernel gave up a bounded wait
+ * since the last read, or GDN_ERR_CUDA if the stream reports an error.
+ */
+int gdn_device_status(void* cuda_stream);
+
+/*
+ * Frees the chunked-mode scratch of `device` (a CUDA device ordinal).  The
+ * caller must ensure no chunked call is still running on it.  The next chunked
+ * call allocates it again.  Returns GDN_OK (also if nothing was allocated).
+ */
+int gdn_release_scratch(int device);
+
+/* Bytes of chunked-mode scratch a device holds once allocated. */
+size_t gdn_chunked_scratch_bytes(int n_vh);
+
+/* Number of kernels this library has launched in this process (all devices). */
+uint64_t gdn_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

@@ -1,0 +1,302 @@
+"""Pins of the FP64 oracle against what the pages and the mathematics fix.
+
+Each ``pin_*`` function takes an ``oracle.Oracle`` and raises AssertionError when
+the oracle disagrees with a closed form, an invariant, a special case that
+reduces to a library routine, or the chunked WY algebra.  None of them retypes
+the oracle's own loop: each states an independent fact about the recurrence
+("#413 prefill: DeltaNet recurrence with the three value heads of a key head in
+one thread", section "What changes"; "#1372 DeltaNet recurrence:
+STRATA_GDN_CHUNKED=1", section "What it does").
+
+The same functions run against deliberately broken copies of the oracle in
+test_oracle_mutants.py, which checks that every planted mistake is caught.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+SMALL = dict(n_kh=2, n_vh=6, d=8)
+
+
+def _rand_inputs(rng, T, n_kh, n_vh, d, s0_scale=0.3):
+    k = rng.standard_normal((T, n_kh, d))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    q = rng.standard_normal((T, n_kh, d)) / math.sqrt(d)
+    v = rng.standard_normal((T, n_vh, d))
+    g = -np.logaddexp(0.0, rng.normal(-2.0, 1.0, (T, n_vh)))
+    beta = 1.0 / (1.0 + np.exp(-rng.standard_normal((T, n_vh))))
+    S0 = s0_scale * rng.standard_normal((n_vh, d, d))
+    f = lambda a: a.astype(np.float32)  # noqa: E731 - the GPU path's input precision
+    return f(q), f(k), f(v), f(g), f(beta), f(S0).astype(np.float64)
+
+
+def _rel(a, b):
+    return float(np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-300))
+
+
+def pin_single_step_closed_form(orc):
+    """T = 1: with a = e^g and u = v - a S0^T k,
+    S1 = a S0 + beta k u^T and o = a S0^T q + beta (k . q) u  (derived by hand)."""
+    rng = np.random.default_rng(11)
+    for shape in (SMALL, dict(n_kh=16, n_vh=48, d=128)):
+        q, k, v, g, beta, S0 = _rand_inputs(rng, 1, **shape)
+        o, S1 = orc.recurrence(q, k, v, g, beta, S0, nthreads=1)
+        n_kh = shape["n_kh"]
+        for h in range(shape["n_vh"]):
+            kh = h % n_kh
+            kk = k[0, kh].astype(np.float64)
+            qq = q[0, kh].astype(np.float64)
+            vv = v[0, h].astype(np.float64)
+            a = math.exp(float(g[0, h]))
+            b = float(beta[0, h])
+            u = vv - a * (S0[h].T @ kk)
+            S1_ref = a * S0[h] + b * np.outer(kk, u)
+            o_ref = a * (S0[h].T @ qq) + b * float(kk @ qq) * u
+            assert _rel(S1[h], S1_ref) < 1e-13, ("state", h, _rel(S1[h], S1_ref))
+            assert _rel(o[0, h], o_ref) < 1e-13, ("out", h, _rel(o[0, h], o_ref))
+
+
+def pin_identity(orc):
+    """beta = 0, g = 0: the state is unchanged bit for bit and o_t = S0^T q_t."""
+    rng = np.random.default_rng(12)
+    T = 9
+    q, k, v, g, beta, S0 = _rand_inputs(rng, T, **SMALL)
+    g[:] = 0.0
+    beta[:] = 0.0
+    o, ST = orc.recurrence(q, k, v, g, beta, S0, nthreads=1)
+    assert np.array_equal(ST, S0)
+    for h in range(SMALL["n_vh"]):
+        kh = h % SMALL["n_kh"]
+        ref = q[:, kh, :].astype(np.float64) @ S0[h]
+        assert _rel(o[:, h, :], ref) < 1e-14
+
+
+def pin_decay_only(orc):
+    """beta = 0: S_T = e^{sum g} S0 and o_t = e^{gamma_t} S0^T q_t, gamma_t the
+    running sum of g over the call up to and including t."""
+    rng = np.random.default_rng(13)
+    T = 12
+    q, k, v, g, beta, S0 = _rand_inputs(rng, T, **SMALL)
+    beta[:] = 0.0
+    o, ST = orc.recurrence(q, k, v, g, beta, S0, nthreads=1)
+    for h in range(SMALL["n_vh"]):
+        kh = h % SMALL["n_kh"]
+        gam = np.cumsum(g[:, h].astype(np.float64))
+        assert _rel(ST[h], math.exp(gam[-1]) * S0[h]) < 1e-13
+        ref = np.exp(gam)[:, None] * (q[:, kh, :].astype(np.float64) @ S0[h])
+        assert _rel(o[:, h, :], ref) < 1e-13
+
+
+def pin_exact_recall(orc):
+    """beta = 1, g = 0, orthonormal keys k_1..k_n: writing v_i under k_i makes
+    S^T k_i = v_i right after the write and at every later step (later writes
+    are orthogonal to k_i), from any starting state.  Queries with q_t = k_t read
+    back v_t; a final block of beta = 0 tokens queries every earlier key."""
+    rng = np.random.default_rng(14)
+    n_kh, n_vh, d = 2, 6, 16
+    n = 10
+    T = 2 * n
+    S0 = rng.standard_normal((n_vh, d, d))
+    # keys [n][n_kh][d]: orthonormal rows per key head (QR of a Gaussian
+    # matrix).  Rounding them to FP32 breaks orthonormality by ~1e-7, so this
+    # check holds to 1e-5; pin_exact_recall_exact_keys repeats it exactly.
+    keys = np.stack([np.linalg.qr(rng.standard_normal((d, d)))[0][:, :n].T for _ in range(n_kh)], 1)
+    k = np.zeros((T, n_kh, d), np.float32)
+    q = np.zeros((T, n_kh, d), np.float32)
+    k[:n] = keys
+    q[:n] = keys
+    q[n:] = keys
+    v = rng.standard_normal((T, n_vh, d)).astype(np.float32)
+    g = np.zeros((T, n_vh), np.float32)
+    beta = np.ones((T, n_vh), np.float32)
+    beta[n:] = 0.0
+    o, ST = orc.recurrence(q, k, v, g, beta, S0, nthreads=1)
+    kk = k.astype(np.float64)
+    for h in range(n_vh):
+        kh = h % n_kh
+        for i in range(n):
+            # right after the write
+            assert np.max(np.abs(o[i, h] - v[i, h])) < 1e-5, ("write", h, i)
+            # after all writes, the final state recalls v_i under k_i
+            assert np.max(np.abs(ST[h].T @ kk[i, kh] - v[i, h])) < 1e-5, ("state", h, i)
+            # the beta = 0 query block reads back v_i
+            assert np.max(np.abs(o[n + i, h] - v[i, h])) < 1e-5, ("query", h, i)
+
+
+def pin_exact_recall_exact_keys(orc):
+    """Same delta-rule recall with keys that are exactly orthonormal in FP32
+    (signed unit vectors e_i): the recall is exact to double rounding (1e-13)."""
+    rng = np.random.default_rng(15)
+    n_kh, n_vh, d = 2, 6, 8
+    n = d
+    T = 2 * n
+    S0 = rng.standard_normal((n_vh, d, d))
+    perm = [rng.permutation(d) for _ in range(n_kh)]
+    k = np.zeros((T, n_kh, d), np.float32)
+    for kh in range(n_kh):
+        for i in range(n):
+            k[i, kh, perm[kh][i]] = 1.0 if (i % 2 == 0) else -1.0
+    q = np.zeros_like(k)
+    q[:n] = k[:n]
+    q[n:] = k[:n]
+    v = rng.standard_normal((T, n_vh, d)).astype(np.float32)
+    g = np.zeros((T, n_vh), np.float32)
+    beta = np.ones((T, n_vh), np.float32)
+    beta[n:] = 0.0
+    o, ST = orc.recurrence(q, k, v, g, beta, S0, nthreads=1)
+    for h in range(n_vh):
+        kh = h % n_kh
+        for i in range(n):
+            assert np.max(np.abs(o[i, h] - v[i, h])) < 1e-13
+            assert np.max(np.abs(ST[h].T @ k[i, kh].astype(np.float64) - v[i, h])) < 1e-13
+            assert np.max(np.abs(o[n + i, h] - v[i, h])) < 1e-13
+
+
+def pin_key_head_mapping(orc):
+    """Value head h reads key head h % n_kh: with S0 = 0 and keys non-zero only
+    on key head 1, exactly the value heads h with h % n_kh == 1 acquire state."""
+    rng = np.random.default_rng(16)
+    n_kh, n_vh, d = 4, 12, 8
+    T = 5
+    q, k, v, g, beta, _ = _rand_inputs(rng, T, n_kh, n_vh, d)
+    k[:, [0, 2, 3], :] = 0.0
+    S0 = np.zeros((n_vh, d, d))
+    o, ST = orc.recurrence(q, k, v, g, beta, S0, nthreads=1)
+    for h in range(n_vh):
+        nz = np.max(np.abs(ST[h])) > 0
+        assert nz == (h % n_kh == 1), (h, nz)
+        assert (np.max(np.abs(o[:, h])) > 0) == (h % n_kh == 1)
+
+
+def pin_linearity(orc):
+    """For fixed k, q, g, beta the map (S0, v) -> (S_T, o) is linear.
+
+    v1 and v2 have disjoint supports (even / odd value columns), so every
+    combination with power-of-two weights is exact in FP32 and the check holds
+    to double rounding."""
+    rng = np.random.default_rng(17)
+    T = 7
+    q, k, v1, g, beta, S1 = _rand_inputs(rng, T, **SMALL)
+    _, _, v2, _, _, S2 = _rand_inputs(rng, T, **SMALL)
+    v1[..., 1::2] = 0.0
+    v2[..., 0::2] = 0.0
+    o1, T1 = orc.recurrence(q, k, v1, g, beta, S1, nthreads=1)
+    o2, T2 = orc.recurrence(q, k, v2, g, beta, S2, nthreads=1)
+    for a, b in ((0.5, 0.25), (-2.0, 1.0), (1.0, 0.0)):
+        v3 = (a * v1.astype(np.float64) + b * v2.astype(np.float64))
+        assert np.array_equal(v3.astype(np.float32).astype(np.float64), v3)
+        o3, T3 = orc.recurrence(q, k, v3.astype(np.float32), g, beta, a * S1 + b * S2, nthreads=1)
+        assert _rel(o3, a * o1 + b * o2) < 1e-13, (a, b, _rel(o3, a * o1 + b * o2))
+        assert _rel(T3, a * T1 + b * T2) < 1e-13, (a, b)
+
+
+def pin_chunked_equals_sequential(orc):
+    """The chunked WY form equals the sequential recurrence (brute force on tiny
+    T, crossing chunk edges 32 and 64, including partial last chunks)."""
+    rng = np.random.default_rng(18)
+    for shape, Ts in ((SMALL, (1, 2, 5, 31, 32, 33, 63, 64, 65, 70)),
+                      (dict(n_kh=1, n_vh=3, d=128), (1, 33, 70))):
+        for T in Ts:
+            q, k, v, g, beta, S0 = _rand_inputs(rng, T, **shape)
+            o, ST = orc.recurrence(q, k, v, g, beta, S0, nthreads=1)
+            oc, STc = orc.chunked(q, k, v, g, beta, S0, 32, nthreads=1)
+            assert _rel(oc, o) < 1e-12, ("out", shape, T, _rel(oc, o))
+            assert _rel(STc, ST) < 1e-12, ("state", shape, T, _rel(STc, ST))
+    # a chunk size of 1 is the sequential recurrence token by token
+    q, k, v, g, beta, S0 = _rand_inputs(rng, 9, **SMALL)
+    o, ST = orc.recurrence(q, k, v, g, beta, S0, nthreads=1)
+    oc, STc = orc.chunked(q, k, v, g, beta, S0, 1, nthreads=1)
+    assert _rel(oc, o) < 1e-13 and _rel(STc, ST) < 1e-13
+
+
+def pin_fp16_rounding(orc):
+    """The oracle's double -> binary16 rounding equals numpy's conversion
+    (round to nearest even, subnormals, overflow to infinity)."""
+    rng = np.random.default_rng(19)
+    xs = list(rng.standard_normal(2000) * 10.0 ** rng.integers(-9, 5, 2000))
+    # exact ties between two halves, in the normal and subnormal ranges
+    for e in (-24, -20, -15, -14, -3, 0, 5, 10, 15):
+        for m in (1, 3, 1023, 1025, 2047):
+            xs.append((m + 0.5) * 2.0 ** (e - 10))
+            xs.append(-(m + 0.5) * 2.0 ** (e - 10))
+    xs += [0.0, -0.0, 65504.0, 65519.99, 65520.0, 1e6, -1e6, 2.0 ** -25, 2.0 ** -25 * 1.0001,
+           2.0 ** -24, 6.1e-5, 5.96e-8, 2.98e-8]
+    for x in xs:
+        got = orc.fp16_rne(x)
+        with np.errstate(over="ignore"):
+            ref = int(np.array([x], dtype=np.float64).astype(np.float16).view(np.uint16)[0])
+        assert got == ref, (x, hex(got), hex(ref))
+    assert orc.fp16_rne(float("nan")) & 0x7c00 == 0x7c00
+
+
+def _np_half_bits(x):
+    with np.errstate(over="ignore"):
+        return np.asarray(x, dtype=np.float64).astype(np.float16).view(np.uint16)
+
+
+def pin_norm_library(orc):
+    """The gated RMSNorm equals torch's rms_norm (a library routine) times w
+    times torch's silu, in float64, rounded by numpy to FP16."""
+    import torch
+
+    rng = np.random.default_rng(20)
+    T, n_vh, d = 5, 6, 128
+    o = rng.standard_normal((T, n_vh, d)) * 0.3
+    z = rng.standard_normal((T, n_vh, d)).astype(np.float32)
+    w = (1.0 + 0.1 * rng.standard_normal(d)).astype(np.float32)
+    eps = 1e-6
+    y = orc.out_norm(o, z, w, eps, nthreads=1)
+    ot = torch.from_numpy(o)
+    ref = torch.nn.functional.rms_norm(ot, (d,), weight=torch.from_numpy(w.astype(np.float64)), eps=eps)
+    ref = ref * torch.nn.functional.silu(torch.from_numpy(z.astype(np.float64)))
+    refb = _np_half_bits(ref.numpy())
+    # the two double computations differ by a few double ulps; a value that
+    # sits within that of an FP16 rounding boundary may round the other way
+    diff = np.abs(y.view(np.int16).astype(np.int32) - refb.view(np.int16).astype(np.int32))
+    assert int(np.max(diff)) <= 1
+    assert np.mean(diff == 0) > 0.999
+
+
+def pin_norm_special_cases(orc):
+    """o constant across the row: o r = sign(o) / sqrt(1 + eps / o^2), so with
+    w = 1 and a large gate z (silu(z) = z to double precision for z = 40) the
+    output is sign(o) z / sqrt(1 + eps / o^2); at |o| = 1e-3 and eps = 1e-6
+    that is sign(o) z / sqrt(2).  Also: scaling o by c > 0 with eps = 0 leaves
+    y unchanged (the norm is scale-free)."""
+    d = 128
+    vals = [1e-3, -1e-3, 0.37, -2.5]
+    o = np.array([[np.full(d, x) for x in vals]])
+    z = np.full((1, len(vals), d), 40.0, np.float32)
+    w = np.ones(d, np.float32)
+    eps = 1e-6
+    y = orc.out_norm(o, z, w, eps, nthreads=1)
+    for hi, x in enumerate(vals):
+        ref = math.copysign(1.0, x) * 40.0 / math.sqrt(1.0 + eps / (x * x))
+        assert np.all(y[0, hi] == _np_half_bits(ref)), (x, ref)
+    rng = np.random.default_rng(21)
+    o = rng.standard_normal((3, 4, d))
+    z = rng.standard_normal((3, 4, d)).astype(np.float32)
+    w = (1.0 + 0.1 * rng.standard_normal(d)).astype(np.float32)
+    y1 = orc.out_norm(o, z, w, 0.0, nthreads=1)
+    y2 = orc.out_norm(o * 8.0, z, w, 0.0, nthreads=1)  # power of two: exact scaling
+    assert np.array_equal(y1, y2)
+    # the gate: z = 0 gives silu = 0, so y = +-0
+    y0 = orc.out_norm(o, np.zeros_like(z), w, eps, nthreads=1)
+    assert np.all((y0 & 0x7fff) == 0)
+
+
+ALL_PINS = [
+    pin_single_step_closed_form,
+    pin_identity,
+    pin_decay_only,
+    pin_exact_recall,
+    pin_exact_recall_exact_keys,
+    pin_key_head_mapping,
+    pin_linearity,
+    pin_chunked_equals_sequential,
+    pin_fp16_rounding,
+    pin_norm_library,
+    pin_norm_special_cases,
+]
