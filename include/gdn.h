@@ -118,6 +118,15 @@ int gdn_device_status(void* cuda_stream);
  */
 int gdn_release_scratch(int device);
 
+/*
+ * Diagnostic: fill the current device's chunked-mode scratch (allocating it
+ * first, sized for n_vh value heads) with the 32-bit pattern `bits`, e.g.
+ * 0x7fc00000 (a quiet NaN), on `cuda_stream`.  A chunked call that followed and
+ * read a scratch word its prep kernel had not written would propagate the
+ * pattern into its results; the tests use this to show it never does.
+ */
+int gdn_poison_scratch(uint32_t bits, int n_vh, void* cuda_stream);
+
 /* Bytes of chunked-mode scratch a device holds once allocated. */
 size_t gdn_chunked_scratch_bytes(int n_vh);
 

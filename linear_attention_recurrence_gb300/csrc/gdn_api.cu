@@ -1,0 +1,324 @@
+// C ABI of libgdn.so (declared in include/gdn.h): argument checks, TMA tensor
+// maps, the per-device status word and chunked-mode scratch, and the launches.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "gdn.h"
+#include "gdn_internal.h"
+
+namespace {
+
+thread_local std::string t_last_error;
+std::atomic<uint64_t> g_launches{0};
+std::mutex g_mu;
+
+constexpr int kMaxDevices = 64;
+struct DeviceState {
+    bool init = false;
+    int sm_count = 0;
+    int* status = nullptr;    // kernel status word (0 = fine)
+    float* scratch = nullptr; // chunked-mode prep records for one super-block
+    size_t scratch_bytes = 0;
+};
+DeviceState g_dev[kMaxDevices];
+
+int fail(int code, const std::string& msg) {
+    t_last_error = msg;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(GDN_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D FP32 tensor map over a row-major [rows][width] array; out-of-range rows read as 0.
+int make_map(CUtensorMap* map, const float* base, uint64_t width, uint64_t rows, uint32_t box_w, uint32_t box_h,
+             CUtensorMapSwizzle swizzle) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return fail(GDN_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[2] = {width, rows};
+    cuuint64_t strides[1] = {width * sizeof(float)};
+    cuuint32_t box[2] = {box_w, box_h};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(GDN_ERR_CUDA, "cuTensorMapEncodeTiled failed: " + std::to_string(r));
+    return GDN_OK;
+}
+
+// Per-device lazy set-up: SM count and the status word.
+int device_state(DeviceState** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(GDN_ERR_UNSUPPORTED, "device ordinal out of range");
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState& d = g_dev[dev];
+    if (!d.init) {
+        e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+        e = cudaMalloc(&d.status, sizeof(int));
+        if (e != cudaSuccess) {
+            d.status = nullptr;
+            cudaGetLastError();
+            return fail(GDN_ERR_ALLOC, std::string("status word allocation failed: ") + cudaGetErrorString(e));
+        }
+        e = cudaMemset(d.status, 0, sizeof(int));
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemset");
+        d.init = true;
+    }
+    *out = &d;
+    return GDN_OK;
+}
+
+size_t scratch_bytes_for(int n_vh) {
+    return static_cast<size_t>(gdn::kChunksPerSuperBlock) * n_vh * gdn::kPrepRecordFloats * sizeof(float);
+}
+
+int ensure_scratch(DeviceState* d, int n_vh) {
+    const size_t need = scratch_bytes_for(n_vh);
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (d->scratch && d->scratch_bytes >= need) return GDN_OK;
+    const char* sim = std::getenv("GDN_SIMULATE_ALLOC_FAILURE");
+    if (sim && sim[0] == '1') return fail(GDN_ERR_ALLOC, "chunked scratch allocation failed (simulated)");
+    if (d->scratch) {
+        // a larger head count than before: the old buffer may still be in use by queued work
+        cudaError_t e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+        cudaFree(d->scratch);
+        d->scratch = nullptr;
+        d->scratch_bytes = 0;
+    }
+    void* p = nullptr;
+    cudaError_t e = cudaMalloc(&p, need);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(GDN_ERR_ALLOC, "chunked scratch allocation of " + std::to_string(need) +
+                                       " bytes failed: " + cudaGetErrorString(e));
+    }
+    d->scratch = static_cast<float*>(p);
+    d->scratch_bytes = need;
+    return GDN_OK;
+}
+
+__global__ void fill_words_kernel(uint32_t* p, size_t n, uint32_t bits) {
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x)
+        p[i] = bits;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool overlap(const void* a, size_t an, const void* b, size_t bn) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + bn && b0 < a0 + an;
+}
+
+int seq_rows_per_thread() {
+    static int v = [] {
+        const char* s = std::getenv("GDN_SEQ_ROWS_PER_THREAD");
+        return (s && std::atoi(s) == 8) ? 8 : 16;
+    }();
+    return v;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gdn_recurrence(const float* q, const float* k, const float* v, const float* g, const float* beta,
+                   float* state_inout, float* out, int64_t T, int n_kh, int n_vh, int d, int mode,
+                   void* cuda_stream) {
+    using namespace gdn;
+    if (T < 0) return fail(GDN_ERR_INVALID_ARG, "T < 0");
+    if (n_kh <= 0 || n_vh <= 0 || d <= 0) return fail(GDN_ERR_INVALID_ARG, "n_kh, n_vh and d must be positive");
+    if (n_vh % n_kh != 0) return fail(GDN_ERR_INVALID_ARG, "n_vh must be a multiple of n_kh");
+    if (mode != GDN_SEQUENTIAL && mode != GDN_CHUNKED) return fail(GDN_ERR_INVALID_ARG, "unknown mode");
+    if (d != kD) return fail(GDN_ERR_UNSUPPORTED, "only d == 128 is supported");
+    if (n_vh != kHeadsPerKey * n_kh) return fail(GDN_ERR_UNSUPPORTED, "only n_vh == 3 * n_kh is supported");
+    if (T > INT32_MAX - 4096) return fail(GDN_ERR_UNSUPPORTED, "T too large for 32-bit TMA coordinates");
+    if (T == 0) return GDN_OK;
+    if (!q || !k || !v || !g || !beta || !state_inout || !out) return fail(GDN_ERR_INVALID_ARG, "null pointer");
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(state_inout, 16))
+        return fail(GDN_ERR_INVALID_ARG, "q, k, v, out and state_inout must be 16-byte aligned");
+    if (!aligned(g, 4) || !aligned(beta, 4)) return fail(GDN_ERR_INVALID_ARG, "g and beta must be 4-byte aligned");
+    const size_t qk_bytes = static_cast<size_t>(T) * n_kh * d * 4, v_bytes = static_cast<size_t>(T) * n_vh * d * 4;
+    const size_t gb_bytes = static_cast<size_t>(T) * n_vh * 4, s_bytes = static_cast<size_t>(n_vh) * d * d * 4;
+    const void* ins[5] = {q, k, v, g, beta};
+    const size_t in_bytes[5] = {qk_bytes, qk_bytes, v_bytes, gb_bytes, gb_bytes};
+    for (int i = 0; i < 5; ++i)
+        if (overlap(out, v_bytes, ins[i], in_bytes[i]) || overlap(state_inout, s_bytes, ins[i], in_bytes[i]))
+            return fail(GDN_ERR_INVALID_ARG, "out / state_inout overlap an input");
+    if (overlap(out, v_bytes, state_inout, s_bytes)) return fail(GDN_ERR_INVALID_ARG, "out overlaps state_inout");
+
+    DeviceState* dev = nullptr;
+    int rc = device_state(&dev);
+    if (rc != GDN_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+
+    if (mode == GDN_SEQUENTIAL) {
+        SeqParams p;
+        std::memset(&p, 0, sizeof(p));
+        const int B = seq_tokens_per_stage();
+        if ((rc = make_map(&p.tm_k, k, static_cast<uint64_t>(n_kh) * d, T, d, B, CU_TENSOR_MAP_SWIZZLE_NONE)))
+            return rc;
+        if ((rc = make_map(&p.tm_q, q, static_cast<uint64_t>(n_kh) * d, T, d, B, CU_TENSOR_MAP_SWIZZLE_NONE)))
+            return rc;
+        if ((rc = make_map(&p.tm_v, v, static_cast<uint64_t>(n_vh) * d, T, seq_box_cols(), B,
+                           CU_TENSOR_MAP_SWIZZLE_NONE)))
+            return rc;
+        p.g = g;
+        p.beta = beta;
+        p.state = state_inout;
+        p.out = out;
+        p.T = T;
+        p.n_kh = n_kh;
+        p.n_vh = n_vh;
+        p.status = dev->status;
+        cudaError_t e = launch_seq(p, seq_rows_per_thread(), s);
+        if (e != cudaSuccess) return cuda_fail(e, "sequential scan launch");
+        g_launches.fetch_add(1);
+        return GDN_OK;
+    }
+
+    if ((rc = ensure_scratch(dev, n_vh)) != GDN_OK) return rc;
+    ChunkScanParams sp;
+    std::memset(&sp, 0, sizeof(sp));
+    if ((rc = make_map(&sp.tm_k, k, static_cast<uint64_t>(n_kh) * d, T, 32, kChunk, CU_TENSOR_MAP_SWIZZLE_128B)))
+        return rc;
+    if ((rc = make_map(&sp.tm_q, q, static_cast<uint64_t>(n_kh) * d, T, 32, kChunk, CU_TENSOR_MAP_SWIZZLE_128B)))
+        return rc;
+    if ((rc = make_map(&sp.tm_v, v, static_cast<uint64_t>(n_vh) * d, T, chunk_scan_box_cols(), kChunk,
+                       CU_TENSOR_MAP_SWIZZLE_NONE)))
+        return rc;
+    sp.prep = dev->scratch;
+    sp.state = state_inout;
+    sp.out = out;
+    sp.n_kh = n_kh;
+    sp.n_vh = n_vh;
+    sp.status = dev->status;
+    ChunkPrepParams pp;
+    pp.q = q;
+    pp.k = k;
+    pp.g = g;
+    pp.beta = beta;
+    pp.prep = dev->scratch;
+    pp.n_kh = n_kh;
+    pp.n_vh = n_vh;
+    for (int64_t t0 = 0; t0 < T; t0 += kSuperBlock) {
+        const int n = static_cast<int>((T - t0) < kSuperBlock ? (T - t0) : kSuperBlock);
+        pp.t_begin = t0;
+        pp.n_tokens = n;
+        cudaError_t e = launch_chunk_prep(pp, s);
+        if (e != cudaSuccess) return cuda_fail(e, "chunk prep launch");
+        g_launches.fetch_add(1);
+        sp.t_begin = t0;
+        sp.n_tokens = n;
+        e = launch_chunk_scan(sp, s);
+        if (e != cudaSuccess) return cuda_fail(e, "chunk scan launch");
+        g_launches.fetch_add(1);
+    }
+    return GDN_OK;
+}
+
+int gdn_out_norm(const float* out, const float* z, const float* w, float eps, uint16_t* y_fp16, int64_t T,
+                 int n_vh, int d, void* cuda_stream) {
+    using namespace gdn;
+    if (T < 0) return fail(GDN_ERR_INVALID_ARG, "T < 0");
+    if (n_vh <= 0 || d <= 0) return fail(GDN_ERR_INVALID_ARG, "n_vh and d must be positive");
+    if (!(eps >= 0.0f) || eps != eps) return fail(GDN_ERR_INVALID_ARG, "eps must be a non-negative number");
+    if (d != kD) return fail(GDN_ERR_UNSUPPORTED, "only d == 128 is supported");
+    if (T == 0) return GDN_OK;
+    if (!out || !z || !w || !y_fp16) return fail(GDN_ERR_INVALID_ARG, "null pointer");
+    if (!aligned(out, 16) || !aligned(z, 16) || !aligned(w, 16) || !aligned(y_fp16, 8))
+        return fail(GDN_ERR_INVALID_ARG, "out, z, w must be 16-byte and y_fp16 8-byte aligned");
+    const size_t nb = static_cast<size_t>(T) * n_vh * d;
+    if (overlap(y_fp16, nb * 2, out, nb * 4) || overlap(y_fp16, nb * 2, z, nb * 4) ||
+        overlap(y_fp16, nb * 2, w, static_cast<size_t>(d) * 4))
+        return fail(GDN_ERR_INVALID_ARG, "y_fp16 overlaps an input");
+    DeviceState* dev = nullptr;
+    int rc = device_state(&dev);
+    if (rc != GDN_OK) return rc;
+    cudaError_t e = launch_out_norm(out, z, w, eps, y_fp16, T * n_vh, dev->sm_count,
+                                    static_cast<cudaStream_t>(cuda_stream));
+    if (e != cudaSuccess) return cuda_fail(e, "output norm launch");
+    g_launches.fetch_add(1);
+    return GDN_OK;
+}
+
+const char* gdn_last_error(void) { return t_last_error.c_str(); }
+
+int gdn_device_status(void* cuda_stream) {
+    DeviceState* dev = nullptr;
+    int rc = device_state(&dev);
+    if (rc != GDN_OK) return rc;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    int word = 0;
+    e = cudaMemcpy(&word, dev->status, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "status read");
+    if (word != 0) {
+        e = cudaMemset(dev->status, 0, sizeof(int));
+        if (e != cudaSuccess) return cuda_fail(e, "status reset");
+        return fail(GDN_ERR_TIMEOUT, "a kernel gave up a bounded wait");
+    }
+    return GDN_OK;
+}
+
+int gdn_release_scratch(int device) {
+    if (device < 0 || device >= kMaxDevices) return fail(GDN_ERR_INVALID_ARG, "device ordinal out of range");
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState& d = g_dev[device];
+    if (!d.scratch) return GDN_OK;
+    int cur = 0;
+    cudaGetDevice(&cur);
+    cudaSetDevice(device);
+    cudaError_t e = cudaFree(d.scratch);
+    cudaSetDevice(cur);
+    d.scratch = nullptr;
+    d.scratch_bytes = 0;
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFree");
+    return GDN_OK;
+}
+
+int gdn_poison_scratch(uint32_t bits, int n_vh, void* cuda_stream) {
+    if (n_vh <= 0) return fail(GDN_ERR_INVALID_ARG, "n_vh must be positive");
+    DeviceState* dev = nullptr;
+    int rc = device_state(&dev);
+    if (rc != GDN_OK) return rc;
+    if ((rc = ensure_scratch(dev, n_vh)) != GDN_OK) return rc;
+    const size_t n = dev->scratch_bytes / sizeof(uint32_t);
+    fill_words_kernel<<<dev->sm_count * 4, 256, 0, static_cast<cudaStream_t>(cuda_stream)>>>(
+        reinterpret_cast<uint32_t*>(dev->scratch), n, bits);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "scratch fill launch");
+    g_launches.fetch_add(1);
+    return GDN_OK;
+}
+
+size_t gdn_chunked_scratch_bytes(int n_vh) { return n_vh > 0 ? scratch_bytes_for(n_vh) : 0; }
+
+uint64_t gdn_launch_count(void) { return g_launches.load(); }
+
+}  // extern "C"

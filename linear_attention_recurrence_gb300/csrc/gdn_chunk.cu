@@ -1,0 +1,440 @@
+// Chunked (32-token WY) Gated DeltaNet recurrence for sm_103a.
+//
+// The math ("#1372 DeltaNet recurrence: STRATA_GDN_CHUNKED=1 - the prompt's
+// recurrence in 32-token chunks", section "What it does"), per value head, with
+// gamma_t the running sum of the gate inside the chunk and S0 the state before it:
+//     A[t][i] = beta_t e^(gamma_t - gamma_i) k_t.k_i   (i < t)
+//     T = (I + A)^-1,  T' = T diag(beta)
+//     U' = V - diag(e^gamma) K S0,  D = T' U'
+//     O = diag(e^gamma) Q S0 + P D,   P[t][i] = e^(gamma_t - gamma_i) q_t.k_i  (i <= t)
+//     S_end = e^gamma_last S0 + K^T diag(e^(gamma_last - gamma)) D
+// All exponents are <= 0.  A last chunk with r < 32 tokens is padded with zero
+// k, q, v, g and beta, which leaves every product above unchanged.
+//
+// Two kernels per 2048-token super-block, as on the page:
+//  * prep: one CTA per (chunk, key head) forms K K^T and Q K^T once for the key
+//    head's three value heads, the gates' running sums, A and P, and solves for T
+//    (one lane per column of T).  It writes a record per (chunk, value head):
+//    T'^T, P^T, e^gamma and e^(gamma_last - gamma).
+//  * scan: one CTA per (key head, 16 value columns) walks the super-block's
+//    chunks with its slice of the three heads' state in registers (and a
+//    transposed copy in shared memory for the K S0 / Q S0 product).  Each chunk's
+//    k and q tiles (TMA, 128-byte swizzle), v columns (TMA) and prep records
+//    (bulk copies) land in a double buffer while the chunk before computes.
+// The large products (K S0, Q S0, K^T D) run as register-tiled packed FP32x2 FMAs;
+// the tolerance the path is held to (2e-6 relative to FP64) leaves no room for
+// TF32 tensor-core inputs there.
+#include "gdn_device.cuh"
+#include "gdn_internal.h"
+
+namespace gdn {
+namespace {
+
+constexpr int D = kD;
+constexpr int C = kChunk;
+constexpr int REC = kPrepRecordFloats;
+constexpr int REC_TP = 0;                 // T'^T [s][t]
+constexpr int REC_PT = C * C;             // P^T  [s][t]
+constexpr int REC_EG = 2 * C * C;         // e^gamma_t
+constexpr int REC_ER = 2 * C * C + C;     // e^(gamma_last - gamma_t)
+
+// ============================ prep ============================
+constexpr int PREP_THREADS = 256;
+constexpr int KP = D + 4;  // padded row stride of the k / q tiles
+
+struct PrepSmem {
+    float K[C][KP];
+    float Q[C][KP];
+    float KK[C][C + 1];
+    float QK[C][C + 1];
+    float A[kHeadsPerKey][C][C + 1];
+    float gam[kHeadsPerKey][C];
+    float bet[kHeadsPerKey][C];
+};
+
+__global__ void __launch_bounds__(PREP_THREADS) gdn_chunk_prep_kernel(const ChunkPrepParams p) {
+    extern __shared__ __align__(16) unsigned char prep_raw[];
+    PrepSmem& sm = *reinterpret_cast<PrepSmem*>(prep_raw);
+    const int ci = blockIdx.x;  // chunk within the super-block
+    const int kh = blockIdx.y;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int t0 = ci * C;
+    const int n = min(C, p.n_tokens - t0);
+    const int64_t tb = p.t_begin + t0;
+
+    for (int idx = tid; idx < C * (D / 4); idx += PREP_THREADS) {
+        const int r = idx / (D / 4), c4 = idx % (D / 4);
+        float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), qv = kv;
+        if (r < n) {
+            const int64_t off = ((tb + r) * p.n_kh + kh) * D + 4 * c4;
+            kv = __ldg(reinterpret_cast<const float4*>(p.k + off));
+            qv = __ldg(reinterpret_cast<const float4*>(p.q + off));
+        }
+        *reinterpret_cast<float4*>(&sm.K[r][4 * c4]) = kv;
+        *reinterpret_cast<float4*>(&sm.Q[r][4 * c4]) = qv;
+    }
+    if (warp < kHeadsPerKey) {
+        const int h = kh + warp * p.n_kh;
+        float gv = 0.f, bv = 0.f;
+        if (lane < n) {
+            gv = __ldg(p.g + (tb + lane) * p.n_vh + h);
+            bv = __ldg(p.beta + (tb + lane) * p.n_vh + h);
+        }
+        // inclusive running sum of the gate over the chunk (fixed shuffle order)
+        float x = gv;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, x, off);
+            if (lane >= off) x += y;
+        }
+        sm.gam[warp][lane] = x;
+        sm.bet[warp][lane] = bv;
+    }
+    __syncthreads();
+
+    // K K^T and Q K^T, shared by the key head's three value heads.
+    {
+        const int t = tid >> 3, ig = tid & 7;
+        float kk[4] = {0.f, 0.f, 0.f, 0.f}, qk[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+        for (int c4 = 0; c4 < D / 4; ++c4) {
+            const float4 kt = *reinterpret_cast<const float4*>(&sm.K[t][4 * c4]);
+            const float4 qt = *reinterpret_cast<const float4*>(&sm.Q[t][4 * c4]);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float4 ki = *reinterpret_cast<const float4*>(&sm.K[ig + 8 * u][4 * c4]);
+                kk[u] = fmaf(kt.x, ki.x, kk[u]);
+                kk[u] = fmaf(kt.y, ki.y, kk[u]);
+                kk[u] = fmaf(kt.z, ki.z, kk[u]);
+                kk[u] = fmaf(kt.w, ki.w, kk[u]);
+                qk[u] = fmaf(qt.x, ki.x, qk[u]);
+                qk[u] = fmaf(qt.y, ki.y, qk[u]);
+                qk[u] = fmaf(qt.z, ki.z, qk[u]);
+                qk[u] = fmaf(qt.w, ki.w, qk[u]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            sm.KK[t][ig + 8 * u] = kk[u];
+            sm.QK[t][ig + 8 * u] = qk[u];
+        }
+    }
+    __syncthreads();
+
+    // A (shared memory) and P^T, e^gamma, e^(gamma_last - gamma) (records).
+    for (int idx = tid; idx < kHeadsPerKey * C * C; idx += PREP_THREADS) {
+        const int m = idx / (C * C), i = (idx / C) % C, t = idx % C;
+        float* rec = p.prep + (static_cast<int64_t>(ci) * p.n_vh + kh + m * p.n_kh) * REC;
+        const float e = (i <= t) ? expf(sm.gam[m][t] - sm.gam[m][i]) : 0.f;
+        sm.A[m][t][i] = (i < t) ? sm.bet[m][t] * e * sm.KK[t][i] : 0.f;
+        rec[REC_PT + i * C + t] = e * sm.QK[t][i];
+    }
+    if (tid < kHeadsPerKey * C) {
+        const int m = tid / C, t = tid % C;
+        float* rec = p.prep + (static_cast<int64_t>(ci) * p.n_vh + kh + m * p.n_kh) * REC;
+        rec[REC_EG + t] = expf(sm.gam[m][t]);
+        rec[REC_ER + t] = expf(sm.gam[m][C - 1] - sm.gam[m][t]);
+    }
+    __syncthreads();
+
+    // T = (I + A)^-1 by forward substitution, lane j owning column j; then
+    // row j of T'^T is T[:, j] * beta_j.
+    if (warp < kHeadsPerKey) {
+        const int m = warp, j = lane;
+        float Tc[C];
+#pragma unroll
+        for (int t = 0; t < C; ++t) {
+            float s = (t == j) ? 1.f : 0.f;
+#pragma unroll
+            for (int i = 0; i < t; ++i) s = fmaf(-sm.A[m][t][i], Tc[i], s);
+            Tc[t] = s;
+        }
+        const float bj = sm.bet[m][j];
+        float* rec = p.prep + (static_cast<int64_t>(ci) * p.n_vh + kh + m * p.n_kh) * REC;
+        float4* dst = reinterpret_cast<float4*>(rec + REC_TP + j * C);
+#pragma unroll
+        for (int t4 = 0; t4 < C / 4; ++t4)
+            dst[t4] = make_float4(Tc[4 * t4] * bj, Tc[4 * t4 + 1] * bj, Tc[4 * t4 + 2] * bj, Tc[4 * t4 + 3] * bj);
+    }
+}
+
+// ============================ scan ============================
+constexpr int SCAN_THREADS = 256;
+constexpr int NC = 16;        // value columns per CTA (per head)
+constexpr int NCC = kHeadsPerKey * NC;  // 48 columns of the CTA
+constexpr int SST = D + 4;    // row stride of the transposed state copy
+
+struct __align__(1024) ScanBuf {
+    float K[D / 32][C][32];        // 4 TMA boxes of [32 rows][32 floats], 128-byte swizzled
+    float Q[D / 32][C][32];
+    float V[kHeadsPerKey][C][NC];  // TMA boxes [32 rows][16 floats]
+    float rec[kHeadsPerKey][REC];  // prep records (bulk copies)
+};
+constexpr uint32_t kScanTxBytes = 2 * C * D * 4 + kHeadsPerKey * C * NC * 4 + kHeadsPerKey * REC * 4;
+
+struct ScanSmem {
+    ScanBuf buf[2];
+    float SsT[NCC][SST];     // S0 transposed: [head*16 + col][key dim]
+    float W[2 * C][NCC];     // rows 0..31: U'; rows 32..63: e^gamma (Q S0)
+    float Dm[C][NCC];        // D
+    float2 Dd[C][NCC];       // e^(gamma_last - gamma) D, duplicated for packed FMAs
+    uint64_t full[2];
+};
+
+// byte offset of float4 chunk `cc` (0..7) of row `r` in a 128-byte-swizzled box
+__device__ __forceinline__ int swz(int r, int cc) { return r * 128 + ((cc ^ (r & 7)) << 4); }
+
+__global__ void __launch_bounds__(SCAN_THREADS, 1) gdn_chunk_scan_kernel(const __grid_constant__ ChunkScanParams p) {
+    extern __shared__ unsigned char scan_raw[];
+    ScanSmem& sm = *reinterpret_cast<ScanSmem*>((reinterpret_cast<uintptr_t>(scan_raw) + 1023) & ~uintptr_t(1023));
+    const int kh = blockIdx.x;
+    const int c0 = blockIdx.y * NC;
+    const int tid = threadIdx.x;
+    const int n_kh = p.n_kh, n_vh = p.n_vh;
+    const int nch = (p.n_tokens + C - 1) / C;
+
+    if (tid == 0) {
+        mbar_init(&sm.full[0], 1);
+        mbar_init(&sm.full[1], 1);
+        mbar_init_fence();
+    }
+
+    // state slice -> registers (G4 tile: rows 8*it..8*it+7, column c0+j of each head)
+    const int it = tid >> 4, jj = tid & 15;
+    float2 Sreg[kHeadsPerKey][4];
+#pragma unroll
+    for (int m = 0; m < kHeadsPerKey; ++m) {
+        const float* sh = p.state + (static_cast<int64_t>(kh + m * n_kh) * D + 8 * it) * D + c0 + jj;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) Sreg[m][q] = make_float2(sh[(2 * q) * D], sh[(2 * q + 1) * D]);
+#pragma unroll
+        for (int h4 = 0; h4 < 2; ++h4)
+            *reinterpret_cast<float4*>(&sm.SsT[m * NC + jj][8 * it + 4 * h4]) =
+                make_float4(Sreg[m][2 * h4].x, Sreg[m][2 * h4].y, Sreg[m][2 * h4 + 1].x, Sreg[m][2 * h4 + 1].y);
+    }
+    __syncthreads();
+
+    auto issue = [&](int c) {
+        ScanBuf& b = sm.buf[c & 1];
+        uint64_t* bar = &sm.full[c & 1];
+        const int y = static_cast<int>(p.t_begin + static_cast<int64_t>(c) * C);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive_expect_tx(bar, kScanTxBytes);
+#pragma unroll
+        for (int bx = 0; bx < D / 32; ++bx) {
+            tma_load_2d(&b.K[bx][0][0], &p.tm_k, bar, kh * D + 32 * bx, y);
+            tma_load_2d(&b.Q[bx][0][0], &p.tm_q, bar, kh * D + 32 * bx, y);
+        }
+#pragma unroll
+        for (int m = 0; m < kHeadsPerKey; ++m) {
+            tma_load_2d(&b.V[m][0][0], &p.tm_v, bar, (kh + m * n_kh) * D + c0, y);
+            bulk_load(&b.rec[m][0], p.prep + (static_cast<int64_t>(c) * n_vh + kh + m * n_kh) * REC, REC * 4, bar);
+        }
+    };
+    if (tid == 0) issue(0);
+
+    // G1 tile: X rows 4*(tt&7)..+3 of K (tt < 8) or Q (tt >= 8), column jj of each head
+    const int tt = tid >> 4;
+    const int xr0 = 4 * (tt & 7);
+    const int xsw = 4 * (tt & 1);  // (xr0 + r) & 7 == xsw + r
+    // P2 / P3 tile: head pm, rows 4*pti..+3, columns 2*pjp, 2*pjp+1
+    const int pm = tid >> 6, pti = (tid >> 3) & 7, pjp = tid & 7;
+    bool ok = true;
+
+    for (int c = 0; c < nch; ++c) {
+        if (tid == 0 && c + 1 < nch) issue(c + 1);
+        if (!mbar_wait(&sm.full[c & 1], static_cast<uint32_t>((c >> 1) & 1))) { ok = false; break; }
+        const ScanBuf& b = sm.buf[c & 1];
+        const int nt = min(C, p.n_tokens - c * C);
+
+        // ---- G1: W = [K; Q] S0 (64 x 48), packed over even/odd key dims ----
+        {
+            const unsigned char* xb = reinterpret_cast<const unsigned char*>(tt < 8 ? &b.K[0][0][0] : &b.Q[0][0][0]);
+            float2 acc[4][kHeadsPerKey];
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int m = 0; m < kHeadsPerKey; ++m) acc[r][m] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int bx = 0; bx < D / 32; ++bx) {
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) {
+                    float4 a[4], s[kHeadsPerKey];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+                        a[r] = *reinterpret_cast<const float4*>(xb + bx * (C * 128) + (xr0 + r) * 128 +
+                                                                (((cc ^ r) ^ xsw) << 4));
+#pragma unroll
+                    for (int m = 0; m < kHeadsPerKey; ++m)
+                        s[m] = *reinterpret_cast<const float4*>(&sm.SsT[m * NC + jj][32 * bx + 4 * cc]);
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+#pragma unroll
+                        for (int m = 0; m < kHeadsPerKey; ++m) {
+                            acc[r][m] = ffma2(make_float2(a[r].x, a[r].y), make_float2(s[m].x, s[m].y), acc[r][m]);
+                            acc[r][m] = ffma2(make_float2(a[r].z, a[r].w), make_float2(s[m].z, s[m].w), acc[r][m]);
+                        }
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int t = xr0 + r;
+#pragma unroll
+                for (int m = 0; m < kHeadsPerKey; ++m) {
+                    const float x = acc[r][m].x + acc[r][m].y;
+                    const float eg = b.rec[m][REC_EG + t];
+                    if (tt < 8)
+                        sm.W[t][m * NC + jj] = b.V[m][t][jj] - eg * x;
+                    else
+                        sm.W[C + t][m * NC + jj] = eg * x;
+                }
+            }
+        }
+        __syncthreads();
+
+        // ---- P2: D = T' U' per head (32x32 by 32x16) ----
+        if (tid < kHeadsPerKey * 64) {
+            const float* tp = &b.rec[pm][REC_TP];
+            float acc[4][2];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) acc[r][0] = acc[r][1] = 0.f;
+#pragma unroll 8
+            for (int s = 0; s < C; ++s) {
+                const float4 a = *reinterpret_cast<const float4*>(tp + s * C + 4 * pti);
+                const float2 u = *reinterpret_cast<const float2*>(&sm.W[s][pm * NC + 2 * pjp]);
+                acc[0][0] = fmaf(a.x, u.x, acc[0][0]);
+                acc[0][1] = fmaf(a.x, u.y, acc[0][1]);
+                acc[1][0] = fmaf(a.y, u.x, acc[1][0]);
+                acc[1][1] = fmaf(a.y, u.y, acc[1][1]);
+                acc[2][0] = fmaf(a.z, u.x, acc[2][0]);
+                acc[2][1] = fmaf(a.z, u.y, acc[2][1]);
+                acc[3][0] = fmaf(a.w, u.x, acc[3][0]);
+                acc[3][1] = fmaf(a.w, u.y, acc[3][1]);
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int t = 4 * pti + r;
+                const float er = b.rec[pm][REC_ER + t];
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int col = pm * NC + 2 * pjp + q;
+                    sm.Dm[t][col] = acc[r][q];
+                    const float dd = er * acc[r][q];
+                    sm.Dd[t][col] = make_float2(dd, dd);
+                }
+            }
+        }
+        __syncthreads();
+
+        // ---- P3: O = e^gamma Q S0 + P D per head -> out ----
+        if (tid < kHeadsPerKey * 64) {
+            const float* pt = &b.rec[pm][REC_PT];
+            float acc[4][2];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const float2 w = *reinterpret_cast<const float2*>(&sm.W[C + 4 * pti + r][pm * NC + 2 * pjp]);
+                acc[r][0] = w.x;
+                acc[r][1] = w.y;
+            }
+#pragma unroll 8
+            for (int s = 0; s < C; ++s) {
+                const float4 a = *reinterpret_cast<const float4*>(pt + s * C + 4 * pti);
+                const float2 d = *reinterpret_cast<const float2*>(&sm.Dm[s][pm * NC + 2 * pjp]);
+                acc[0][0] = fmaf(a.x, d.x, acc[0][0]);
+                acc[0][1] = fmaf(a.x, d.y, acc[0][1]);
+                acc[1][0] = fmaf(a.y, d.x, acc[1][0]);
+                acc[1][1] = fmaf(a.y, d.y, acc[1][1]);
+                acc[2][0] = fmaf(a.z, d.x, acc[2][0]);
+                acc[2][1] = fmaf(a.z, d.y, acc[2][1]);
+                acc[3][0] = fmaf(a.w, d.x, acc[3][0]);
+                acc[3][1] = fmaf(a.w, d.y, acc[3][1]);
+            }
+            const int h = kh + pm * n_kh;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int t = 4 * pti + r;
+                if (t < nt) {
+                    float* o = p.out + ((p.t_begin + static_cast<int64_t>(c) * C + t) * n_vh + h) * D + c0 + 2 * pjp;
+                    *reinterpret_cast<float2*>(o) = make_float2(acc[r][0], acc[r][1]);
+                }
+            }
+        }
+
+        // ---- G4: S_end = e^gamma_last S0 + K^T (e^(gamma_last-gamma) D), packed over key-dim pairs ----
+        {
+            const unsigned char* kb = reinterpret_cast<const unsigned char*>(&b.K[it >> 2][0][0]);
+            const int cc0 = 2 * (it & 3);
+            float2 acc[kHeadsPerKey][4];
+#pragma unroll
+            for (int m = 0; m < kHeadsPerKey; ++m) {
+                const float el = b.rec[m][REC_EG + C - 1];
+                const float2 el2 = make_float2(el, el);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc[m][q] = fmul2(el2, Sreg[m][q]);
+            }
+#pragma unroll 8
+            for (int t = 0; t < C; ++t) {
+                const float4 klo = *reinterpret_cast<const float4*>(kb + swz(t, cc0));
+                const float4 khi = *reinterpret_cast<const float4*>(kb + swz(t, cc0 + 1));
+#pragma unroll
+                for (int m = 0; m < kHeadsPerKey; ++m) {
+                    const float2 d2 = sm.Dd[t][m * NC + jj];
+                    acc[m][0] = ffma2(make_float2(klo.x, klo.y), d2, acc[m][0]);
+                    acc[m][1] = ffma2(make_float2(klo.z, klo.w), d2, acc[m][1]);
+                    acc[m][2] = ffma2(make_float2(khi.x, khi.y), d2, acc[m][2]);
+                    acc[m][3] = ffma2(make_float2(khi.z, khi.w), d2, acc[m][3]);
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < kHeadsPerKey; ++m) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) Sreg[m][q] = acc[m][q];
+#pragma unroll
+                for (int h4 = 0; h4 < 2; ++h4)
+                    *reinterpret_cast<float4*>(&sm.SsT[m * NC + jj][8 * it + 4 * h4]) =
+                        make_float4(acc[m][2 * h4].x, acc[m][2 * h4].y, acc[m][2 * h4 + 1].x, acc[m][2 * h4 + 1].y);
+            }
+        }
+        __syncthreads();
+    }
+
+    if (!ok) {
+        if (tid == 0) report_timeout(p.status);
+        return;
+    }
+#pragma unroll
+    for (int m = 0; m < kHeadsPerKey; ++m) {
+        float* sh = p.state + (static_cast<int64_t>(kh + m * n_kh) * D + 8 * it) * D + c0 + jj;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            sh[(2 * q) * D] = Sreg[m][q].x;
+            sh[(2 * q + 1) * D] = Sreg[m][q].y;
+        }
+    }
+}
+
+}  // namespace
+
+int chunk_scan_box_cols() { return NC; }
+
+cudaError_t launch_chunk_prep(const ChunkPrepParams& p, cudaStream_t s) {
+    const size_t smem = sizeof(PrepSmem);
+    cudaError_t e = cudaFuncSetAttribute(gdn_chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    dim3 grid((p.n_tokens + C - 1) / C, p.n_kh);
+    gdn_chunk_prep_kernel<<<grid, PREP_THREADS, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_chunk_scan(const ChunkScanParams& p, cudaStream_t s) {
+    const size_t smem = sizeof(ScanSmem) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(gdn_chunk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.n_kh, D / NC);
+    gdn_chunk_scan_kernel<<<grid, SCAN_THREADS, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -1,0 +1,71 @@
+// Host-side interface between the C ABI (gdn_api.cu) and the kernel files.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace gdn {
+
+constexpr int kD = 128;          // key and value head dimension these kernels support
+constexpr int kHeadsPerKey = 3;  // value heads per key head (h, h + n_kh, h + 2 n_kh)
+constexpr int kChunk = 32;       // chunked mode: tokens per WY chunk
+constexpr int kSuperBlock = 2048;  // chunked mode: tokens per prep/scan pass
+constexpr int kChunksPerSuperBlock = kSuperBlock / kChunk;
+// Per (chunk, value head) prep record: T'^T [32][32], P^T [32][32], e^gamma [32],
+// e^(gamma_last - gamma) [32], in floats.
+constexpr int kPrepRecordFloats = 2 * kChunk * kChunk + 2 * kChunk;
+
+// ---- sequential scan ----
+struct SeqParams {
+    CUtensorMap tm_k;  // k viewed as [T][n_kh*128] FP32, box {128, B}
+    CUtensorMap tm_q;  // q, same
+    CUtensorMap tm_v;  // v viewed as [T][n_vh*128] FP32, box {16, B}
+    const float* g;
+    const float* beta;
+    float* state;
+    float* out;
+    int64_t T;
+    int n_kh;
+    int n_vh;
+    int* status;
+};
+int seq_tokens_per_stage();
+int seq_box_cols();
+// rows_per_thread: 8 or 16.  Returns the CUDA error of the launch.
+cudaError_t launch_seq(const SeqParams& p, int rows_per_thread, cudaStream_t s);
+
+// ---- output norm ----
+cudaError_t launch_out_norm(const float* out, const float* z, const float* w, float eps, uint16_t* y,
+                            int64_t rows, int sm_count, cudaStream_t s);
+
+// ---- chunked mode ----
+struct ChunkScanParams {
+    CUtensorMap tm_k;  // k viewed as [T][n_kh*128], box {32, 32}, 128-byte swizzle
+    CUtensorMap tm_q;  // q, same
+    CUtensorMap tm_v;  // v viewed as [T][n_vh*128], box {16, 32}
+    const float* prep;  // prep records of this super-block, [chunk][n_vh][kPrepRecordFloats]
+    float* state;
+    float* out;
+    int64_t t_begin;  // first token of the super-block (row in the tensor maps and in out)
+    int n_tokens;     // tokens in this super-block (1..2048)
+    int n_kh;
+    int n_vh;
+    int* status;
+};
+struct ChunkPrepParams {
+    const float* q;
+    const float* k;
+    const float* g;
+    const float* beta;
+    float* prep;
+    int64_t t_begin;
+    int n_tokens;
+    int n_kh;
+    int n_vh;
+};
+cudaError_t launch_chunk_prep(const ChunkPrepParams& p, cudaStream_t s);
+cudaError_t launch_chunk_scan(const ChunkScanParams& p, cudaStream_t s);
+int chunk_scan_box_cols();
+
+}  // namespace gdn

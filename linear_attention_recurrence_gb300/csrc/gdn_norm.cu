@@ -1,0 +1,84 @@
+// Gated RMSNorm of the recurrence output to FP16 ("#413 prefill: DeltaNet
+// recurrence with the three value heads of a key head in one thread", section
+// "What changes": gdn_out_norm_kernel writes only the FP16 copy y_h that the
+// output projection reads).  Per (token, value head) row of 128 values:
+//     r = 1 / sqrt(mean_j o_j^2 + eps),  y_j = fp16_rn(o_j * r * w_j * silu(z_j)).
+//
+// HBM-bound (per row: 512 B of o, 512 B of z read, 256 B of y written).  One warp
+// per row, one float4 of o and of z per lane, streamed past L1; two rows in flight
+// per warp and a grid of 2 CTAs of 512 threads per SM, grid-striding.
+#include <cuda_fp16.h>
+
+#include "gdn_device.cuh"
+#include "gdn_internal.h"
+
+namespace gdn {
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kRowsInFlight = 2;
+
+__device__ __forceinline__ float4 ld_stream(const float* p) {
+    float4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+__global__ void __launch_bounds__(kThreads, 2) gdn_out_norm_kernel(const float* __restrict__ o,
+                                                                 const float* __restrict__ z,
+                                                                 const float* __restrict__ w, float eps,
+                                                                 uint2* __restrict__ y, int64_t rows) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
+    const float4 w4 = reinterpret_cast<const float4*>(w)[lane];
+    for (int64_t base = warp0; base < rows; base += nwarps * kRowsInFlight) {
+        float4 ov[kRowsInFlight], zv[kRowsInFlight];
+#pragma unroll
+        for (int u = 0; u < kRowsInFlight; ++u) {
+            const int64_t row = base + u * nwarps;
+            if (row < rows) {
+                ov[u] = ld_stream(o + row * kD + 4 * lane);
+                zv[u] = ld_stream(z + row * kD + 4 * lane);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kRowsInFlight; ++u) {
+            const int64_t row = base + u * nwarps;
+            if (row >= rows) break;  // uniform across the warp
+            float ss = ov[u].x * ov[u].x;
+            ss = fmaf(ov[u].y, ov[u].y, ss);
+            ss = fmaf(ov[u].z, ov[u].z, ss);
+            ss = fmaf(ov[u].w, ov[u].w, ss);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            const float r = rsqrtf(ss * (1.0f / kD) + eps);
+            const __half2 lo = __floats2half2_rn(ov[u].x * r * w4.x * silu(zv[u].x),
+                                                 ov[u].y * r * w4.y * silu(zv[u].y));
+            const __half2 hi = __floats2half2_rn(ov[u].z * r * w4.z * silu(zv[u].z),
+                                                 ov[u].w * r * w4.w * silu(zv[u].w));
+            uint2 pkd;
+            pkd.x = *reinterpret_cast<const uint32_t*>(&lo);
+            pkd.y = *reinterpret_cast<const uint32_t*>(&hi);
+            __stcs(y + row * (kD / 4) + lane, pkd);
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_out_norm(const float* out, const float* z, const float* w, float eps, uint16_t* y,
+                            int64_t rows, int sm_count, cudaStream_t s) {
+    const int64_t warps_per_cta = kThreads / 32;
+    int64_t want = (rows + warps_per_cta * kRowsInFlight - 1) / (warps_per_cta * kRowsInFlight);
+    const int64_t cap = static_cast<int64_t>(sm_count) * 2;
+    const int grid = static_cast<int>(want < cap ? want : cap);
+    gdn_out_norm_kernel<<<grid, kThreads, 0, s>>>(out, z, w, eps, reinterpret_cast<uint2*>(y), rows);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -1,0 +1,172 @@
+"""Python binding of libgdn.so (the C ABI in include/gdn.h).
+
+Argument marshalling only: tensors are checked for device, dtype, shape and
+contiguity, and their data pointers plus the current CUDA stream go to the C
+functions of the same names.  Every step of the computation runs in the CUDA
+kernels of libgdn.so; there is no fallback.  If the library has not been built
+the first call raises.
+
+PyTorch provides device memory and streams; nothing here computes with it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgdn.so")
+
+GDN_SEQUENTIAL = 0
+GDN_CHUNKED = 1
+GDN_OK = 0
+GDN_ERR_INVALID_ARG = -1
+GDN_ERR_UNSUPPORTED = -2
+GDN_ERR_ALLOC = -3
+GDN_ERR_CUDA = -4
+GDN_ERR_TIMEOUT = -5
+
+_MODES = {"sequential": GDN_SEQUENTIAL, "seq": GDN_SEQUENTIAL, "chunked": GDN_CHUNKED,
+          GDN_SEQUENTIAL: GDN_SEQUENTIAL, GDN_CHUNKED: GDN_CHUNKED}
+
+_lock = threading.Lock()
+_lib = None
+
+EXPORTS = ("gdn_recurrence", "gdn_out_norm", "gdn_last_error", "gdn_device_status",
+           "gdn_release_scratch", "gdn_poison_scratch", "gdn_chunked_scratch_bytes", "gdn_launch_count")
+
+
+class GDNError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{message} (status {status})")
+        self.status = status
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libgdn.so and declare its C signatures.  Raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None and path == LIB_PATH:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is not built; run linear_attention_recurrence_gb300.build.build() "
+                               "(or __graft_entry__.build()) first")
+        lib = ctypes.CDLL(path)
+        vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        lib.gdn_recurrence.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, vp]
+        lib.gdn_recurrence.restype = i32
+        lib.gdn_out_norm.argtypes = [vp, vp, vp, ctypes.c_float, vp, i64, i32, i32, vp]
+        lib.gdn_out_norm.restype = i32
+        lib.gdn_last_error.argtypes = []
+        lib.gdn_last_error.restype = ctypes.c_char_p
+        lib.gdn_device_status.argtypes = [vp]
+        lib.gdn_device_status.restype = i32
+        lib.gdn_release_scratch.argtypes = [i32]
+        lib.gdn_release_scratch.restype = i32
+        lib.gdn_poison_scratch.argtypes = [ctypes.c_uint32, i32, vp]
+        lib.gdn_poison_scratch.restype = i32
+        lib.gdn_chunked_scratch_bytes.argtypes = [i32]
+        lib.gdn_chunked_scratch_bytes.restype = ctypes.c_size_t
+        lib.gdn_launch_count.argtypes = []
+        lib.gdn_launch_count.restype = ctypes.c_uint64
+        if path == LIB_PATH:
+            _lib = lib
+        return lib
+
+
+def _check(rc: int):
+    if rc != GDN_OK:
+        raise GDNError(rc, load_library().gdn_last_error().decode(errors="replace"))
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _want(t, name, shape=None, dtype=torch.float32):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def gdn_recurrence(q, k, v, g, beta, state, out=None, mode="sequential", stream=None):
+    """Gated delta-rule recurrence; updates ``state`` in place and returns ``out``.
+
+    q, k: [T][n_kh][d]; v: [T][n_vh][d]; g, beta: [T][n_vh]; state: [n_vh][d][d]
+    (FP32, CUDA, contiguous).  ``out`` ([T][n_vh][d]) is allocated if None.
+    """
+    T, n_kh, d = q.shape
+    n_vh = v.shape[1]
+    _want(q, "q", (T, n_kh, d))
+    _want(k, "k", (T, n_kh, d))
+    _want(v, "v", (T, n_vh, d))
+    _want(g, "g", (T, n_vh))
+    _want(beta, "beta", (T, n_vh))
+    _want(state, "state", (n_vh, d, d))
+    if out is None:
+        out = torch.empty((T, n_vh, d), dtype=torch.float32, device=q.device)
+    _want(out, "out", (T, n_vh, d))
+    if mode not in _MODES:
+        raise ValueError(f"unknown mode {mode!r}")
+    lib = load_library()
+    rc = lib.gdn_recurrence(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state), _ptr(out),
+                            T, n_kh, n_vh, d, _MODES[mode], _stream_ptr(stream))
+    _check(rc)
+    return out
+
+
+def gdn_out_norm(out, z, w, eps: float = 1e-6, y=None, stream=None):
+    """Gated RMSNorm of ``out`` ([T][n_vh][d] FP32) with gate ``z`` and weight ``w``
+    ([d]) to FP16; returns ``y`` ([T][n_vh][d] float16, allocated if None)."""
+    T, n_vh, d = out.shape
+    _want(out, "out", (T, n_vh, d))
+    _want(z, "z", (T, n_vh, d))
+    _want(w, "w", (d,))
+    if y is None:
+        y = torch.empty((T, n_vh, d), dtype=torch.float16, device=out.device)
+    _want(y, "y", (T, n_vh, d), dtype=torch.float16)
+    lib = load_library()
+    rc = lib.gdn_out_norm(_ptr(out), _ptr(z), _ptr(w), float(eps), _ptr(y), T, n_vh, d, _stream_ptr(stream))
+    _check(rc)
+    return y
+
+
+def gdn_device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status word."""
+    return int(load_library().gdn_device_status(_stream_ptr(stream)))
+
+
+def gdn_release_scratch(device: int = 0):
+    _check(load_library().gdn_release_scratch(int(device)))
+
+
+def gdn_poison_scratch(bits: int = 0x7FC00000, n_vh: int = 48, stream=None):
+    """Fill the chunked-mode scratch with a 32-bit pattern (default: quiet NaN)."""
+    _check(load_library().gdn_poison_scratch(int(bits) & 0xFFFFFFFF, int(n_vh), _stream_ptr(stream)))
+
+
+def gdn_chunked_scratch_bytes(n_vh: int = 48) -> int:
+    return int(load_library().gdn_chunked_scratch_bytes(int(n_vh)))
+
+
+def gdn_launch_count() -> int:
+    return int(load_library().gdn_launch_count())
+
+
+def gdn_last_error() -> str:
+    return load_library().gdn_last_error().decode(errors="replace")

@@ -1,0 +1,93 @@
+"""The C-ABI library loads and exports every function include/gdn.h declares;
+host-side argument checks return their status without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from gdn_testutil import ROOT
+
+HEADER = os.path.join(ROOT, "include", "gdn.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from linear_attention_recurrence_gb300 import build, gdn
+
+    build.build()
+    return gdn.load_library()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert "gdn_recurrence" in names and "gdn_out_norm" in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_binding_covers_the_header():
+    from linear_attention_recurrence_gb300 import gdn
+
+    assert sorted(gdn.EXPORTS) == _declared()
+
+
+def test_host_side_validation(lib):
+    from linear_attention_recurrence_gb300 import gdn
+
+    nil = ctypes.c_void_p(0)
+    one = ctypes.c_void_p(256)  # never dereferenced: every call below fails its checks first
+    r = lib.gdn_recurrence
+    assert r(nil, nil, nil, nil, nil, nil, nil, -1, 16, 48, 128, 0, nil) == gdn.GDN_ERR_INVALID_ARG
+    assert r(nil, nil, nil, nil, nil, nil, nil, 5, 16, 47, 128, 0, nil) == gdn.GDN_ERR_INVALID_ARG
+    assert r(nil, nil, nil, nil, nil, nil, nil, 5, 16, 48, 128, 7, nil) == gdn.GDN_ERR_INVALID_ARG
+    assert r(nil, nil, nil, nil, nil, nil, nil, 5, 0, 48, 128, 0, nil) == gdn.GDN_ERR_INVALID_ARG
+    assert r(nil, nil, nil, nil, nil, nil, nil, 5, 16, 48, 64, 0, nil) == gdn.GDN_ERR_UNSUPPORTED
+    assert r(nil, nil, nil, nil, nil, nil, nil, 5, 16, 32, 128, 1, nil) == gdn.GDN_ERR_UNSUPPORTED
+    assert r(nil, nil, nil, nil, nil, nil, nil, 5, 16, 48, 128, 0, nil) == gdn.GDN_ERR_INVALID_ARG
+    assert "null" in lib.gdn_last_error().decode()
+    # T == 0 is a no-op, even with null pointers
+    assert r(nil, nil, nil, nil, nil, nil, nil, 0, 16, 48, 128, 1, nil) == gdn.GDN_OK
+    # misaligned pointers
+    bad = ctypes.c_void_p(258)
+    assert r(bad, one, one, one, one, one, one, 5, 16, 48, 128, 0, nil) == gdn.GDN_ERR_INVALID_ARG
+    n = lib.gdn_out_norm
+    assert n(nil, nil, nil, 1e-6, nil, -1, 48, 128, nil) == gdn.GDN_ERR_INVALID_ARG
+    assert n(nil, nil, nil, -1.0, nil, 3, 48, 128, nil) == gdn.GDN_ERR_INVALID_ARG
+    assert n(nil, nil, nil, float("nan"), nil, 3, 48, 128, nil) == gdn.GDN_ERR_INVALID_ARG
+    assert n(nil, nil, nil, 1e-6, nil, 3, 48, 96, nil) == gdn.GDN_ERR_UNSUPPORTED
+    assert n(nil, nil, nil, 1e-6, nil, 0, 48, 128, nil) == gdn.GDN_OK
+    assert n(nil, nil, nil, 1e-6, nil, 3, 48, 128, nil) == gdn.GDN_ERR_INVALID_ARG
+
+
+def test_overlap_rejected(lib):
+    from linear_attention_recurrence_gb300 import gdn
+
+    base = 1 << 20
+    T, nkh, nvh, d = 4, 16, 48, 128
+    qk = T * nkh * d * 4
+    vb = T * nvh * d * 4
+    q = base
+    k = q + qk
+    v = k + qk
+    g = v + vb
+    be = g + 4096
+    st = be + 4096
+    out = v + 256  # inside v
+    P = ctypes.c_void_p
+    rc = lib.gdn_recurrence(P(q), P(k), P(v), P(g), P(be), P(st), P(out), T, nkh, nvh, d, 0, None)
+    assert rc == gdn.GDN_ERR_INVALID_ARG and "overlap" in lib.gdn_last_error().decode()
+
+
+def test_scratch_size_and_counters(lib):
+    assert lib.gdn_chunked_scratch_bytes(48) == 64 * 48 * (2 * 32 * 32 + 2 * 32) * 4
+    assert lib.gdn_chunked_scratch_bytes(0) == 0
+    assert lib.gdn_release_scratch(0) == 0
+    assert lib.gdn_release_scratch(-1) != 0
+    assert lib.gdn_launch_count() >= 0

@@ -1,0 +1,76 @@
+"""Error paths that need a CUDA context: a failed scratch allocation (simulated
+on the host) returns GDN_ERR_ALLOC and launches nothing; argument errors from
+the binding; no status left behind by normal runs."""
+import os
+import subprocess
+import sys
+
+import pytest
+import torch
+
+from gdn_testutil import ROOT, to_dev
+from linear_attention_recurrence_gb300 import gdn
+from linear_attention_recurrence_gb300.inputs import make_inputs
+
+pytestmark = pytest.mark.gpu
+
+CHILD = r"""
+import sys, torch
+sys.path.insert(0, {root!r})
+from linear_attention_recurrence_gb300 import gdn
+from linear_attention_recurrence_gb300.inputs import make_inputs
+x = make_inputs(64, seed=0, norm=False)
+t = {{k: torch.from_numpy(v).cuda() for k, v in x.items()}}
+st = t["S0"].clone()
+n0 = gdn.gdn_launch_count()
+try:
+    gdn.gdn_recurrence(t["q"], t["k"], t["v"], t["g"], t["beta"], st, mode="chunked")
+    print("NO-ERROR")
+except gdn.GDNError as e:
+    torch.cuda.synchronize()
+    same = torch.equal(st, t["S0"])
+    print("STATUS", e.status, "LAUNCHES", gdn.gdn_launch_count() - n0, "STATE-UNCHANGED", same)
+# the sequential mode needs no scratch and still works
+gdn.gdn_recurrence(t["q"], t["k"], t["v"], t["g"], t["beta"], st, mode="sequential")
+torch.cuda.synchronize()
+print("SEQ-OK", gdn.gdn_device_status())
+"""
+
+
+def test_simulated_scratch_allocation_failure():
+    env = dict(os.environ, GDN_SIMULATE_ALLOC_FAILURE="1")
+    r = subprocess.run([sys.executable, "-c", CHILD.format(root=ROOT)], env=env, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stderr
+    assert f"STATUS {gdn.GDN_ERR_ALLOC} LAUNCHES 0 STATE-UNCHANGED True" in r.stdout, r.stdout
+    assert "SEQ-OK 0" in r.stdout, r.stdout
+
+
+def test_binding_rejects_bad_tensors():
+    x = make_inputs(8, seed=0, norm=False)
+    t = to_dev(x)
+    with pytest.raises(ValueError):
+        gdn.gdn_recurrence(t["q"].double(), t["k"], t["v"], t["g"], t["beta"], t["S0"].clone())
+    with pytest.raises(ValueError):
+        gdn.gdn_recurrence(t["q"], t["k"], t["v"], t["g"], t["beta"][:, :47].contiguous(), t["S0"].clone())
+    with pytest.raises(ValueError):
+        gdn.gdn_recurrence(t["q"].cpu(), t["k"], t["v"], t["g"], t["beta"], t["S0"].clone())
+    with pytest.raises(ValueError):
+        gdn.gdn_recurrence(t["q"], t["k"], t["v"], t["g"], t["beta"], t["S0"].clone(), mode="fast")
+    with pytest.raises(gdn.GDNError) as e:
+        # out aliasing v is rejected by the library
+        gdn.gdn_recurrence(t["q"], t["k"], t["v"], t["g"], t["beta"], t["S0"].clone(), out=t["v"])
+    assert e.value.status == gdn.GDN_ERR_INVALID_ARG
+    assert gdn.gdn_device_status() == gdn.GDN_OK
+
+
+def test_launch_counter_counts_kernels():
+    x = make_inputs(4100, seed=0, norm=False)
+    t = to_dev(x)
+    n0 = gdn.gdn_launch_count()
+    gdn.gdn_recurrence(t["q"], t["k"], t["v"], t["g"], t["beta"], t["S0"].clone(), mode="sequential")
+    assert gdn.gdn_launch_count() - n0 == 1
+    n0 = gdn.gdn_launch_count()
+    gdn.gdn_recurrence(t["q"], t["k"], t["v"], t["g"], t["beta"], t["S0"].clone(), mode="chunked")
+    assert gdn.gdn_launch_count() - n0 == 2 * 3  # prep + scan per 2048-token super-block
+    torch.cuda.synchronize()

@@ -1,0 +1,203 @@
+"""GPU parity: the CUDA path through the C ABI against the FP64 oracle.
+
+Bar: max|diff| / max|value| <= 2e-6 for the FP32 output and the final state
+(both modes); the FP16 norm within 1 ulp of the oracle's norm of the same FP32
+input, and end to end within 1 ulp plus the propagated output tolerance.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gdn_testutil import (TOL, fp16_ulp_at, fp16_ulp_distance, half_bits_to_float, parity_token_counts, rel_err,
+                          to_dev)
+from linear_attention_recurrence_gb300 import gdn
+from linear_attention_recurrence_gb300.inputs import make_inputs
+
+pytestmark = pytest.mark.gpu
+
+MODES = ("sequential", "chunked")
+NAN = float("nan")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from linear_attention_recurrence_gb300 import build
+
+    build.build()
+    oracle.build()
+
+
+def _run(t, mode, splits=None, state=None):
+    """Run the recurrence over t (device tensors), optionally as several calls."""
+    T = t["q"].shape[0]
+    st = (t["S0"] if state is None else state).clone()
+    out = torch.full((T,) + tuple(t["v"].shape[1:]), NAN, device=t["q"].device)
+    bounds = [0] + list(np.cumsum(splits if splits else [T]))
+    assert bounds[-1] == T
+    for a, b in zip(bounds[:-1], bounds[1:]):
+        gdn.gdn_recurrence(t["q"][a:b], t["k"][a:b], t["v"][a:b], t["g"][a:b], t["beta"][a:b], st,
+                           out=out[a:b], mode=mode)
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_status() == gdn.GDN_OK
+    return out, st
+
+
+def _check_norm(out_gpu, o_ref, x, t, eps=1e-6):
+    """Isolated: the GPU norm of the GPU output vs the oracle norm of the same
+    FP32 values, <= 1 ulp everywhere.  End to end: vs the oracle norm of the
+    oracle output, <= 1 ulp plus the error the 2e-6 output tolerance can move."""
+    y = gdn.gdn_out_norm(out_gpu, t["z"], t["w"], eps)
+    torch.cuda.synchronize()
+    yb = y.cpu().numpy().view(np.uint16)
+    o32 = out_gpu.double().cpu().numpy()
+    y_iso = oracle.out_norm(o32, x["z"], x["w"], eps)
+    d_iso = fp16_ulp_distance(yb, y_iso)
+    assert int(d_iso.max()) <= 1, f"isolated norm off by {int(d_iso.max())} ulp"
+    y_e2e = oracle.out_norm(o_ref, x["z"], x["w"], eps)
+    rms = np.sqrt(np.mean(o_ref * o_ref, axis=-1, keepdims=True) + eps)
+    z = x["z"].astype(np.float64)
+    gate = np.abs(x["w"].astype(np.float64) * z / (1.0 + np.exp(-z)))
+    bound = TOL * np.max(np.abs(o_ref)) / rms * gate
+    err = np.abs(half_bits_to_float(yb) - half_bits_to_float(y_e2e))
+    ok = (fp16_ulp_distance(yb, y_e2e) <= 1) | (err <= fp16_ulp_at(y_e2e) + 1.01 * bound)
+    assert ok.all(), f"{int((~ok).sum())} FP16 outputs outside 1 ulp + propagated tolerance"
+    return float(np.mean(d_iso == 0))
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_T64(mode):
+    """One layer, T=64, page shapes, non-zero S0 (sequential mode is the
+    configuration's own; chunked runs the same inputs)."""
+    x = make_inputs(64, seed=0)
+    o_ref, s_ref = oracle.recurrence(x["q"], x["k"], x["v"], x["g"], x["beta"], x["S0"])
+    out, st = _run(to_dev(x), mode)
+    assert rel_err(out.cpu().numpy(), o_ref) <= TOL
+    assert rel_err(st.cpu().numpy(), s_ref) <= TOL
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("seed", [1, 2])
+def test_page_token_counts(mode, seed):
+    """T in the page's parity list (1 ... 4099) from a non-zero state, plus the norm."""
+    Ts = parity_token_counts()
+    full = make_inputs(max(Ts), seed=seed)
+    td = to_dev(full)
+    for T in Ts:
+        x = {kk: (vv[:T] if vv.ndim >= 2 and kk not in ("S0",) else vv) for kk, vv in full.items()}
+        t = {kk: (vv[:T] if vv.dim() >= 2 and kk != "S0" else vv) for kk, vv in td.items()}
+        o_ref, s_ref = oracle.recurrence(x["q"], x["k"], x["v"], x["g"], x["beta"], x["S0"])
+        out, st = _run(t, mode)
+        eo = rel_err(out.cpu().numpy(), o_ref)
+        es = rel_err(st.cpu().numpy(), s_ref)
+        assert eo <= TOL and es <= TOL, (T, eo, es)
+        _check_norm(out, o_ref, x, t)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_T8192_with_norm(mode):
+    x = make_inputs(8192, seed=0)
+    o_ref, s_ref = oracle.recurrence(x["q"], x["k"], x["v"], x["g"], x["beta"], x["S0"])
+    t = to_dev(x)
+    out, st = _run(t, mode)
+    assert rel_err(out.cpu().numpy(), o_ref) <= TOL
+    assert rel_err(st.cpu().numpy(), s_ref) <= TOL
+    _check_norm(out, o_ref, x, t)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_T32768_superblocks_carried(mode):
+    """T = 32768 as 16 calls of 2048 with the state carried (the bench's launch
+    configuration): the output against FP64 on the first 8192 tokens and the
+    state after every call."""
+    T, SB = 32768, 2048
+    x = make_inputs(T, seed=0, norm=False)
+    t = to_dev(x)
+    st = t["S0"].clone()
+    s_ref = x["S0"].astype(np.float64)
+    out = torch.full((T, 48, 128), NAN, device="cuda")
+    for i in range(T // SB):
+        a, b = i * SB, (i + 1) * SB
+        gdn.gdn_recurrence(t["q"][a:b], t["k"][a:b], t["v"][a:b], t["g"][a:b], t["beta"][a:b], st,
+                           out=out[a:b], mode=mode)
+        o_ref, s_ref = oracle.recurrence(x["q"][a:b], x["k"][a:b], x["v"][a:b], x["g"][a:b], x["beta"][a:b],
+                                         s_ref)
+        es = rel_err(st.cpu().numpy(), s_ref)
+        assert es <= TOL, (i, es)
+        if a < 8192:
+            eo = rel_err(out[a:b].cpu().numpy(), o_ref)
+            assert eo <= TOL, (i, eo)
+    assert gdn.gdn_device_status() == gdn.GDN_OK
+    assert torch.isfinite(out).all()
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("T", [2047, 2048, 2049, 4097])
+def test_superblock_edges(mode, T):
+    """Token counts around the 2048-token super-block and 32-token chunk edges."""
+    x = make_inputs(T, seed=3, norm=False)
+    o_ref, s_ref = oracle.recurrence(x["q"], x["k"], x["v"], x["g"], x["beta"], x["S0"])
+    out, st = _run(to_dev(x), mode)
+    assert rel_err(out.cpu().numpy(), o_ref) <= TOL
+    assert rel_err(st.cpu().numpy(), s_ref) <= TOL
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("n_kh", [1, 5, 32])
+def test_other_head_counts(mode, n_kh):
+    """Any number of key heads with three value heads each."""
+    T = 97
+    x = make_inputs(T, seed=4, n_kh=n_kh, n_vh=3 * n_kh, norm=False)
+    o_ref, s_ref = oracle.recurrence(x["q"], x["k"], x["v"], x["g"], x["beta"], x["S0"])
+    out, st = _run(to_dev(x), mode)
+    assert rel_err(out.cpu().numpy(), o_ref) <= TOL
+    assert rel_err(st.cpu().numpy(), s_ref) <= TOL
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_T0_is_noop(mode):
+    x = make_inputs(1, seed=5, norm=False)
+    t = to_dev(x)
+    st = t["S0"].clone()
+    out = torch.full((0, 48, 128), NAN, device="cuda")
+    gdn.gdn_recurrence(t["q"][:0], t["k"][:0], t["v"][:0], t["g"][:0], t["beta"][:0], st, out=out, mode=mode)
+    torch.cuda.synchronize()
+    assert torch.equal(st, t["S0"])
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_special_inputs(mode):
+    """beta = 0 and g = 0 leave the state unchanged (sequential: bit for bit)
+    and read out S0^T q; a strongly decaying gate (g = -20) wipes the old state."""
+    T = 40
+    x = make_inputs(T, seed=6, norm=False)
+    x["beta"][:] = 0.0
+    x["g"][:] = 0.0
+    o_ref, s_ref = oracle.recurrence(x["q"], x["k"], x["v"], x["g"], x["beta"], x["S0"])
+    out, st = _run(to_dev(x), mode)
+    if mode == "sequential":
+        assert np.array_equal(st.cpu().numpy(), x["S0"])
+    assert rel_err(st.cpu().numpy(), s_ref) <= TOL
+    assert rel_err(out.cpu().numpy(), o_ref) <= TOL
+    y = make_inputs(T, seed=7, norm=False)
+    y["g"][:] = -20.0
+    o_ref, s_ref = oracle.recurrence(y["q"], y["k"], y["v"], y["g"], y["beta"], y["S0"])
+    out, st = _run(to_dev(y), mode)
+    assert rel_err(out.cpu().numpy(), o_ref) <= TOL
+    assert rel_err(st.cpu().numpy(), s_ref) <= TOL
+
+
+def test_norm_edge_cases():
+    """Norm of rows of zeros (y = 0), huge and tiny magnitudes, T = 1."""
+    T = 3
+    x = make_inputs(T, seed=8)
+    o = np.zeros((T, 48, 128), np.float32)
+    o[1] = 1e4 * x["v"][1]
+    o[2] = 1e-4 * x["v"][2]
+    t = to_dev({"o": o, "z": x["z"], "w": x["w"]})
+    y = gdn.gdn_out_norm(t["o"], t["z"], t["w"], 1e-6)
+    torch.cuda.synchronize()
+    yb = y.cpu().numpy().view(np.uint16)
+    y_ref = oracle.out_norm(o.astype(np.float64), x["z"], x["w"], 1e-6)
+    assert int(fp16_ulp_distance(yb, y_ref).max()) <= 1
+    assert np.all((yb[0] & 0x7FFF) == 0)
