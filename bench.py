@@ -1,0 +1,380 @@
+"""Bench: one layer of Gated DeltaNet prefill on GB300 through the C ABI.
+
+Workload (default): one layer, 16 key heads x 3 = 48 value heads, d = 128,
+T = 32768 tokens processed as 16 calls of 2048 tokens with the state carried
+between calls, then the gated RMSNorm of all 32768 outputs to FP16.  Seeded
+synthetic inputs of the prefill distributions (inputs.py); q/k/v/z are larger
+than the 129 MB L2, so every step streams them from HBM.
+
+One step = the 16 recurrence calls in the selected mode + the norm.  The other
+mode is timed in the same run and reported under "modes".  Printed: one JSON
+line with the metric (us per token per layer, lower is better), per-mode
+kernel timings, the roofline of the dominant kernel, the end-to-end number with
+host buffers, clocks during the timed region, and the FP64 oracle timed on the
+host cores (cpu_baseline).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--mode chunked|sequential]
+  python bench.py --impl reference     # the FP64 oracle as the reference arm
+Under torchrun (N > 1) every rank runs an independent replica (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GDN prefill recurrence µs/token/layer (48 vh, d=128) and % of roofline"
+N_KH, N_VH, D = 16, 48, 128
+# algorithmic work per token and layer (48 value heads, d = 128)
+FLOP_SEQ = 48 * 7 * D * D                                            # 5.505 Mflop
+FLOP_CHUNKED = 48 * (6 * D * D + D * D // 32 + (10 * 32 * D) / 3 + 32 * 32 / 3)  # ~5.42 Mflop
+BYTES_REC = 16 * D * 4 * 2 + 48 * D * 4 + 48 * 4 * 2 + 48 * D * 4   # q,k + v + g,beta + o = 65,920 B
+BYTES_NORM = 48 * D * 4 * 2 + 48 * D * 2                             # o + z + y = 61,440 B
+FP32_LANES_PER_SM = 128
+SM_MAX_MHZ = 2070.0
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d.get("hbm_gbs", 6800.0)), float(d.get("sm_max_mhz", SM_MAX_MHZ)), "measured"
+    return 6800.0, SM_MAX_MHZ, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    Q = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.window = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def mark(self, t_begin: float, t_end: float):
+        """Wall-clock bounds of the timed region (time.time())."""
+        self.window = (t_begin, t_end)
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=10)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        import datetime
+
+        rows = []
+        for ln in (self.out or "").splitlines():
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) >= 9:
+                try:
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                except ValueError:
+                    continue
+                if self.window is None or self.window[0] <= ts <= self.window[1]:
+                    rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+def cpu_baseline(tokens_target_s: float = 10.0, seed: int = 0):
+    """The FP64 oracle (unchanged) on the host cores: recurrence + norm over a
+    bounded prefix of the workload, sized for ~tokens_target_s of CPU time."""
+    import oracle
+    from linear_attention_recurrence_gb300.inputs import make_inputs
+
+    nt = oracle.max_threads()
+    probe = 128
+    x = make_inputs(probe, seed=seed)
+    t0 = time.perf_counter()
+    o, _ = oracle.recurrence(x["q"], x["k"], x["v"], x["g"], x["beta"], x["S0"], nthreads=nt)
+    oracle.out_norm(o, x["z"], x["w"], 1e-6, nthreads=nt)
+    per_tok = (time.perf_counter() - t0) / probe
+    T = int(min(32768, max(256, tokens_target_s / max(per_tok, 1e-9))))
+    T = (T // 128) * 128
+    x = make_inputs(T, seed=seed)
+    t0 = time.perf_counter()
+    o, _ = oracle.recurrence(x["q"], x["k"], x["v"], x["g"], x["beta"], x["S0"], nthreads=nt)
+    oracle.out_norm(o, x["z"], x["w"], 1e-6, nthreads=nt)
+    dt = time.perf_counter() - t0
+    return {"value": dt / T * 1e6, "unit": "µs/token/layer", "cores": nt, "kind": "oracle",
+            "sample": f"first {T} tokens of the T=32768 workload, 48 value heads, FP64 recurrence + norm, "
+                      f"{nt} OpenMP threads, {dt:.1f} s"}
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    steps = []
+    cb = None
+    for i in range(args.warmup + args.steps):
+        cb = cpu_baseline(tokens_target_s=args.ref_seconds)
+        if i >= args.warmup:
+            steps.append(cb["value"])
+    v = statistics.median(steps)
+    cb["value"] = v
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "µs/token/layer", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": v * 32768 / 1e3,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": _config(args), "cpu_baseline": cb,
+            "e2e": {"value": v, "unit": "µs/token/layer", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _config(args):
+    return {"workload": f"gdn-prefill 1 layer, T={args.tokens} as {args.tokens // args.call_tokens} calls of "
+                        f"{args.call_tokens} with the state carried, then the FP16 norm",
+            "T": args.tokens, "tokens_per_call": args.call_tokens, "n_kh": N_KH, "n_vh": N_VH, "d": D,
+            "mode": args.mode, "global_batch": 1, "seq_len": args.tokens,
+            "l2": "inputs larger than L2 (q/k/v/z stream from HBM every step)",
+            "parallelism": "replicas" if _dist()[0] > 1 else "single"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--mode", default="chunked", choices=["chunked", "sequential"])
+    ap.add_argument("--tokens", type=int, default=32768)
+    ap.add_argument("--call-tokens", type=int, default=2048)
+    ap.add_argument("--skip-cpu", action="store_true", help="no oracle timing")
+    ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--skip-other-mode", action="store_true")
+    ap.add_argument("--ref-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    assert args.tokens % args.call_tokens == 0
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+
+    from linear_attention_recurrence_gb300 import build, gdn
+    from linear_attention_recurrence_gb300.inputs import make_inputs
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if rank == 0 or ws == 1:
+        build.build()
+    if ws > 1:
+        dist.barrier()
+    gdn.load_library()
+
+    T, CT = args.tokens, args.call_tokens
+    ncalls = T // CT
+    x = make_inputs(T, seed=0, layer=rank)
+    h = {k: torch.from_numpy(v).pin_memory() for k, v in x.items()}
+    t = {k: v.to(dev, non_blocking=True) for k, v in h.items()}
+    state = torch.empty_like(t["S0"])
+    out = torch.empty((T, N_VH, D), device=dev)
+    y = torch.empty((T, N_VH, D), device=dev, dtype=torch.float16)
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+
+    def step(mode, ev=None):
+        state.copy_(t["S0"])
+        for i in range(ncalls):
+            a, b = i * CT, (i + 1) * CT
+            if ev is not None:
+                ev[0].append(torch.cuda.Event(enable_timing=True))
+                ev[0][-1].record(stream)
+            gdn.gdn_recurrence(t["q"][a:b], t["k"][a:b], t["v"][a:b], t["g"][a:b], t["beta"][a:b], state,
+                               out=out[a:b], mode=mode, stream=stream)
+            if ev is not None:
+                ev[1].append(torch.cuda.Event(enable_timing=True))
+                ev[1][-1].record(stream)
+        if ev is not None:
+            ev[2].append(torch.cuda.Event(enable_timing=True))
+            ev[2][-1].record(stream)
+        gdn.gdn_out_norm(out, t["z"], t["w"], 1e-6, y=y, stream=stream)
+        if ev is not None:
+            ev[3].append(torch.cuda.Event(enable_timing=True))
+            ev[3][-1].record(stream)
+
+    def timed(mode, steps, warmup, per_kernel, clk=None):
+        for _ in range(warmup):
+            step(mode)
+        torch.cuda.synchronize()
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        wall0 = time.time()
+        ev = ([], [], [], []) if per_kernel else None
+        n0 = gdn.gdn_launch_count()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step(mode, ev)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if ws > 1:
+            dist.barrier()
+        launches = gdn.gdn_launch_count() - n0
+        if clk is not None:
+            clk.mark(wall0, time.time())
+        total_ms = e0.elapsed_time(e1)
+        if ws > 1:
+            tt = torch.tensor([total_ms], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            total_ms = float(tt.item())
+        res = {"ms_per_step": total_ms / steps, "launches": launches}
+        if per_kernel:
+            rec = [a.elapsed_time(b) for a, b in zip(ev[0], ev[1])]
+            nrm = [a.elapsed_time(b) for a, b in zip(ev[2], ev[3])]
+            res["rec_call_ms"] = statistics.mean(rec)
+            res["rec_ms_per_step"] = sum(rec) / steps
+            res["norm_ms"] = statistics.mean(nrm)
+        return res
+
+    other = "sequential" if args.mode == "chunked" else "chunked"
+    with Clocks(dev.index) as clk:
+        time.sleep(0.5)  # nvidia-smi's first samples
+        main_res = timed(args.mode, args.steps, args.warmup, per_kernel=False, clk=clk)
+        time.sleep(0.1)
+    kern = timed(args.mode, args.steps, 1, per_kernel=True)
+    other_res = None if args.skip_other_mode else timed(other, args.steps, 1, per_kernel=True)
+    assert gdn.gdn_device_status() == gdn.GDN_OK
+
+    # end to end through the public API with host buffers: H2D of the step's
+    # inputs from pinned memory, the calls, D2H of the FP16 output and the state
+    e2e = None
+    if not args.skip_e2e:
+        hy = torch.empty((T, N_VH, D), dtype=torch.float16).pin_memory()
+        hs = torch.empty_like(h["S0"]).pin_memory()
+        names = ["q", "k", "v", "g", "beta", "S0", "z", "w"]
+        h2d = sum(h[n].numel() * h[n].element_size() for n in names)
+        d2h = hy.numel() * 2 + hs.numel() * 4
+
+        def e2e_step():
+            for n in names:
+                t[n].copy_(h[n], non_blocking=True)
+            step(args.mode)
+            hy.copy_(y, non_blocking=True)
+            hs.copy_(state, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        if ws > 1:
+            dist.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        if ws > 1:
+            tt = torch.tensor([ms], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            ms = float(tt.item())
+        e2e = {"value": ms * 1e3 / (T * ws), "unit": "µs/token/layer", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+
+    if rank != 0:
+        if ws > 1:
+            dist.destroy_process_group()
+        return 0
+
+    hbm_gbs, sm_mhz_max, peak_src = _peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    alu_peak_tflops = sms * FP32_LANES_PER_SM * 2 * sm_mhz_max * 1e6 / 1e12
+    clocks = clk.summary()
+
+    def mode_summary(mode, r):
+        flop = FLOP_SEQ if mode == "sequential" else FLOP_CHUNKED
+        achieved = flop * CT / (r["rec_call_ms"] * 1e-3) / 1e12
+        return {"us_per_token_layer": r["rec_ms_per_step"] * 1e3 / T,
+                "recurrence_call_ms": r["rec_call_ms"], "norm_ms": r["norm_ms"],
+                "alu_tflops": achieved, "alu_frac": achieved / alu_peak_tflops,
+                "launches_per_step": r["launches"] / args.steps}
+
+    modes = {args.mode: mode_summary(args.mode, kern)}
+    if other_res is not None:
+        modes[other] = mode_summary(other, other_res)
+    flop = FLOP_SEQ if args.mode == "sequential" else FLOP_CHUNKED
+    achieved = flop * CT / (kern["rec_call_ms"] * 1e-3) / 1e12
+    norm_gbs = BYTES_NORM * T / (kern["norm_ms"] * 1e-3) / 1e9
+    value = main_res["ms_per_step"] * 1e3 / (T * ws)
+    line = {
+        "metric": METRIC, "value": value, "unit": "µs/token/layer", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": main_res["ms_per_step"], "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": _config(args),
+        "tokens_per_s": T * ws / (main_res["ms_per_step"] * 1e-3),
+        "gpu_launches": main_res["launches"],
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": alu_peak_tflops, "unit": "TFLOP/s",
+                     "frac": achieved / alu_peak_tflops, "traffic": None,
+                     "kernel": "gdn_chunk_prep+gdn_chunk_scan per 2048-token call" if args.mode == "chunked"
+                     else "gdn_seq_kernel per 2048-token call",
+                     "peak_basis": f"{sms} SMs x 128 FP32 lanes x 2 x {sm_mhz_max:.0f} MHz ({peak_src} max clock)",
+                     "frac_at_observed_clock": (achieved / (sms * FP32_LANES_PER_SM * 2 * clocks["sm_mhz"] * 1e6
+                                                            / 1e12)) if clocks.get("sm_mhz") else None},
+        "norm_roofline": {"bound": "hbm", "achieved": norm_gbs, "peak": hbm_gbs, "unit": "GB/s",
+                          "frac": norm_gbs / hbm_gbs, "peak_basis": f"{peak_src} copy bandwidth"},
+        "modes": modes,
+        "clocks": clocks,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if not args.skip_cpu and ws == 1:
+        line["cpu_baseline"] = cpu_baseline()
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

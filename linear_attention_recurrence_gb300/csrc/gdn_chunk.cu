@@ -53,8 +53,7 @@ struct PrepSmem {
 };
 
 __global__ void __launch_bounds__(PREP_THREADS) gdn_chunk_prep_kernel(const ChunkPrepParams p) {
-    extern __shared__ __align__(16) unsigned char prep_raw[];
-    PrepSmem& sm = *reinterpret_cast<PrepSmem*>(prep_raw);
+    PrepSmem& sm = *aligned_dynamic_smem<PrepSmem, 16>();
     const int ci = blockIdx.x;  // chunk within the super-block
     const int kh = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -185,8 +184,7 @@ struct ScanSmem {
 __device__ __forceinline__ int swz(int r, int cc) { return r * 128 + ((cc ^ (r & 7)) << 4); }
 
 __global__ void __launch_bounds__(SCAN_THREADS, 1) gdn_chunk_scan_kernel(const __grid_constant__ ChunkScanParams p) {
-    extern __shared__ unsigned char scan_raw[];
-    ScanSmem& sm = *reinterpret_cast<ScanSmem*>((reinterpret_cast<uintptr_t>(scan_raw) + 1023) & ~uintptr_t(1023));
+    ScanSmem& sm = *aligned_dynamic_smem<ScanSmem, 1024>();
     const int kh = blockIdx.x;
     const int c0 = blockIdx.y * NC;
     const int tid = threadIdx.x;
@@ -418,7 +416,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) gdn_chunk_scan_kernel(const _
 int chunk_scan_box_cols() { return NC; }
 
 cudaError_t launch_chunk_prep(const ChunkPrepParams& p, cudaStream_t s) {
-    const size_t smem = sizeof(PrepSmem);
+    const size_t smem = sizeof(PrepSmem) + 16;
     cudaError_t e = cudaFuncSetAttribute(gdn_chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;

@@ -21,6 +21,16 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// The dynamic shared memory window, rounded up to ALIGN bytes.  The offset is
+// added to the __shared__ array itself (not through an integer cast) so the
+// compiler keeps the shared address space and emits LDS/STS, not generic loads.
+template <class T, uint32_t ALIGN>
+__device__ __forceinline__ T* aligned_dynamic_smem() {
+    extern __shared__ __align__(16) unsigned char gdn_dyn_smem[];
+    const uint32_t a = smem_addr(gdn_dyn_smem);
+    return reinterpret_cast<T*>(gdn_dyn_smem + ((ALIGN - (a & (ALIGN - 1))) & (ALIGN - 1)));
+}
+
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
 }

@@ -62,15 +62,10 @@ struct SeqSmem {
     uint64_t empty[NS];  // every consumer warp is done with the stage
 };
 
-__device__ __forceinline__ SeqSmem& seq_smem() {
-    extern __shared__ unsigned char smem_raw[];
-    return *reinterpret_cast<SeqSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-}
-
 template <int R>
 __global__ void __launch_bounds__(SeqShape<R>::THREADS, 1) gdn_seq_kernel(const __grid_constant__ SeqParams p) {
     using Sh = SeqShape<R>;
-    SeqSmem& sm = seq_smem();
+    SeqSmem& sm = *aligned_dynamic_smem<SeqSmem, 1024>();
     const int kh = blockIdx.x;
     const int c0 = blockIdx.y * NCOL;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -170,6 +165,76 @@ __global__ void __launch_bounds__(SeqShape<R>::THREADS, 1) gdn_seq_kernel(const 
     }
     float* out_col = p.out + static_cast<int64_t>(kh + (rg < kHeadsPerKey ? rg : 0) * n_kh) * D + c;
 
+    // One token's operands, loaded from the stage one token ahead of use.
+    struct Ops {
+        float4 k[Sh::P4], q[Sh::P4];
+        float a[kHeadsPerKey], b[kHeadsPerKey], v[kHeadsPerKey], kq;
+    };
+    auto load = [&](Ops& o, const Stage& st, int tt) {
+        const float4* k4 = reinterpret_cast<const float4*>(st.k[tt]);
+        const float4* q4 = reinterpret_cast<const float4*>(st.q[tt]);
+#pragma unroll
+        for (int pp = 0; pp < Sh::P4; ++pp) {
+            o.k[pp] = k4[rg + Sh::G * pp];
+            o.q[pp] = q4[rg + Sh::G * pp];
+        }
+#pragma unroll
+        for (int m = 0; m < kHeadsPerKey; ++m) {
+            o.a[m] = st.a[tt][m];
+            o.b[m] = st.b[tt][m];
+            o.v[m] = st.v[m][tt][cl];
+        }
+        o.kq = st.kq[tt];
+    };
+    // One token: both column sums from one pass over the state, the shuffle
+    // reduction, delta and the output, then the state update.
+    auto token = [&](const Ops& o, int64_t t) {
+        float2 ak[kHeadsPerKey], aq[kHeadsPerKey];
+#pragma unroll
+        for (int m = 0; m < kHeadsPerKey; ++m) ak[m] = aq[m] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int pp = 0; pp < Sh::P4; ++pp) {
+            const float2 k01 = make_float2(o.k[pp].x, o.k[pp].y), k23 = make_float2(o.k[pp].z, o.k[pp].w);
+            const float2 q01 = make_float2(o.q[pp].x, o.q[pp].y), q23 = make_float2(o.q[pp].z, o.q[pp].w);
+#pragma unroll
+            for (int m = 0; m < kHeadsPerKey; ++m) {
+                ak[m] = ffma2(S[m][pp][0], k01, ak[m]);
+                aq[m] = ffma2(S[m][pp][0], q01, aq[m]);
+                ak[m] = ffma2(S[m][pp][1], k23, ak[m]);
+                aq[m] = ffma2(S[m][pp][1], q23, aq[m]);
+            }
+        }
+        float sk[kHeadsPerKey], sq[kHeadsPerKey];
+#pragma unroll
+        for (int m = 0; m < kHeadsPerKey; ++m) {
+            sk[m] = ak[m].x + ak[m].y;
+            sq[m] = aq[m].x + aq[m].y;
+        }
+#pragma unroll
+        for (int off = 1; off < Sh::G; off <<= 1) {
+#pragma unroll
+            for (int m = 0; m < kHeadsPerKey; ++m) {
+                sk[m] += __shfl_xor_sync(0xffffffffu, sk[m], off);
+                sq[m] += __shfl_xor_sync(0xffffffffu, sq[m], off);
+            }
+        }
+        float o_mine = 0.f;
+#pragma unroll
+        for (int m = 0; m < kHeadsPerKey; ++m) {
+            const float a = o.a[m];
+            const float delta = o.b[m] * (o.v[m] - a * sk[m]);
+            const float out = fmaf(o.kq, delta, a * sq[m]);
+            if (rg == m) o_mine = out;
+            const float2 a2 = make_float2(a, a), d2 = make_float2(delta, delta);
+#pragma unroll
+            for (int pp = 0; pp < Sh::P4; ++pp) {
+                S[m][pp][0] = ffma2(make_float2(o.k[pp].x, o.k[pp].y), d2, fmul2(a2, S[m][pp][0]));
+                S[m][pp][1] = ffma2(make_float2(o.k[pp].z, o.k[pp].w), d2, fmul2(a2, S[m][pp][1]));
+            }
+        }
+        if (rg < kHeadsPerKey) out_col[t * static_cast<int64_t>(n_vh) * D] = o_mine;
+    };
+
     for (int64_t s = 0; s < nst; ++s) {
         const int buf = static_cast<int>(s % NS);
         const uint32_t par = static_cast<uint32_t>((s / NS) & 1);
@@ -180,64 +245,18 @@ __global__ void __launch_bounds__(SeqShape<R>::THREADS, 1) gdn_seq_kernel(const 
         const Stage& st = sm.st[buf];
         const int64_t rem = T - s * B;
         const int nt = rem < B ? static_cast<int>(rem) : B;
+        const int64_t t0 = s * B;
+        Ops x0, x1;
+        load(x0, st, 0);
+        int tt = 0;
 #pragma unroll 1
-        for (int tt = 0; tt < nt; ++tt) {
-            const float4* k4 = reinterpret_cast<const float4*>(st.k[tt]);
-            const float4* q4 = reinterpret_cast<const float4*>(st.q[tt]);
-            float4 kr[Sh::P4], qr[Sh::P4];
-#pragma unroll
-            for (int pp = 0; pp < Sh::P4; ++pp) {
-                kr[pp] = k4[rg + Sh::G * pp];
-                qr[pp] = q4[rg + Sh::G * pp];
-            }
-            float2 ak[kHeadsPerKey], aq[kHeadsPerKey];
-#pragma unroll
-            for (int m = 0; m < kHeadsPerKey; ++m) ak[m] = aq[m] = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int pp = 0; pp < Sh::P4; ++pp) {
-                const float2 k01 = make_float2(kr[pp].x, kr[pp].y), k23 = make_float2(kr[pp].z, kr[pp].w);
-                const float2 q01 = make_float2(qr[pp].x, qr[pp].y), q23 = make_float2(qr[pp].z, qr[pp].w);
-#pragma unroll
-                for (int m = 0; m < kHeadsPerKey; ++m) {
-                    ak[m] = ffma2(S[m][pp][0], k01, ak[m]);
-                    aq[m] = ffma2(S[m][pp][0], q01, aq[m]);
-                    ak[m] = ffma2(S[m][pp][1], k23, ak[m]);
-                    aq[m] = ffma2(S[m][pp][1], q23, aq[m]);
-                }
-            }
-            float sk[kHeadsPerKey], sq[kHeadsPerKey];
-#pragma unroll
-            for (int m = 0; m < kHeadsPerKey; ++m) {
-                sk[m] = ak[m].x + ak[m].y;
-                sq[m] = aq[m].x + aq[m].y;
-            }
-#pragma unroll
-            for (int off = 1; off < Sh::G; off <<= 1) {
-#pragma unroll
-                for (int m = 0; m < kHeadsPerKey; ++m) {
-                    sk[m] += __shfl_xor_sync(0xffffffffu, sk[m], off);
-                    sq[m] += __shfl_xor_sync(0xffffffffu, sq[m], off);
-                }
-            }
-            const float kq = st.kq[tt];
-            float o_mine = 0.f;
-#pragma unroll
-            for (int m = 0; m < kHeadsPerKey; ++m) {
-                const float a = st.a[tt][m];
-                const float bt = st.b[tt][m];
-                const float v = st.v[m][tt][cl];
-                const float delta = bt * (v - a * sk[m]);
-                const float o = fmaf(kq, delta, a * sq[m]);
-                if (rg == m) o_mine = o;
-                const float2 a2 = make_float2(a, a), d2 = make_float2(delta, delta);
-#pragma unroll
-                for (int pp = 0; pp < Sh::P4; ++pp) {
-                    S[m][pp][0] = ffma2(make_float2(kr[pp].x, kr[pp].y), d2, fmul2(a2, S[m][pp][0]));
-                    S[m][pp][1] = ffma2(make_float2(kr[pp].z, kr[pp].w), d2, fmul2(a2, S[m][pp][1]));
-                }
-            }
-            if (rg < kHeadsPerKey) out_col[(s * B + tt) * static_cast<int64_t>(n_vh) * D] = o_mine;
+        for (; tt + 1 < nt; tt += 2) {
+            load(x1, st, tt + 1);
+            token(x0, t0 + tt);
+            if (tt + 2 < nt) load(x0, st, tt + 2);
+            token(x1, t0 + tt + 1);
         }
+        if (tt < nt) token(x0, t0 + tt);
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.empty[buf]);
     }
