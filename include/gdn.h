@@ -101,6 +101,37 @@ int gdn_recurrence(const float* q, const float* k, const float* v,
 int gdn_out_norm(const float* out, const float* z, const float* w, float eps,
                  uint16_t* y_fp16, int64_t T, int n_vh, int d, void* cuda_stream);
 
+/*
+ * gdn_recurrence_chunked_noalloc - gdn_recurrence(..., GDN_CHUNKED, ...) without
+ * any device allocation.  The pages have no counterpart to this entry point.
+ *
+ * For callers that cannot let a library call cudaMalloc: for example a serving
+ * process that reserved all of the GPU's memory for its own arena at start-up,
+ * where an allocation from inside a library fails or fragments that arena, or a
+ * latency-critical path that must not take cudaMalloc's implicit device
+ * synchronisation.  The caller passes inputs and outputs exactly as for
+ * gdn_recurrence (same layouts, same alignment rules, device pointers it owns).
+ *
+ * Scratch: a fixed 12,976,128-byte array in the library's static device memory
+ * (one 512-token super-block of prep records for up to 96 value heads), which
+ * every GPU that loads the library holds until the process exits.  Calls with
+ * n_vh > 96 are rejected with GDN_ERR_UNSUPPORTED and a message saying so.
+ * The first call on each device looks up that array's device address (with the
+ * device current); make that first call before any stream capture.  Every call
+ * in the process shares the one array per device and leaves its last contents
+ * there; each call writes every scratch word it reads before reading it, so no
+ * clearing is needed, but two calls whose kernels overlap on a GPU (different
+ * streams, or different host threads) race on the array and corrupt each
+ * other's results: serialise them.  This call has no status word:
+ * gdn_device_status() does not report a bounded wait that gives up here.
+ * Results equal gdn_recurrence's chunked mode for the same inputs.
+ */
+int gdn_recurrence_chunked_noalloc(const float* q, const float* k, const float* v,
+                                   const float* g, const float* beta,
+                                   float* state_inout, float* out,
+                                   int64_t T, int n_kh, int n_vh, int d,
+                                   void* cuda_stream);
+
 /* Message for the calling thread's last non-OK status ("" if none). */
 const char* gdn_last_error(void);
 

@@ -145,6 +145,11 @@ int seq_rows_per_thread() {
 
 }  // namespace
 
+namespace gdn {
+int internal_fail(int code, const std::string& msg) { return fail(code, msg); }
+void internal_count_launch() { g_launches.fetch_add(1); }
+}  // namespace gdn
+
 extern "C" {
 
 int gdn_recurrence(const float* q, const float* k, const float* v, const float* g, const float* beta,

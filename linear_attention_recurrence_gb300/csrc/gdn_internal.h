@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <string>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -67,5 +68,11 @@ struct ChunkPrepParams {
 cudaError_t launch_chunk_prep(const ChunkPrepParams& p, cudaStream_t s);
 cudaError_t launch_chunk_scan(const ChunkScanParams& p, cudaStream_t s);
 int chunk_scan_box_cols();
+
+// ---- shared by the C-ABI entry points (implemented in gdn_api.cu) ----
+// Records `msg` as the calling thread's gdn_last_error() and returns `code`.
+int internal_fail(int code, const std::string& msg);
+// Adds one kernel launch to gdn_launch_count().
+void internal_count_launch();
 
 }  // namespace gdn

@@ -35,7 +35,8 @@ _lock = threading.Lock()
 _lib = None
 
 EXPORTS = ("gdn_recurrence", "gdn_out_norm", "gdn_last_error", "gdn_device_status",
-           "gdn_release_scratch", "gdn_poison_scratch", "gdn_chunked_scratch_bytes", "gdn_launch_count")
+           "gdn_release_scratch", "gdn_poison_scratch", "gdn_chunked_scratch_bytes", "gdn_launch_count",
+           "gdn_recurrence_chunked_noalloc")
 
 
 class GDNError(RuntimeError):
@@ -57,6 +58,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
         lib.gdn_recurrence.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, vp]
         lib.gdn_recurrence.restype = i32
+        lib.gdn_recurrence_chunked_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, vp]
+        lib.gdn_recurrence_chunked_noalloc.restype = i32
         lib.gdn_out_norm.argtypes = [vp, vp, vp, ctypes.c_float, vp, i64, i32, i32, vp]
         lib.gdn_out_norm.restype = i32
         lib.gdn_last_error.argtypes = []
@@ -126,6 +129,32 @@ def gdn_recurrence(q, k, v, g, beta, state, out=None, mode="sequential", stream=
     lib = load_library()
     rc = lib.gdn_recurrence(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state), _ptr(out),
                             T, n_kh, n_vh, d, _MODES[mode], _stream_ptr(stream))
+    _check(rc)
+    return out
+
+
+def gdn_recurrence_chunked_noalloc(q, k, v, g, beta, state, out, stream=None):
+    """The chunked recurrence through the entry point that allocates nothing.
+
+    For callers that cannot allocate device memory from inside a library (their
+    own arena owns the GPU's memory, or the path must not synchronise): ``out``
+    must be passed in, and the library's scratch is a fixed static device array
+    (at most 96 value heads).  Calls that overlap on the GPU share that array and
+    race; serialise them.  Same shapes and results as ``gdn_recurrence(...,
+    mode="chunked")``.
+    """
+    T, n_kh, d = q.shape
+    n_vh = v.shape[1]
+    _want(q, "q", (T, n_kh, d))
+    _want(k, "k", (T, n_kh, d))
+    _want(v, "v", (T, n_vh, d))
+    _want(g, "g", (T, n_vh))
+    _want(beta, "beta", (T, n_vh))
+    _want(state, "state", (n_vh, d, d))
+    _want(out, "out", (T, n_vh, d))
+    lib = load_library()
+    rc = lib.gdn_recurrence_chunked_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
+                                            _ptr(out), T, n_kh, n_vh, d, _stream_ptr(stream))
     _check(rc)
     return out
 
