@@ -240,7 +240,7 @@ int gdn_recurrence(const float* q, const float* k, const float* v, const float* 
         g_launches.fetch_add(1);
         sp.t_begin = t0;
         sp.n_tokens = n;
-        e = launch_chunk_scan(sp, s);
+        e = launch_chunk_scan_default(sp, s);
         if (e != cudaSuccess) return cuda_fail(e, "chunk scan launch");
         g_launches.fetch_add(1);
     }

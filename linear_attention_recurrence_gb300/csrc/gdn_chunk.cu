@@ -33,10 +33,10 @@ namespace {
 constexpr int D = kD;
 constexpr int C = kChunk;
 constexpr int REC = kPrepRecordFloats;
-constexpr int REC_TP = 0;                 // T'^T [s][t]
-constexpr int REC_PT = C * C;             // P^T  [s][t]
-constexpr int REC_EG = 2 * C * C;         // e^gamma_t
-constexpr int REC_ER = 2 * C * C + C;     // e^(gamma_last - gamma_t)
+constexpr int REC_TP = kRecTP;
+constexpr int REC_PT = kRecPT;
+constexpr int REC_EG = kRecEG;
+constexpr int REC_ER = kRecER;
 
 // ============================ prep ============================
 constexpr int PREP_THREADS = 256;
@@ -240,7 +240,6 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) gdn_chunk_scan_kernel(const _
     bool ok = true;
 
     for (int c = 0; c < nch; ++c) {
-        if (tid == 0 && c + 1 < nch) issue(c + 1);
         if (!mbar_wait(&sm.full[c & 1], static_cast<uint32_t>((c >> 1) & 1))) { ok = false; break; }
         const ScanBuf& b = sm.buf[c & 1];
         const int nt = min(C, p.n_tokens - c * C);
@@ -290,7 +289,8 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) gdn_chunk_scan_kernel(const _
         }
         __syncthreads();
 
-        // ---- P2: D = T' U' per head (32x32 by 32x16) ----
+        // ---- P2: D = T' U' per head (32x32 by 32x16); warp 7, idle here, loads the next chunk ----
+        if (tid == SCAN_THREADS - 32 && c + 1 < nch) issue(c + 1);  // its buffer was last read in chunk c-1
         if (tid < kHeadsPerKey * 64) {
             const float* tp = &b.rec[pm][REC_TP];
             float acc[4][2];

@@ -16,6 +16,10 @@ constexpr int kChunksPerSuperBlock = kSuperBlock / kChunk;
 // Per (chunk, value head) prep record: T'^T [32][32], P^T [32][32], e^gamma [32],
 // e^(gamma_last - gamma) [32], in floats.
 constexpr int kPrepRecordFloats = 2 * kChunk * kChunk + 2 * kChunk;
+constexpr int kRecTP = 0;                            // T'^T [s][t]
+constexpr int kRecPT = kChunk * kChunk;              // P^T  [s][t]
+constexpr int kRecEG = 2 * kChunk * kChunk;          // e^gamma_t
+constexpr int kRecER = 2 * kChunk * kChunk + kChunk;  // e^(gamma_last - gamma_t)
 
 // ---- sequential scan ----
 struct SeqParams {
@@ -67,6 +71,14 @@ struct ChunkPrepParams {
 };
 cudaError_t launch_chunk_prep(const ChunkPrepParams& p, cudaStream_t s);
 cudaError_t launch_chunk_scan(const ChunkScanParams& p, cudaStream_t s);
+// The same scan with the chunk's large products (K S0, Q S0, K^T D) on the tensor
+// cores as split-TF32 (3 passes); same parameters and results within tolerance.
+cudaError_t launch_chunk_scan_tc(const ChunkScanParams& p, cudaStream_t s);
+// The scan the entry points use: the CUDA-core scan, or the tensor-core scan when
+// the environment variable GDN_CHUNK_SCAN is "tc" (for A/B measurements: at 48
+// columns per CTA each tcgen05.mma costs a near-fixed ~80 cycles, so the two run
+// at the same speed).
+cudaError_t launch_chunk_scan_default(const ChunkScanParams& p, cudaStream_t s);
 int chunk_scan_box_cols();
 
 // ---- shared by the C-ABI entry points (implemented in gdn_api.cu) ----

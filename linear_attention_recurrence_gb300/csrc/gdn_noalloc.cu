@@ -160,7 +160,7 @@ extern "C" int gdn_recurrence_chunked_noalloc(const float* q, const float* k, co
         internal_count_launch();
         sp.t_begin = t0;
         sp.n_tokens = n;
-        e = launch_chunk_scan(sp, s);
+        e = launch_chunk_scan_default(sp, s);
         if (e != cudaSuccess)
             return internal_fail(GDN_ERR_CUDA, std::string("chunk scan launch: ") + cudaGetErrorString(e));
         internal_count_launch();

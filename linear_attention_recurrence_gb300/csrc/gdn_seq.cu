@@ -32,7 +32,8 @@ namespace {
 
 constexpr int D = kD;
 constexpr int NCOL = 16;  // value columns per CTA (per head)
-constexpr int B = 16;     // tokens per stage
+constexpr int B = 16;     // tokens per stage (the producer's k.q reduce-scatter assumes 16)
+static_assert(B == 16, "k.q reduce-scatter layout");
 constexpr int NS = 4;     // stages in the ring
 
 template <int R>
@@ -117,15 +118,30 @@ __global__ void __launch_bounds__(SeqShape<R>::THREADS, 1) gdn_seq_kernel(const 
             }
             if (!mbar_wait(&sm.full[buf], static_cast<uint32_t>((s / NS) & 1))) { ok = false; break; }
             landed = s + 1;
-#pragma unroll 1
+            // k.q of the block's 16 tokens: lane partials over dims 4*lane..4*lane+3, then
+            // a reduce-scatter over the warp (keep half the tokens at each xor level),
+            // so lanes 2u and 2u+1 end with token 8*b4 + 4*b3 + 2*b2 + b1 of lane 2u.
+            float kqv[B];
+#pragma unroll
             for (int tt = 0; tt < B; ++tt) {
-                float acc = 0.f;
-#pragma unroll
-                for (int r = 0; r < D / 32; ++r) acc = fmaf(st.k[tt][lane + 32 * r], st.q[tt][lane + 32 * r], acc);
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-                if (lane == 0) st.kq[tt] = acc;
+                const float4 k4 = reinterpret_cast<const float4*>(st.k[tt])[lane];
+                const float4 q4 = reinterpret_cast<const float4*>(st.q[tt])[lane];
+                kqv[tt] = fmaf(k4.w, q4.w, fmaf(k4.z, q4.z, fmaf(k4.y, q4.y, k4.x * q4.x)));
             }
+#pragma unroll
+            for (int lvl = 0; lvl < 4; ++lvl) {
+                const int off = 16 >> lvl, half = B >> (lvl + 1);
+                const bool upper = (lane & off) != 0;
+#pragma unroll
+                for (int i = 0; i < half; ++i) {
+                    const float send = upper ? kqv[i] : kqv[i + half];
+                    const float keep = upper ? kqv[i + half] : kqv[i];
+                    kqv[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                }
+            }
+            kqv[0] += __shfl_xor_sync(0xffffffffu, kqv[0], 1);
+            if ((lane & 1) == 0)
+                st.kq[((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1)] = kqv[0];
             __threadfence_block();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.ready[buf]);
@@ -186,51 +202,69 @@ __global__ void __launch_bounds__(SeqShape<R>::THREADS, 1) gdn_seq_kernel(const 
         }
         o.kq = st.kq[tt];
     };
-    // One token: both column sums from one pass over the state, the shuffle
-    // reduction, delta and the output, then the state update.
+    // One token: both column sums from one pass over the state (12 independent
+    // packed accumulator chains), the k-sum reduction first (it gates delta), the
+    // decay product a*S formed while the shuffles are in flight, then the update;
+    // the q-sum reduction and the output come last, off the state's critical path.
     auto token = [&](const Ops& o, int64_t t) {
-        float2 ak[kHeadsPerKey], aq[kHeadsPerKey];
+        float2 ak[kHeadsPerKey][2], aq[kHeadsPerKey][2];
 #pragma unroll
-        for (int m = 0; m < kHeadsPerKey; ++m) ak[m] = aq[m] = make_float2(0.f, 0.f);
+        for (int m = 0; m < kHeadsPerKey; ++m)
+            ak[m][0] = ak[m][1] = aq[m][0] = aq[m][1] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int pp = 0; pp < Sh::P4; ++pp) {
             const float2 k01 = make_float2(o.k[pp].x, o.k[pp].y), k23 = make_float2(o.k[pp].z, o.k[pp].w);
             const float2 q01 = make_float2(o.q[pp].x, o.q[pp].y), q23 = make_float2(o.q[pp].z, o.q[pp].w);
 #pragma unroll
             for (int m = 0; m < kHeadsPerKey; ++m) {
-                ak[m] = ffma2(S[m][pp][0], k01, ak[m]);
-                aq[m] = ffma2(S[m][pp][0], q01, aq[m]);
-                ak[m] = ffma2(S[m][pp][1], k23, ak[m]);
-                aq[m] = ffma2(S[m][pp][1], q23, aq[m]);
+                ak[m][0] = ffma2(S[m][pp][0], k01, ak[m][0]);
+                ak[m][1] = ffma2(S[m][pp][1], k23, ak[m][1]);
+                aq[m][0] = ffma2(S[m][pp][0], q01, aq[m][0]);
+                aq[m][1] = ffma2(S[m][pp][1], q23, aq[m][1]);
             }
         }
         float sk[kHeadsPerKey], sq[kHeadsPerKey];
 #pragma unroll
         for (int m = 0; m < kHeadsPerKey; ++m) {
-            sk[m] = ak[m].x + ak[m].y;
-            sq[m] = aq[m].x + aq[m].y;
+            sk[m] = (ak[m][0].x + ak[m][0].y) + (ak[m][1].x + ak[m][1].y);
+            sq[m] = (aq[m][0].x + aq[m][0].y) + (aq[m][1].x + aq[m][1].y);
         }
 #pragma unroll
         for (int off = 1; off < Sh::G; off <<= 1) {
 #pragma unroll
-            for (int m = 0; m < kHeadsPerKey; ++m) {
-                sk[m] += __shfl_xor_sync(0xffffffffu, sk[m], off);
-                sq[m] += __shfl_xor_sync(0xffffffffu, sq[m], off);
+            for (int m = 0; m < kHeadsPerKey; ++m) sk[m] += __shfl_xor_sync(0xffffffffu, sk[m], off);
+        }
+        float delta[kHeadsPerKey];
+#pragma unroll
+        for (int m = 0; m < kHeadsPerKey; ++m) {
+            const float a = o.a[m];
+            const float2 a2 = make_float2(a, a);
+#pragma unroll
+            for (int pp = 0; pp < Sh::P4; ++pp) {
+                S[m][pp][0] = fmul2(a2, S[m][pp][0]);
+                S[m][pp][1] = fmul2(a2, S[m][pp][1]);
             }
+            delta[m] = o.b[m] * (o.v[m] - a * sk[m]);
+        }
+#pragma unroll
+        for (int m = 0; m < kHeadsPerKey; ++m) {
+            const float2 d2 = make_float2(delta[m], delta[m]);
+#pragma unroll
+            for (int pp = 0; pp < Sh::P4; ++pp) {
+                S[m][pp][0] = ffma2(make_float2(o.k[pp].x, o.k[pp].y), d2, S[m][pp][0]);
+                S[m][pp][1] = ffma2(make_float2(o.k[pp].z, o.k[pp].w), d2, S[m][pp][1]);
+            }
+        }
+#pragma unroll
+        for (int off = 1; off < Sh::G; off <<= 1) {
+#pragma unroll
+            for (int m = 0; m < kHeadsPerKey; ++m) sq[m] += __shfl_xor_sync(0xffffffffu, sq[m], off);
         }
         float o_mine = 0.f;
 #pragma unroll
         for (int m = 0; m < kHeadsPerKey; ++m) {
-            const float a = o.a[m];
-            const float delta = o.b[m] * (o.v[m] - a * sk[m]);
-            const float out = fmaf(o.kq, delta, a * sq[m]);
+            const float out = fmaf(o.kq, delta[m], o.a[m] * sq[m]);
             if (rg == m) o_mine = out;
-            const float2 a2 = make_float2(a, a), d2 = make_float2(delta, delta);
-#pragma unroll
-            for (int pp = 0; pp < Sh::P4; ++pp) {
-                S[m][pp][0] = ffma2(make_float2(o.k[pp].x, o.k[pp].y), d2, fmul2(a2, S[m][pp][0]));
-                S[m][pp][1] = ffma2(make_float2(o.k[pp].z, o.k[pp].w), d2, fmul2(a2, S[m][pp][1]));
-            }
         }
         if (rg < kHeadsPerKey) out_col[t * static_cast<int64_t>(n_vh) * D] = o_mine;
     };
