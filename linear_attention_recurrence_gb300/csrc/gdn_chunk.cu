@@ -176,7 +176,8 @@ struct ScanSmem {
     float SsT[NCC][SST];     // S0 transposed: [head*16 + col][key dim]
     float W[2 * C][NCC];     // rows 0..31: U'; rows 32..63: e^gamma (Q S0)
     float Dm[C][NCC];        // D
-    float2 Dd[C][NCC];       // e^(gamma_last - gamma) D, duplicated for packed FMAs
+    float Dp[C][NCC];        // e^(gamma_last - gamma) D
+    float Wp[2 * C][NCC];    // second half (key dims 64..127) of [K; Q] S0
     uint64_t full[2];
 };
 
@@ -231,10 +232,10 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) gdn_chunk_scan_kernel(const _
     };
     if (tid == 0) issue(0);
 
-    // G1 tile: X rows 4*(tt&7)..+3 of K (tt < 8) or Q (tt >= 8), column jj of each head
-    const int tt = tid >> 4;
-    const int xr0 = 4 * (tt & 7);
-    const int xsw = 4 * (tt & 1);  // (xr0 + r) & 7 == xsw + r
+    // G1 tile: key-dim half kgrp (threads 0-127: dims 0..63, 128-255: dims 64..127),
+    // X rows 8*(tg&3)..+7 of K (tg < 4) or Q (tg >= 4), column jw of each head.  Each
+    // quarter-warp shares its rows, so the X loads are broadcasts.
+    const int kgrp = tid >> 7, tg = (tid >> 4) & 7, jw = tid & 15;
     // P2 / P3 tile: head pm, rows 4*pti..+3, columns 2*pjp, 2*pjp+1
     const int pm = tid >> 6, pti = (tid >> 3) & 7, pjp = tid & 7;
     bool ok = true;
@@ -244,46 +245,57 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) gdn_chunk_scan_kernel(const _
         const ScanBuf& b = sm.buf[c & 1];
         const int nt = min(C, p.n_tokens - c * C);
 
-        // ---- G1: W = [K; Q] S0 (64 x 48), packed over even/odd key dims ----
+        // ---- G1: W = [K; Q] S0 (64 x 48), packed over even/odd key dims, the key dims
+        //      split over the two thread halves and their partial sums added once ----
         {
-            const unsigned char* xb = reinterpret_cast<const unsigned char*>(tt < 8 ? &b.K[0][0][0] : &b.Q[0][0][0]);
-            float2 acc[4][kHeadsPerKey];
+            const unsigned char* xb = reinterpret_cast<const unsigned char*>(tg < 4 ? &b.K[0][0][0] : &b.Q[0][0][0]) +
+                                      (8 * (tg & 3)) * 128;
+            float2 acc[8][kHeadsPerKey];
 #pragma unroll
-            for (int r = 0; r < 4; ++r)
+            for (int r = 0; r < 8; ++r)
 #pragma unroll
                 for (int m = 0; m < kHeadsPerKey; ++m) acc[r][m] = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int bx = 0; bx < D / 32; ++bx) {
+            for (int bh = 0; bh < 2; ++bh) {
+                const int bx = 2 * kgrp + bh;
 #pragma unroll
                 for (int cc = 0; cc < 8; ++cc) {
-                    float4 a[4], s[kHeadsPerKey];
-#pragma unroll
-                    for (int r = 0; r < 4; ++r)
-                        a[r] = *reinterpret_cast<const float4*>(xb + bx * (C * 128) + (xr0 + r) * 128 +
-                                                                (((cc ^ r) ^ xsw) << 4));
+                    float4 s4[kHeadsPerKey];
 #pragma unroll
                     for (int m = 0; m < kHeadsPerKey; ++m)
-                        s[m] = *reinterpret_cast<const float4*>(&sm.SsT[m * NC + jj][32 * bx + 4 * cc]);
+                        s4[m] = *reinterpret_cast<const float4*>(&sm.SsT[m * NC + jw][32 * bx + 4 * cc]);
 #pragma unroll
-                    for (int r = 0; r < 4; ++r)
+                    for (int r = 0; r < 8; ++r) {  // row 8*(tg&3) + r has (row & 7) == r
+                        const float4 a = *reinterpret_cast<const float4*>(xb + bx * (C * 128) + r * 128 + ((cc ^ r) << 4));
 #pragma unroll
                         for (int m = 0; m < kHeadsPerKey; ++m) {
-                            acc[r][m] = ffma2(make_float2(a[r].x, a[r].y), make_float2(s[m].x, s[m].y), acc[r][m]);
-                            acc[r][m] = ffma2(make_float2(a[r].z, a[r].w), make_float2(s[m].z, s[m].w), acc[r][m]);
+                            acc[r][m] = ffma2(make_float2(a.x, a.y), make_float2(s4[m].x, s4[m].y), acc[r][m]);
+                            acc[r][m] = ffma2(make_float2(a.z, a.w), make_float2(s4[m].z, s4[m].w), acc[r][m]);
                         }
+                    }
                 }
             }
+            const int row0 = (tg < 4 ? 0 : C) + 8 * (tg & 3);
+            if (kgrp == 1) {
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int t = xr0 + r;
+                for (int r = 0; r < 8; ++r)
 #pragma unroll
-                for (int m = 0; m < kHeadsPerKey; ++m) {
-                    const float x = acc[r][m].x + acc[r][m].y;
-                    const float eg = b.rec[m][REC_EG + t];
-                    if (tt < 8)
-                        sm.W[t][m * NC + jj] = b.V[m][t][jj] - eg * x;
-                    else
-                        sm.W[C + t][m * NC + jj] = eg * x;
+                    for (int m = 0; m < kHeadsPerKey; ++m) sm.Wp[row0 + r][m * NC + jw] = acc[r][m].x + acc[r][m].y;
+            }
+            __syncthreads();
+            if (kgrp == 0) {
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const int t = 8 * (tg & 3) + r;
+#pragma unroll
+                    for (int m = 0; m < kHeadsPerKey; ++m) {
+                        const float x = (acc[r][m].x + acc[r][m].y) + sm.Wp[row0 + r][m * NC + jw];
+                        const float eg = b.rec[m][REC_EG + t];
+                        if (tg < 4)
+                            sm.W[t][m * NC + jw] = b.V[m][t][jw] - eg * x;
+                        else
+                            sm.W[C + t][m * NC + jw] = eg * x;
+                    }
                 }
             }
         }
@@ -317,8 +329,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) gdn_chunk_scan_kernel(const _
                 for (int q = 0; q < 2; ++q) {
                     const int col = pm * NC + 2 * pjp + q;
                     sm.Dm[t][col] = acc[r][q];
-                    const float dd = er * acc[r][q];
-                    sm.Dd[t][col] = make_float2(dd, dd);
+                    sm.Dp[t][col] = er * acc[r][q];
                 }
             }
         }
@@ -376,7 +387,8 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) gdn_chunk_scan_kernel(const _
                 const float4 khi = *reinterpret_cast<const float4*>(kb + swz(t, cc0 + 1));
 #pragma unroll
                 for (int m = 0; m < kHeadsPerKey; ++m) {
-                    const float2 d2 = sm.Dd[t][m * NC + jj];
+                    const float dv = sm.Dp[t][m * NC + jj];
+                    const float2 d2 = make_float2(dv, dv);
                     acc[m][0] = ffma2(make_float2(klo.x, klo.y), d2, acc[m][0]);
                     acc[m][1] = ffma2(make_float2(klo.z, klo.w), d2, acc[m][1]);
                     acc[m][2] = ffma2(make_float2(khi.x, khi.y), d2, acc[m][2]);
