@@ -182,6 +182,54 @@ def run_reference(args):
     return 0
 
 
+def run_sweep(args):
+    """GPU time per call of each recurrence mode against T: back-to-back calls
+    captured in a CUDA graph and replayed (so host-side call overhead is not
+    counted), medians of 3 replays; one layer, 48 value heads."""
+    import torch
+
+    from linear_attention_recurrence_gb300 import build, gdn
+    from linear_attention_recurrence_gb300.inputs import make_inputs
+
+    build.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    Ts = [1, 8, 16, 32, 64, 96, 128, 192, 256, 512, 1024, 2048, 8192, 32768]
+    x = make_inputs(max(Ts), seed=0, norm=False)
+    t = {k: torch.from_numpy(v).to(dev) for k, v in x.items()}
+    out = torch.empty((max(Ts), N_VH, D), device=dev)
+    st = torch.empty_like(t["S0"])
+    res = {}
+    for T in Ts:
+        reps = 20 if T <= 8192 else 5
+        res[T] = {}
+        for mode in ("sequential", "chunked"):
+            def calls():
+                for _ in range(reps):
+                    gdn.gdn_recurrence(t["q"][:T], t["k"][:T], t["v"][:T], t["g"][:T], t["beta"][:T], st,
+                                       out=out[:T], mode=mode)
+            st.copy_(t["S0"])
+            calls()  # warm-up (allocates the chunked scratch once)
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                calls()
+            samples = []
+            for _ in range(3):
+                st.copy_(t["S0"])
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                graph.replay()
+                e1.record()
+                torch.cuda.synchronize()
+                samples.append(e0.elapsed_time(e1) * 1e3 / reps)
+            res[T][mode] = statistics.median(samples)
+    line = {"metric": "GDN recurrence GPU time per call (µs) by mode and T", "unit": "µs", "data": "synthetic",
+            "config": {"n_kh": N_KH, "n_vh": N_VH, "d": D, "state": "carried, non-zero", "timing": "CUDA graph replay"},
+            "sweep": {str(T): v for T, v in res.items()}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def _config(args):
     return {"workload": f"gdn-prefill 1 layer, T={args.tokens} as {args.tokens // args.call_tokens} calls of "
                         f"{args.call_tokens} with the state carried, then the FP16 norm",
@@ -204,7 +252,11 @@ def main():
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-other-mode", action="store_true")
     ap.add_argument("--ref-seconds", type=float, default=10.0)
+    ap.add_argument("--sweep", action="store_true",
+                    help="time one call of each mode for T = 1 .. 32768 (one JSON line) instead of the step")
     args = ap.parse_args()
+    if args.sweep:
+        return run_sweep(args)
     assert args.tokens % args.call_tokens == 0
     if args.impl == "reference":
         return run_reference(args)

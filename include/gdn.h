@@ -53,8 +53,13 @@ extern "C" {
 
 typedef enum gdn_mode {
     GDN_SEQUENTIAL = 0, /* one token at a time; bit-identical across reruns and T splits */
-    GDN_CHUNKED = 1     /* 32-token WY chunks in 2048-token super-blocks */
+    GDN_CHUNKED = 1,    /* 32-token WY chunks in 2048-token super-blocks */
+    GDN_AUTO = 2        /* GDN_SEQUENTIAL for T < GDN_AUTO_CHUNKED_MIN_T, else GDN_CHUNKED */
 } gdn_mode;
+
+/* Token count from which GDN_AUTO takes the chunked form: the measured crossover
+ * of the two modes' GPU time per call on GB300 (48 value heads, d = 128). */
+#define GDN_AUTO_CHUNKED_MIN_T 128
 
 typedef enum gdn_status {
     GDN_OK = 0,
@@ -78,7 +83,8 @@ typedef enum gdn_status {
  * GDN_SEQUENTIAL mode a sequence split over several calls gives the same bits
  * as one call.  GDN_CHUNKED evaluates the same recurrence in 32-token WY
  * chunks (other FP32 rounding; within 2e-6 of the FP64 result, relative to
- * the largest magnitude).
+ * the largest magnitude).  GDN_AUTO picks one of the two by T per call (so a
+ * sequence split into calls of different lengths may mix the two roundings).
  *
  * Supported shapes: d == 128 and n_vh == 3 * n_kh (n_kh >= 1).  T == 0 is a
  * no-op returning GDN_OK.  The first GDN_CHUNKED call on a device allocates the

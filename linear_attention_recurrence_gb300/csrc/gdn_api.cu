@@ -146,6 +146,25 @@ int seq_rows_per_thread() {
 }  // namespace
 
 namespace gdn {
+cudaError_t set_smem_once(const void* kernel, int bytes) {
+    struct Entry {
+        const void* kernel;
+        int device;
+        int bytes;
+    };
+    static Entry table[64];
+    static int used = 0;
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < used; ++i)
+        if (table[i].kernel == kernel && table[i].device == dev && table[i].bytes >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && used < 64) table[used++] = Entry{kernel, dev, bytes};
+    return e;
+}
 int internal_fail(int code, const std::string& msg) { return fail(code, msg); }
 void internal_count_launch() { g_launches.fetch_add(1); }
 }  // namespace gdn
@@ -159,7 +178,9 @@ int gdn_recurrence(const float* q, const float* k, const float* v, const float* 
     if (T < 0) return fail(GDN_ERR_INVALID_ARG, "T < 0");
     if (n_kh <= 0 || n_vh <= 0 || d <= 0) return fail(GDN_ERR_INVALID_ARG, "n_kh, n_vh and d must be positive");
     if (n_vh % n_kh != 0) return fail(GDN_ERR_INVALID_ARG, "n_vh must be a multiple of n_kh");
-    if (mode != GDN_SEQUENTIAL && mode != GDN_CHUNKED) return fail(GDN_ERR_INVALID_ARG, "unknown mode");
+    if (mode != GDN_SEQUENTIAL && mode != GDN_CHUNKED && mode != GDN_AUTO)
+        return fail(GDN_ERR_INVALID_ARG, "unknown mode");
+    if (mode == GDN_AUTO) mode = (T < GDN_AUTO_CHUNKED_MIN_T) ? GDN_SEQUENTIAL : GDN_CHUNKED;
     if (d != kD) return fail(GDN_ERR_UNSUPPORTED, "only d == 128 is supported");
     if (n_vh != kHeadsPerKey * n_kh) return fail(GDN_ERR_UNSUPPORTED, "only n_vh == 3 * n_kh is supported");
     if (T > INT32_MAX - 4096) return fail(GDN_ERR_UNSUPPORTED, "T too large for 32-bit TMA coordinates");

@@ -429,8 +429,7 @@ int chunk_scan_box_cols() { return NC; }
 
 cudaError_t launch_chunk_prep(const ChunkPrepParams& p, cudaStream_t s) {
     const size_t smem = sizeof(PrepSmem) + 16;
-    cudaError_t e = cudaFuncSetAttribute(gdn_chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(gdn_chunk_prep_kernel), static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     dim3 grid((p.n_tokens + C - 1) / C, p.n_kh);
     gdn_chunk_prep_kernel<<<grid, PREP_THREADS, smem, s>>>(p);
@@ -439,8 +438,7 @@ cudaError_t launch_chunk_prep(const ChunkPrepParams& p, cudaStream_t s) {
 
 cudaError_t launch_chunk_scan(const ChunkScanParams& p, cudaStream_t s) {
     const size_t smem = sizeof(ScanSmem) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(gdn_chunk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(gdn_chunk_scan_kernel), static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     dim3 grid(p.n_kh, D / NC);
     gdn_chunk_scan_kernel<<<grid, SCAN_THREADS, smem, s>>>(p);

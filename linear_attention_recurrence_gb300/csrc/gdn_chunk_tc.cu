@@ -374,8 +374,7 @@ __global__ void __launch_bounds__(THREADS, 1) gdn_chunk_scan_tc_kernel(const __g
 
 cudaError_t launch_chunk_scan_tc(const ChunkScanParams& p, cudaStream_t s) {
     const size_t smem = SMEM_BYTES + 1024;
-    cudaError_t e = cudaFuncSetAttribute(gdn_chunk_scan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(gdn_chunk_scan_tc_kernel), static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     dim3 grid(p.n_kh, D / NC);
     gdn_chunk_scan_tc_kernel<<<grid, THREADS, smem, s>>>(p);

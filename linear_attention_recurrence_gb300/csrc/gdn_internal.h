@@ -81,6 +81,10 @@ cudaError_t launch_chunk_scan_tc(const ChunkScanParams& p, cudaStream_t s);
 cudaError_t launch_chunk_scan_default(const ChunkScanParams& p, cudaStream_t s);
 int chunk_scan_box_cols();
 
+// Raises a kernel's dynamic shared-memory limit to `bytes` on the current device,
+// once per (kernel, device); later calls return at once (implemented in gdn_api.cu).
+cudaError_t set_smem_once(const void* kernel, int bytes);
+
 // ---- shared by the C-ABI entry points (implemented in gdn_api.cu) ----
 // Records `msg` as the calling thread's gdn_last_error() and returns `code`.
 int internal_fail(int code, const std::string& msg);

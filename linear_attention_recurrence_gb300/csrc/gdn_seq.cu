@@ -313,8 +313,7 @@ template <int R>
 cudaError_t launch_seq_t(const SeqParams& p, cudaStream_t s) {
     using Sh = SeqShape<R>;
     const size_t smem = sizeof(SeqSmem) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(gdn_seq_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(gdn_seq_kernel<R>), static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     dim3 grid(p.n_kh, D / NCOL);
     gdn_seq_kernel<R><<<grid, Sh::THREADS, smem, s>>>(p);

@@ -21,6 +21,8 @@ LIB_PATH = os.path.join(_PKG, "libgdn.so")
 
 GDN_SEQUENTIAL = 0
 GDN_CHUNKED = 1
+GDN_AUTO = 2
+GDN_AUTO_CHUNKED_MIN_T = 128
 GDN_OK = 0
 GDN_ERR_INVALID_ARG = -1
 GDN_ERR_UNSUPPORTED = -2
@@ -28,8 +30,8 @@ GDN_ERR_ALLOC = -3
 GDN_ERR_CUDA = -4
 GDN_ERR_TIMEOUT = -5
 
-_MODES = {"sequential": GDN_SEQUENTIAL, "seq": GDN_SEQUENTIAL, "chunked": GDN_CHUNKED,
-          GDN_SEQUENTIAL: GDN_SEQUENTIAL, GDN_CHUNKED: GDN_CHUNKED}
+_MODES = {"sequential": GDN_SEQUENTIAL, "seq": GDN_SEQUENTIAL, "chunked": GDN_CHUNKED, "auto": GDN_AUTO,
+          GDN_SEQUENTIAL: GDN_SEQUENTIAL, GDN_CHUNKED: GDN_CHUNKED, GDN_AUTO: GDN_AUTO}
 
 _lock = threading.Lock()
 _lib = None

@@ -47,6 +47,7 @@ def test_host_side_validation(lib):
     assert r(nil, nil, nil, nil, nil, nil, nil, -1, 16, 48, 128, 0, nil) == gdn.GDN_ERR_INVALID_ARG
     assert r(nil, nil, nil, nil, nil, nil, nil, 5, 16, 47, 128, 0, nil) == gdn.GDN_ERR_INVALID_ARG
     assert r(nil, nil, nil, nil, nil, nil, nil, 5, 16, 48, 128, 7, nil) == gdn.GDN_ERR_INVALID_ARG
+    assert r(nil, nil, nil, nil, nil, nil, nil, 0, 16, 48, 128, gdn.GDN_AUTO, nil) == gdn.GDN_OK
     assert r(nil, nil, nil, nil, nil, nil, nil, 5, 0, 48, 128, 0, nil) == gdn.GDN_ERR_INVALID_ARG
     assert r(nil, nil, nil, nil, nil, nil, nil, 5, 16, 48, 64, 0, nil) == gdn.GDN_ERR_UNSUPPORTED
     assert r(nil, nil, nil, nil, nil, nil, nil, 5, 16, 32, 128, 1, nil) == gdn.GDN_ERR_UNSUPPORTED
@@ -91,3 +92,14 @@ def test_scratch_size_and_counters(lib):
     assert lib.gdn_release_scratch(0) == 0
     assert lib.gdn_release_scratch(-1) != 0
     assert lib.gdn_launch_count() >= 0
+
+
+def test_binding_constants_match_the_header():
+    from linear_attention_recurrence_gb300 import gdn
+
+    src = open(HEADER).read()
+    assert int(re.search(r"#define GDN_AUTO_CHUNKED_MIN_T (\d+)", src).group(1)) == gdn.GDN_AUTO_CHUNKED_MIN_T
+    for name in ("GDN_SEQUENTIAL", "GDN_CHUNKED", "GDN_AUTO", "GDN_OK", "GDN_ERR_INVALID_ARG", "GDN_ERR_UNSUPPORTED",
+                 "GDN_ERR_ALLOC", "GDN_ERR_CUDA", "GDN_ERR_TIMEOUT"):
+        m = re.search(name + r"\s*=\s*(-?\d+)", src)
+        assert m and int(m.group(1)) == getattr(gdn, name), name

@@ -81,3 +81,15 @@ def test_norm_reruns_bit_identical():
     for _ in range(3):
         y = gdn.gdn_out_norm(o, t["z"], t["w"]).cpu().numpy().view(np.uint16)
         assert np.array_equal(y0, y)
+
+
+@pytest.mark.parametrize("T", [1, 127, 128, 1000])
+def test_auto_mode_is_the_chosen_mode_bit_for_bit(T):
+    """GDN_AUTO runs the sequential kernel below the threshold and the chunked
+    kernels from it on, with identical bits to calling that mode directly."""
+    t = to_dev(make_inputs(T, seed=13, norm=False))
+    chosen = "sequential" if T < gdn.GDN_AUTO_CHUNKED_MIN_T else "chunked"
+    oa, sa = _run(t, "auto", [T])
+    oc, sc = _run(t, chosen, [T])
+    assert np.array_equal(oa.view(np.uint32), oc.view(np.uint32))
+    assert np.array_equal(sa.view(np.uint32), sc.view(np.uint32))
