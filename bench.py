@@ -230,6 +230,55 @@ def run_sweep(args):
     return 0
 
 
+def run_decode(args):
+    """Batched decode: one token for each of B independent sequences (own states),
+    48 value heads.  HBM-bound: every step reads and rewrites all states once."""
+    import torch
+
+    from linear_attention_recurrence_gb300 import build, gdn
+    from linear_attention_recurrence_gb300.inputs import make_inputs
+
+    build.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    B = args.decode
+    x = make_inputs(B, seed=0, norm=False)  # token b of the draw is sequence b's input
+    t = {k: torch.from_numpy(v).to(dev) for k, v in x.items() if k != "S0"}
+    states = torch.from_numpy(x["S0"]).to(dev)[None].repeat(B, 1, 1, 1).contiguous()
+    out = torch.empty((B, N_VH, D), device=dev)
+    step = lambda: gdn.gdn_decode(t["q"], t["k"], t["v"], t["g"], t["beta"], states, out=out)  # noqa: E731
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    n0 = gdn.gdn_launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks(dev.index) as clk:
+        time.sleep(0.5)
+        wall0 = time.time()
+        e0.record()
+        for _ in range(args.steps):
+            step()
+        e1.record()
+        torch.cuda.synchronize()
+        clk.mark(wall0, time.time())
+        time.sleep(0.1)
+    ms = e0.elapsed_time(e1) / args.steps
+    assert gdn.gdn_device_status() == gdn.GDN_OK
+    hbm_gbs, _, peak_src = _peaks()
+    # algorithmic bytes per sequence: state read + write, q, k, v, g, beta, o
+    bytes_step = B * (2 * N_VH * D * D * 4 + 2 * N_KH * D * 4 + 2 * N_VH * D * 4 + 2 * N_VH * 4)
+    gbs = bytes_step / (ms * 1e-3) / 1e9
+    line = {"metric": "GDN decode step µs (48 vh, d=128) and % of HBM roofline", "value": ms * 1e3, "unit": "µs/step",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "higher_is_better": False, "dtype": "f32",
+            "data": "synthetic", "config": {"workload": f"decode, {B} sequences x 1 token", "batch": B, "n_kh": N_KH,
+                                            "n_vh": N_VH, "d": D, "l2": f"states {B * 3} MB, read and written per step"},
+            "gpu_launches": gdn.gdn_launch_count() - n0,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_gbs, "unit": "GB/s", "frac": gbs / hbm_gbs,
+                         "peak_basis": f"{peak_src} copy bandwidth", "traffic": None},
+            "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def _config(args):
     return {"workload": f"gdn-prefill 1 layer, T={args.tokens} as {args.tokens // args.call_tokens} calls of "
                         f"{args.call_tokens} with the state carried, then the FP16 norm",
@@ -254,9 +303,13 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=10.0)
     ap.add_argument("--sweep", action="store_true",
                     help="time one call of each mode for T = 1 .. 32768 (one JSON line) instead of the step")
+    ap.add_argument("--decode", type=int, default=0, metavar="B",
+                    help="time the batched decode step for B sequences (one JSON line) instead of the prefill step")
     args = ap.parse_args()
     if args.sweep:
         return run_sweep(args)
+    if args.decode:
+        return run_decode(args)
     assert args.tokens % args.call_tokens == 0
     if args.impl == "reference":
         return run_reference(args)

@@ -97,6 +97,22 @@ int gdn_recurrence(const float* q, const float* k, const float* v,
                    void* cuda_stream);
 
 /*
+ * gdn_decode - one token of the recurrence for each of `batch` independent
+ * sequences (the decode step; [P413] "What changes" applied to T = 1), each
+ * sequence with its own state:
+ *     q, k        [batch][n_kh][d]       v, out   [batch][n_vh][d]
+ *     g, beta     [batch][n_vh]          states   [batch][n_vh][d][d] (in/out)
+ * Per sequence b and value head h this is gdn_recurrence over one token;
+ * results agree with it to FP32 rounding (another summation order).
+ * Supported: d == 128, n_vh == 3 * n_kh, 1 <= batch <= 65535; batch == 0 is a
+ * no-op.  Device pointers owned by the caller; asynchronous on `cuda_stream`.
+ */
+int gdn_decode(const float* q, const float* k, const float* v,
+               const float* g, const float* beta,
+               float* states, float* out,
+               int batch, int n_kh, int n_vh, int d, void* cuda_stream);
+
+/*
  * gdn_out_norm - gated RMSNorm of the recurrence output to FP16 ([P413] "What
  * changes": gdn_out_norm_kernel writes the FP16 copy y_h).  Per (t, h) row:
  *     r = 1 / sqrt(mean_j out[t][h][j]^2 + eps)

@@ -268,6 +268,36 @@ int gdn_recurrence(const float* q, const float* k, const float* v, const float* 
     return GDN_OK;
 }
 
+int gdn_decode(const float* q, const float* k, const float* v, const float* g, const float* beta, float* states,
+               float* out, int batch, int n_kh, int n_vh, int d, void* cuda_stream) {
+    using namespace gdn;
+    if (batch < 0) return fail(GDN_ERR_INVALID_ARG, "batch < 0");
+    if (n_kh <= 0 || n_vh <= 0 || d <= 0) return fail(GDN_ERR_INVALID_ARG, "n_kh, n_vh and d must be positive");
+    if (n_vh % n_kh != 0) return fail(GDN_ERR_INVALID_ARG, "n_vh must be a multiple of n_kh");
+    if (d != kD) return fail(GDN_ERR_UNSUPPORTED, "only d == 128 is supported");
+    if (n_vh != kHeadsPerKey * n_kh) return fail(GDN_ERR_UNSUPPORTED, "only n_vh == 3 * n_kh is supported");
+    if (batch > 65535) return fail(GDN_ERR_UNSUPPORTED, "batch > 65535");
+    if (batch == 0) return GDN_OK;
+    if (!q || !k || !v || !g || !beta || !states || !out) return fail(GDN_ERR_INVALID_ARG, "null pointer");
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(states, 16))
+        return fail(GDN_ERR_INVALID_ARG, "q, k and states must be 16-byte aligned");
+    if (!aligned(v, 4) || !aligned(g, 4) || !aligned(beta, 4) || !aligned(out, 4))
+        return fail(GDN_ERR_INVALID_ARG, "v, g, beta and out must be 4-byte aligned");
+    const size_t s_bytes = static_cast<size_t>(batch) * n_vh * d * d * 4, o_bytes = static_cast<size_t>(batch) * n_vh * d * 4;
+    const void* ins[5] = {q, k, v, g, beta};
+    const size_t in_bytes[5] = {static_cast<size_t>(batch) * n_kh * d * 4, static_cast<size_t>(batch) * n_kh * d * 4,
+                                o_bytes, static_cast<size_t>(batch) * n_vh * 4, static_cast<size_t>(batch) * n_vh * 4};
+    for (int i = 0; i < 5; ++i)
+        if (overlap(out, o_bytes, ins[i], in_bytes[i]) || overlap(states, s_bytes, ins[i], in_bytes[i]))
+            return fail(GDN_ERR_INVALID_ARG, "out / states overlap an input");
+    if (overlap(out, o_bytes, states, s_bytes)) return fail(GDN_ERR_INVALID_ARG, "out overlaps states");
+    DecodeParams p{q, k, v, g, beta, states, out, batch, n_kh, n_vh};
+    cudaError_t e = launch_decode(p, static_cast<cudaStream_t>(cuda_stream));
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    g_launches.fetch_add(1);
+    return GDN_OK;
+}
+
 int gdn_out_norm(const float* out, const float* z, const float* w, float eps, uint16_t* y_fp16, int64_t T,
                  int n_vh, int d, void* cuda_stream) {
     using namespace gdn;

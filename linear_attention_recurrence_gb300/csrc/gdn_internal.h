@@ -40,6 +40,21 @@ int seq_box_cols();
 // rows_per_thread: 8 or 16.  Returns the CUDA error of the launch.
 cudaError_t launch_seq(const SeqParams& p, int rows_per_thread, cudaStream_t s);
 
+// ---- batched decode (one token per sequence) ----
+struct DecodeParams {
+    const float* q;      // [batch][n_kh][128]
+    const float* k;      // [batch][n_kh][128]
+    const float* v;      // [batch][n_vh][128]
+    const float* g;      // [batch][n_vh]
+    const float* beta;   // [batch][n_vh]
+    float* state;        // [batch][n_vh][128][128]
+    float* out;          // [batch][n_vh][128]
+    int batch;
+    int n_kh;
+    int n_vh;
+};
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s);
+
 // ---- output norm ----
 cudaError_t launch_out_norm(const float* out, const float* z, const float* w, float eps, uint16_t* y,
                             int64_t rows, int sm_count, cudaStream_t s);

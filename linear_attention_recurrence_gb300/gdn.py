@@ -38,7 +38,7 @@ _lib = None
 
 EXPORTS = ("gdn_recurrence", "gdn_out_norm", "gdn_last_error", "gdn_device_status",
            "gdn_release_scratch", "gdn_poison_scratch", "gdn_chunked_scratch_bytes", "gdn_launch_count",
-           "gdn_recurrence_chunked_noalloc")
+           "gdn_recurrence_chunked_noalloc", "gdn_decode")
 
 
 class GDNError(RuntimeError):
@@ -62,6 +62,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gdn_recurrence.restype = i32
         lib.gdn_recurrence_chunked_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, vp]
         lib.gdn_recurrence_chunked_noalloc.restype = i32
+        lib.gdn_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp]
+        lib.gdn_decode.restype = i32
         lib.gdn_out_norm.argtypes = [vp, vp, vp, ctypes.c_float, vp, i64, i32, i32, vp]
         lib.gdn_out_norm.restype = i32
         lib.gdn_last_error.argtypes = []
@@ -131,6 +133,31 @@ def gdn_recurrence(q, k, v, g, beta, state, out=None, mode="sequential", stream=
     lib = load_library()
     rc = lib.gdn_recurrence(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state), _ptr(out),
                             T, n_kh, n_vh, d, _MODES[mode], _stream_ptr(stream))
+    _check(rc)
+    return out
+
+
+def gdn_decode(q, k, v, g, beta, states, out=None, stream=None):
+    """One decode step for a batch of independent sequences; updates ``states``
+    in place and returns ``out``.
+
+    q, k: [B][n_kh][d]; v: [B][n_vh][d]; g, beta: [B][n_vh]; states:
+    [B][n_vh][d][d].  ``out`` ([B][n_vh][d]) is allocated if None.
+    """
+    B, n_kh, d = q.shape
+    n_vh = v.shape[1]
+    _want(q, "q", (B, n_kh, d))
+    _want(k, "k", (B, n_kh, d))
+    _want(v, "v", (B, n_vh, d))
+    _want(g, "g", (B, n_vh))
+    _want(beta, "beta", (B, n_vh))
+    _want(states, "states", (B, n_vh, d, d))
+    if out is None:
+        out = torch.empty((B, n_vh, d), dtype=torch.float32, device=q.device)
+    _want(out, "out", (B, n_vh, d))
+    lib = load_library()
+    rc = lib.gdn_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(states), _ptr(out),
+                        B, n_kh, n_vh, d, _stream_ptr(stream))
     _check(rc)
     return out
 
