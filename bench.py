@@ -70,6 +70,24 @@ def aggregate(local_ms: float, tokens_per_rank: int, world_size: int, device=Non
     return ms, ms * 1e3 / tokens, tokens / (ms * 1e-3)
 
 
+def captured_traffic(source_file: str):
+    """DRAM bytes per launch from profiles/dram_traffic.md for the unit whose kernel
+    source is `source_file`, or None when that file changed since the capture."""
+    import hashlib
+    import re
+
+    table = os.path.join(ROOT, "profiles", "dram_traffic.md")
+    src = os.path.join(ROOT, "linear_attention_recurrence_gb300", "csrc", source_file)
+    if not (os.path.exists(table) and os.path.exists(src)):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    for line in open(table):
+        m = re.match(r"\|[^|]*\|\s*csrc/(\S+)\s*\|\s*([0-9a-f]{16})\s*\|\s*(\d+)\s*\|", line)
+        if m and m.group(1) == source_file:
+            return int(m.group(3)) if m.group(2) == sha else None
+    return None
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -273,7 +291,8 @@ def run_decode(args):
                                             "n_vh": N_VH, "d": D, "l2": f"states {B * 3} MB, read and written per step"},
             "gpu_launches": gdn.gdn_launch_count() - n0,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_gbs, "unit": "GB/s", "frac": gbs / hbm_gbs,
-                         "peak_basis": f"{peak_src} copy bandwidth", "traffic": None},
+                         "peak_basis": f"{peak_src} copy bandwidth",
+                         "traffic": captured_traffic("gdn_decode.cu") if B == 64 else None},
             "clocks": clk.summary()}
     print(json.dumps(line), flush=True)
     return 0
@@ -469,7 +488,8 @@ def main():
         "tokens_per_s": T * ws / (main_res["ms_per_step"] * 1e-3),
         "gpu_launches": main_res["launches"],
         "roofline": {"bound": "alu", "achieved": achieved, "peak": alu_peak_tflops, "unit": "TFLOP/s",
-                     "frac": achieved / alu_peak_tflops, "traffic": None,
+                     "frac": achieved / alu_peak_tflops,
+                     "traffic": captured_traffic("gdn_chunk.cu" if args.mode == "chunked" else "gdn_seq.cu"),
                      "kernel": "gdn_chunk_prep+gdn_chunk_scan per 2048-token call" if args.mode == "chunked"
                      else "gdn_seq_kernel per 2048-token call",
                      "peak_basis": f"{sms} SMs x 128 FP32 lanes x 2 x {sm_mhz_max:.0f} MHz ({peak_src} max clock)",
