@@ -248,6 +248,56 @@ def run_sweep(args):
     return 0
 
 
+def run_stack(args):
+    """A stack of L independent layers, 2048 tokens each (every layer its own seeded
+    q/k/v/g/beta/S0/z/w), recurrence in the selected mode then the FP16 norm per
+    layer: the whole-stack prefill time of one 2048-token prompt chunk."""
+    import torch
+
+    from linear_attention_recurrence_gb300 import build, gdn
+    from linear_attention_recurrence_gb300.inputs import make_inputs
+
+    build.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    L, T = args.stack, 2048
+    layers = [{k: torch.from_numpy(v).to(dev) for k, v in make_inputs(T, seed=0, layer=i).items()} for i in range(L)]
+    states = [torch.empty_like(x["S0"]) for x in layers]
+    out = torch.empty((T, N_VH, D), device=dev)
+    y = torch.empty((T, N_VH, D), device=dev, dtype=torch.float16)
+
+    def step():
+        for x, st in zip(layers, states):
+            st.copy_(x["S0"])
+            gdn.gdn_recurrence(x["q"], x["k"], x["v"], x["g"], x["beta"], st, out=out, mode=args.mode)
+            gdn.gdn_out_norm(out, x["z"], x["w"], 1e-6, y=y)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    n0 = gdn.gdn_launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks(dev.index) as clk:
+        time.sleep(0.5)
+        wall0 = time.time()
+        e0.record()
+        for _ in range(args.steps):
+            step()
+        e1.record()
+        torch.cuda.synchronize()
+        clk.mark(wall0, time.time())
+        time.sleep(0.1)
+    ms = e0.elapsed_time(e1) / args.steps
+    assert gdn.gdn_device_status() == gdn.GDN_OK
+    line = {"metric": "GDN prefill stack time, recurrence + norm (ms per 2048-token chunk)", "value": ms, "unit": "ms",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "higher_is_better": False, "dtype": "f32",
+            "data": "synthetic", "us_per_token_layer": ms * 1e3 / (T * L),
+            "config": {"workload": f"{L} independent layers x {T} tokens, recurrence + FP16 norm", "layers": L,
+                       "T": T, "mode": args.mode, "n_kh": N_KH, "n_vh": N_VH, "d": D},
+            "gpu_launches": gdn.gdn_launch_count() - n0, "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_decode(args):
     """Batched decode: one token for each of B independent sequences (own states),
     48 value heads.  HBM-bound: every step reads and rewrites all states once."""
@@ -322,6 +372,8 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=10.0)
     ap.add_argument("--sweep", action="store_true",
                     help="time one call of each mode for T = 1 .. 32768 (one JSON line) instead of the step")
+    ap.add_argument("--stack", type=int, default=0, metavar="L",
+                    help="time L independent layers x 2048 tokens (recurrence + norm per layer, one JSON line)")
     ap.add_argument("--decode", type=int, default=0, metavar="B",
                     help="time the batched decode step for B sequences (one JSON line) instead of the prefill step")
     args = ap.parse_args()
@@ -329,6 +381,8 @@ def main():
         return run_sweep(args)
     if args.decode:
         return run_decode(args)
+    if args.stack:
+        return run_stack(args)
     assert args.tokens % args.call_tokens == 0
     if args.impl == "reference":
         return run_reference(args)

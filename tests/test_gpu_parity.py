@@ -201,3 +201,17 @@ def test_norm_edge_cases():
     y_ref = oracle.out_norm(o.astype(np.float64), x["z"], x["w"], 1e-6)
     assert int(fp16_ulp_distance(yb, y_ref).max()) <= 1
     assert np.all((yb[0] & 0x7FFF) == 0)
+
+
+@pytest.mark.parametrize("layer", [0, 35])
+def test_stack_layers_2048(layer):
+    """Layers of the 36-layer stack (own seeds, T = 2048, recurrence in both modes
+    plus the norm): each against the oracle."""
+    x = make_inputs(2048, seed=0, layer=layer)
+    o_ref, s_ref = oracle.recurrence(x["q"], x["k"], x["v"], x["g"], x["beta"], x["S0"])
+    t = to_dev(x)
+    for mode in MODES:
+        out, st = _run(t, mode)
+        assert rel_err(out.cpu().numpy(), o_ref) <= TOL
+        assert rel_err(st.cpu().numpy(), s_ref) <= TOL
+        _check_norm(out, o_ref, x, t)
