@@ -532,6 +532,9 @@ def main():
         modes[other] = mode_summary(other, other_res)
     flop = FLOP_SEQ if args.mode == "sequential" else FLOP_CHUNKED
     achieved = flop * CT / (kern["rec_call_ms"] * 1e-3) / 1e12
+    per_call = (kern["launches"] / args.steps - 1) / ncalls  # the norm is one launch per step
+    chunk_label = ("gdn_chunk_fused_kernel (prep and scan in one launch) per 2048-token call" if per_call < 1.5
+                   else "gdn_chunk_prep_kernel + gdn_chunk_scan_kernel per 2048-token call")
     norm_gbs = BYTES_NORM * T / (kern["norm_ms"] * 1e-3) / 1e9
     value = main_res["ms_per_step"] * 1e3 / (T * ws)  # already the max over ranks
     line = {
@@ -544,8 +547,7 @@ def main():
         "roofline": {"bound": "alu", "achieved": achieved, "peak": alu_peak_tflops, "unit": "TFLOP/s",
                      "frac": achieved / alu_peak_tflops,
                      "traffic": captured_traffic("gdn_chunk.cu" if args.mode == "chunked" else "gdn_seq.cu"),
-                     "kernel": "gdn_chunk_prep+gdn_chunk_scan per 2048-token call" if args.mode == "chunked"
-                     else "gdn_seq_kernel per 2048-token call",
+                     "kernel": chunk_label if args.mode == "chunked" else "gdn_seq_kernel per 2048-token call",
                      "peak_basis": f"{sms} SMs x 128 FP32 lanes x 2 x {sm_mhz_max:.0f} MHz ({peak_src} max clock)",
                      "frac_at_observed_clock": (achieved / (sms * FP32_LANES_PER_SM * 2 * clocks["sm_mhz"] * 1e6
                                                             / 1e12)) if clocks.get("sm_mhz") else None},

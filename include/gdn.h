@@ -27,8 +27,10 @@
  * Ownership: every pointer is a DEVICE pointer owned by the caller, on the
  * current CUDA device.  The library allocates only (a) a 4-byte status word per
  * device and (b) the chunked mode's per-device scratch (one 2048-token
- * super-block of prep results, about 25.9 MB), both on first use and kept until
- * gdn_release_scratch() or process exit.
+ * super-block of prep results, about 25.9 MB, plus 12 KB of hand-off flags),
+ * both on first use and kept until gdn_release_scratch() or process exit.
+ * Chunked calls on one device share that scratch: enqueue them on one stream
+ * (or otherwise order them); two in flight at once would corrupt each other.
  *
  * Asynchrony: every compute call only validates its arguments on the host and
  * enqueues kernels on `cuda_stream` (a cudaStream_t; NULL = the legacy default
@@ -38,8 +40,9 @@
  *
  * Errors: no call throws.  Each returns a gdn_status; on a non-OK status
  * gdn_last_error() returns a message for the calling thread.  A kernel that
- * gives up a bounded wait records GDN_ERR_TIMEOUT in the device status word,
- * which gdn_device_status() reads.
+ * gives up a bounded wait records it in the device status word, which
+ * gdn_device_status() reads (returning GDN_ERR_TIMEOUT, with the kind of wait in
+ * the message).
  */
 #ifndef GDN_H
 #define GDN_H

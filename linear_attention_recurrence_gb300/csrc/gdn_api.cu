@@ -11,6 +11,7 @@
 
 #include "gdn.h"
 #include "gdn_internal.h"
+#include "gdn_device.cuh"
 
 namespace {
 
@@ -25,6 +26,8 @@ struct DeviceState {
     int* status = nullptr;    // kernel status word (0 = fine)
     float* scratch = nullptr; // chunked-mode prep records for one super-block
     size_t scratch_bytes = 0;
+    uint32_t* flags = nullptr; // one-launch chunked form: per-(chunk, key head) flags, then 2 sync words
+    uint32_t* sync = nullptr;
 };
 DeviceState g_dev[kMaxDevices];
 
@@ -96,6 +99,17 @@ size_t scratch_bytes_for(int n_vh) {
     return static_cast<size_t>(gdn::kChunksPerSuperBlock) * n_vh * gdn::kPrepRecordFloats * sizeof(float);
 }
 
+// Flag words of the one-launch chunked form for up to n_vh key heads (n_kh <= n_vh).
+size_t flag_words_for(int n_vh) { return static_cast<size_t>(gdn::kChunksPerSuperBlock) * n_vh; }
+
+void free_scratch(DeviceState* d) {
+    cudaFree(d->scratch);
+    cudaFree(d->flags);
+    d->scratch = nullptr;
+    d->flags = d->sync = nullptr;
+    d->scratch_bytes = 0;
+}
+
 int ensure_scratch(DeviceState* d, int n_vh) {
     const size_t need = scratch_bytes_for(n_vh);
     std::lock_guard<std::mutex> lk(g_mu);
@@ -106,20 +120,43 @@ int ensure_scratch(DeviceState* d, int n_vh) {
         // a larger head count than before: the old buffer may still be in use by queued work
         cudaError_t e = cudaDeviceSynchronize();
         if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
-        cudaFree(d->scratch);
-        d->scratch = nullptr;
-        d->scratch_bytes = 0;
+        free_scratch(d);
     }
     void* p = nullptr;
+    void* f = nullptr;
+    const size_t flag_bytes = (flag_words_for(n_vh) + gdn::kSyncWords) * sizeof(uint32_t);
     cudaError_t e = cudaMalloc(&p, need);
+    if (e == cudaSuccess) {
+        e = cudaMalloc(&f, flag_bytes);
+        if (e != cudaSuccess) cudaFree(p);
+    }
     if (e != cudaSuccess) {
         cudaGetLastError();
-        return fail(GDN_ERR_ALLOC, "chunked scratch allocation of " + std::to_string(need) +
+        return fail(GDN_ERR_ALLOC, "chunked scratch allocation of " + std::to_string(need + flag_bytes) +
                                        " bytes failed: " + cudaGetErrorString(e));
     }
     d->scratch = static_cast<float*>(p);
     d->scratch_bytes = need;
+    d->flags = static_cast<uint32_t*>(f);
+    d->sync = d->flags + flag_words_for(n_vh);
+    // zero flags and generation before any stream (blocking or not) can use them
+    e = cudaMemset(f, 0, flag_bytes);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        free_scratch(d);
+        return cuda_fail(e, "flag initialisation");
+    }
     return GDN_OK;
+}
+
+// The chunked form runs prep and scan in one launch unless the environment sets
+// GDN_CHUNK_OVERLAP=0 or selects the tensor-core scan (GDN_CHUNK_SCAN=tc), both
+// for A/B measurements; read on every call.
+bool fused_chunk_launch_enabled() {
+    const char* o = std::getenv("GDN_CHUNK_OVERLAP");
+    if (o && std::strcmp(o, "0") == 0) return false;
+    const char* t = std::getenv("GDN_CHUNK_SCAN");
+    return !(t && std::strcmp(t, "tc") == 0);
 }
 
 __global__ void fill_words_kernel(uint32_t* p, size_t n, uint32_t bits) {
@@ -252,15 +289,32 @@ int gdn_recurrence(const float* q, const float* k, const float* v, const float* 
     pp.prep = dev->scratch;
     pp.n_kh = n_kh;
     pp.n_vh = n_vh;
+    int n_prep = fused_chunk_launch_enabled() ? chunk_fused_prep_ctas(n_kh, dev->sm_count) : 0;
     for (int64_t t0 = 0; t0 < T; t0 += kSuperBlock) {
         const int n = static_cast<int>((T - t0) < kSuperBlock ? (T - t0) : kSuperBlock);
         pp.t_begin = t0;
         pp.n_tokens = n;
+        sp.t_begin = t0;
+        sp.n_tokens = n;
+        if (n_prep > 0) {
+            ChunkFusedParams fp;
+            fp.scan = sp;
+            fp.prep = pp;
+            fp.flags = dev->flags;
+            fp.sync = dev->sync;
+            fp.n_prep = n_prep;
+            cudaError_t e = launch_chunk_fused(fp, s);
+            if (e == cudaSuccess) {
+                g_launches.fetch_add(1);
+                continue;
+            }
+            if (e != cudaErrorCooperativeLaunchTooLarge) return cuda_fail(e, "chunk prep+scan launch");
+            cudaGetLastError();  // fewer SMs available than the device has: two launches instead
+            n_prep = 0;
+        }
         cudaError_t e = launch_chunk_prep(pp, s);
         if (e != cudaSuccess) return cuda_fail(e, "chunk prep launch");
         g_launches.fetch_add(1);
-        sp.t_begin = t0;
-        sp.n_tokens = n;
         e = launch_chunk_scan_default(sp, s);
         if (e != cudaSuccess) return cuda_fail(e, "chunk scan launch");
         g_launches.fetch_add(1);
@@ -337,7 +391,13 @@ int gdn_device_status(void* cuda_stream) {
     if (word != 0) {
         e = cudaMemset(dev->status, 0, sizeof(int));
         if (e != cudaSuccess) return cuda_fail(e, "status reset");
-        return fail(GDN_ERR_TIMEOUT, "a kernel gave up a bounded wait");
+        std::string msg = "a kernel gave up a bounded wait (status word " + std::to_string(word) + ")";
+        uint32_t diag[3] = {0, 0, 0};
+        if ((word & gdn::kDevErrFlagTimeout) && dev->sync &&
+            cudaMemcpy(diag, dev->sync + 2, sizeof(diag), cudaMemcpyDeviceToHost) == cudaSuccess)
+            msg += ": prep flag " + std::to_string(diag[0]) + " held " + std::to_string(diag[1]) + ", awaited " +
+                   std::to_string(diag[2]);
+        return fail(GDN_ERR_TIMEOUT, msg);
     }
     return GDN_OK;
 }
@@ -351,10 +411,13 @@ int gdn_release_scratch(int device) {
     cudaGetDevice(&cur);
     cudaSetDevice(device);
     cudaError_t e = cudaFree(d.scratch);
+    cudaError_t e2 = cudaFree(d.flags);
     cudaSetDevice(cur);
     d.scratch = nullptr;
+    d.flags = d.sync = nullptr;
     d.scratch_bytes = 0;
     if (e != cudaSuccess) return cuda_fail(e, "cudaFree");
+    if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFree");
     return GDN_OK;
 }
 

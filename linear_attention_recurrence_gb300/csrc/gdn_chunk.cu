@@ -21,6 +21,9 @@
 //    transposed copy in shared memory for the K S0 / Q S0 product).  Each chunk's
 //    k and q tiles (TMA, 128-byte swizzle), v columns (TMA) and prep records
 //    (bulk copies) land in a double buffer while the chunk before computes.
+// When the SMs the scan leaves free number at least n_kh, one cooperative launch
+// runs both: the prep on those SMs, chunk by chunk ahead of the scan, which waits
+// on a per-(chunk, key head) flag instead of a kernel boundary (gdn_chunk_fused_kernel).
 // The large products (K S0, Q S0, K^T D) run as register-tiled packed FP32x2 FMAs;
 // the tolerance the path is held to (2e-6 relative to FP64) leaves no room for
 // TF32 tensor-core inputs there.
@@ -52,10 +55,10 @@ struct PrepSmem {
     float bet[kHeadsPerKey][C];
 };
 
-__global__ void __launch_bounds__(PREP_THREADS) gdn_chunk_prep_kernel(const ChunkPrepParams p) {
-    PrepSmem& sm = *aligned_dynamic_smem<PrepSmem, 16>();
-    const int ci = blockIdx.x;  // chunk within the super-block
-    const int kh = blockIdx.y;
+// Prep records of chunk `ci` (within the super-block) for key head `kh` and its
+// three value heads, by the CTA's PREP_THREADS threads.  Reads only q, k, g, beta;
+// ends without a barrier (the caller syncs before reusing `sm`).
+__device__ __forceinline__ void prep_task(const ChunkPrepParams& p, PrepSmem& sm, const int ci, const int kh) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int t0 = ci * C;
     const int n = min(C, p.n_tokens - t0);
@@ -157,6 +160,11 @@ __global__ void __launch_bounds__(PREP_THREADS) gdn_chunk_prep_kernel(const Chun
     }
 }
 
+// One CTA per (chunk, key head).
+__global__ void __launch_bounds__(PREP_THREADS) gdn_chunk_prep_kernel(const ChunkPrepParams p) {
+    prep_task(p, *aligned_dynamic_smem<PrepSmem, 16>(), blockIdx.x, blockIdx.y);
+}
+
 // ============================ scan ============================
 constexpr int SCAN_THREADS = 256;
 constexpr int NC = 16;        // value columns per CTA (per head)
@@ -179,15 +187,23 @@ struct ScanSmem {
     float Dp[C][NCC];        // e^(gamma_last - gamma) D
     float Wp[2 * C][NCC];    // second half (key dims 64..127) of [K; Q] S0
     uint64_t full[2];
+    int copy_gave_up;        // 1 + the chunk whose copy wait ran out, else 0
+    int flag_gave_up;        // a prep flag wait ran out (later ones are skipped)
 };
 
 // byte offset of float4 chunk `cc` (0..7) of row `r` in a 128-byte-swizzled box
 __device__ __forceinline__ int swz(int r, int cc) { return r * 128 + ((cc ^ (r & 7)) << 4); }
 
-__global__ void __launch_bounds__(SCAN_THREADS, 1) gdn_chunk_scan_kernel(const __grid_constant__ ChunkScanParams p) {
-    ScanSmem& sm = *aligned_dynamic_smem<ScanSmem, 1024>();
-    const int kh = blockIdx.x;
-    const int c0 = blockIdx.y * NC;
+// The scan of key head `kh`, value columns c0..c0+15 of its three heads, over the
+// super-block's chunks.  With `flags` set, chunk c's prep records are read only
+// once flags[c * n_kh + kh] == gen (records written by other CTAs of the same
+// launch); a flag wait that runs out records the flag's index, its last value and
+// `gen` in diag[0..2].  A wait that runs out is reported in the status word and
+// the state is left as it was; every thread still takes the same path through
+// the chunk loop (a thread that gave up computes on whatever landed), so the
+// CTA's barriers stay matched and the CTA ends.
+__device__ __forceinline__ void scan_body(const ChunkScanParams& p, ScanSmem& sm, const int kh, const int c0,
+                                          const uint32_t* flags, uint32_t* diag, const uint32_t gen) {
     const int tid = threadIdx.x;
     const int n_kh = p.n_kh, n_vh = p.n_vh;
     const int nch = (p.n_tokens + C - 1) / C;
@@ -196,6 +212,8 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) gdn_chunk_scan_kernel(const _
         mbar_init(&sm.full[0], 1);
         mbar_init(&sm.full[1], 1);
         mbar_init_fence();
+        sm.copy_gave_up = 0;
+        sm.flag_gave_up = 0;
     }
 
     // state slice -> registers (G4 tile: rows 8*it..8*it+7, column c0+j of each head)
@@ -213,7 +231,9 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) gdn_chunk_scan_kernel(const _
     }
     __syncthreads();
 
-    auto issue = [&](int c) {
+    // k, q and v tiles of chunk c (TMA), on the chunk's buffer barrier, which expects
+    // the records too
+    auto issue_tiles = [&](int c) {
         ScanBuf& b = sm.buf[c & 1];
         uint64_t* bar = &sm.full[c & 1];
         const int y = static_cast<int>(p.t_begin + static_cast<int64_t>(c) * C);
@@ -225,12 +245,41 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) gdn_chunk_scan_kernel(const _
             tma_load_2d(&b.Q[bx][0][0], &p.tm_q, bar, kh * D + 32 * bx, y);
         }
 #pragma unroll
-        for (int m = 0; m < kHeadsPerKey; ++m) {
-            tma_load_2d(&b.V[m][0][0], &p.tm_v, bar, (kh + m * n_kh) * D + c0, y);
-            bulk_load(&b.rec[m][0], p.prep + (static_cast<int64_t>(c) * n_vh + kh + m * n_kh) * REC, REC * 4, bar);
-        }
+        for (int m = 0; m < kHeadsPerKey; ++m) tma_load_2d(&b.V[m][0][0], &p.tm_v, bar, (kh + m * n_kh) * D + c0, y);
     };
-    if (tid == 0) issue(0);
+    // prep records of chunk c (bulk copies); with flags, once the prep task has published them
+    auto issue_records = [&](int c) {
+        ScanBuf& b = sm.buf[c & 1];
+        uint64_t* bar = &sm.full[c & 1];
+        if (flags) {
+            // records from another CTA: acquire its flag, then read them through the async proxy
+            uint32_t seen = 0;
+            if (!sm.flag_gave_up && !wait_flag(flags + c * n_kh + kh, gen, &seen)) {
+                sm.flag_gave_up = 1;
+                report_error(p.status, kDevErrFlagTimeout);
+                if (diag) {
+                    diag[0] = static_cast<uint32_t>(c * n_kh + kh);
+                    diag[1] = seen;
+                    diag[2] = gen;
+                }
+            }
+            fence_proxy_async_global();
+        }
+#pragma unroll
+        for (int m = 0; m < kHeadsPerKey; ++m)
+            bulk_load(&b.rec[m][0], p.prep + (static_cast<int64_t>(c) * n_vh + kh + m * n_kh) * REC, REC * 4, bar);
+    };
+    // The issuing lane's warp waits for it at __syncwarp: left to spin on the copy
+    // barrier while lane 0 spins on a prep flag, the other lanes can starve lane 0
+    // of issue slots until their own wait runs out.
+    const int warp = tid >> 5, lane = tid & 31;
+    if (warp == 0) {
+        if (lane == 0) {
+            issue_tiles(0);
+            issue_records(0);
+        }
+        __syncwarp();
+    }
 
     // G1 tile: key-dim half kgrp (threads 0-127: dims 0..63, 128-255: dims 64..127),
     // X rows 8*(tg&3)..+7 of K (tg < 4) or Q (tg >= 4), column jw of each head.  Each
@@ -238,10 +287,14 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) gdn_chunk_scan_kernel(const _
     const int kgrp = tid >> 7, tg = (tid >> 4) & 7, jw = tid & 15;
     // P2 / P3 tile: head pm, rows 4*pti..+3, columns 2*pjp, 2*pjp+1
     const int pm = tid >> 6, pti = (tid >> 3) & 7, pjp = tid & 7;
-    bool ok = true;
 
     for (int c = 0; c < nch; ++c) {
-        if (!mbar_wait(&sm.full[c & 1], static_cast<uint32_t>((c >> 1) & 1))) { ok = false; break; }
+        // once a copy wait has run out (seen by all after the previous chunk's last
+        // barrier), nothing more is issued or waited for
+        if (!sm.copy_gave_up && !mbar_wait(&sm.full[c & 1], static_cast<uint32_t>((c >> 1) & 1))) {
+            sm.copy_gave_up = c + 1;
+            report_timeout(p.status);
+        }
         const ScanBuf& b = sm.buf[c & 1];
         const int nt = min(C, p.n_tokens - c * C);
 
@@ -301,8 +354,17 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) gdn_chunk_scan_kernel(const _
         }
         __syncthreads();
 
-        // ---- P2: D = T' U' per head (32x32 by 32x16); warp 7, idle here, loads the next chunk ----
-        if (tid == SCAN_THREADS - 32 && c + 1 < nch) issue(c + 1);  // its buffer was last read in chunk c-1
+        // ---- P2: D = T' U' per head (32x32 by 32x16); warp 7, idle here, loads the next
+        //      chunk's tiles into the buffer chunk c-1 last read (and its records, unless
+        //      they come from another CTA: those follow in P3, off this phase's barrier) ----
+        const bool next = c + 1 < nch && !sm.copy_gave_up;  // copy_gave_up is fixed until the next chunk
+        if (warp == SCAN_THREADS / 32 - 1) {
+            if (lane == 0 && next) {
+                issue_tiles(c + 1);
+                if (!flags) issue_records(c + 1);
+            }
+            __syncwarp();
+        }
         if (tid < kHeadsPerKey * 64) {
             const float* tp = &b.rec[pm][REC_TP];
             float acc[4][2];
@@ -367,6 +429,10 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) gdn_chunk_scan_kernel(const _
                     *reinterpret_cast<float2*>(o) = make_float2(acc[r][0], acc[r][1]);
                 }
             }
+        } else if (flags && warp == SCAN_THREADS / 32 - 1) {
+            // warp 7 is idle in P3: wait here for the next chunk's prep flag and copy its records
+            if (lane == 0 && next) issue_records(c + 1);
+            __syncwarp();
         }
 
         // ---- G4: S_end = e^gamma_last S0 + K^T (e^(gamma_last-gamma) D), packed over key-dim pairs ----
@@ -408,10 +474,13 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) gdn_chunk_scan_kernel(const _
         __syncthreads();
     }
 
-    if (!ok) {
-        if (tid == 0) report_timeout(p.status);
+    // (the loop ended on a barrier, so copy_gave_up and flag_gave_up are final here)
+    if (sm.copy_gave_up) {
+        const int cf = sm.copy_gave_up - 1;  // the one chunk whose copies may still be landing
+        if (tid == 0) mbar_wait(&sm.full[cf & 1], static_cast<uint32_t>((cf >> 1) & 1));
         return;
     }
+    if (sm.flag_gave_up) return;
 #pragma unroll
     for (int m = 0; m < kHeadsPerKey; ++m) {
         float* sh = p.state + (static_cast<int64_t>(kh + m * n_kh) * D + 8 * it) * D + c0 + jj;
@@ -419,6 +488,53 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) gdn_chunk_scan_kernel(const _
         for (int q = 0; q < 4; ++q) {
             sh[(2 * q) * D] = Sreg[m][q].x;
             sh[(2 * q + 1) * D] = Sreg[m][q].y;
+        }
+    }
+}
+
+// One CTA per (key head, 16 value columns); the prep kernel has run before.
+__global__ void __launch_bounds__(SCAN_THREADS, 1) gdn_chunk_scan_kernel(const __grid_constant__ ChunkScanParams p) {
+    scan_body(p, *aligned_dynamic_smem<ScanSmem, 1024>(), blockIdx.x, blockIdx.y * NC, nullptr, nullptr, 0u);
+}
+
+// ====================== prep and scan in one launch ======================
+// The scan occupies 8 n_kh SMs for the whole super-block, the prep only a short
+// burst before it.  Here the remaining SMs run the prep while the scan runs: CTAs
+// 0..n_prep-1 take the (chunk, key head) prep tasks in chunk order, each
+// publishing its records with a release store of this launch's generation
+// number; the scan CTAs acquire that flag before copying a chunk's records.  The
+// prep CTAs wait on nothing, so the scan's waits end as long as every CTA is
+// resident (a cooperative launch guarantees it).  The generation number lives in
+// device memory and the last CTA to finish advances it, so a replayed CUDA graph
+// of this launch never matches a stale flag.
+__global__ void __launch_bounds__(SCAN_THREADS, 1) gdn_chunk_fused_kernel(const __grid_constant__ ChunkFusedParams p) {
+    __shared__ uint32_t s_gen;
+    const int tid = threadIdx.x;
+    if (tid == 0) s_gen = ld_acquire_gpu(p.sync) + 1u;
+    __syncthreads();
+    const uint32_t gen = s_gen;
+    const int b = static_cast<int>(blockIdx.x);
+    if (b < p.n_prep) {
+        PrepSmem& sm = *aligned_dynamic_smem<PrepSmem, 1024>();
+        const int n_kh = p.prep.n_kh;
+        const int tasks = ((p.prep.n_tokens + C - 1) / C) * n_kh;
+        for (int task = b; task < tasks; task += p.n_prep) {
+            prep_task(p.prep, sm, task / n_kh, task % n_kh);
+            fence_proxy_async_global();
+            __syncthreads();
+            if (tid == 0) st_release_gpu(p.flags + task, gen);
+        }
+    } else {
+        const int s = b - p.n_prep, n_kh = p.scan.n_kh;
+        scan_body(p.scan, *aligned_dynamic_smem<ScanSmem, 1024>(), s % n_kh, (s / n_kh) * NC, p.flags, p.sync + 2,
+                  gen);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();
+        if (atomicAdd(p.sync + 1, 1u) == gridDim.x - 1) {
+            p.sync[1] = 0u;
+            st_release_gpu(p.sync, gen);
         }
     }
 }
@@ -434,6 +550,29 @@ cudaError_t launch_chunk_prep(const ChunkPrepParams& p, cudaStream_t s) {
     dim3 grid((p.n_tokens + C - 1) / C, p.n_kh);
     gdn_chunk_prep_kernel<<<grid, PREP_THREADS, smem, s>>>(p);
     return cudaGetLastError();
+}
+
+int chunk_fused_prep_ctas(int n_kh, int sm_count) {
+    const int n_prep = sm_count - (D / NC) * n_kh;
+    return n_prep >= n_kh ? n_prep : 0;
+}
+
+cudaError_t launch_chunk_fused(const ChunkFusedParams& p, cudaStream_t s) {
+    constexpr size_t body = sizeof(ScanSmem) > sizeof(PrepSmem) ? sizeof(ScanSmem) : sizeof(PrepSmem);
+    const size_t smem = body + 1024;
+    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(gdn_chunk_fused_kernel), static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.n_prep + (D / NC) * p.scan.n_kh);
+    cfg.blockDim = dim3(SCAN_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gdn_chunk_fused_kernel, p);
 }
 
 cudaError_t launch_chunk_scan(const ChunkScanParams& p, cudaStream_t s) {

@@ -145,6 +145,7 @@ __global__ void __launch_bounds__(THREADS, 1) gdn_chunk_scan_tc_kernel(const __g
         issue_v(0);
         issue_rec(0);
     }
+    __syncwarp();  // warp 0's other lanes wait for lane 0's issues before spinning on barriers
 
     const int pm = tid >> 6, pti = (tid >> 3) & 7, pjp = tid & 7;  // D and O tiles (threads 0..191)
     float el[kHeadsPerKey] = {1.f, 1.f, 1.f};
@@ -204,9 +205,11 @@ __global__ void __launch_bounds__(THREADS, 1) gdn_chunk_scan_tc_kernel(const __g
                 }
             umma_commit(&bar[BAR_G1]);
         }
+        __syncwarp();
         if (!mbar_wait(&bar[BAR_G1], par)) failed = true;
         tc_fence_after_sync();
         if (tid == 0 && !failed && c + 1 < nch) issue_kq(c + 1);  // the product has read the k / q tile
+        __syncwarp();
         if (!mbar_wait(&bar[BAR_V], par) || !mbar_wait(&bar[BAR_REC], par)) failed = true;
         // ---- U' = V - e^gamma W_K and QS' = e^gamma W_Q (warps 0-3; W row r sits in lane 32*(r/16) + r%16) ----
         if (warp < 4 && !__any_sync(0xffffffffu, failed)) {
@@ -241,6 +244,7 @@ __global__ void __launch_bounds__(THREADS, 1) gdn_chunk_scan_tc_kernel(const __g
         tc_fence_before_sync();
         if (__syncthreads_or(failed)) break;
         if (tid == 0 && c + 1 < nch) issue_v(c + 1);
+        __syncwarp();
 
         // ---- D = T' U' per head (threads 0..191); D'^T = (e^(gamma_last - gamma) D)^T as TF32 hi / lo ----
         if (tid < kHeadsPerKey * 64) {
@@ -294,6 +298,7 @@ __global__ void __launch_bounds__(THREADS, 1) gdn_chunk_scan_tc_kernel(const __g
                               umma_desc_sw128(sm + b_off[pass] + ks * 32), id, pass > 0 || ks > 0);
             umma_commit(&bar[BAR_G4]);
         }
+        __syncwarp();
         // ---- O = QS' + P D per head -> out (threads 0..191) ----
         if (tid < kHeadsPerKey * 64) {
             const float* pt = R + pm * REC + kRecPT;
@@ -329,6 +334,7 @@ __global__ void __launch_bounds__(THREADS, 1) gdn_chunk_scan_tc_kernel(const __g
         }
         __syncthreads();
         if (tid == 0 && c + 1 < nch) issue_rec(c + 1);  // the records of this chunk are no longer read
+        __syncwarp();
 
         // ---- S = e^gamma_last S0 + K^T D' (warps 0-3), then S^T as TF32 hi / lo for the next chunk ----
         if (warp < 4) {

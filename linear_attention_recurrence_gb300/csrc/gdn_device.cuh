@@ -10,7 +10,8 @@
 namespace gdn {
 
 // Status word values written by kernels (read by gdn_device_status()).
-constexpr int kDevErrTimeout = 1;
+constexpr int kDevErrTimeout = 1;      // a wait for an asynchronous copy gave up
+constexpr int kDevErrFlagTimeout = 2;  // a wait for another CTA's flag gave up
 
 // A wait gives up after this many unsuccessful mbarrier.try_wait polls (each
 // poll may itself suspend the thread for a hardware-chosen interval).  Legit
@@ -70,8 +71,46 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     return false;
 }
 
-__device__ __forceinline__ void report_timeout(int* status) {
-    if (status) atomicExch(status, kDevErrTimeout);
+// Status codes are bits: a word with several set records several kinds of wait giving up.
+__device__ __forceinline__ void report_error(int* status, int code) {
+    if (status) atomicOr(status, code);
+}
+
+__device__ __forceinline__ void report_timeout(int* status) { report_error(status, kDevErrTimeout); }
+
+// ---- flags between CTAs of one launch (GPU-scope release / acquire) ----
+// A flag wait gives up after this many polls (each an L2 round trip plus a
+// short sleep): a tenth of a second or more, against waits of microseconds, and
+// shorter than a copy wait that gives up (so a stuck flag is reported as such).
+constexpr uint32_t kFlagPolls = 1u << 18;
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Order this thread's earlier generic-proxy global accesses with its later
+// async-proxy (bulk copy) ones, and the reverse.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Waits until *flag == value.  Returns false if the poll limit ran out, with
+// the last value read in *seen.
+__device__ __forceinline__ bool wait_flag(const uint32_t* flag, uint32_t value, uint32_t* seen) {
+    uint32_t v = 0;
+    for (uint32_t i = 0; i < kFlagPolls; ++i) {
+        v = ld_acquire_gpu(flag);
+        if (v == value) return true;
+        __nanosleep(64);
+    }
+    *seen = v;
+    return false;
 }
 
 // 2-D tiled TMA load of box (x, y) into shared memory, completing on `bar`.

@@ -85,6 +85,22 @@ struct ChunkPrepParams {
     int n_vh;
 };
 cudaError_t launch_chunk_prep(const ChunkPrepParams& p, cudaStream_t s);
+// Prep and scan of one super-block in one cooperative launch: CTAs 0..n_prep-1 run
+// the prep tasks, the next 8 n_kh CTAs the scan.
+struct ChunkFusedParams {
+    ChunkScanParams scan;
+    ChunkPrepParams prep;  // same prep, t_begin and n_tokens as scan
+    uint32_t* flags;       // [kChunksPerSuperBlock][n_kh]: generation of each finished prep task
+    uint32_t* sync;        // [0]: generation of the last finished launch, [1]: CTAs finished so far,
+                           // [2..4]: the first flag wait that ran out (index, value seen, value awaited)
+    int n_prep;
+};
+// CTAs the one-launch form gives the prep on a device with sm_count SMs, or 0
+// when too few SMs are left beside the scan (the two-launch form is used then).
+int chunk_fused_prep_ctas(int n_kh, int sm_count);
+constexpr int kSyncWords = 8;  // words of ChunkFusedParams::sync
+// Fails (cudaErrorCooperativeLaunchTooLarge) when the grid cannot be resident at once.
+cudaError_t launch_chunk_fused(const ChunkFusedParams& p, cudaStream_t s);
 cudaError_t launch_chunk_scan(const ChunkScanParams& p, cudaStream_t s);
 // The same scan with the chunk's large products (K S0, Q S0, K^T D) on the tensor
 // cores as split-TF32 (3 passes); same parameters and results within tolerance.

@@ -100,6 +100,7 @@ __global__ void __launch_bounds__(SeqShape<R>::THREADS, 1) gdn_seq_kernel(const 
         int64_t issued = nst < NS ? nst : NS;
         if (lane == 0)
             for (int64_t s = 0; s < issued; ++s) issue(s);
+        __syncwarp();  // lanes 1..31 must not spin on a barrier while lane 0 still has copies to issue
         int64_t landed = 0;  // stages whose full barrier this warp has observed
         bool ok = true;
         for (int64_t s = 0; s < nst && ok; ++s) {
@@ -150,6 +151,7 @@ __global__ void __launch_bounds__(SeqShape<R>::THREADS, 1) gdn_seq_kernel(const 
                 const int64_t r = s - 1;
                 if (!mbar_wait(&sm.empty[r % NS], static_cast<uint32_t>((r / NS) & 1))) { ok = false; break; }
                 if (lane == 0) issue(r + NS);
+                __syncwarp();
                 issued = r + NS + 1;
             }
         }

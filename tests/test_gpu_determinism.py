@@ -93,3 +93,78 @@ def test_auto_mode_is_the_chosen_mode_bit_for_bit(T):
     oc, sc = _run(t, chosen, [T])
     assert np.array_equal(oa.view(np.uint32), oc.view(np.uint32))
     assert np.array_equal(sa.view(np.uint32), sc.view(np.uint32))
+
+
+def _env(name, value):
+    """Context manager setting one environment variable (read by the library per call)."""
+    import contextlib
+    import os
+
+    @contextlib.contextmanager
+    def cm():
+        old = os.environ.get(name)
+        os.environ[name] = value
+        try:
+            yield
+        finally:
+            if old is None:
+                del os.environ[name]
+            else:
+                os.environ[name] = old
+
+    return cm()
+
+
+def _sm_count():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+@pytest.mark.parametrize("T", [1, 130, 2048, 4099])
+def test_one_launch_chunked_matches_two_launch_bits(T):
+    """Prep and scan in one cooperative launch (prep on the SMs the scan leaves
+    free, handing records over through flags) give the same bits as the prep
+    kernel followed by the scan kernel, with one launch per super-block instead
+    of two."""
+    if _sm_count() < 9 * 16:
+        pytest.skip("too few SMs for the one-launch form at 16 key heads")
+    t = to_dev(make_inputs(T, seed=14, norm=False))
+    n_sb = (T + 2047) // 2048
+    with _env("GDN_CHUNK_OVERLAP", "0"):
+        n0 = gdn.gdn_launch_count()
+        o2, s2 = _run(t, "chunked", [T])
+        assert gdn.gdn_launch_count() - n0 == 2 * n_sb
+    for i in range(3):
+        gdn.gdn_poison_scratch(0x7FC00000 if i % 2 == 0 else 0xFF800000)
+        n0 = gdn.gdn_launch_count()
+        o1, s1 = _run(t, "chunked", [T])
+        assert gdn.gdn_launch_count() - n0 == n_sb
+        assert np.array_equal(o1.view(np.uint32), o2.view(np.uint32))
+        assert np.array_equal(s1.view(np.uint32), s2.view(np.uint32))
+
+
+def test_one_launch_chunked_under_graph_replay():
+    """A captured chunked call replayed several times, with the scratch poisoned
+    with NaN between replays: each replay gives the eager bits.  The flags carry
+    a generation number kept in device memory, so a replay cannot take the
+    previous replay's flags for its own and read stale (here NaN) records."""
+    T = 4099
+    t = to_dev(make_inputs(T, seed=15, norm=False))
+    o_ref, s_ref = _run(t, "chunked", [T])  # eager; also allocates the scratch before capture
+    st = t["S0"].clone()
+    out = torch.empty((T, 48, 128), device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            gdn.gdn_recurrence(t["q"], t["k"], t["v"], t["g"], t["beta"], st, out=out, mode="chunked")
+    torch.cuda.synchronize()
+    for i in range(4):
+        st.copy_(t["S0"])
+        out.fill_(float("nan"))
+        gdn.gdn_poison_scratch(0x7FC00000)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert gdn.gdn_device_status() == gdn.GDN_OK
+        assert np.array_equal(out.cpu().numpy().view(np.uint32), o_ref.view(np.uint32)), i
+        assert np.array_equal(st.cpu().numpy().view(np.uint32), s_ref.view(np.uint32)), i

@@ -72,5 +72,8 @@ def test_launch_counter_counts_kernels():
     assert gdn.gdn_launch_count() - n0 == 1
     n0 = gdn.gdn_launch_count()
     gdn.gdn_recurrence(t["q"], t["k"], t["v"], t["g"], t["beta"], t["S0"].clone(), mode="chunked")
-    assert gdn.gdn_launch_count() - n0 == 2 * 3  # prep + scan per 2048-token super-block
+    # per 2048-token super-block: prep and scan in one launch when 8 n_kh scan CTAs
+    # leave at least n_kh SMs for the prep, else a prep launch and a scan launch
+    one_launch = torch.cuda.get_device_properties(0).multi_processor_count >= 9 * 16
+    assert gdn.gdn_launch_count() - n0 == (1 if one_launch else 2) * 3
     torch.cuda.synchronize()
