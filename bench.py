@@ -368,6 +368,8 @@ def main():
     ap.add_argument("--call-tokens", type=int, default=2048)
     ap.add_argument("--skip-cpu", action="store_true", help="no oracle timing")
     ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--e2e-copy-streams", type=int, default=1,
+                    help="host-to-device copy streams of the pipelined end-to-end step")
     ap.add_argument("--skip-other-mode", action="store_true")
     ap.add_argument("--ref-seconds", type=float, default=10.0)
     ap.add_argument("--sweep", action="store_true",
@@ -476,22 +478,54 @@ def main():
     other_res = None if args.skip_other_mode else timed(other, args.steps, 1, per_kernel=True)
     assert gdn.gdn_device_status() == gdn.GDN_OK
 
-    # end to end through the public API with host buffers: H2D of the step's
-    # inputs from pinned memory, the calls, D2H of the FP16 output and the state
+    # end to end through the public API with host buffers: every step copies its inputs
+    # from pinned host memory and reads the FP16 output and the final state back, inside
+    # the timed region.  The copies are pipelined per call: a copy-in stream brings call
+    # i+1's rows (q, k, v, g, beta, z) while the compute stream runs call i (recurrence,
+    # then the norm of its rows) and a copy-out stream returns call i-1's y rows.
     e2e = None
     if not args.skip_e2e:
         hy = torch.empty((T, N_VH, D), dtype=torch.float16).pin_memory()
         hs = torch.empty_like(h["S0"]).pin_memory()
-        names = ["q", "k", "v", "g", "beta", "S0", "z", "w"]
-        h2d = sum(h[n].numel() * h[n].element_size() for n in names)
+        row_names = ["q", "k", "v", "g", "beta", "z"]
+        h2d = sum(h[n].numel() * h[n].element_size() for n in row_names + ["S0", "w"])
         d2h = hy.numel() * 2 + hs.numel() * 4
+        s_ins = [torch.cuda.Stream(dev) for _ in range(args.e2e_copy_streams)]
+        s_out = torch.cuda.Stream(dev)
 
         def e2e_step():
-            for n in names:
-                t[n].copy_(h[n], non_blocking=True)
-            step(args.mode)
-            hy.copy_(y, non_blocking=True)
-            hs.copy_(state, non_blocking=True)
+            landed = [[] for _ in range(ncalls)]
+            for j, s_in in enumerate(s_ins):
+                s_in.wait_stream(stream)  # the previous step's calls have read their rows
+                with torch.cuda.stream(s_in):
+                    if j == 0:
+                        t["S0"].copy_(h["S0"], non_blocking=True)
+                        t["w"].copy_(h["w"], non_blocking=True)
+                    for i in range(ncalls):
+                        a, b = i * CT, (i + 1) * CT
+                        for n in row_names[j::len(s_ins)]:
+                            t[n][a:b].copy_(h[n][a:b], non_blocking=True)
+                        landed[i].append(torch.cuda.Event())
+                        landed[i][-1].record(s_in)
+            for ev in landed[0]:
+                stream.wait_event(ev)
+            state.copy_(t["S0"])
+            for i in range(ncalls):
+                a, b = i * CT, (i + 1) * CT
+                for ev in landed[i]:
+                    stream.wait_event(ev)
+                gdn.gdn_recurrence(t["q"][a:b], t["k"][a:b], t["v"][a:b], t["g"][a:b], t["beta"][a:b], state,
+                                   out=out[a:b], mode=args.mode, stream=stream)
+                gdn.gdn_out_norm(out[a:b], t["z"][a:b], t["w"], 1e-6, y=y[a:b], stream=stream)
+                done = torch.cuda.Event()
+                done.record(stream)
+                s_out.wait_event(done)
+                with torch.cuda.stream(s_out):
+                    hy[a:b].copy_(y[a:b], non_blocking=True)
+            s_out.wait_stream(stream)
+            with torch.cuda.stream(s_out):
+                hs.copy_(state, non_blocking=True)
+            stream.wait_stream(s_out)
 
         for _ in range(2):
             e2e_step()
@@ -507,7 +541,15 @@ def main():
         torch.cuda.synchronize()
         ms, e2e_us, _ = aggregate(e0.elapsed_time(e1) / args.steps, T, ws, device=dev)
         e2e = {"value": e2e_us, "unit": "µs/token/layer", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+               "d2h_bytes_per_step": d2h, "ms_per_step": ms,
+               "pipelining": f"per {CT}-token call: copy-in ({len(s_ins)} stream(s)), compute (recurrence "
+                             "+ norm of its rows), copy-out, on separate streams"}
+        # the pipelined step must give the bits of the plain one
+        ref_y = y.clone()
+        step(args.mode)
+        torch.cuda.synchronize()
+        assert torch.equal(ref_y, y), "pipelined end-to-end step differs from the plain step"
+        assert torch.equal(hy, y.cpu()) and torch.equal(hs, state.cpu())
 
     if rank != 0:
         if ws > 1:
