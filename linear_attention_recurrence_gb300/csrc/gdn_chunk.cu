@@ -185,7 +185,6 @@ struct ScanSmem {
     float W[2 * C][NCC];     // rows 0..31: U'; rows 32..63: e^gamma (Q S0)
     float Dm[C][NCC];        // D
     float Dp[C][NCC];        // e^(gamma_last - gamma) D
-    float Wp[2 * C][NCC];    // second half (key dims 64..127) of [K; Q] S0
     uint64_t full[2];
     int copy_gave_up;        // 1 + the chunk whose copy wait ran out, else 0
     int flag_gave_up;        // a prep flag wait ran out (later ones are skipped)
@@ -281,10 +280,11 @@ __device__ __forceinline__ void scan_body(const ChunkScanParams& p, ScanSmem& sm
         __syncwarp();
     }
 
-    // G1 tile: key-dim half kgrp (threads 0-127: dims 0..63, 128-255: dims 64..127),
-    // X rows 8*(tg&3)..+7 of K (tg < 4) or Q (tg >= 4), column jw of each head.  Each
-    // quarter-warp shares its rows, so the X loads are broadcasts.
-    const int kgrp = tid >> 7, tg = (tid >> 4) & 7, jw = tid & 15;
+    // G1 tile: warp tg takes X rows 8*(tg&3)..+7 of K (tg < 4) or Q (tg >= 4); lane
+    // bit 4 picks the key-dim half kgrp (dims 0..63 or 64..127) and the low four bits
+    // the column jw of each head.  Each quarter-warp shares its rows and half, so the
+    // X loads are broadcasts; the halves' partial sums meet by a shuffle.
+    const int tg = warp, kgrp = (lane >> 4) & 1, jw = lane & 15;
     // P2 / P3 tile: head pm, rows 4*pti..+3, columns 2*pjp, 2*pjp+1
     const int pm = tid >> 6, pti = (tid >> 3) & 7, pjp = tid & 7;
 
@@ -299,7 +299,7 @@ __device__ __forceinline__ void scan_body(const ChunkScanParams& p, ScanSmem& sm
         const int nt = min(C, p.n_tokens - c * C);
 
         // ---- G1: W = [K; Q] S0 (64 x 48), packed over even/odd key dims, the key dims
-        //      split over the two thread halves and their partial sums added once ----
+        //      split over the two half-warps and their partial sums added once ----
         {
             const unsigned char* xb = reinterpret_cast<const unsigned char*>(tg < 4 ? &b.K[0][0][0] : &b.Q[0][0][0]) +
                                       (8 * (tg & 3)) * 128;
@@ -328,27 +328,22 @@ __device__ __forceinline__ void scan_body(const ChunkScanParams& p, ScanSmem& sm
                     }
                 }
             }
-            const int row0 = (tg < 4 ? 0 : C) + 8 * (tg & 3);
-            if (kgrp == 1) {
+            // reduce-scatter with lane ^ 16: kgrp 0 finishes the even rows, kgrp 1 the odd
+            // ones, each as (dims 0..63) + (dims 64..127)
 #pragma unroll
-                for (int r = 0; r < 8; ++r)
+            for (int r2 = 0; r2 < 4; ++r2) {
+                const int t = 8 * (tg & 3) + 2 * r2 + kgrp;
 #pragma unroll
-                    for (int m = 0; m < kHeadsPerKey; ++m) sm.Wp[row0 + r][m * NC + jw] = acc[r][m].x + acc[r][m].y;
-            }
-            __syncthreads();
-            if (kgrp == 0) {
-#pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    const int t = 8 * (tg & 3) + r;
-#pragma unroll
-                    for (int m = 0; m < kHeadsPerKey; ++m) {
-                        const float x = (acc[r][m].x + acc[r][m].y) + sm.Wp[row0 + r][m * NC + jw];
-                        const float eg = b.rec[m][REC_EG + t];
-                        if (tg < 4)
-                            sm.W[t][m * NC + jw] = b.V[m][t][jw] - eg * x;
-                        else
-                            sm.W[C + t][m * NC + jw] = eg * x;
-                    }
+                for (int m = 0; m < kHeadsPerKey; ++m) {
+                    const float ev = acc[2 * r2][m].x + acc[2 * r2][m].y;
+                    const float od = acc[2 * r2 + 1][m].x + acc[2 * r2 + 1][m].y;
+                    const float other = __shfl_xor_sync(0xffffffffu, kgrp ? ev : od, 16);
+                    const float x = kgrp ? other + od : ev + other;
+                    const float eg = b.rec[m][REC_EG + t];
+                    if (tg < 4)
+                        sm.W[t][m * NC + jw] = b.V[m][t][jw] - eg * x;
+                    else
+                        sm.W[C + t][m * NC + jw] = eg * x;
                 }
             }
         }
