@@ -15,6 +15,16 @@ Shapes (all row-major, contiguous, FP32):
 * z      ``[T][n_vh][d]``: N(0,1), the output gate.
 * w      ``[d]``: 1 + N(0, 0.1), the norm weight shared by all heads.
 
+Pre-stage inputs (``make_prestage_inputs``), the layer's projections before the
+causal convolution:
+
+* qkv     ``[T][(2 n_kh + n_vh) d]``: N(0,1), the packed q, k, v projections.
+* conv_w  ``[(2 n_kh + n_vh) d][4]``: U(-0.5, 0.5), the 4 causal taps per channel.
+* conv_hist ``[3][(2 n_kh + n_vh) d]``: N(0,1), the three rows before the call.
+* a, b    ``[T][n_vh]``: N(0,1), the gate and beta projections.
+* A_log   ``[n_vh]``: log U(1, 16); dt_bias ``[n_vh]``: log(e^dt - 1) with
+  dt = exp(U(log 1e-3, log 0.1)).
+
 Each tensor comes from its own Philox stream keyed by (seed * 1000 + layer,
 tensor id), so tensors can be drawn separately, and a draw for T tokens equals
 the first T tokens of a draw for more tokens (the streams are consumed in
@@ -28,7 +38,8 @@ N_KH = 16
 N_VH = 48
 D = 128
 
-_IDS = {"q": 1, "k": 2, "v": 3, "g": 4, "beta": 5, "S0": 6, "z": 7, "w": 8}
+_IDS = {"q": 1, "k": 2, "v": 3, "g": 4, "beta": 5, "S0": 6, "z": 7, "w": 8,
+        "qkv": 9, "conv_w": 10, "conv_hist": 11, "a": 12, "b": 13, "A_log": 14, "dt_bias": 15}
 
 
 def _rng(seed: int, layer: int, name: str) -> np.random.Generator:
@@ -68,4 +79,22 @@ def make_inputs(T: int, seed: int = 0, layer: int = 0, n_kh: int = N_KH, n_vh: i
         out["z"] = _rng(seed, layer, "z").standard_normal((T, n_vh, d), dtype=np.float32)
     if "w" in want:
         out["w"] = (1.0 + 0.1 * _rng(seed, layer, "w").standard_normal(d)).astype(np.float32)
+    return out
+
+
+def make_prestage_inputs(T: int, seed: int = 0, layer: int = 0, n_kh: int = N_KH, n_vh: int = N_VH,
+                         d: int = D) -> dict:
+    """Draw one layer's pre-stage inputs for T tokens: qkv, conv_w, conv_hist, a, b,
+    A_log, dt_bias (numpy FP32 arrays, shapes in the module docstring)."""
+    cw = (2 * n_kh + n_vh) * d
+    out = {
+        "qkv": _rng(seed, layer, "qkv").standard_normal((T, cw), dtype=np.float32),
+        "conv_w": _rng(seed, layer, "conv_w").uniform(-0.5, 0.5, (cw, 4)).astype(np.float32),
+        "conv_hist": _rng(seed, layer, "conv_hist").standard_normal((3, cw), dtype=np.float32),
+        "a": _rng(seed, layer, "a").standard_normal((T, n_vh), dtype=np.float32),
+        "b": _rng(seed, layer, "b").standard_normal((T, n_vh), dtype=np.float32),
+        "A_log": np.log(_rng(seed, layer, "A_log").uniform(1.0, 16.0, n_vh)).astype(np.float32),
+    }
+    dt = np.exp(_rng(seed, layer, "dt_bias").uniform(np.log(1e-3), np.log(0.1), n_vh))
+    out["dt_bias"] = np.log(np.expm1(dt)).astype(np.float32)
     return out

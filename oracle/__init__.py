@@ -13,6 +13,8 @@ compiles it with gcc and wraps it with ctypes.  Sources, by page title:
   sharing ``head % 16`` and the FP16 output norm.
 * "#1372 DeltaNet recurrence: STRATA_GDN_CHUNKED=1 - the prompt's recurrence in
   32-token chunks", section "What it does": the chunked WY form.
+* "Round 20 Track C Audit: gdn_pre ... gdn_scan_r ...", section 1 "Summary of
+  Changes": the pre-stage's 4-tap causal convolution over the packed qkv rows.
 """
 from __future__ import annotations
 
@@ -78,6 +80,9 @@ class Oracle:
         lib.oracle_gdn_out_norm.restype = i32
         lib.oracle_fp16_rne.argtypes = [ctypes.c_double]
         lib.oracle_fp16_rne.restype = ctypes.c_uint16
+        lib.oracle_gdn_prestage.argtypes = [f, f, f, f, f, f, f, i32, ctypes.c_double, f, f, f, f, f, f,
+                                            i64, i32, i32, i32]
+        lib.oracle_gdn_prestage.restype = i32
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = i32
         self.lib = lib
@@ -137,6 +142,29 @@ class Oracle:
             raise RuntimeError(f"oracle_gdn_out_norm failed: {rc}")
         return y
 
+    def prestage(self, qkv, conv_w, hist, a, b, A_log, dt_bias, n_kh: int, n_vh: int, act: int = 1,
+                 eps: float = 1e-6):
+        """FP64 pre-stage.  Returns dict q, k, v, g, beta, hist (all float64).
+
+        qkv: [T][(2 n_kh + n_vh) d]; conv_w: [(2 n_kh + n_vh) d][4]; hist: [3][Cw] or None;
+        a, b: [T][n_vh]; A_log, dt_bias: [n_vh].
+        """
+        qkv, conv_w, a, b = _f32(qkv), _f32(conv_w), _f32(a), _f32(b)
+        A_log, dt_bias = _f32(A_log), _f32(dt_bias)
+        T, Cw = qkv.shape
+        d = Cw // (2 * n_kh + n_vh)
+        assert d * (2 * n_kh + n_vh) == Cw and conv_w.shape == (Cw, 4)
+        h_in = None if hist is None else _f32(hist)
+        out = {"q": np.empty((T, n_kh, d)), "k": np.empty((T, n_kh, d)), "v": np.empty((T, n_vh, d)),
+               "g": np.empty((T, n_vh)), "beta": np.empty((T, n_vh)), "hist": np.empty((3, Cw))}
+        rc = self.lib.oracle_gdn_prestage(_ptr(qkv), _ptr(conv_w), None if h_in is None else _ptr(h_in),
+                                          _ptr(a), _ptr(b), _ptr(A_log), _ptr(dt_bias), int(act), float(eps),
+                                          _ptr(out["q"]), _ptr(out["k"]), _ptr(out["v"]), _ptr(out["g"]),
+                                          _ptr(out["beta"]), _ptr(out["hist"]), T, n_kh, n_vh, d)
+        if rc != 0:
+            raise RuntimeError(f"oracle_gdn_prestage failed: {rc}")
+        return out
+
     def fp16_rne(self, x: float) -> int:
         """The oracle's own double -> binary16 rounding (bits)."""
         return int(self.lib.oracle_fp16_rne(float(x)))
@@ -166,6 +194,10 @@ def chunked(*a, **kw):
 
 def out_norm(*a, **kw):
     return default().out_norm(*a, **kw)
+
+
+def prestage(*a, **kw):
+    return default().prestage(*a, **kw)
 
 
 def fp16_rne(x: float) -> int:

@@ -295,6 +295,104 @@ int oracle_gdn_out_norm(const double* o, const float* z, const float* w,
     return ORACLE_OK;
 }
 
+/*
+ * Pre-stage: the recurrence's inputs from the layer's projections ("Round 20
+ * Track C Audit: gdn_pre Key-Head t >= 3 Vectorized conv_w Fast Path + gdn_scan_r
+ * ...", section 1 "Summary of Changes": a 4-tap causal convolution per channel of
+ * the packed qkv rows, with the q channels of key head kh at kh*d and its k
+ * channels at (n_kh + kh)*d, taps applied to rows t-3 .. t; the stage hands the
+ * scan normalised q and k, the convolved v and the gates, and keeps a history).
+ *
+ * qkv     : [T][Cw] float, Cw = (2 n_kh + n_vh) d: q of the key heads, k of the
+ *           key heads, then v of the value heads
+ * conv_w  : [Cw][4] float; tap j multiplies row t - 3 + j of the same channel
+ * hist_in : [3][Cw] float, rows -3, -2, -1 (the last rows before this call), or
+ *           NULL for the start of a sequence (zeros)
+ * a, b    : [T][n_vh] float, gate and beta projections; A_log, dt_bias: [n_vh] float
+ * act     : 1 applies SiLU to every convolved channel, 0 none
+ * eps     : added to the sum of squares in the q and k L2 norms
+ * q, k    : [T][n_kh][d] double; v: [T][n_vh][d] double; g, beta: [T][n_vh] double
+ * hist_out: [3][Cw] double, the last three rows of (hist_in, qkv), or NULL
+ *
+ * Per token t and channel c:
+ *     x_c  = sum_{j=0..3} conv_w[c][j] X[t-3+j][c]        (X[-3..-1] = hist_in)
+ *     u_c  = act ? x_c / (1 + e^{-x_c}) : x_c
+ *     q[t][kh] = u_q / sqrt(|u_q|^2 + eps) / sqrt(d);   k[t][kh] = u_k / sqrt(|u_k|^2 + eps)
+ *     v[t][h]  = u_v
+ *     g[t][h]  = -e^{A_log[h]} softplus(a[t][h] + dt_bias[h]),  softplus(x) = log(1 + e^x)
+ *     beta[t][h] = 1 / (1 + e^{-b[t][h]})
+ * The pages give neither the activation, the norm's eps, the 1/sqrt(d) on q nor
+ * the gate formula; these are the readings this oracle takes (the GDN layer's
+ * usual form; the recurrence's tests draw q with norm 1/sqrt(d) and g = -softplus).
+ */
+static double oracle_softplus(double x) {
+    /* log(1 + e^x) = max(x, 0) + log(1 + e^{-|x|}) */
+    return (x > 0.0 ? x : 0.0) + log1p(exp(-fabs(x)));
+}
+
+int oracle_gdn_prestage(const float* qkv, const float* conv_w, const float* hist_in,
+                        const float* a, const float* b, const float* A_log, const float* dt_bias,
+                        int act, double eps, double* q, double* k, double* v, double* g,
+                        double* beta, double* hist_out, int64_t T, int n_kh, int n_vh, int d) {
+    if (check_shapes(T, n_kh, n_vh, d) != ORACLE_OK) return ORACLE_BAD_ARG;
+    const int64_t Cw = (int64_t)(2 * n_kh + n_vh) * d;
+    double* u = (double*)malloc(sizeof(double) * (size_t)Cw);
+    if (!u) return ORACLE_NO_MEM;
+    for (int64_t t = 0; t < T; ++t) {
+        /* convolution and activation of every channel of row t */
+        for (int64_t c = 0; c < Cw; ++c) {
+            double x = 0.0;
+            for (int j = 0; j < 4; ++j) {
+                const int64_t r = t - 3 + j;
+                double xr;
+                if (r >= 0)
+                    xr = (double)qkv[r * Cw + c];
+                else
+                    xr = hist_in ? (double)hist_in[(3 + r) * Cw + c] : 0.0;
+                x += (double)conv_w[c * 4 + j] * xr;
+            }
+            u[c] = act ? x / (1.0 + exp(-x)) : x;
+        }
+        for (int kh = 0; kh < n_kh; ++kh) {
+            const double* uq = u + (int64_t)kh * d;
+            const double* uk = u + (int64_t)(n_kh + kh) * d;
+            double sq = 0.0, sk = 0.0;
+            for (int i = 0; i < d; ++i) {
+                sq += uq[i] * uq[i];
+                sk += uk[i] * uk[i];
+            }
+            const double nq = sqrt(sq + eps) * sqrt((double)d), nk = sqrt(sk + eps);
+            for (int i = 0; i < d; ++i) {
+                q[(t * n_kh + kh) * d + i] = uq[i] / nq;
+                k[(t * n_kh + kh) * d + i] = uk[i] / nk;
+            }
+        }
+        for (int h = 0; h < n_vh; ++h) {
+            const double* uv = u + (int64_t)(2 * n_kh + h) * d;
+            for (int j = 0; j < d; ++j) v[(t * n_vh + h) * d + j] = uv[j];
+            const double x = (double)a[t * n_vh + h] + (double)dt_bias[h];
+            g[t * n_vh + h] = -exp((double)A_log[h]) * oracle_softplus(x);
+            beta[t * n_vh + h] = 1.0 / (1.0 + exp(-(double)b[t * n_vh + h]));
+        }
+    }
+    free(u);
+    if (hist_out) {
+        /* row -3 + i of the next call is row T - 3 + i of this one */
+        for (int i = 0; i < 3; ++i) {
+            const int64_t r = T - 3 + i;
+            for (int64_t c = 0; c < Cw; ++c) {
+                double x;
+                if (r >= 0)
+                    x = (double)qkv[r * Cw + c];
+                else
+                    x = hist_in ? (double)hist_in[(3 + r) * Cw + c] : 0.0;
+                hist_out[i * Cw + c] = x;
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
 int oracle_max_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

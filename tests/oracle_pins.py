@@ -287,6 +287,181 @@ def pin_norm_special_cases(orc):
     assert np.all((y0 & 0x7fff) == 0)
 
 
+# ---------------- pre-stage ("Round 20 Track C Audit: gdn_pre ...", section 1) ----------------
+
+PRE = dict(n_kh=2, n_vh=6, d=8)
+
+
+def _pre_inputs(rng, T, n_kh, n_vh, d):
+    Cw = (2 * n_kh + n_vh) * d
+    f = lambda a: a.astype(np.float32)  # noqa: E731
+    return dict(qkv=f(rng.standard_normal((T, Cw))), conv_w=f(0.5 * rng.standard_normal((Cw, 4))),
+                hist=f(rng.standard_normal((3, Cw))), a=f(rng.standard_normal((T, n_vh))),
+                b=f(rng.standard_normal((T, n_vh))), A_log=f(rng.uniform(0.0, 2.7, n_vh)),
+                dt_bias=f(rng.standard_normal(n_vh)))
+
+
+def _pre(orc, x, act=1, eps=1e-6, **shape):
+    return orc.prestage(x["qkv"], x["conv_w"], x["hist"], x["a"], x["b"], x["A_log"], x["dt_bias"],
+                        shape["n_kh"], shape["n_vh"], act=act, eps=eps)
+
+
+def _taps(Cw, j):
+    w = np.zeros((Cw, 4), np.float32)
+    w[:, j] = 1.0
+    return w
+
+
+def pin_prestage_conv_library(orc):
+    """Without the activation, every v channel is the causal 4-tap convolution of
+    its column of (history, qkv): numpy.convolve of the column with the reversed
+    taps, 'valid' part, the history rows first."""
+    rng = np.random.default_rng(30)
+    T, sh = 9, PRE
+    x = _pre_inputs(rng, T, **sh)
+    out = _pre(orc, x, act=0, **sh)
+    d, n_kh, n_vh = sh["d"], sh["n_kh"], sh["n_vh"]
+    col = np.concatenate([x["hist"], x["qkv"]]).astype(np.float64)
+    for h in range(n_vh):
+        for j in range(d):
+            c = (2 * n_kh + h) * d + j
+            ref = np.convolve(col[:, c], x["conv_w"][c, ::-1].astype(np.float64), mode="valid")
+            assert np.max(np.abs(out["v"][:, h, j] - ref)) < 1e-12, (h, j)
+
+
+def pin_prestage_shift_and_identity(orc):
+    """Tap 0 alone shifts the rows by three (the history fills t < 3); tap 3
+    alone passes row t through; both exactly.  With tap 3 and no activation, k
+    is a unit vector (up to eps) parallel to the k channels of row t, and
+    q sqrt(d) likewise for the q channels."""
+    rng = np.random.default_rng(31)
+    T, sh = 7, PRE
+    d, n_kh, n_vh = sh["d"], sh["n_kh"], sh["n_vh"]
+    x = _pre_inputs(rng, T, **sh)
+    Cw = x["qkv"].shape[1]
+    col = np.concatenate([x["hist"], x["qkv"]]).astype(np.float64)
+    x["conv_w"] = _taps(Cw, 0)
+    out = _pre(orc, x, act=0, **sh)
+    assert np.array_equal(out["v"].reshape(T, -1), col[:T, 2 * n_kh * d:])
+    x["conv_w"] = _taps(Cw, 3)
+    out = _pre(orc, x, act=0, **sh)
+    assert np.array_equal(out["v"].reshape(T, -1), col[3:, 2 * n_kh * d:])
+    xq = col[3:, :n_kh * d].reshape(T, n_kh, d)
+    xk = col[3:, n_kh * d:2 * n_kh * d].reshape(T, n_kh, d)
+    for got, src, scale in ((out["q"], xq, math.sqrt(d)), (out["k"], xk, 1.0)):
+        n = np.linalg.norm(got, axis=-1) * scale
+        assert np.max(np.abs(n - 1.0)) < 1e-5
+        cos = np.einsum("tki,tki->tk", got, src) / (np.linalg.norm(got, axis=-1) * np.linalg.norm(src, axis=-1))
+        assert np.max(np.abs(cos - 1.0)) < 1e-12
+
+
+def pin_prestage_norm_eps_closed_form(orc):
+    """A k (or q) head whose only non-zero channel is c: k = c / sqrt(c^2 + eps),
+    so at c = 1e-3 and eps = 1e-6, k = 1/sqrt(2); q sqrt(d) the same."""
+    sh = dict(n_kh=1, n_vh=3, d=8)
+    d = sh["d"]
+    Cw = 5 * d
+    qkv = np.zeros((1, Cw), np.float32)
+    qkv[0, 0] = 1e-3       # q channel 0
+    qkv[0, d] = 1e-3       # k channel 0
+    x = dict(qkv=qkv, conv_w=_taps(Cw, 3), hist=None, a=np.zeros((1, 3), np.float32),
+             b=np.zeros((1, 3), np.float32), A_log=np.zeros(3, np.float32), dt_bias=np.zeros(3, np.float32))
+    out = _pre(orc, x, act=0, eps=1e-6, **sh)
+    c = float(np.float32(1e-3))
+    assert abs(out["k"][0, 0, 0] - c / math.sqrt(c * c + 1e-6)) < 1e-15
+    assert abs(out["k"][0, 0, 0] - 1.0 / math.sqrt(2.0)) < 1e-7
+    assert abs(out["q"][0, 0, 0] * math.sqrt(d) - c / math.sqrt(c * c + 1e-6)) < 1e-15
+
+
+def pin_prestage_activation_library(orc):
+    """With tap 3 alone and the activation on, v = silu(row t) = X * expit(X)
+    (scipy's logistic function) and the q, k directions follow silu too."""
+    from scipy.special import expit
+
+    rng = np.random.default_rng(32)
+    T, sh = 5, PRE
+    d, n_kh = sh["d"], sh["n_kh"]
+    x = _pre_inputs(rng, T, **sh)
+    x["conv_w"] = _taps(x["qkv"].shape[1], 3)
+    out = _pre(orc, x, act=1, **sh)
+    X = x["qkv"].astype(np.float64)
+    ref = X * expit(X)
+    assert np.max(np.abs(out["v"].reshape(T, -1) - ref[:, 2 * n_kh * d:])) < 1e-14
+    refk = ref[:, n_kh * d:2 * n_kh * d].reshape(T, n_kh, d)
+    refk = refk / np.sqrt(np.sum(refk * refk, axis=-1, keepdims=True) + 1e-6)
+    assert np.max(np.abs(out["k"] - refk)) < 1e-14
+
+
+def pin_prestage_gates_library(orc):
+    """g = -exp(A_log) softplus(a + dt_bias) and beta = sigmoid(b) against numpy's
+    logaddexp(0, x) and scipy's expit; special values: a + dt_bias = 0 gives
+    g = -exp(A_log) ln 2, b = 0 gives beta = 1/2, and g < 0 always."""
+    from scipy.special import expit
+
+    rng = np.random.default_rng(33)
+    T, sh = 6, PRE
+    x = _pre_inputs(rng, T, **sh)
+    x["a"][0] = -x["dt_bias"]
+    x["a"][1] = 40.0
+    x["a"][2] = -40.0
+    x["b"][0] = 0.0
+    out = _pre(orc, x, **sh)
+    z = x["a"].astype(np.float64) + x["dt_bias"].astype(np.float64)
+    g_ref = -np.exp(x["A_log"].astype(np.float64)) * np.logaddexp(0.0, z)
+    assert np.max(np.abs(out["g"] - g_ref) / np.abs(g_ref)) < 1e-14
+    assert np.max(np.abs(out["beta"] - expit(x["b"].astype(np.float64)))) < 1e-15
+    assert np.max(np.abs(out["g"][0] + np.exp(x["A_log"].astype(np.float64)) * math.log(2.0))) < 1e-14
+    assert np.all(out["beta"][0] == 0.5)
+    assert np.all(out["g"] < 0.0)
+
+
+def pin_prestage_history_chaining(orc):
+    """One call over T tokens equals two calls with the history carried (the
+    second call's history is the first call's last three rows), for every
+    split; the history handed on is those three rows."""
+    rng = np.random.default_rng(34)
+    T, sh = 8, PRE
+    x = _pre_inputs(rng, T, **sh)
+    full = _pre(orc, x, **sh)
+    col = np.concatenate([x["hist"], x["qkv"]]).astype(np.float64)
+    assert np.array_equal(full["hist"], col[-3:])
+    for cut in (1, 2, 3, 5):
+        xa = dict(x, qkv=x["qkv"][:cut], a=x["a"][:cut], b=x["b"][:cut])
+        oa = _pre(orc, xa, **sh)
+        xb = dict(x, qkv=x["qkv"][cut:], a=x["a"][cut:], b=x["b"][cut:], hist=oa["hist"].astype(np.float32))
+        ob = _pre(orc, xb, **sh)
+        for key in ("q", "k", "v", "g", "beta"):
+            assert np.array_equal(np.concatenate([oa[key], ob[key]]), full[key]), (cut, key)
+
+
+def pin_prestage_layout(orc):
+    """q of key head kh comes from channels kh*d.., k from (n_kh + kh)*d.., v of
+    value head h from (2 n_kh + h)*d..: with tap 3, no activation and each
+    channel block holding its own constant, every output reads its block."""
+    sh = PRE
+    d, n_kh, n_vh = sh["d"], sh["n_kh"], sh["n_vh"]
+    nb = 2 * n_kh + n_vh
+    Cw = nb * d
+    qkv = np.repeat(np.arange(1, nb + 1, dtype=np.float32), d)[None, :].copy()
+    qkv[0, ::2] *= -1.0  # not a constant vector within a head
+    x = dict(qkv=qkv, conv_w=_taps(Cw, 3), hist=None, a=np.zeros((1, n_vh), np.float32),
+             b=np.zeros((1, n_vh), np.float32), A_log=np.zeros(n_vh, np.float32),
+             dt_bias=np.zeros(n_vh, np.float32))
+    out = _pre(orc, x, act=0, eps=0.0, **sh)
+    for h in range(n_vh):
+        assert np.all(np.abs(out["v"][0, h]) == 2 * n_kh + h + 1)
+    sign = np.where(np.arange(d) % 2 == 0, -1.0, 1.0)
+    for kh in range(n_kh):
+        assert np.allclose(out["q"][0, kh] * math.sqrt(d) * math.sqrt(d), sign, rtol=0, atol=1e-14)
+        assert np.allclose(out["k"][0, kh] * math.sqrt(d), sign, rtol=0, atol=1e-14)
+    # the blocks' magnitudes reach the outputs only through v, so also check a
+    # block-dependent sign pattern: flip the k block of key head 0 only
+    qkv2 = qkv.copy()
+    qkv2[0, n_kh * d:(n_kh + 1) * d] *= -1.0
+    out2 = _pre(orc, dict(x, qkv=qkv2), act=0, eps=0.0, **sh)
+    assert np.array_equal(out2["k"][0, 0], -out["k"][0, 0]) and np.array_equal(out2["q"], out["q"])
+
+
 ALL_PINS = [
     pin_single_step_closed_form,
     pin_identity,
@@ -299,4 +474,11 @@ ALL_PINS = [
     pin_fp16_rounding,
     pin_norm_library,
     pin_norm_special_cases,
+    pin_prestage_conv_library,
+    pin_prestage_shift_and_identity,
+    pin_prestage_norm_eps_closed_form,
+    pin_prestage_activation_library,
+    pin_prestage_gates_library,
+    pin_prestage_history_chaining,
+    pin_prestage_layout,
 ]

@@ -43,3 +43,21 @@ def test_prefix_property():
     for key in ("q", "k", "v", "g", "beta", "z"):
         assert np.array_equal(a[key], b[key][:40]), key
     assert np.array_equal(a["S0"], b["S0"]) and np.array_equal(a["w"], b["w"])
+
+
+def test_prestage_inputs_shapes_and_prefix():
+    from linear_attention_recurrence_gb300.inputs import make_prestage_inputs
+
+    a = make_prestage_inputs(40, seed=3, n_kh=2, n_vh=6, d=8)
+    b = make_prestage_inputs(25, seed=3, n_kh=2, n_vh=6, d=8)
+    cw = (2 * 2 + 6) * 8
+    assert a["qkv"].shape == (40, cw) and a["conv_w"].shape == (cw, 4) and a["conv_hist"].shape == (3, cw)
+    assert a["a"].shape == (40, 6) and a["A_log"].shape == (6,) and a["dt_bias"].shape == (6,)
+    assert all(v.dtype == np.float32 for v in a.values())
+    for key in ("qkv", "a", "b"):
+        assert np.array_equal(a[key][:25], b[key])
+    assert np.all(np.abs(a["conv_w"]) <= 0.5)
+    A = np.exp(a["A_log"].astype(np.float64))
+    assert np.all((A >= 1.0 - 1e-5) & (A <= 16.0 + 1e-4))
+    dt = np.logaddexp(0.0, a["dt_bias"].astype(np.float64))  # softplus(dt_bias) = dt
+    assert np.all((dt > 0.9e-3) & (dt < 0.11))

@@ -37,6 +37,21 @@ MUTANTS = [
     ("norm_sigmoid_gate", "const double silu = zj / (1.0 + exp(-zj));",
      "const double silu = 1.0 / (1.0 + exp(-zj));", 0),
     ("norm_drop_weight", "orow[j] * rs * (double)w[j] * silu", "orow[j] * rs * silu", 0),
+    ("pre_taps_reversed", "x += (double)conv_w[c * 4 + j] * xr;", "x += (double)conv_w[c * 4 + (3 - j)] * xr;", 0),
+    ("pre_drop_history", "xr = hist_in ? (double)hist_in[(3 + r) * Cw + c] : 0.0;", "xr = 0.0;", 0),
+    ("pre_history_order", "hist_in[(3 + r) * Cw + c]", "hist_in[(-1 - r) * Cw + c]", 0),
+    ("pre_q_no_scale", "sqrt(sq + eps) * sqrt((double)d)", "sqrt(sq + eps)", 0),
+    ("pre_k_scaled", "nk = sqrt(sk + eps);", "nk = sqrt(sk + eps) * sqrt((double)d);", 0),
+    ("pre_drop_eps", "nk = sqrt(sk + eps);", "nk = sqrt(sk);", 0),
+    ("pre_silu_as_sigmoid", "u[c] = act ? x / (1.0 + exp(-x)) : x;", "u[c] = act ? 1.0 / (1.0 + exp(-x)) : x;", 0),
+    ("pre_gate_sign", "g[t * n_vh + h] = -exp(", "g[t * n_vh + h] = exp(", 0),
+    ("pre_gate_no_exp", "-exp((double)A_log[h])", "-((double)A_log[h])", 0),
+    ("pre_gate_drop_bias", "(double)a[t * n_vh + h] + (double)dt_bias[h]", "(double)a[t * n_vh + h]", 0),
+    ("pre_beta_tanh", "1.0 / (1.0 + exp(-(double)b[t * n_vh + h]))", "tanh((double)b[t * n_vh + h])", 0),
+    ("pre_k_from_q", "const double* uk = u + (int64_t)(n_kh + kh) * d;", "const double* uk = u + (int64_t)kh * d;", 0),
+    ("pre_v_offset", "u + (int64_t)(2 * n_kh + h) * d", "u + (int64_t)(n_kh + h) * d", 0),
+    ("pre_hist_out_shift", "const int64_t r = T - 3 + i;", "const int64_t r = T - 4 + i;", 0),
+    ("pre_softplus_as_exp", "return (x > 0.0 ? x : 0.0) + log1p(exp(-fabs(x)));", "return exp(x);", 0),
 ]
 
 
