@@ -348,6 +348,67 @@ def run_decode(args):
     return 0
 
 
+def run_prestage(args):
+    """The pre-stage over T tokens of one layer in one call (causal conv of the
+    packed qkv rows, SiLU, q/k L2 norms, gates).  HBM-bound: reads every qkv row
+    once (plus three halo rows per 64-token run, mostly from L2) and writes q, k,
+    v, g, beta once."""
+    import torch
+
+    from linear_attention_recurrence_gb300 import build, gdn
+    from linear_attention_recurrence_gb300.inputs import make_prestage_inputs
+
+    build.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    T = args.tokens
+    x = make_prestage_inputs(T, seed=0)
+    t = {k: torch.from_numpy(v).to(dev) for k, v in x.items()}
+    cw = t["qkv"].shape[1]
+    hist_out = torch.empty((3, cw), device=dev)
+    res = gdn.gdn_prestage(t["qkv"], t["conv_w"], t["a"], t["b"], t["A_log"], t["dt_bias"], N_KH, N_VH,
+                           hist_in=t["conv_hist"], hist_out=hist_out)
+    step = lambda: gdn.gdn_prestage(t["qkv"], t["conv_w"], t["a"], t["b"], t["A_log"], t["dt_bias"],  # noqa: E731
+                                    N_KH, N_VH, hist_in=t["conv_hist"], hist_out=hist_out, out=res)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    # enough steps for about a second of timed work, so the clock sampler sees it
+    t0 = time.time()
+    for _ in range(10):
+        step()
+    torch.cuda.synchronize()
+    steps = max(args.steps, int(1.0 / max((time.time() - t0) / 10, 1e-6)))
+    n0 = gdn.gdn_launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks(dev.index) as clk:
+        time.sleep(0.5)
+        wall0 = time.time()
+        e0.record()
+        for _ in range(steps):
+            step()
+        e1.record()
+        torch.cuda.synchronize()
+        clk.mark(wall0, time.time())
+        time.sleep(0.1)
+    ms = e0.elapsed_time(e1) / steps
+    hbm_gbs, _, peak_src = _peaks()
+    bytes_tok = 2 * cw * 4 + 4 * N_VH * 4  # qkv in, q/k/v out; a, b in, g, beta out
+    gbs = bytes_tok * T / (ms * 1e-3) / 1e9
+    line = {"metric": "GDN pre-stage µs/token/layer (conv + norms + gates, 48 vh, d=128) and % of HBM roofline",
+            "value": ms * 1e3 / T, "unit": "µs/token/layer", "n_gpus": 1, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False, "dtype": "f32",
+            "data": "synthetic", "config": {"workload": f"pre-stage, 1 layer, T={T} in one call", "T": T,
+                                            "n_kh": N_KH, "n_vh": N_VH, "d": D, "activation": "silu",
+                                            "l2": f"inputs {T * cw * 4 / 1e9:.2f} GB, larger than L2"},
+            "gpu_launches": gdn.gdn_launch_count() - n0,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_gbs, "unit": "GB/s", "frac": gbs / hbm_gbs,
+                         "peak_basis": f"{peak_src} copy bandwidth", "bytes_per_token": bytes_tok,
+                         "traffic": captured_traffic("gdn_prestage.cu") if T == 32768 else None},
+            "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def _config(args):
     return {"workload": f"gdn-prefill 1 layer, T={args.tokens} as {args.tokens // args.call_tokens} calls of "
                         f"{args.call_tokens} with the state carried, then the FP16 norm",
@@ -368,6 +429,8 @@ def main():
     ap.add_argument("--call-tokens", type=int, default=2048)
     ap.add_argument("--skip-cpu", action="store_true", help="no oracle timing")
     ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--prestage", action="store_true",
+                    help="time the pre-stage (conv + norms + gates) over --tokens tokens in one call")
     ap.add_argument("--e2e-copy-streams", type=int, default=1,
                     help="host-to-device copy streams of the pipelined end-to-end step")
     ap.add_argument("--skip-other-mode", action="store_true")
@@ -381,6 +444,8 @@ def main():
     args = ap.parse_args()
     if args.sweep:
         return run_sweep(args)
+    if args.prestage:
+        return run_prestage(args)
     if args.decode:
         return run_decode(args)
     if args.stack:

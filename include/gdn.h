@@ -13,6 +13,9 @@
  *           recurrence in 32-token chunks" - section "What it does" (the 32-token
  *           WY form, 2048-token super-blocks, the per-device scratch kept between
  *           calls).
+ *   [R20C]  "Round 20 Track C Audit: gdn_pre Key-Head t >= 3 Vectorized conv_w
+ *           Fast Path + gdn_scan_r ..." - section 1 "Summary of Changes" (the
+ *           pre-stage's causal convolution over the packed qkv rows).
  *
  * Layout (all tensors dense, row-major, contiguous, FP32 unless stated):
  *   q, k        [T][n_kh][d]      query / key rows per key head
@@ -98,6 +101,40 @@ int gdn_recurrence(const float* q, const float* k, const float* v,
                    float* state_inout, float* out,
                    int64_t T, int n_kh, int n_vh, int d, int mode,
                    void* cuda_stream);
+
+/*
+ * gdn_prestage - the recurrence's inputs from a layer's projections ([R20C]
+ * section 1: a 4-tap causal convolution per channel over the packed qkv rows,
+ * q of key head kh at channels kh*d, k at (n_kh + kh)*d, v of value head h at
+ * (2 n_kh + h)*d).  With Cw = (2 n_kh + n_vh) d channels per row, per token t and
+ * channel c:
+ *     x_c = sum_{j=0..3} conv_w[c][j] X[t-3+j][c]    (X[-3..-1] = conv_hist_in)
+ *     u_c = activation ? x_c / (1 + exp(-x_c)) : x_c
+ *     q[t][kh] = u_q / sqrt(|u_q|^2 + eps) / sqrt(d);   k[t][kh] = u_k / sqrt(|u_k|^2 + eps)
+ *     v[t][h]  = u_v
+ *     g[t][h]  = -exp(A_log[h]) log(1 + exp(a[t][h] + dt_bias[h]));   beta[t][h] = 1 / (1 + exp(-b[t][h]))
+ * The outputs are gdn_recurrence's q, k, v, g, beta in its layout.  The
+ * activation, eps, the 1/sqrt(d) on q and the gate formula are readings: the page
+ * names the convolution and the outputs only.
+ *
+ *   qkv [T][Cw], conv_w [Cw][4] (tap j multiplies row t-3+j), a, b [T][n_vh],
+ *   A_log, dt_bias [n_vh]: inputs.  conv_hist_in [3][Cw]: the three rows before
+ *   this call (oldest first), or NULL at the start of a sequence (zeros).
+ *   conv_hist_out [3][Cw] or NULL: receives the last three rows of (conv_hist_in,
+ *   qkv), the conv_hist_in of the next call; it must not overlap conv_hist_in.
+ *   q, k [T][n_kh][d], v [T][n_vh][d], g, beta [T][n_vh]: outputs.
+ *   activation: 1 (SiLU) or 0; eps >= 0.
+ * Alignment: qkv, conv_w, the histories, q, k, v 16 bytes; the rest 4 bytes.
+ * No output may overlap an input or another output.  d == 128 only.  T == 0
+ * only copies the history (if conv_hist_out is given).  A sequence split over
+ * calls with the history carried gives the same bits as one call.
+ */
+int gdn_prestage(const float* qkv, const float* conv_w,
+                 const float* conv_hist_in, float* conv_hist_out,
+                 const float* a, const float* b, const float* A_log, const float* dt_bias,
+                 float* q, float* k, float* v, float* g, float* beta,
+                 int64_t T, int n_kh, int n_vh, int d, int activation, float eps,
+                 void* cuda_stream);
 
 /*
  * gdn_decode - one token of the recurrence for each of `batch` independent

@@ -3,6 +3,7 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <cmath>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -319,6 +320,54 @@ int gdn_recurrence(const float* q, const float* k, const float* v, const float* 
         if (e != cudaSuccess) return cuda_fail(e, "chunk scan launch");
         g_launches.fetch_add(1);
     }
+    return GDN_OK;
+}
+
+int gdn_prestage(const float* qkv, const float* conv_w, const float* conv_hist_in, float* conv_hist_out,
+                 const float* a, const float* b, const float* A_log, const float* dt_bias, float* q, float* k,
+                 float* v, float* g, float* beta, int64_t T, int n_kh, int n_vh, int d, int activation, float eps,
+                 void* cuda_stream) {
+    using namespace gdn;
+    if (T < 0) return fail(GDN_ERR_INVALID_ARG, "T < 0");
+    if (n_kh <= 0 || n_vh <= 0 || d <= 0) return fail(GDN_ERR_INVALID_ARG, "n_kh, n_vh and d must be positive");
+    if (activation != 0 && activation != 1) return fail(GDN_ERR_INVALID_ARG, "activation must be 0 or 1");
+    if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(GDN_ERR_INVALID_ARG, "eps must be finite and >= 0");
+    if (d != kD) return fail(GDN_ERR_UNSUPPORTED, "only d == 128 is supported");
+    if (T > (int64_t{1} << 40)) return fail(GDN_ERR_UNSUPPORTED, "T too large");
+    const int64_t cw = static_cast<int64_t>(2 * n_kh + n_vh) * d;
+    if (T > 0 && (!qkv || !a || !b || !q || !k || !v || !g || !beta))
+        return fail(GDN_ERR_INVALID_ARG, "null pointer");
+    if (!conv_w || !A_log || !dt_bias) return fail(GDN_ERR_INVALID_ARG, "null pointer");
+    const void* a16[] = {qkv, conv_w, conv_hist_in, conv_hist_out, q, k, v};
+    for (const void* ptr : a16)
+        if (ptr && !aligned(ptr, 16))
+            return fail(GDN_ERR_INVALID_ARG, "qkv, conv_w, the histories, q, k and v must be 16-byte aligned");
+    const void* a4[] = {a, b, A_log, dt_bias, g, beta};
+    for (const void* ptr : a4)
+        if (ptr && !aligned(ptr, 4)) return fail(GDN_ERR_INVALID_ARG, "a, b, A_log, dt_bias, g and beta must be 4-byte aligned");
+    const size_t f4 = sizeof(float);
+    const size_t row_b = static_cast<size_t>(cw) * f4, gate_b = static_cast<size_t>(T) * n_vh * f4;
+    const void* ins[] = {qkv, conv_w, conv_hist_in, a, b, A_log, dt_bias};
+    const size_t in_b[] = {static_cast<size_t>(T) * row_b, static_cast<size_t>(cw) * 4 * f4, 3 * row_b, gate_b, gate_b,
+                           n_vh * f4, n_vh * f4};
+    const void* outs[] = {q, k, v, g, beta, conv_hist_out};
+    const size_t out_b[] = {static_cast<size_t>(T) * n_kh * d * f4, static_cast<size_t>(T) * n_kh * d * f4,
+                            static_cast<size_t>(T) * n_vh * d * f4, gate_b, gate_b, 3 * row_b};
+    for (int i = 0; i < 6; ++i) {
+        if (!outs[i] || out_b[i] == 0) continue;
+        for (int j = 0; j < 7; ++j)
+            if (ins[j] && in_b[j] && overlap(outs[i], out_b[i], ins[j], in_b[j]))
+                return fail(GDN_ERR_INVALID_ARG, "an output overlaps an input");
+        for (int j = i + 1; j < 6; ++j)
+            if (outs[j] && out_b[j] && overlap(outs[i], out_b[i], outs[j], out_b[j]))
+                return fail(GDN_ERR_INVALID_ARG, "two outputs overlap");
+    }
+    if (T == 0 && !conv_hist_out) return GDN_OK;
+    PrestageParams p{qkv, conv_w, conv_hist_in, conv_hist_out, a, b, A_log, dt_bias, q, k, v, g, beta,
+                     T, cw, n_kh, n_vh, activation, eps, static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)))};
+    cudaError_t e = launch_prestage(p, static_cast<cudaStream_t>(cuda_stream));
+    if (e != cudaSuccess) return cuda_fail(e, "pre-stage launch");
+    g_launches.fetch_add(1);
     return GDN_OK;
 }
 

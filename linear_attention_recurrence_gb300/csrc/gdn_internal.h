@@ -55,6 +55,31 @@ struct DecodeParams {
 };
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s);
 
+// ---- pre-stage ----
+struct PrestageParams {
+    const float* qkv;      // [T][cw], cw = (2 n_kh + n_vh) * 128
+    const float* conv_w;   // [cw][4]
+    const float* hist_in;  // [3][cw] or nullptr (zeros)
+    float* hist_out;       // [3][cw] or nullptr
+    const float* a;        // [T][n_vh]
+    const float* b;        // [T][n_vh]
+    const float* A_log;    // [n_vh]
+    const float* dt_bias;  // [n_vh]
+    float* q;              // [T][n_kh][128]
+    float* k;              // [T][n_kh][128]
+    float* v;              // [T][n_vh][128]
+    float* g;              // [T][n_vh]
+    float* beta;           // [T][n_vh]
+    int64_t T;
+    int64_t cw;
+    int n_kh;
+    int n_vh;
+    int activation;
+    float eps;
+    float q_scale;         // 1 / sqrt(128)
+};
+cudaError_t launch_prestage(const PrestageParams& p, cudaStream_t s);
+
 // ---- output norm ----
 cudaError_t launch_out_norm(const float* out, const float* z, const float* w, float eps, uint16_t* y,
                             int64_t rows, int sm_count, cudaStream_t s);

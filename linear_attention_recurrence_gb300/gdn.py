@@ -38,7 +38,7 @@ _lib = None
 
 EXPORTS = ("gdn_recurrence", "gdn_out_norm", "gdn_last_error", "gdn_device_status",
            "gdn_release_scratch", "gdn_poison_scratch", "gdn_chunked_scratch_bytes", "gdn_launch_count",
-           "gdn_recurrence_chunked_noalloc", "gdn_decode")
+           "gdn_recurrence_chunked_noalloc", "gdn_decode", "gdn_prestage")
 
 
 class GDNError(RuntimeError):
@@ -64,6 +64,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gdn_recurrence_chunked_noalloc.restype = i32
         lib.gdn_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp]
         lib.gdn_decode.restype = i32
+        lib.gdn_prestage.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32,
+                                     ctypes.c_float, vp]
+        lib.gdn_prestage.restype = i32
         lib.gdn_out_norm.argtypes = [vp, vp, vp, ctypes.c_float, vp, i64, i32, i32, vp]
         lib.gdn_out_norm.restype = i32
         lib.gdn_last_error.argtypes = []
@@ -160,6 +163,43 @@ def gdn_decode(q, k, v, g, beta, states, out=None, stream=None):
                         B, n_kh, n_vh, d, _stream_ptr(stream))
     _check(rc)
     return out
+
+
+def gdn_prestage(qkv, conv_w, a, b, A_log, dt_bias, n_kh: int, n_vh: int, hist_in=None, hist_out=None,
+                 activation: int = 1, eps: float = 1e-6, out=None, stream=None):
+    """The pre-stage: q, k, v, g, beta for gdn_recurrence from the packed qkv
+    projections (causal 4-tap convolution, optional SiLU, q/k L2 norms, gates).
+
+    qkv: [T][(2 n_kh + n_vh) d]; conv_w: [(2 n_kh + n_vh) d][4]; a, b: [T][n_vh];
+    A_log, dt_bias: [n_vh]; hist_in / hist_out: [3][(2 n_kh + n_vh) d] or None.
+    ``out`` may hold preallocated q, k, v, g, beta tensors.  Returns the dict.
+    """
+    T, cw = qkv.shape
+    d = cw // (2 * n_kh + n_vh)
+    if d * (2 * n_kh + n_vh) != cw:
+        raise ValueError("qkv's row length is not (2 n_kh + n_vh) * d")
+    _want(qkv, "qkv", (T, cw))
+    _want(conv_w, "conv_w", (cw, 4))
+    _want(a, "a", (T, n_vh))
+    _want(b, "b", (T, n_vh))
+    _want(A_log, "A_log", (n_vh,))
+    _want(dt_bias, "dt_bias", (n_vh,))
+    for name, h in (("hist_in", hist_in), ("hist_out", hist_out)):
+        if h is not None:
+            _want(h, name, (3, cw))
+    shapes = {"q": (T, n_kh, d), "k": (T, n_kh, d), "v": (T, n_vh, d), "g": (T, n_vh), "beta": (T, n_vh)}
+    res = dict(out) if out is not None else {}
+    for name, shape in shapes.items():
+        if name not in res:
+            res[name] = torch.empty(shape, dtype=torch.float32, device=qkv.device)
+        _want(res[name], name, shape)
+    opt = lambda t: None if t is None else _ptr(t)  # noqa: E731
+    lib = load_library()
+    rc = lib.gdn_prestage(_ptr(qkv), _ptr(conv_w), opt(hist_in), opt(hist_out), _ptr(a), _ptr(b), _ptr(A_log),
+                          _ptr(dt_bias), _ptr(res["q"]), _ptr(res["k"]), _ptr(res["v"]), _ptr(res["g"]),
+                          _ptr(res["beta"]), T, n_kh, n_vh, d, int(activation), float(eps), _stream_ptr(stream))
+    _check(rc)
+    return res
 
 
 def gdn_recurrence_chunked_noalloc(q, k, v, g, beta, state, out, stream=None):

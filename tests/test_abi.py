@@ -103,3 +103,55 @@ def test_binding_constants_match_the_header():
                  "GDN_ERR_ALLOC", "GDN_ERR_CUDA", "GDN_ERR_TIMEOUT"):
         m = re.search(name + r"\s*=\s*(-?\d+)", src)
         assert m and int(m.group(1)) == getattr(gdn, name), name
+
+
+def test_prestage_host_side_validation(lib):
+    from linear_attention_recurrence_gb300 import gdn
+
+    nil = ctypes.c_void_p(0)
+    P = ctypes.c_void_p
+    f = lib.gdn_prestage
+
+    def call(T=5, n_kh=16, n_vh=48, d=128, act=1, eps=1e-6, ptrs=None):
+        ptrs = ptrs if ptrs is not None else [nil] * 13
+        return f(*ptrs, T, n_kh, n_vh, d, act, eps, nil)
+
+    assert call(T=-1) == gdn.GDN_ERR_INVALID_ARG
+    assert call(n_kh=0) == gdn.GDN_ERR_INVALID_ARG
+    assert call(act=2) == gdn.GDN_ERR_INVALID_ARG
+    assert call(eps=-1.0) == gdn.GDN_ERR_INVALID_ARG
+    assert call(eps=float("inf")) == gdn.GDN_ERR_INVALID_ARG
+    assert call(d=64) == gdn.GDN_ERR_UNSUPPORTED
+    assert call() == gdn.GDN_ERR_INVALID_ARG and "null" in lib.gdn_last_error().decode()
+    # addresses are never dereferenced: every call below fails its checks first
+    T, nkh, nvh, d = 4, 16, 48, 128
+    cw = (2 * nkh + nvh) * d
+    base = 1 << 24
+    qkv = base
+    cwt = qkv + T * cw * 4
+    a = cwt + cw * 16
+    b = a + 4096
+    al = b + 4096
+    dt = al + 4096
+    q = dt + 4096
+    k = q + T * nkh * d * 4
+    v = k + T * nkh * d * 4
+    g = v + T * nvh * d * 4
+    be = g + 4096
+    good = [P(qkv), P(cwt), nil, nil, P(a), P(b), P(al), P(dt), P(q), P(k), P(v), P(g), P(be)]
+    bad = list(good)
+    bad[8] = P(q + 4)  # q not 16-byte aligned
+    assert call(T=T, ptrs=bad) == gdn.GDN_ERR_INVALID_ARG and "aligned" in lib.gdn_last_error().decode()
+    bad = list(good)
+    bad[10] = P(qkv + 256)  # v inside qkv
+    assert call(T=T, ptrs=bad) == gdn.GDN_ERR_INVALID_ARG and "overlap" in lib.gdn_last_error().decode()
+    bad = list(good)
+    bad[11] = P(v + 512)  # g inside v
+    assert call(T=T, ptrs=bad) == gdn.GDN_ERR_INVALID_ARG and "overlap" in lib.gdn_last_error().decode()
+    bad = list(good)
+    bad[2] = P(base + (1 << 26))
+    bad[3] = P(base + (1 << 26) + 16)  # history out overlapping history in
+    assert call(T=T, ptrs=bad) == gdn.GDN_ERR_INVALID_ARG and "overlap" in lib.gdn_last_error().decode()
+    # T == 0 without a history to hand on: a no-op
+    zero = [nil, P(cwt), nil, nil, nil, nil, P(al), P(dt), nil, nil, nil, nil, nil]
+    assert call(T=0, ptrs=zero) == gdn.GDN_OK
