@@ -429,6 +429,8 @@ def main():
     ap.add_argument("--call-tokens", type=int, default=2048)
     ap.add_argument("--skip-cpu", action="store_true", help="no oracle timing")
     ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--overlap-norm", type=int, default=1,
+                    help="1: norm each call's rows on a second stream beside the next call (timed step and e2e)")
     ap.add_argument("--prestage", action="store_true",
                     help="time the pre-stage (conv + norms + gates) over --tokens tokens in one call")
     ap.add_argument("--e2e-copy-streams", type=int, default=1,
@@ -482,7 +484,27 @@ def main():
     stream = torch.cuda.current_stream()
     torch.cuda.synchronize()
 
+    norm_stream = torch.cuda.Stream(dev)
+
+    def overlapped_step(mode):
+        """The same work as step(): each call's rows are normed on a second stream as
+        soon as that call has finished, beside the next call's recurrence (the norm
+        is HBM-bound, the recurrence ALU-bound)."""
+        state.copy_(t["S0"])
+        norm_stream.wait_stream(stream)
+        for i in range(ncalls):
+            a, b = i * CT, (i + 1) * CT
+            gdn.gdn_recurrence(t["q"][a:b], t["k"][a:b], t["v"][a:b], t["g"][a:b], t["beta"][a:b], state,
+                               out=out[a:b], mode=mode, stream=stream)
+            done = torch.cuda.Event()
+            done.record(stream)
+            norm_stream.wait_event(done)
+            gdn.gdn_out_norm(out[a:b], t["z"][a:b], t["w"], 1e-6, y=y[a:b], stream=norm_stream)
+        stream.wait_stream(norm_stream)
+
     def step(mode, ev=None):
+        if ev is None and args.overlap_norm:
+            return overlapped_step(mode)
         state.copy_(t["S0"])
         for i in range(ncalls):
             a, b = i * CT, (i + 1) * CT
@@ -539,7 +561,10 @@ def main():
         time.sleep(0.5)  # nvidia-smi's first samples
         main_res = timed(args.mode, args.steps, args.warmup, per_kernel=False, clk=clk)
         time.sleep(0.1)
+    y_main = y.clone()
     kern = timed(args.mode, args.steps, 1, per_kernel=True)
+    torch.cuda.synchronize()
+    assert torch.equal(y_main, y), "the overlapped step's output differs from the plain step's"
     other_res = None if args.skip_other_mode else timed(other, args.steps, 1, per_kernel=True)
     assert gdn.gdn_device_status() == gdn.GDN_OK
 
@@ -650,6 +675,8 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": _config(args),
         "tokens_per_s": T * ws / (main_res["ms_per_step"] * 1e-3),
+        "step_schedule": ("16 recurrence calls on one stream; each call's rows normed on a second stream once "
+                          "that call is done" if args.overlap_norm else "16 recurrence calls, then the norm"),
         "gpu_launches": main_res["launches"],
         "roofline": {"bound": "alu", "achieved": achieved, "peak": alu_peak_tflops, "unit": "TFLOP/s",
                      "frac": achieved / alu_peak_tflops,
