@@ -45,9 +45,14 @@ constexpr int REC_ER = kRecER;
 constexpr int PREP_THREADS = 256;
 constexpr int KP = D + 4;  // padded row stride of the k / q tiles
 
-struct PrepSmem {
-    float K[C][KP];
-    float Q[C][KP];
+// NB tile buffers: two when a CTA runs several tasks (a task's tiles load while
+// the task before computes), one for the one-task-per-CTA prep kernel.
+template <int NB>
+struct PrepSmemT {
+    float K[NB][C][KP];
+    float Q[NB][C][KP];
+    float graw[NB][kHeadsPerKey][C];
+    float braw[NB][kHeadsPerKey][C];
     float KK[C][C + 1];
     float QK[C][C + 1];
     float A[kHeadsPerKey][C][C + 1];
@@ -55,33 +60,57 @@ struct PrepSmem {
     float bet[kHeadsPerKey][C];
 };
 
-// Prep records of chunk `ci` (within the super-block) for key head `kh` and its
-// three value heads, by the CTA's PREP_THREADS threads.  Reads only q, k, g, beta;
-// ends without a barrier (the caller syncs before reusing `sm`).
-__device__ __forceinline__ void prep_task(const ChunkPrepParams& p, PrepSmem& sm, const int ci, const int kh) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+// Asynchronous copies (cp.async) of `bytes` (16 or 4) from global memory; with
+// `valid` false nothing is read and the destination is zero-filled.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src, bool valid) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(valid ? 4 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Starts the copies of chunk `ci`'s k and q rows of key head `kh` and the gates
+// of its three value heads into buffer `buf` (one commit group; rows past the
+// super-block's end are zero-filled: exactly neutral, see the file comment).
+template <class PrepSmem>
+__device__ __forceinline__ void prep_load(const ChunkPrepParams& p, PrepSmem& sm, const int buf, const int ci,
+                                          const int kh) {
+    const int tid = threadIdx.x;
     const int t0 = ci * C;
     const int n = min(C, p.n_tokens - t0);
     const int64_t tb = p.t_begin + t0;
-
     for (int idx = tid; idx < C * (D / 4); idx += PREP_THREADS) {
         const int r = idx / (D / 4), c4 = idx % (D / 4);
-        float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), qv = kv;
-        if (r < n) {
-            const int64_t off = ((tb + r) * p.n_kh + kh) * D + 4 * c4;
-            kv = __ldg(reinterpret_cast<const float4*>(p.k + off));
-            qv = __ldg(reinterpret_cast<const float4*>(p.q + off));
-        }
-        *reinterpret_cast<float4*>(&sm.K[r][4 * c4]) = kv;
-        *reinterpret_cast<float4*>(&sm.Q[r][4 * c4]) = qv;
+        const int64_t off = ((tb + min(r, n - 1)) * p.n_kh + kh) * D + 4 * c4;  // in bounds even when unused
+        cp_async16(&sm.K[buf][r][4 * c4], p.k + off, r < n);
+        cp_async16(&sm.Q[buf][r][4 * c4], p.q + off, r < n);
     }
+    if (tid < kHeadsPerKey * C) {
+        const int m = tid / C, t = tid % C;
+        const int64_t off = (tb + min(t, n - 1)) * p.n_vh + kh + m * p.n_kh;
+        cp_async4(&sm.graw[buf][m][t], p.g + off, t < n);
+        cp_async4(&sm.braw[buf][m][t], p.beta + off, t < n);
+    }
+    cp_async_commit();
+}
+
+// Prep records of chunk `ci` (within the super-block) for key head `kh` and its
+// three value heads, by the CTA's PREP_THREADS threads, from buffer `buf` (whose
+// copies the caller has waited for and made visible with a barrier).  Ends
+// without a barrier (the caller syncs before reusing `sm`).
+template <class PrepSmem>
+__device__ __forceinline__ void prep_task(const ChunkPrepParams& p, PrepSmem& sm, const int buf, const int ci,
+                                          const int kh) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    float (*const K)[KP] = sm.K[buf];
+    float (*const Q)[KP] = sm.Q[buf];
     if (warp < kHeadsPerKey) {
-        const int h = kh + warp * p.n_kh;
-        float gv = 0.f, bv = 0.f;
-        if (lane < n) {
-            gv = __ldg(p.g + (tb + lane) * p.n_vh + h);
-            bv = __ldg(p.beta + (tb + lane) * p.n_vh + h);
-        }
+        const float gv = sm.graw[buf][warp][lane], bv = sm.braw[buf][warp][lane];
         // inclusive running sum of the gate over the chunk (fixed shuffle order)
         float x = gv;
 #pragma unroll
@@ -100,11 +129,11 @@ __device__ __forceinline__ void prep_task(const ChunkPrepParams& p, PrepSmem& sm
         float kk[4] = {0.f, 0.f, 0.f, 0.f}, qk[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
         for (int c4 = 0; c4 < D / 4; ++c4) {
-            const float4 kt = *reinterpret_cast<const float4*>(&sm.K[t][4 * c4]);
-            const float4 qt = *reinterpret_cast<const float4*>(&sm.Q[t][4 * c4]);
+            const float4 kt = *reinterpret_cast<const float4*>(&K[t][4 * c4]);
+            const float4 qt = *reinterpret_cast<const float4*>(&Q[t][4 * c4]);
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const float4 ki = *reinterpret_cast<const float4*>(&sm.K[ig + 8 * u][4 * c4]);
+                const float4 ki = *reinterpret_cast<const float4*>(&K[ig + 8 * u][4 * c4]);
                 kk[u] = fmaf(kt.x, ki.x, kk[u]);
                 kk[u] = fmaf(kt.y, ki.y, kk[u]);
                 kk[u] = fmaf(kt.z, ki.z, kk[u]);
@@ -162,7 +191,11 @@ __device__ __forceinline__ void prep_task(const ChunkPrepParams& p, PrepSmem& sm
 
 // One CTA per (chunk, key head).
 __global__ void __launch_bounds__(PREP_THREADS) gdn_chunk_prep_kernel(const ChunkPrepParams p) {
-    prep_task(p, *aligned_dynamic_smem<PrepSmem, 16>(), blockIdx.x, blockIdx.y);
+    PrepSmemT<1>& sm = *aligned_dynamic_smem<PrepSmemT<1>, 16>();
+    prep_load(p, sm, 0, blockIdx.x, blockIdx.y);
+    cp_async_wait<0>();
+    __syncthreads();
+    prep_task(p, sm, 0, blockIdx.x, blockIdx.y);
 }
 
 // ============================ scan ============================
@@ -510,11 +543,21 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) gdn_chunk_fused_kernel(const 
     const uint32_t gen = s_gen;
     const int b = static_cast<int>(blockIdx.x);
     if (b < p.n_prep) {
-        PrepSmem& sm = *aligned_dynamic_smem<PrepSmem, 1024>();
+        PrepSmemT<2>& sm = *aligned_dynamic_smem<PrepSmemT<2>, 1024>();
         const int n_kh = p.prep.n_kh;
         const int tasks = ((p.prep.n_tokens + C - 1) / C) * n_kh;
-        for (int task = b; task < tasks; task += p.n_prep) {
-            prep_task(p.prep, sm, task / n_kh, task % n_kh);
+        // software pipeline: task i computes from buffer i & 1 while task i+1's tiles load
+        if (b < tasks) prep_load(p.prep, sm, 0, b / n_kh, b % n_kh);
+        for (int task = b, i = 0; task < tasks; task += p.n_prep, ++i) {
+            const int next = task + p.n_prep;
+            if (next < tasks) {
+                prep_load(p.prep, sm, (i + 1) & 1, next / n_kh, next % n_kh);  // its buffer was freed by task i-1
+                cp_async_wait<1>();
+            } else {
+                cp_async_wait<0>();
+            }
+            __syncthreads();
+            prep_task(p.prep, sm, i & 1, task / n_kh, task % n_kh);
             fence_proxy_async_global();
             __syncthreads();
             if (tid == 0) st_release_gpu(p.flags + task, gen);
@@ -539,7 +582,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) gdn_chunk_fused_kernel(const 
 int chunk_scan_box_cols() { return NC; }
 
 cudaError_t launch_chunk_prep(const ChunkPrepParams& p, cudaStream_t s) {
-    const size_t smem = sizeof(PrepSmem) + 16;
+    const size_t smem = sizeof(PrepSmemT<1>) + 16;
     cudaError_t e = set_smem_once(reinterpret_cast<const void*>(gdn_chunk_prep_kernel), static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     dim3 grid((p.n_tokens + C - 1) / C, p.n_kh);
@@ -553,7 +596,7 @@ int chunk_fused_prep_ctas(int n_kh, int sm_count) {
 }
 
 cudaError_t launch_chunk_fused(const ChunkFusedParams& p, cudaStream_t s) {
-    constexpr size_t body = sizeof(ScanSmem) > sizeof(PrepSmem) ? sizeof(ScanSmem) : sizeof(PrepSmem);
+    constexpr size_t body = sizeof(ScanSmem) > sizeof(PrepSmemT<2>) ? sizeof(ScanSmem) : sizeof(PrepSmemT<2>);
     const size_t smem = body + 1024;
     cudaError_t e = set_smem_once(reinterpret_cast<const void*>(gdn_chunk_fused_kernel), static_cast<int>(smem));
     if (e != cudaSuccess) return e;
