@@ -429,8 +429,10 @@ def main():
     ap.add_argument("--call-tokens", type=int, default=2048)
     ap.add_argument("--skip-cpu", action="store_true", help="no oracle timing")
     ap.add_argument("--skip-e2e", action="store_true")
-    ap.add_argument("--overlap-norm", type=int, default=1,
-                    help="1: norm each call's rows on a second stream beside the next call (timed step and e2e)")
+    ap.add_argument("--step-api", choices=["fused", "overlap", "plain"], default="overlap",
+                    help="timed step: fused = gdn_recurrence_norm per call (the norm inside the recurrence's "
+                         "launch); overlap = each call's rows normed on a second stream; plain = the calls, then "
+                         "one norm")
     ap.add_argument("--prestage", action="store_true",
                     help="time the pre-stage (conv + norms + gates) over --tokens tokens in one call")
     ap.add_argument("--e2e-copy-streams", type=int, default=1,
@@ -502,8 +504,20 @@ def main():
             gdn.gdn_out_norm(out[a:b], t["z"][a:b], t["w"], 1e-6, y=y[a:b], stream=norm_stream)
         stream.wait_stream(norm_stream)
 
+    def fused_step(mode):
+        """The same work as step(), each call through gdn_recurrence_norm: the
+        recurrence and the norm of its rows in one call (in chunked mode, inside the
+        one launch)."""
+        state.copy_(t["S0"])
+        for i in range(ncalls):
+            a, b = i * CT, (i + 1) * CT
+            gdn.gdn_recurrence_norm(t["q"][a:b], t["k"][a:b], t["v"][a:b], t["g"][a:b], t["beta"][a:b], state,
+                                    t["z"][a:b], t["w"], 1e-6, out=out[a:b], y=y[a:b], mode=mode, stream=stream)
+
     def step(mode, ev=None):
-        if ev is None and args.overlap_norm:
+        if ev is None and args.step_api == "fused":
+            return fused_step(mode)
+        if ev is None and args.step_api == "overlap":
             return overlapped_step(mode)
         state.copy_(t["S0"])
         for i in range(ncalls):
@@ -675,8 +689,10 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": _config(args),
         "tokens_per_s": T * ws / (main_res["ms_per_step"] * 1e-3),
-        "step_schedule": ("16 recurrence calls on one stream; each call's rows normed on a second stream once "
-                          "that call is done" if args.overlap_norm else "16 recurrence calls, then the norm"),
+        "step_schedule": {"fused": "16 gdn_recurrence_norm calls (recurrence + norm of the call's rows)",
+                          "overlap": "16 recurrence calls on one stream; each call's rows normed on a second "
+                                     "stream once that call is done",
+                          "plain": "16 recurrence calls, then the norm"}[args.step_api],
         "gpu_launches": main_res["launches"],
         "roofline": {"bound": "alu", "achieved": achieved, "peak": alu_peak_tflops, "unit": "TFLOP/s",
                      "frac": achieved / alu_peak_tflops,

@@ -164,6 +164,24 @@ int gdn_out_norm(const float* out, const float* z, const float* w, float eps,
                  uint16_t* y_fp16, int64_t T, int n_vh, int d, void* cuda_stream);
 
 /*
+ * gdn_recurrence_norm - gdn_recurrence followed by gdn_out_norm of its output, in
+ * one call: out (FP32, written as by gdn_recurrence) and y_fp16 (the same bits
+ * gdn_out_norm would give for that out).  The norm of each 2048-token
+ * super-block is launched after its recurrence.  With the environment variable
+ * GDN_FUSED_NORM=1 and the one-launch chunked form, the norm instead runs inside
+ * that launch, on the SMs that prepare the chunks, as the scan finishes each
+ * (chunk, key head), reading the output back from L2 (same bits; on GB300 slower,
+ * those SMs cannot stream the norm's traffic as fast as the scan produces it).
+ * Arguments as the two calls'; y_fp16 may overlap no other argument.
+ */
+int gdn_recurrence_norm(const float* q, const float* k, const float* v,
+                        const float* g, const float* beta,
+                        float* state_inout, float* out,
+                        const float* z, const float* w, float eps, uint16_t* y_fp16,
+                        int64_t T, int n_kh, int n_vh, int d, int mode,
+                        void* cuda_stream);
+
+/*
  * gdn_recurrence_chunked_noalloc - gdn_recurrence(..., GDN_CHUNKED, ...) without
  * any device allocation.  The pages have no counterpart to this entry point.
  *

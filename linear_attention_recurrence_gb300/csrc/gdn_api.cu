@@ -29,6 +29,7 @@ struct DeviceState {
     size_t scratch_bytes = 0;
     uint32_t* flags = nullptr; // one-launch chunked form: per-(chunk, key head) flags, then 2 sync words
     uint32_t* sync = nullptr;
+    uint32_t* out_flags = nullptr;
 };
 DeviceState g_dev[kMaxDevices];
 
@@ -102,12 +103,14 @@ size_t scratch_bytes_for(int n_vh) {
 
 // Flag words of the one-launch chunked form for up to n_vh key heads (n_kh <= n_vh).
 size_t flag_words_for(int n_vh) { return static_cast<size_t>(gdn::kChunksPerSuperBlock) * n_vh; }
+// Output flags of the one-launch form with the norm: [chunk][key head][8 scan CTAs] (n_kh <= n_vh).
+size_t out_flag_words_for(int n_vh) { return static_cast<size_t>(gdn::kChunksPerSuperBlock) * n_vh * 8; }
 
 void free_scratch(DeviceState* d) {
     cudaFree(d->scratch);
     cudaFree(d->flags);
     d->scratch = nullptr;
-    d->flags = d->sync = nullptr;
+    d->flags = d->sync = d->out_flags = nullptr;
     d->scratch_bytes = 0;
 }
 
@@ -125,7 +128,7 @@ int ensure_scratch(DeviceState* d, int n_vh) {
     }
     void* p = nullptr;
     void* f = nullptr;
-    const size_t flag_bytes = (flag_words_for(n_vh) + gdn::kSyncWords) * sizeof(uint32_t);
+    const size_t flag_bytes = (flag_words_for(n_vh) + out_flag_words_for(n_vh) + gdn::kSyncWords) * sizeof(uint32_t);
     cudaError_t e = cudaMalloc(&p, need);
     if (e == cudaSuccess) {
         e = cudaMalloc(&f, flag_bytes);
@@ -139,7 +142,8 @@ int ensure_scratch(DeviceState* d, int n_vh) {
     d->scratch = static_cast<float*>(p);
     d->scratch_bytes = need;
     d->flags = static_cast<uint32_t*>(f);
-    d->sync = d->flags + flag_words_for(n_vh);
+    d->out_flags = d->flags + flag_words_for(n_vh);
+    d->sync = d->out_flags + out_flag_words_for(n_vh);
     // zero flags and generation before any stream (blocking or not) can use them
     e = cudaMemset(f, 0, flag_bytes);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -153,6 +157,16 @@ int ensure_scratch(DeviceState* d, int n_vh) {
 // The chunked form runs prep and scan in one launch unless the environment sets
 // GDN_CHUNK_OVERLAP=0 or selects the tensor-core scan (GDN_CHUNK_SCAN=tc), both
 // for A/B measurements; read on every call.
+// gdn_recurrence_norm runs the norm inside the one-launch chunked kernel (on the
+// prep CTAs, as the scan finishes each chunk) only when GDN_FUSED_NORM=1: on GB300
+// those 24 SMs cannot stream the norm's traffic as fast as the scan produces it
+// (measured 562 vs 362 us per 2048-token call), so by default the norm is a
+// launch of its own after the recurrence.  Read on every call.
+bool fused_norm_enabled() {
+    const char* v = std::getenv("GDN_FUSED_NORM");
+    return v && std::strcmp(v, "1") == 0;
+}
+
 bool fused_chunk_launch_enabled() {
     const char* o = std::getenv("GDN_CHUNK_OVERLAP");
     if (o && std::strcmp(o, "0") == 0) return false;
@@ -207,11 +221,18 @@ int internal_fail(int code, const std::string& msg) { return fail(code, msg); }
 void internal_count_launch() { g_launches.fetch_add(1); }
 }  // namespace gdn
 
-extern "C" {
+namespace {
+// The gated RMSNorm that gdn_recurrence_norm applies to the recurrence's output.
+struct NormArgs {
+    const float* z;
+    const float* w;
+    float eps;
+    uint16_t* y;
+};
 
-int gdn_recurrence(const float* q, const float* k, const float* v, const float* g, const float* beta,
+int run_recurrence(const float* q, const float* k, const float* v, const float* g, const float* beta,
                    float* state_inout, float* out, int64_t T, int n_kh, int n_vh, int d, int mode,
-                   void* cuda_stream) {
+                   void* cuda_stream, const NormArgs* norm) {
     using namespace gdn;
     if (T < 0) return fail(GDN_ERR_INVALID_ARG, "T < 0");
     if (n_kh <= 0 || n_vh <= 0 || d <= 0) return fail(GDN_ERR_INVALID_ARG, "n_kh, n_vh and d must be positive");
@@ -263,6 +284,11 @@ int gdn_recurrence(const float* q, const float* k, const float* v, const float* 
         cudaError_t e = launch_seq(p, seq_rows_per_thread(), s);
         if (e != cudaSuccess) return cuda_fail(e, "sequential scan launch");
         g_launches.fetch_add(1);
+        if (norm) {
+            e = launch_out_norm(out, norm->z, norm->w, norm->eps, norm->y, T * n_vh, dev->sm_count, s);
+            if (e != cudaSuccess) return cuda_fail(e, "output norm launch");
+            g_launches.fetch_add(1);
+        }
         return GDN_OK;
     }
 
@@ -304,9 +330,21 @@ int gdn_recurrence(const float* q, const float* k, const float* v, const float* 
             fp.flags = dev->flags;
             fp.sync = dev->sync;
             fp.n_prep = n_prep;
+            const bool in_launch = norm && fused_norm_enabled();
+            fp.z = in_launch ? norm->z : nullptr;
+            fp.w = in_launch ? norm->w : nullptr;
+            fp.y = in_launch ? norm->y : nullptr;
+            fp.eps = in_launch ? norm->eps : 0.f;
+            fp.out_flags = dev->out_flags;
             cudaError_t e = launch_chunk_fused(fp, s);
             if (e == cudaSuccess) {
                 g_launches.fetch_add(1);
+                if (norm && !in_launch) {  // the norm of this super-block's rows after it
+                    e = launch_out_norm(out + t0 * n_vh * d, norm->z + t0 * n_vh * d, norm->w, norm->eps,
+                                        norm->y + t0 * n_vh * d, static_cast<int64_t>(n) * n_vh, dev->sm_count, s);
+                    if (e != cudaSuccess) return cuda_fail(e, "output norm launch");
+                    g_launches.fetch_add(1);
+                }
                 continue;
             }
             if (e != cudaErrorCooperativeLaunchTooLarge) return cuda_fail(e, "chunk prep+scan launch");
@@ -319,8 +357,48 @@ int gdn_recurrence(const float* q, const float* k, const float* v, const float* 
         e = launch_chunk_scan_default(sp, s);
         if (e != cudaSuccess) return cuda_fail(e, "chunk scan launch");
         g_launches.fetch_add(1);
+        if (norm) {  // the two-launch form: the norm of this super-block's rows after its scan
+            e = launch_out_norm(out + t0 * n_vh * d, norm->z + t0 * n_vh * d, norm->w, norm->eps,
+                                norm->y + t0 * n_vh * d, static_cast<int64_t>(n) * n_vh, dev->sm_count, s);
+            if (e != cudaSuccess) return cuda_fail(e, "output norm launch");
+            g_launches.fetch_add(1);
+        }
     }
     return GDN_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int gdn_recurrence(const float* q, const float* k, const float* v, const float* g, const float* beta,
+                   float* state_inout, float* out, int64_t T, int n_kh, int n_vh, int d, int mode,
+                   void* cuda_stream) {
+    return run_recurrence(q, k, v, g, beta, state_inout, out, T, n_kh, n_vh, d, mode, cuda_stream, nullptr);
+}
+
+int gdn_recurrence_norm(const float* q, const float* k, const float* v, const float* g, const float* beta,
+                        float* state_inout, float* out, const float* z, const float* w, float eps,
+                        uint16_t* y_fp16, int64_t T, int n_kh, int n_vh, int d, int mode, void* cuda_stream) {
+    using namespace gdn;
+    if (!(eps >= 0.0f) || eps != eps) return fail(GDN_ERR_INVALID_ARG, "eps must be a non-negative number");
+    if (T > 0 && n_vh > 0 && d > 0) {
+        if (!z || !w || !y_fp16) return fail(GDN_ERR_INVALID_ARG, "null pointer");
+        if (!aligned(z, 16) || !aligned(w, 16) || !aligned(y_fp16, 8))
+            return fail(GDN_ERR_INVALID_ARG, "z, w must be 16-byte and y_fp16 8-byte aligned");
+        const size_t nb = static_cast<size_t>(T) * n_vh * d;
+        const size_t qk_b = static_cast<size_t>(T) * (n_kh > 0 ? n_kh : 0) * d * 4, gb_b = static_cast<size_t>(T) * n_vh * 4;
+        const void* reads[] = {q, k, v, g, beta, z, w, out, state_inout};
+        const size_t rb[] = {qk_b, qk_b, nb * 4, gb_b, gb_b, nb * 4, static_cast<size_t>(d) * 4, nb * 4,
+                             static_cast<size_t>(n_vh) * d * d * 4};
+        for (int i = 0; i < 9; ++i)
+            if (reads[i] && overlap(y_fp16, nb * 2, reads[i], rb[i]))
+                return fail(GDN_ERR_INVALID_ARG, "y_fp16 overlaps another argument");
+        if (overlap(z, nb * 4, out, nb * 4) || overlap(z, nb * 4, state_inout, static_cast<size_t>(n_vh) * d * d * 4) ||
+            overlap(w, static_cast<size_t>(d) * 4, out, nb * 4))
+            return fail(GDN_ERR_INVALID_ARG, "out / state_inout overlap an input");
+    }
+    const NormArgs na{z, w, eps, y_fp16};
+    return run_recurrence(q, k, v, g, beta, state_inout, out, T, n_kh, n_vh, d, mode, cuda_stream, &na);
 }
 
 int gdn_prestage(const float* qkv, const float* conv_w, const float* conv_hist_in, float* conv_hist_out,
@@ -463,7 +541,7 @@ int gdn_release_scratch(int device) {
     cudaError_t e2 = cudaFree(d.flags);
     cudaSetDevice(cur);
     d.scratch = nullptr;
-    d.flags = d.sync = nullptr;
+    d.flags = d.sync = d.out_flags = nullptr;
     d.scratch_bytes = 0;
     if (e != cudaSuccess) return cuda_fail(e, "cudaFree");
     if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFree");

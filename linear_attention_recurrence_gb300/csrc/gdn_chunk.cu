@@ -29,6 +29,7 @@
 // TF32 tensor-core inputs there.
 #include "gdn_device.cuh"
 #include "gdn_internal.h"
+#include "gdn_norm_row.cuh"
 
 namespace gdn {
 namespace {
@@ -235,7 +236,8 @@ __device__ __forceinline__ int swz(int r, int cc) { return r * 128 + ((cc ^ (r &
 // the chunk loop (a thread that gave up computes on whatever landed), so the
 // CTA's barriers stay matched and the CTA ends.
 __device__ __forceinline__ void scan_body(const ChunkScanParams& p, ScanSmem& sm, const int kh, const int c0,
-                                          const uint32_t* flags, uint32_t* diag, const uint32_t gen) {
+                                          const uint32_t* flags, uint32_t* diag, const uint32_t gen,
+                                          uint32_t* out_flags = nullptr) {
     const int tid = threadIdx.x;
     const int n_kh = p.n_kh, n_vh = p.n_vh;
     const int nch = (p.n_tokens + C - 1) / C;
@@ -391,6 +393,8 @@ __device__ __forceinline__ void scan_body(const ChunkScanParams& p, ScanSmem& sm
                 issue_tiles(c + 1);
                 if (!flags) issue_records(c + 1);
             }
+            // chunk c-1's outputs are stored (barriers since): tell its norm
+            if (lane == 0 && out_flags && c > 0) st_release_gpu(out_flags + ((c - 1) * n_kh + kh) * 8 + c0 / NC, gen);
             __syncwarp();
         }
         if (tid < kHeadsPerKey * 64) {
@@ -503,6 +507,7 @@ __device__ __forceinline__ void scan_body(const ChunkScanParams& p, ScanSmem& sm
     }
 
     // (the loop ended on a barrier, so copy_gave_up and flag_gave_up are final here)
+    if (out_flags && tid == SCAN_THREADS - 32) st_release_gpu(out_flags + ((nch - 1) * n_kh + kh) * 8 + c0 / NC, gen);
     if (sm.copy_gave_up) {
         const int cf = sm.copy_gave_up - 1;  // the one chunk whose copies may still be landing
         if (tid == 0) mbar_wait(&sm.full[cf & 1], static_cast<uint32_t>((cf >> 1) & 1));
@@ -523,6 +528,60 @@ __device__ __forceinline__ void scan_body(const ChunkScanParams& p, ScanSmem& sm
 // One CTA per (key head, 16 value columns); the prep kernel has run before.
 __global__ void __launch_bounds__(SCAN_THREADS, 1) gdn_chunk_scan_kernel(const __grid_constant__ ChunkScanParams p) {
     scan_body(p, *aligned_dynamic_smem<ScanSmem, 1024>(), blockIdx.x, blockIdx.y * NC, nullptr, nullptr, 0u);
+}
+
+// 16-byte load through L2 only: out is written by other CTAs of the same launch.
+__device__ __forceinline__ float4 ld_cg4(const float* ptr) {
+    float4 r;
+    asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w) : "l"(ptr));
+    return r;
+}
+
+// The norm of the super-block's outputs by one prep CTA: units (chunk c, key head
+// kh) = b, b + n_prep, ... in chunk order; a unit waits until the 8 scan CTAs of
+// kh have published chunk c, then norms its 3 heads x (up to) 32 token rows, one
+// warp per row (12 rows per warp, six loaded at a time).
+__device__ __forceinline__ void norm_units(const ChunkFusedParams& p, const int b, const uint32_t gen) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int n_kh = p.scan.n_kh, n_vh = p.scan.n_vh;
+    const int nch = (p.scan.n_tokens + C - 1) / C;
+    const float4 w4 = __ldg(reinterpret_cast<const float4*>(p.w) + lane);
+    for (int u = b; u < nch * n_kh; u += p.n_prep) {
+        const int c = u / n_kh, kh = u % n_kh;
+        if (warp == 0) {
+            uint32_t seen = 0;
+            bool ok = true;
+            if (lane < 8) ok = wait_flag(p.out_flags + (c * n_kh + kh) * 8 + lane, gen, &seen);
+            if (!ok) {
+                report_error(p.scan.status, kDevErrFlagTimeout);
+                p.sync[2] = static_cast<uint32_t>(0x80000000u | ((c * n_kh + kh) * 8 + lane));
+                p.sync[3] = seen;
+                p.sync[4] = gen;
+            }
+            __syncwarp();
+        }
+        __syncthreads();  // the acquires above order the scan CTAs' stores before every warp's loads
+        const int nt = min(C, p.scan.n_tokens - c * C);
+#pragma unroll
+        for (int pass = 0; pass < 2; ++pass) {
+            float4 ov[6], zv[6];
+            int64_t rows[6];
+#pragma unroll
+            for (int j = 0; j < 6; ++j) {
+                const int i = warp + 8 * (6 * pass + j);  // 0..95: head m = i / 32, token t = i % 32
+                const int m = i >> 5, t = i & 31;
+                rows[j] = (t < nt) ? (p.scan.t_begin + static_cast<int64_t>(c) * C + t) * n_vh + kh + m * n_kh : -1;
+                if (rows[j] >= 0) {
+                    ov[j] = ld_cg4(p.scan.out + rows[j] * D + 4 * lane);
+                    zv[j] = __ldg(reinterpret_cast<const float4*>(p.z + rows[j] * D) + lane);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 6; ++j)
+                if (rows[j] >= 0)
+                    __stcs(reinterpret_cast<uint2*>(p.y) + rows[j] * (D / 4) + lane, norm_row_lane(ov[j], zv[j], w4, p.eps));
+        }
+    }
 }
 
 // ====================== prep and scan in one launch ======================
@@ -562,10 +621,11 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) gdn_chunk_fused_kernel(const 
             __syncthreads();
             if (tid == 0) st_release_gpu(p.flags + task, gen);
         }
+        if (p.y) norm_units(p, b, gen);
     } else {
         const int s = b - p.n_prep, n_kh = p.scan.n_kh;
         scan_body(p.scan, *aligned_dynamic_smem<ScanSmem, 1024>(), s % n_kh, (s / n_kh) * NC, p.flags, p.sync + 2,
-                  gen);
+                  gen, p.y ? p.out_flags : nullptr);
     }
     __syncthreads();
     if (tid == 0) {

@@ -119,6 +119,14 @@ struct ChunkFusedParams {
     uint32_t* sync;        // [0]: generation of the last finished launch, [1]: CTAs finished so far,
                            // [2..4]: the first flag wait that ran out (index, value seen, value awaited)
     int n_prep;
+    // The gated RMSNorm of the outputs by the prep CTAs once their tasks are done,
+    // when y != nullptr (out is then read back, through L2, after the scan CTAs of a
+    // (chunk, key head) have published it in out_flags).
+    const float* z;        // [T][n_vh][128], absolute token rows like out
+    const float* w;        // [128]
+    uint16_t* y;           // [T][n_vh][128] binary16 bits
+    float eps;
+    uint32_t* out_flags;   // [kChunksPerSuperBlock][n_kh][8]: generation of each scan CTA's finished chunk
 };
 // CTAs the one-launch form gives the prep on a device with sm_count SMs, or 0
 // when too few SMs are left beside the scan (the two-launch form is used then).

@@ -11,6 +11,7 @@
 
 #include "gdn_device.cuh"
 #include "gdn_internal.h"
+#include "gdn_norm_row.cuh"
 
 namespace gdn {
 namespace {
@@ -25,8 +26,6 @@ __device__ __forceinline__ float4 ld_stream(const float* p) {
                  : "l"(p));
     return r;
 }
-
-__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
 __global__ void __launch_bounds__(kThreads, 2) gdn_out_norm_kernel(const float* __restrict__ o,
                                                                  const float* __restrict__ z,
@@ -50,21 +49,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_out_norm_kernel(const float* 
         for (int u = 0; u < kRowsInFlight; ++u) {
             const int64_t row = base + u * nwarps;
             if (row >= rows) break;  // uniform across the warp
-            float ss = ov[u].x * ov[u].x;
-            ss = fmaf(ov[u].y, ov[u].y, ss);
-            ss = fmaf(ov[u].z, ov[u].z, ss);
-            ss = fmaf(ov[u].w, ov[u].w, ss);
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-            const float r = rsqrtf(ss * (1.0f / kD) + eps);
-            const __half2 lo = __floats2half2_rn(ov[u].x * r * w4.x * silu(zv[u].x),
-                                                 ov[u].y * r * w4.y * silu(zv[u].y));
-            const __half2 hi = __floats2half2_rn(ov[u].z * r * w4.z * silu(zv[u].z),
-                                                 ov[u].w * r * w4.w * silu(zv[u].w));
-            uint2 pkd;
-            pkd.x = *reinterpret_cast<const uint32_t*>(&lo);
-            pkd.y = *reinterpret_cast<const uint32_t*>(&hi);
-            __stcs(y + row * (kD / 4) + lane, pkd);
+            __stcs(y + row * (kD / 4) + lane, norm_row_lane(ov[u], zv[u], w4, eps));
         }
     }
 }

@@ -38,7 +38,7 @@ _lib = None
 
 EXPORTS = ("gdn_recurrence", "gdn_out_norm", "gdn_last_error", "gdn_device_status",
            "gdn_release_scratch", "gdn_poison_scratch", "gdn_chunked_scratch_bytes", "gdn_launch_count",
-           "gdn_recurrence_chunked_noalloc", "gdn_decode", "gdn_prestage")
+           "gdn_recurrence_chunked_noalloc", "gdn_decode", "gdn_prestage", "gdn_recurrence_norm")
 
 
 class GDNError(RuntimeError):
@@ -67,6 +67,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gdn_prestage.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32,
                                      ctypes.c_float, vp]
         lib.gdn_prestage.restype = i32
+        lib.gdn_recurrence_norm.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, i64, i32, i32, i32,
+                                            i32, vp]
+        lib.gdn_recurrence_norm.restype = i32
         lib.gdn_out_norm.argtypes = [vp, vp, vp, ctypes.c_float, vp, i64, i32, i32, vp]
         lib.gdn_out_norm.restype = i32
         lib.gdn_last_error.argtypes = []
@@ -138,6 +141,39 @@ def gdn_recurrence(q, k, v, g, beta, state, out=None, mode="sequential", stream=
                             T, n_kh, n_vh, d, _MODES[mode], _stream_ptr(stream))
     _check(rc)
     return out
+
+
+def gdn_recurrence_norm(q, k, v, g, beta, state, z, w, eps: float = 1e-6, out=None, y=None, mode="chunked",
+                        stream=None):
+    """gdn_recurrence and gdn_out_norm of its output in one call; returns (out, y).
+
+    ``out`` ([T][n_vh][d] FP32) and ``y`` ([T][n_vh][d] float16) are allocated if
+    None.  In chunked mode the norm runs inside the recurrence's launch when the
+    one-launch form applies.
+    """
+    T, n_kh, d = q.shape
+    n_vh = v.shape[1]
+    _want(q, "q", (T, n_kh, d))
+    _want(k, "k", (T, n_kh, d))
+    _want(v, "v", (T, n_vh, d))
+    _want(g, "g", (T, n_vh))
+    _want(beta, "beta", (T, n_vh))
+    _want(state, "state", (n_vh, d, d))
+    _want(z, "z", (T, n_vh, d))
+    _want(w, "w", (d,))
+    if out is None:
+        out = torch.empty((T, n_vh, d), dtype=torch.float32, device=q.device)
+    if y is None:
+        y = torch.empty((T, n_vh, d), dtype=torch.float16, device=q.device)
+    _want(out, "out", (T, n_vh, d))
+    _want(y, "y", (T, n_vh, d), dtype=torch.float16)
+    if mode not in _MODES:
+        raise ValueError(f"unknown mode {mode!r}")
+    lib = load_library()
+    rc = lib.gdn_recurrence_norm(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state), _ptr(out), _ptr(z),
+                                 _ptr(w), float(eps), _ptr(y), T, n_kh, n_vh, d, _MODES[mode], _stream_ptr(stream))
+    _check(rc)
+    return out, y
 
 
 def gdn_decode(q, k, v, g, beta, states, out=None, stream=None):

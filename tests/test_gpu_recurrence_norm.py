@@ -1,0 +1,156 @@
+"""gdn_recurrence_norm: the recurrence and the gated RMSNorm of its output in one
+call.  Its FP32 output must be the bits gdn_recurrence gives, and its FP16 output
+the bits gdn_out_norm gives for that output, whichever way the call runs the norm
+(inside the one-launch chunked kernel, on the SMs that prepare the chunks, or as
+a launch after the recurrence); and the FP16 output within 1 ulp of the FP64 norm
+of the same FP32 output ("#413 prefill: DeltaNet recurrence with the three value
+heads of a key head in one thread", section "What changes")."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gdn_testutil import fp16_ulp_distance, to_dev
+from linear_attention_recurrence_gb300 import gdn
+from linear_attention_recurrence_gb300.inputs import make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from linear_attention_recurrence_gb300 import build
+
+    build.build()
+    oracle.build()
+
+
+def _one_launch_available():
+    return torch.cuda.get_device_properties(0).multi_processor_count >= 9 * 16
+
+
+def _bits(t):
+    return t.cpu().numpy().view(np.uint16 if t.dtype == torch.float16 else np.uint32)
+
+
+def _pair(t, T, mode):
+    """(out, y, state) from gdn_recurrence_norm and from gdn_recurrence + gdn_out_norm."""
+    st1 = t["S0"].clone()
+    n0 = gdn.gdn_launch_count()
+    out1, y1 = gdn.gdn_recurrence_norm(t["q"], t["k"], t["v"], t["g"], t["beta"], st1, t["z"], t["w"], 1e-6,
+                                       mode=mode)
+    launches = gdn.gdn_launch_count() - n0
+    st2 = t["S0"].clone()
+    out2 = gdn.gdn_recurrence(t["q"], t["k"], t["v"], t["g"], t["beta"], st2, mode=mode)
+    y2 = gdn.gdn_out_norm(out2, t["z"], t["w"], 1e-6)
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_status() == gdn.GDN_OK
+    return (out1, y1, st1), (out2, y2, st2), launches
+
+
+@pytest.mark.parametrize("mode", ["chunked", "sequential", "auto"])
+@pytest.mark.parametrize("T", [1, 33, 130, 2048, 4099])
+def test_recurrence_norm_matches_the_two_calls(mode, T):
+    t = to_dev(make_inputs(T, seed=21))
+    (o1, y1, s1), (o2, y2, s2), launches = _pair(t, T, mode)
+    assert np.array_equal(_bits(o1), _bits(o2))
+    assert np.array_equal(_bits(s1), _bits(s2))
+    assert np.array_equal(_bits(y1), _bits(y2))
+    chunked = mode == "chunked" or (mode == "auto" and T >= gdn.GDN_AUTO_CHUNKED_MIN_T)
+    if chunked and _one_launch_available():
+        assert launches == 2 * ((T + 2047) // 2048)  # one launch and its norm per super-block
+
+
+def _with_env(name, value, fn):
+    old = os.environ.get(name)
+    os.environ[name] = value
+    try:
+        return fn()
+    finally:
+        if old is None:
+            del os.environ[name]
+        else:
+            os.environ[name] = old
+
+
+@pytest.mark.parametrize("T", [1, 33, 130, 2048, 4099])
+def test_norm_inside_the_one_launch_same_bits(T):
+    """GDN_FUSED_NORM=1: the prep CTAs norm each (chunk, key head) once its 8 scan
+    CTAs have published it, inside the one launch; same bits as the two calls."""
+    if not _one_launch_available():
+        pytest.skip("too few SMs for the one-launch form")
+    t = to_dev(make_inputs(T, seed=25))
+    (o1, y1, s1), (o2, y2, s2), launches = _with_env("GDN_FUSED_NORM", "1", lambda: _pair(t, T, "chunked"))
+    assert launches == (T + 2047) // 2048
+    assert np.array_equal(_bits(o1), _bits(o2)) and np.array_equal(_bits(s1), _bits(s2))
+    assert np.array_equal(_bits(y1), _bits(y2))
+
+
+def test_recurrence_norm_within_one_ulp_of_fp64():
+    T = 777
+    x = make_inputs(T, seed=22)
+    t = to_dev(x)
+    st = t["S0"].clone()
+    out, y = gdn.gdn_recurrence_norm(t["q"], t["k"], t["v"], t["g"], t["beta"], st, t["z"], t["w"], 1e-6)
+    torch.cuda.synchronize()
+    y_ref = oracle.out_norm(out.double().cpu().numpy(), x["z"], x["w"], 1e-6)
+    assert int(fp16_ulp_distance(y.cpu().numpy().view(np.uint16), y_ref).max()) <= 1
+
+
+def test_recurrence_norm_two_launch_form_same_bits():
+    """With the one-launch form off, the norm runs after each super-block's scan:
+    same bits."""
+    T = 4099
+    t = to_dev(make_inputs(T, seed=23))
+    st = t["S0"].clone()
+    o1, y1 = gdn.gdn_recurrence_norm(t["q"], t["k"], t["v"], t["g"], t["beta"], st, t["z"], t["w"], 1e-6)
+    torch.cuda.synchronize()
+    old = os.environ.get("GDN_CHUNK_OVERLAP")
+    os.environ["GDN_CHUNK_OVERLAP"] = "0"
+    try:
+        st2 = t["S0"].clone()
+        n0 = gdn.gdn_launch_count()
+        o2, y2 = gdn.gdn_recurrence_norm(t["q"], t["k"], t["v"], t["g"], t["beta"], st2, t["z"], t["w"], 1e-6)
+        torch.cuda.synchronize()
+        assert gdn.gdn_launch_count() - n0 == 3 * 3  # prep, scan, norm per super-block
+    finally:
+        if old is None:
+            del os.environ["GDN_CHUNK_OVERLAP"]
+        else:
+            os.environ["GDN_CHUNK_OVERLAP"] = old
+    assert np.array_equal(_bits(o1), _bits(o2)) and np.array_equal(_bits(y1), _bits(y2))
+
+
+@pytest.mark.parametrize("fused", ["0", "1"])
+def test_recurrence_norm_graph_replay_with_poisoned_outputs(fused, monkeypatch):
+    """Captured once, replayed with out and y poisoned with NaN and the scratch
+    poisoned in between: every replay gives the eager bits (the output flags
+    carry the launch's generation number, so no replay norms stale rows)."""
+    monkeypatch.setenv("GDN_FUSED_NORM", fused)
+    T = 4099
+    t = to_dev(make_inputs(T, seed=24))
+    st = t["S0"].clone()
+    o_ref, y_ref = gdn.gdn_recurrence_norm(t["q"], t["k"], t["v"], t["g"], t["beta"], st, t["z"], t["w"], 1e-6)
+    torch.cuda.synchronize()
+    o_ref, y_ref = _bits(o_ref), _bits(y_ref)
+    st = t["S0"].clone()
+    out = torch.empty((T, 48, 128), device="cuda")
+    y = torch.empty((T, 48, 128), device="cuda", dtype=torch.float16)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            gdn.gdn_recurrence_norm(t["q"], t["k"], t["v"], t["g"], t["beta"], st, t["z"], t["w"], 1e-6, out=out, y=y)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        st.copy_(t["S0"])
+        out.fill_(float("nan"))
+        y.fill_(float("nan"))
+        gdn.gdn_poison_scratch(0x7FC00000)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert gdn.gdn_device_status() == gdn.GDN_OK
+        assert np.array_equal(_bits(out), o_ref) and np.array_equal(_bits(y), y_ref)
