@@ -155,3 +155,43 @@ def test_prestage_host_side_validation(lib):
     # T == 0 without a history to hand on: a no-op
     zero = [nil, P(cwt), nil, nil, nil, nil, P(al), P(dt), nil, nil, nil, nil, nil]
     assert call(T=0, ptrs=zero) == gdn.GDN_OK
+
+
+def test_recurrence_norm_host_side_validation(lib):
+    from linear_attention_recurrence_gb300 import gdn
+
+    nil = ctypes.c_void_p(0)
+    P = ctypes.c_void_p
+    f = lib.gdn_recurrence_norm
+
+    def call(T=5, eps=1e-6, ptrs=None, mode=1):
+        ptrs = ptrs if ptrs is not None else [nil] * 10
+        return f(*ptrs[:9], eps, ptrs[9], T, 16, 48, 128, mode, nil)
+
+    assert call(eps=-1.0) == gdn.GDN_ERR_INVALID_ARG
+    assert call(eps=float("nan")) == gdn.GDN_ERR_INVALID_ARG
+    assert call() == gdn.GDN_ERR_INVALID_ARG and "null" in lib.gdn_last_error().decode()
+    assert call(T=0) == gdn.GDN_OK
+    T, nkh, nvh, d = 4, 16, 48, 128
+    base = 1 << 24
+    qk, vb = T * nkh * d * 4, T * nvh * d * 4
+    q = base
+    k = q + qk
+    v = k + qk
+    g = v + vb
+    be = g + 4096
+    st = be + 4096
+    out = st + nvh * d * d * 4
+    z = out + vb
+    w = z + vb
+    y = w + 4096
+    good = [P(q), P(k), P(v), P(g), P(be), P(st), P(out), P(z), P(w), P(y)]
+    bad = list(good)
+    bad[9] = P(z + 64)  # y inside z
+    assert call(T=T, ptrs=bad) == gdn.GDN_ERR_INVALID_ARG and "overlap" in lib.gdn_last_error().decode()
+    bad = list(good)
+    bad[9] = P(y + 2)  # y not 8-byte aligned
+    assert call(T=T, ptrs=bad) == gdn.GDN_ERR_INVALID_ARG and "aligned" in lib.gdn_last_error().decode()
+    bad = list(good)
+    bad[7] = P(out + 256)  # z inside out
+    assert call(T=T, ptrs=bad) == gdn.GDN_ERR_INVALID_ARG and "overlap" in lib.gdn_last_error().decode()
