@@ -192,7 +192,7 @@ def run_reference(args):
     v = statistics.median(steps)
     cb["value"] = v
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "µs/token/layer", "n_gpus": ws,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": v * 32768 / 1e3,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": v * args.tokens / 1e3,
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": _config(args), "cpu_baseline": cb,
             "e2e": {"value": v, "unit": "µs/token/layer", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
