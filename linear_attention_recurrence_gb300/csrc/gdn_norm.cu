@@ -6,7 +6,7 @@
 //
 // HBM-bound (per row: 512 B of o, 512 B of z read, 256 B of y written).  One warp
 // per row, one float4 of o and of z per lane, streamed past L1; two rows in flight
-// per warp and a grid of 2 CTAs of 512 threads per SM, grid-striding.
+// per warp and a grid of 4 CTAs of 256 threads per SM, grid-striding.
 #include <cuda_fp16.h>
 
 #include "gdn_device.cuh"
@@ -16,7 +16,11 @@
 namespace gdn {
 namespace {
 
-constexpr int kThreads = 512;
+// 256-thread CTAs (4 per SM): small enough (threads, registers, no shared memory)
+// to run beside a one-launch chunked recurrence CTA, so a norm on a second stream
+// overlaps the next recurrence call instead of delaying its launch.
+constexpr int kThreads = 256;
+constexpr int kCtasPerSm = 4;
 constexpr int kRowsInFlight = 2;
 
 __device__ __forceinline__ float4 ld_stream(const float* p) {
@@ -27,7 +31,7 @@ __device__ __forceinline__ float4 ld_stream(const float* p) {
     return r;
 }
 
-__global__ void __launch_bounds__(kThreads, 2) gdn_out_norm_kernel(const float* __restrict__ o,
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) gdn_out_norm_kernel(const float* __restrict__ o,
                                                                  const float* __restrict__ z,
                                                                  const float* __restrict__ w, float eps,
                                                                  uint2* __restrict__ y, int64_t rows) {
@@ -60,7 +64,7 @@ cudaError_t launch_out_norm(const float* out, const float* z, const float* w, fl
                             int64_t rows, int sm_count, cudaStream_t s) {
     const int64_t warps_per_cta = kThreads / 32;
     int64_t want = (rows + warps_per_cta * kRowsInFlight - 1) / (warps_per_cta * kRowsInFlight);
-    const int64_t cap = static_cast<int64_t>(sm_count) * 2;
+    const int64_t cap = static_cast<int64_t>(sm_count) * kCtasPerSm;
     const int grid = static_cast<int>(want < cap ? want : cap);
     gdn_out_norm_kernel<<<grid, kThreads, 0, s>>>(out, z, w, eps, reinterpret_cast<uint2*>(y), rows);
     return cudaGetLastError();
