@@ -262,14 +262,29 @@ def run_stack(args):
     L, T = args.stack, 2048
     layers = [{k: torch.from_numpy(v).to(dev) for k, v in make_inputs(T, seed=0, layer=i).items()} for i in range(L)]
     states = [torch.empty_like(x["S0"]) for x in layers]
-    out = torch.empty((T, N_VH, D), device=dev)
+    outs = [torch.empty((T, N_VH, D), device=dev) for _ in range(2)]
     y = torch.empty((T, N_VH, D), device=dev, dtype=torch.float16)
+    main, side = torch.cuda.current_stream(), torch.cuda.Stream(dev)
 
     def step():
-        for x, st in zip(layers, states):
+        """Layer i's recurrence on the main stream, its norm on a second stream beside
+        layer i+1's recurrence; the two output buffers alternate, and a layer's
+        recurrence waits for the norm that last read its buffer."""
+        side.wait_stream(main)
+        norm_done = [None, None]
+        for i, (x, st) in enumerate(zip(layers, states)):
+            o = outs[i % 2]
+            if norm_done[i % 2] is not None:
+                main.wait_event(norm_done[i % 2])
             st.copy_(x["S0"])
-            gdn.gdn_recurrence(x["q"], x["k"], x["v"], x["g"], x["beta"], st, out=out, mode=args.mode)
-            gdn.gdn_out_norm(out, x["z"], x["w"], 1e-6, y=y)
+            gdn.gdn_recurrence(x["q"], x["k"], x["v"], x["g"], x["beta"], st, out=o, mode=args.mode, stream=main)
+            rec_done = torch.cuda.Event()
+            rec_done.record(main)
+            side.wait_event(rec_done)
+            gdn.gdn_out_norm(o, x["z"], x["w"], 1e-6, y=y, stream=side)
+            norm_done[i % 2] = torch.cuda.Event()
+            norm_done[i % 2].record(side)
+        main.wait_stream(side)
 
     for _ in range(args.warmup):
         step()
@@ -291,6 +306,7 @@ def run_stack(args):
     line = {"metric": "GDN prefill stack time, recurrence + norm (ms per 2048-token chunk)", "value": ms, "unit": "ms",
             "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "higher_is_better": False, "dtype": "f32",
             "data": "synthetic", "us_per_token_layer": ms * 1e3 / (T * L),
+            "step_schedule": "layer i's norm on a second stream beside layer i+1's recurrence",
             "config": {"workload": f"{L} independent layers x {T} tokens, recurrence + FP16 norm", "layers": L,
                        "T": T, "mode": args.mode, "n_kh": N_KH, "n_vh": N_VH, "d": D},
             "gpu_launches": gdn.gdn_launch_count() - n0, "clocks": clk.summary()}
