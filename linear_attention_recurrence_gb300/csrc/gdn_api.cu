@@ -167,6 +167,15 @@ bool fused_norm_enabled() {
     return v && std::strcmp(v, "1") == 0;
 }
 
+// Failure-path test hook: GDN_TEST_WITHHOLD_PREP_FLAG=<task> keeps that prep task
+// (chunk * n_kh + key head of each super-block) from publishing its flag, so the
+// scan CTAs that wait for it run out their bounded wait and report
+// GDN_ERR_TIMEOUT (nothing faults or hangs; the next call runs normally).
+int withheld_prep_task() {
+    const char* v = std::getenv("GDN_TEST_WITHHOLD_PREP_FLAG");
+    return v ? std::atoi(v) : -1;
+}
+
 bool fused_chunk_launch_enabled() {
     const char* o = std::getenv("GDN_CHUNK_OVERLAP");
     if (o && std::strcmp(o, "0") == 0) return false;
@@ -336,6 +345,7 @@ int run_recurrence(const float* q, const float* k, const float* v, const float* 
             fp.y = in_launch ? norm->y : nullptr;
             fp.eps = in_launch ? norm->eps : 0.f;
             fp.out_flags = dev->out_flags;
+            fp.withhold_task = withheld_prep_task();
             cudaError_t e = launch_chunk_fused(fp, s);
             if (e == cudaSuccess) {
                 g_launches.fetch_add(1);

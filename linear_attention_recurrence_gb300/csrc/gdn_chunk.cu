@@ -619,7 +619,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) gdn_chunk_fused_kernel(const 
             prep_task(p.prep, sm, i & 1, task / n_kh, task % n_kh);
             fence_proxy_async_global();
             __syncthreads();
-            if (tid == 0) st_release_gpu(p.flags + task, gen);
+            if (tid == 0 && task != p.withhold_task) st_release_gpu(p.flags + task, gen);
         }
         if (p.y) norm_units(p, b, gen);
     } else {

@@ -127,6 +127,7 @@ struct ChunkFusedParams {
     uint16_t* y;           // [T][n_vh][128] binary16 bits
     float eps;
     uint32_t* out_flags;   // [kChunksPerSuperBlock][n_kh][8]: generation of each scan CTA's finished chunk
+    int withhold_task;     // failure-path test: this prep task's flag is never published (-1: none)
 };
 // CTAs the one-launch form gives the prep on a device with sm_count SMs, or 0
 // when too few SMs are left beside the scan (the two-launch form is used then).

@@ -77,3 +77,41 @@ def test_launch_counter_counts_kernels():
     one_launch = torch.cuda.get_device_properties(0).multi_processor_count >= 9 * 16
     assert gdn.gdn_launch_count() - n0 == (1 if one_launch else 2) * 3
     torch.cuda.synchronize()
+
+
+def test_bounded_flag_wait_runs_out_and_reports():
+    """A prep flag that nothing sets (the test hook withholds one task's flag): the
+    scan CTAs waiting for it give up after their bounded wait, the kernel ends, and
+    gdn_device_status() reports GDN_ERR_TIMEOUT naming the flag; the context stays
+    usable and the next call is correct."""
+    import time
+
+    import numpy as np
+
+    import oracle
+    from gdn_testutil import TOL, rel_err
+
+    if torch.cuda.get_device_properties(0).multi_processor_count < 9 * 16:
+        pytest.skip("too few SMs for the one-launch form")
+    x = make_inputs(64, seed=31, norm=False)
+    t = to_dev(x)
+    st = t["S0"].clone()
+    os.environ["GDN_TEST_WITHHOLD_PREP_FLAG"] = "5"  # chunk 0, key head 5
+    try:
+        t0 = time.time()
+        gdn.gdn_recurrence(t["q"], t["k"], t["v"], t["g"], t["beta"], st, mode="chunked")
+        rc = gdn.gdn_device_status()
+        elapsed = time.time() - t0
+    finally:
+        del os.environ["GDN_TEST_WITHHOLD_PREP_FLAG"]
+    assert rc == gdn.GDN_ERR_TIMEOUT
+    msg = gdn.gdn_last_error()
+    assert "prep flag 5" in msg, msg
+    assert elapsed < 30.0
+    # the context is usable and the next call is right
+    st = t["S0"].clone()
+    out = gdn.gdn_recurrence(t["q"], t["k"], t["v"], t["g"], t["beta"], st, mode="chunked")
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_status() == gdn.GDN_OK
+    o_ref, s_ref = oracle.recurrence(x["q"], x["k"], x["v"], x["g"], x["beta"], x["S0"])
+    assert rel_err(out.cpu().numpy(), o_ref) <= TOL and rel_err(st.cpu().numpy(), s_ref) <= TOL
