@@ -451,8 +451,6 @@ def main():
                          "one norm")
     ap.add_argument("--prestage", action="store_true",
                     help="time the pre-stage (conv + norms + gates) over --tokens tokens in one call")
-    ap.add_argument("--e2e-copy-streams", type=int, default=1,
-                    help="host-to-device copy streams of the pipelined end-to-end step")
     ap.add_argument("--skip-other-mode", action="store_true")
     ap.add_argument("--ref-seconds", type=float, default=10.0)
     ap.add_argument("--sweep", action="store_true",
@@ -602,7 +600,9 @@ def main():
     # from pinned host memory and reads the FP16 output and the final state back, inside
     # the timed region.  The copies are pipelined per call: a copy-in stream brings call
     # i+1's rows (q, k, v, g, beta, z) while the compute stream runs call i (recurrence,
-    # then the norm of its rows) and a copy-out stream returns call i-1's y rows.
+    # then the norm of its rows) and a copy-out stream returns call i-1's y rows.  The
+    # device inputs and y are double-buffered across steps, so step k+1's rows start
+    # landing while step k still computes (the host link is the bound).
     e2e = None
     if not args.skip_e2e:
         hy = torch.empty((T, N_VH, D), dtype=torch.float16).pin_memory()
@@ -610,65 +610,76 @@ def main():
         row_names = ["q", "k", "v", "g", "beta", "z"]
         h2d = sum(h[n].numel() * h[n].element_size() for n in row_names + ["S0", "w"])
         d2h = hy.numel() * 2 + hs.numel() * 4
-        s_ins = [torch.cuda.Stream(dev) for _ in range(args.e2e_copy_streams)]
-        s_out = torch.cuda.Stream(dev)
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        tb = [t, {n: torch.empty_like(t[n]) for n in row_names + ["S0", "w"]}]
+        yb = [y, torch.empty_like(y)]
+        inputs_free = [None, None]  # compute of the last step that read this input set is done
+        y_free = [None, None]       # copy-out of the last step that wrote this y is done
+        last_out = [None]           # the previous step's copy-outs (state included) are done
 
-        def e2e_step():
-            landed = [[] for _ in range(ncalls)]
-            for j, s_in in enumerate(s_ins):
-                s_in.wait_stream(stream)  # the previous step's calls have read their rows
-                with torch.cuda.stream(s_in):
-                    if j == 0:
-                        t["S0"].copy_(h["S0"], non_blocking=True)
-                        t["w"].copy_(h["w"], non_blocking=True)
-                    for i in range(ncalls):
-                        a, b = i * CT, (i + 1) * CT
-                        for n in row_names[j::len(s_ins)]:
-                            t[n][a:b].copy_(h[n][a:b], non_blocking=True)
-                        landed[i].append(torch.cuda.Event())
-                        landed[i][-1].record(s_in)
-            for ev in landed[0]:
-                stream.wait_event(ev)
-            state.copy_(t["S0"])
+        def e2e_step(k):
+            ti, yi = tb[k % 2], yb[k % 2]
+            if inputs_free[k % 2] is not None:
+                s_in.wait_event(inputs_free[k % 2])
+            landed = []
+            with torch.cuda.stream(s_in):
+                ti["S0"].copy_(h["S0"], non_blocking=True)
+                ti["w"].copy_(h["w"], non_blocking=True)
+                for i in range(ncalls):
+                    a, b = i * CT, (i + 1) * CT
+                    for n in row_names:
+                        ti[n][a:b].copy_(h[n][a:b], non_blocking=True)
+                    landed.append(torch.cuda.Event())
+                    landed[-1].record(s_in)
+            stream.wait_event(landed[0])
+            for ev in (last_out[0], y_free[k % 2]):
+                if ev is not None:
+                    stream.wait_event(ev)
+            state.copy_(ti["S0"])
             for i in range(ncalls):
                 a, b = i * CT, (i + 1) * CT
-                for ev in landed[i]:
-                    stream.wait_event(ev)
-                gdn.gdn_recurrence(t["q"][a:b], t["k"][a:b], t["v"][a:b], t["g"][a:b], t["beta"][a:b], state,
+                stream.wait_event(landed[i])
+                gdn.gdn_recurrence(ti["q"][a:b], ti["k"][a:b], ti["v"][a:b], ti["g"][a:b], ti["beta"][a:b], state,
                                    out=out[a:b], mode=args.mode, stream=stream)
-                gdn.gdn_out_norm(out[a:b], t["z"][a:b], t["w"], 1e-6, y=y[a:b], stream=stream)
+                gdn.gdn_out_norm(out[a:b], ti["z"][a:b], ti["w"], 1e-6, y=yi[a:b], stream=stream)
                 done = torch.cuda.Event()
                 done.record(stream)
                 s_out.wait_event(done)
                 with torch.cuda.stream(s_out):
-                    hy[a:b].copy_(y[a:b], non_blocking=True)
+                    hy[a:b].copy_(yi[a:b], non_blocking=True)
+            inputs_free[k % 2] = torch.cuda.Event()
+            inputs_free[k % 2].record(stream)
             s_out.wait_stream(stream)
             with torch.cuda.stream(s_out):
                 hs.copy_(state, non_blocking=True)
-            stream.wait_stream(s_out)
+            last_out[0] = torch.cuda.Event()
+            last_out[0].record(s_out)
+            y_free[k % 2] = last_out[0]
 
-        for _ in range(2):
-            e2e_step()
+        for k in range(2):
+            e2e_step(k)
         torch.cuda.synchronize()
         if ws > 1:
             dist.barrier()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
+        s_in.wait_event(e0)  # no copy of the timed steps starts before the clock does
+        for k in range(2, 2 + args.steps):
+            e2e_step(k)
+        stream.wait_stream(s_out)
         e1.record(stream)
         torch.cuda.synchronize()
         ms, e2e_us, _ = aggregate(e0.elapsed_time(e1) / args.steps, T, ws, device=dev)
         e2e = {"value": e2e_us, "unit": "µs/token/layer", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": ms,
-               "pipelining": f"per {CT}-token call: copy-in ({len(s_ins)} stream(s)), compute (recurrence "
-                             "+ norm of its rows), copy-out, on separate streams"}
+               "pipelining": f"per {CT}-token call: copy-in, compute (recurrence + norm of its rows), copy-out, "
+                             "on separate streams; inputs and y double-buffered across steps"}
+        y_last = yb[(1 + args.steps) % 2].clone()
         # the pipelined step must give the bits of the plain one
-        ref_y = y.clone()
         step(args.mode)
         torch.cuda.synchronize()
-        assert torch.equal(ref_y, y), "pipelined end-to-end step differs from the plain step"
+        assert torch.equal(y_last, y), "pipelined end-to-end step differs from the plain step"
         assert torch.equal(hy, y.cpu()) and torch.equal(hs, state.cpu())
 
     if rank != 0:
