@@ -179,8 +179,7 @@ int withheld_prep_task() {
 bool fused_chunk_launch_enabled() {
     const char* o = std::getenv("GDN_CHUNK_OVERLAP");
     if (o && std::strcmp(o, "0") == 0) return false;
-    const char* t = std::getenv("GDN_CHUNK_SCAN");
-    return !(t && std::strcmp(t, "tc") == 0);
+    return gdn::chunk_scan_kind() != gdn::ScanKind::kTcgen05;
 }
 
 __global__ void fill_words_kernel(uint32_t* p, size_t n, uint32_t bits) {
@@ -346,7 +345,7 @@ int run_recurrence(const float* q, const float* k, const float* v, const float* 
             fp.eps = in_launch ? norm->eps : 0.f;
             fp.out_flags = dev->out_flags;
             fp.withhold_task = withheld_prep_task();
-            cudaError_t e = launch_chunk_fused(fp, s);
+            cudaError_t e = launch_chunk_fused(fp, chunk_scan_kind() == ScanKind::kMma, s);
             if (e == cudaSuccess) {
                 g_launches.fetch_add(1);
                 if (norm && !in_launch) {  // the norm of this super-block's rows after it

@@ -42,6 +42,34 @@ constexpr int REC_PT = kRecPT;
 constexpr int REC_EG = kRecEG;
 constexpr int REC_ER = kRecER;
 
+// ---- products on the tensor cores (warp-level m16n8k8 TF32 MMAs) ----
+//
+// Each FP32 operand x is split as hi = x rounded to TF32 and lo = x - hi (exact),
+// and a product a b is taken as hi_a hi_b + (hi_a lo_b + lo_a hi_b): the dropped
+// lo_a lo_b and the MMA's truncation of lo to TF32 are below 2^-21 of |a b|, so
+// with FP32 accumulation the products keep FP32-level accuracy.  The cross terms
+// go to an accumulator of their own and join the main one once.  Operands are
+// stored in FP32 and split as they are loaded (three integer / FP32 operations).
+
+// D += A B for one m16n8k8 tile; fragments as the PTX ISA lays them out for .tf32:
+// A rows g, g+8 x cols t, t+4; B rows t, t+4 x col g; D rows g, g+8 x cols 2t, 2t+1
+// (g = lane / 4, t = lane % 4).
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    asm("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// hi: x rounded to TF32, to nearest with ties away from zero, by adding half a TF32
+// ulp to the bit pattern and clearing the 13 bits below it (two integer operations:
+// the conversion instruction issues at a quarter of their rate); finite |x| < 2^127.
+// lo: x - hi, exact, whose low 13 bits the MMA ignores.
+__device__ __forceinline__ void split_tf32(const float x, uint32_t& hi, uint32_t& lo) {
+    hi = (__float_as_uint(x) + 0x1000u) & 0xFFFFE000u;
+    lo = __float_as_uint(x - __uint_as_float(hi));
+}
+
 // ============================ prep ============================
 constexpr int PREP_THREADS = 256;
 constexpr int KP = D + 4;  // padded row stride of the k / q tiles
@@ -54,9 +82,9 @@ struct PrepSmemT {
     float Q[NB][C][KP];
     float graw[NB][kHeadsPerKey][C];
     float braw[NB][kHeadsPerKey][C];
-    float KK[C][C + 1];
-    float QK[C][C + 1];
-    float A[kHeadsPerKey][C][C + 1];
+    float KK[2][C][C + 1];  // K K^T (lower triangle), partial sums over key dims 0..63 and 64..127
+    float QK[2][C][C + 1];  // Q K^T (lower triangle), the same
+    float A[kHeadsPerKey][C][C + 4];
     float gam[kHeadsPerKey][C];
     float bet[kHeadsPerKey][C];
 };
@@ -124,42 +152,82 @@ __device__ __forceinline__ void prep_task(const ChunkPrepParams& p, PrepSmem& sm
     }
     __syncthreads();
 
-    // K K^T and Q K^T, shared by the key head's three value heads.
+    // K K^T and Q K^T (only the tiles on or below the diagonal), shared by the key
+    // head's three value heads, as split-TF32 MMAs: warp w sums key dims
+    // 64 (w >> 2) .. +63 for three 16 x 8 tiles of K K^T (w & 3 < 2) or Q K^T, rows
+    // t, columns i: (t 0..15, i 0..7), (0..15, 8..15), (16..31, 0..7) for even w & 3,
+    // (16..31, 8..15), (16..31, 16..23), (16..31, 24..31) for odd.  The two halves'
+    // sums go to KK[0 / 1] and QK[0 / 1] and are added in a fixed order below.
     {
-        const int t = tid >> 3, ig = tid & 7;
-        float kk[4] = {0.f, 0.f, 0.f, 0.f}, qk[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-        for (int c4 = 0; c4 < D / 4; ++c4) {
-            const float4 kt = *reinterpret_cast<const float4*>(&K[t][4 * c4]);
-            const float4 qt = *reinterpret_cast<const float4*>(&Q[t][4 * c4]);
+        const int g = lane >> 2, t4 = lane & 3;
+        const int h = warp >> 2, odd = warp & 1;
+        const float (*X)[KP] = (warp & 2) ? Q : K;
+        const int mt0 = odd ? 1 : 0, mt1 = 1;           // A row tiles of the three MMA tiles
+        const int nb0 = odd ? 1 : 0, nb1 = odd ? 2 : 1;  // B column tiles
+        const int nb2 = odd ? 3 : 0;                     // third tile: (mt1, nb2)
+        float acc[3][4], accx[3][4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float4 ki = *reinterpret_cast<const float4*>(&K[ig + 8 * u][4 * c4]);
-                kk[u] = fmaf(kt.x, ki.x, kk[u]);
-                kk[u] = fmaf(kt.y, ki.y, kk[u]);
-                kk[u] = fmaf(kt.z, ki.z, kk[u]);
-                kk[u] = fmaf(kt.w, ki.w, kk[u]);
-                qk[u] = fmaf(qt.x, ki.x, qk[u]);
-                qk[u] = fmaf(qt.y, ki.y, qk[u]);
-                qk[u] = fmaf(qt.z, ki.z, qk[u]);
-                qk[u] = fmaf(qt.w, ki.w, qk[u]);
+        for (int u = 0; u < 3; ++u)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[u][e] = accx[u][e] = 0.f;
+#pragma unroll 2
+        for (int j = 8 * h; j < 8 * h + 8; ++j) {
+            uint32_t ah[2][4], al[2][4], bh[3][2], bl[3][2];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int row = 16 * (r ? mt1 : mt0) + g;
+                split_tf32(X[row][8 * j + t4], ah[r][0], al[r][0]);
+                split_tf32(X[row + 8][8 * j + t4], ah[r][1], al[r][1]);
+                split_tf32(X[row][8 * j + t4 + 4], ah[r][2], al[r][2]);
+                split_tf32(X[row + 8][8 * j + t4 + 4], ah[r][3], al[r][3]);
             }
-        }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            sm.KK[t][ig + 8 * u] = kk[u];
-            sm.QK[t][ig + 8 * u] = qk[u];
+            for (int u = 0; u < 3; ++u) {
+                const int col = 8 * (u == 0 ? nb0 : u == 1 ? nb1 : nb2) + g;
+                split_tf32(K[col][8 * j + t4], bh[u][0], bl[u][0]);
+                split_tf32(K[col][8 * j + t4 + 4], bh[u][1], bl[u][1]);
+            }
+            // tiles (mt0, nb0), (mt0 or mt1, nb1), (mt1, nb2): for even w the first two
+            // share row tile 0, for odd w all three share row tile 1
+            uint32_t mh[4], ml[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                mh[e] = odd ? ah[1][e] : ah[0][e];
+                ml[e] = odd ? al[1][e] : al[0][e];
+            }
+            mma_tf32(acc[0], ah[0], bh[0]);
+            mma_tf32(acc[1], mh, bh[1]);
+            mma_tf32(acc[2], ah[1], bh[2]);
+            mma_tf32(accx[0], ah[0], bl[0]);
+            mma_tf32(accx[1], mh, bl[1]);
+            mma_tf32(accx[2], ah[1], bl[2]);
+            mma_tf32(accx[0], al[0], bh[0]);
+            mma_tf32(accx[1], ml, bh[1]);
+            mma_tf32(accx[2], al[1], bh[2]);
+        }
+        float (*const dst)[C + 1] = (warp & 2) ? sm.QK[h] : sm.KK[h];
+#pragma unroll
+        for (int u = 0; u < 3; ++u) {
+            const int rt = u == 0 ? mt0 : u == 1 ? (odd ? mt1 : mt0) : mt1;
+            const int ct = u == 0 ? nb0 : u == 1 ? nb1 : nb2;
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                dst[16 * rt + g + 8 * (e >> 1)][8 * ct + 2 * t4 + (e & 1)] = acc[u][e] + accx[u][e];
         }
     }
     __syncthreads();
 
     // A (shared memory) and P^T, e^gamma, e^(gamma_last - gamma) (records).
-    for (int idx = tid; idx < kHeadsPerKey * C * C; idx += PREP_THREADS) {
+#pragma unroll 4
+    for (int r = 0; r < kHeadsPerKey * C * C / PREP_THREADS; ++r) {
+        const int idx = tid + r * PREP_THREADS;
         const int m = idx / (C * C), i = (idx / C) % C, t = idx % C;
         float* rec = p.prep + (static_cast<int64_t>(ci) * p.n_vh + kh + m * p.n_kh) * REC;
-        const float e = (i <= t) ? expf(sm.gam[m][t] - sm.gam[m][i]) : 0.f;
-        sm.A[m][t][i] = (i < t) ? sm.bet[m][t] * e * sm.KK[t][i] : 0.f;
-        rec[REC_PT + i * C + t] = e * sm.QK[t][i];
+        const bool lower = i <= t;
+        const float e = lower ? expf(sm.gam[m][t] - sm.gam[m][i]) : 0.f;
+        const float kk = sm.KK[0][t][i] + sm.KK[1][t][i], qk = sm.QK[0][t][i] + sm.QK[1][t][i];
+        sm.A[m][t][i] = (i < t) ? sm.bet[m][t] * e * kk : 0.f;
+        rec[REC_PT + i * C + t] = lower ? e * qk : 0.f;
     }
     if (tid < kHeadsPerKey * C) {
         const int m = tid / C, t = tid % C;
@@ -169,17 +237,26 @@ __device__ __forceinline__ void prep_task(const ChunkPrepParams& p, PrepSmem& sm
     }
     __syncthreads();
 
-    // T = (I + A)^-1 by forward substitution, lane j owning column j; then
-    // row j of T'^T is T[:, j] * beta_j.
+    // T = (I + A)^-1 by forward substitution, lane j owning column j, each row's
+    // sum taken as four partial sums over i mod 4 (A is zero from the diagonal on,
+    // and so is Tc beyond the rows done); then row j of T'^T is T[:, j] * beta_j.
     if (warp < kHeadsPerKey) {
         const int m = warp, j = lane;
         float Tc[C];
 #pragma unroll
-        for (int t = 0; t < C; ++t) {
-            float s = (t == j) ? 1.f : 0.f;
+        for (int t = 0; t < C; ++t) Tc[t] = 0.f;
 #pragma unroll
-            for (int i = 0; i < t; ++i) s = fmaf(-sm.A[m][t][i], Tc[i], s);
-            Tc[t] = s;
+        for (int t = 0; t < C; ++t) {
+            float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int i4 = 0; i4 < (t + 3) / 4; ++i4) {
+                const float4 a = *reinterpret_cast<const float4*>(&sm.A[m][t][4 * i4]);
+                s[0] = fmaf(-a.x, Tc[4 * i4], s[0]);
+                s[1] = fmaf(-a.y, Tc[4 * i4 + 1], s[1]);
+                s[2] = fmaf(-a.z, Tc[4 * i4 + 2], s[2]);
+                s[3] = fmaf(-a.w, Tc[4 * i4 + 3], s[3]);
+            }
+            Tc[t] = ((t == j) ? 1.f : 0.f) + ((s[0] + s[1]) + (s[2] + s[3]));
         }
         const float bj = sm.bet[m][j];
         float* rec = p.prep + (static_cast<int64_t>(ci) * p.n_vh + kh + m * p.n_kh) * REC;
@@ -213,28 +290,453 @@ struct __align__(1024) ScanBuf {
 };
 constexpr uint32_t kScanTxBytes = 2 * C * D * 4 + kHeadsPerKey * C * NC * 4 + kHeadsPerKey * REC * 4;
 
+constexpr int WST = NCC + 8;  // row stride of W and Dp: 16-byte aligned rows on which the
+                              // MMA form's fragment accesses hit 32 distinct banks
+
 struct ScanSmem {
     ScanBuf buf[2];
-    float SsT[NCC][SST];     // S0 transposed: [head*16 + col][key dim]
-    float W[2 * C][NCC];     // rows 0..31: U'; rows 32..63: e^gamma (Q S0)
-    float Dm[C][NCC];        // D
-    float Dp[C][NCC];        // e^(gamma_last - gamma) D
+    float SsT[NCC][SST];        // S0 transposed: [head*16 + col][key dim]
+    float W[2 * C][WST];        // rows 0..31: U'; rows 32..63: e^gamma (Q S0)
+    float Dm[C][WST];           // D
+    float Dp[C][WST];           // e^(gamma_last - gamma) D
     uint64_t full[2];
-    int copy_gave_up;        // 1 + the chunk whose copy wait ran out, else 0
-    int flag_gave_up;        // a prep flag wait ran out (later ones are skipped)
+    int copy_gave_up;           // 1 + the chunk whose copy wait ran out, else 0
+    int flag_gave_up;           // a prep flag wait ran out (later ones are skipped)
 };
+static_assert(sizeof(ScanSmem) + 1024 <= 227 * 1024, "scan shared memory");
+static_assert(kHeadsPerKey * C * C % 256 == 0, "prep A / P loop");
 
 // byte offset of float4 chunk `cc` (0..7) of row `r` in a 128-byte-swizzled box
 __device__ __forceinline__ int swz(int r, int cc) { return r * 128 + ((cc ^ (r & 7)) << 4); }
 
+__device__ __forceinline__ float ldsf(const unsigned char* p) { return *reinterpret_cast<const float*>(p); }
+
+// The CTA's 128 x 48 slice of the state (key dims x the 16 columns of each of the
+// three heads), 24 floats per thread, in the layout each form of the update uses:
+//  * FMA: thread (it = tid / 16, jj = tid % 16) holds key dims 8 it .. 8 it + 7 of
+//    column jj of each head, as pairs of consecutive key dims;
+//  * MMA: warp w holds 16 key dims (mma_key) of all 48 columns as six m16n8
+//    accumulator tiles (rows = key dims, columns = the CTA's columns 8n .. 8n + 7).
+template <bool kMma>
+struct ScanState;
+template <>
+struct ScanState<false> {
+    float2 v[kHeadsPerKey][4];
+};
+template <>
+struct ScanState<true> {
+    float v[NCC / 8][4];
+};
+
+// Key dim of accumulator row `row` (0..15) in warp w's update tile.  Warps 2b and
+// 2b + 1 share the 32 key dims of k-tile box b, each taking four of its 16-byte
+// chunks, {0, 1, 4, 5} or {2, 3, 6, 7}: rows g and g + 8 of a fragment then fall in
+// chunks four apart, so a warp's loads of K^T from the swizzled box hit 32 banks.
+__device__ __forceinline__ int mma_key(const int w, const int row) {
+    return 32 * (w >> 1) + 4 * (2 * (w & 1) + 4 * ((row >> 2) & 1) + (row >> 3)) + (row & 3);
+}
+
+// state slice -> registers and the transposed copy SsT
+__device__ __forceinline__ void state_load(const ChunkScanParams& p, ScanSmem& sm, ScanState<false>& S, const int kh,
+                                           const int c0) {
+    const int tid = threadIdx.x, it = tid >> 4, jj = tid & 15;
+#pragma unroll
+    for (int m = 0; m < kHeadsPerKey; ++m) {
+        const float* sh = p.state + (static_cast<int64_t>(kh + m * p.n_kh) * D + 8 * it) * D + c0 + jj;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) S.v[m][q] = make_float2(sh[(2 * q) * D], sh[(2 * q + 1) * D]);
+#pragma unroll
+        for (int h4 = 0; h4 < 2; ++h4)
+            *reinterpret_cast<float4*>(&sm.SsT[m * NC + jj][8 * it + 4 * h4]) =
+                make_float4(S.v[m][2 * h4].x, S.v[m][2 * h4].y, S.v[m][2 * h4 + 1].x, S.v[m][2 * h4 + 1].y);
+    }
+}
+__device__ __forceinline__ void state_load(const ChunkScanParams& p, ScanSmem& sm, ScanState<true>& S, const int kh,
+                                           const int c0) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int key = mma_key(threadIdx.x >> 5, g);  // rows g; rows g + 8 are key + 4
+#pragma unroll
+    for (int n = 0; n < NCC / 8; ++n) {
+        const int col = 8 * n + 2 * t;  // the CTA's column: head col / 16, column c0 + col % 16
+        const float* sh = p.state + (static_cast<int64_t>(kh + (n >> 1) * p.n_kh) * D + key) * D + c0 + (col & 15);
+        const float2 lo = *reinterpret_cast<const float2*>(sh);
+        const float2 hi = *reinterpret_cast<const float2*>(sh + 4 * D);
+        S.v[n][0] = lo.x;
+        S.v[n][1] = lo.y;
+        S.v[n][2] = hi.x;
+        S.v[n][3] = hi.y;
+        sm.SsT[col][key] = lo.x;
+        sm.SsT[col + 1][key] = lo.y;
+        sm.SsT[col][key + 4] = hi.x;
+        sm.SsT[col + 1][key + 4] = hi.y;
+    }
+}
+
+__device__ __forceinline__ void state_store(const ChunkScanParams& p, const ScanState<false>& S, const int kh,
+                                            const int c0) {
+    const int tid = threadIdx.x, it = tid >> 4, jj = tid & 15;
+#pragma unroll
+    for (int m = 0; m < kHeadsPerKey; ++m) {
+        float* sh = p.state + (static_cast<int64_t>(kh + m * p.n_kh) * D + 8 * it) * D + c0 + jj;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            sh[(2 * q) * D] = S.v[m][q].x;
+            sh[(2 * q + 1) * D] = S.v[m][q].y;
+        }
+    }
+}
+__device__ __forceinline__ void state_store(const ChunkScanParams& p, const ScanState<true>& S, const int kh,
+                                            const int c0) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int key = mma_key(threadIdx.x >> 5, g);
+#pragma unroll
+    for (int n = 0; n < NCC / 8; ++n) {
+        const int col = 8 * n + 2 * t;
+        float* sh = p.state + (static_cast<int64_t>(kh + (n >> 1) * p.n_kh) * D + key) * D + c0 + (col & 15);
+        *reinterpret_cast<float2*>(sh) = make_float2(S.v[n][0], S.v[n][1]);
+        *reinterpret_cast<float2*>(sh + 4 * D) = make_float2(S.v[n][2], S.v[n][3]);
+    }
+}
+
+// ---- G1: W = [K; Q] S0 (64 x 48), then U' = V - e^gamma K S0 and e^gamma Q S0 into W ----
+
+// FMA form: packed over even/odd key dims, the key dims split over the two
+// half-warps and their partial sums added once.  Warp tg takes X rows
+// 8*(tg&3)..+7 of K (tg < 4) or Q (tg >= 4); lane bit 4 picks the key-dim half
+// kgrp (dims 0..63 or 64..127) and the low four bits the column jw of each head.
+// Each quarter-warp shares its rows and half, so the X loads are broadcasts; the
+// halves' partial sums meet by a shuffle.
+__device__ __forceinline__ void g1_fma(const ScanBuf& b, ScanSmem& sm) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tg = warp, kgrp = (lane >> 4) & 1, jw = lane & 15;
+    const unsigned char* xb = reinterpret_cast<const unsigned char*>(tg < 4 ? &b.K[0][0][0] : &b.Q[0][0][0]) +
+                              (8 * (tg & 3)) * 128;
+    float2 acc[8][kHeadsPerKey];
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+#pragma unroll
+        for (int m = 0; m < kHeadsPerKey; ++m) acc[r][m] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int bh = 0; bh < 2; ++bh) {
+        const int bx = 2 * kgrp + bh;
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+            float4 s4[kHeadsPerKey];
+#pragma unroll
+            for (int m = 0; m < kHeadsPerKey; ++m)
+                s4[m] = *reinterpret_cast<const float4*>(&sm.SsT[m * NC + jw][32 * bx + 4 * cc]);
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {  // row 8*(tg&3) + r has (row & 7) == r
+                const float4 a = *reinterpret_cast<const float4*>(xb + bx * (C * 128) + r * 128 + ((cc ^ r) << 4));
+#pragma unroll
+                for (int m = 0; m < kHeadsPerKey; ++m) {
+                    acc[r][m] = ffma2(make_float2(a.x, a.y), make_float2(s4[m].x, s4[m].y), acc[r][m]);
+                    acc[r][m] = ffma2(make_float2(a.z, a.w), make_float2(s4[m].z, s4[m].w), acc[r][m]);
+                }
+            }
+        }
+    }
+    // reduce-scatter with lane ^ 16: kgrp 0 finishes the even rows, kgrp 1 the odd
+    // ones, each as (dims 0..63) + (dims 64..127)
+#pragma unroll
+    for (int r2 = 0; r2 < 4; ++r2) {
+        const int t = 8 * (tg & 3) + 2 * r2 + kgrp;
+#pragma unroll
+        for (int m = 0; m < kHeadsPerKey; ++m) {
+            const float ev = acc[2 * r2][m].x + acc[2 * r2][m].y;
+            const float od = acc[2 * r2 + 1][m].x + acc[2 * r2 + 1][m].y;
+            const float other = __shfl_xor_sync(0xffffffffu, kgrp ? ev : od, 16);
+            const float x = kgrp ? other + od : ev + other;
+            const float eg = b.rec[m][REC_EG + t];
+            if (tg < 4)
+                sm.W[t][m * NC + jw] = b.V[m][t][jw] - eg * x;
+            else
+                sm.W[C + t][m * NC + jw] = eg * x;
+        }
+    }
+}
+
+// MMA form: warp w computes rows 16*(w&3)..+15 of [K; Q] (K for w&3 < 2) times
+// the CTA's columns 24*(w>>2)..+23 (three n8 tiles), over the 16 k8 steps of the
+// key dims; A from the swizzled k / q box (row & 7 == g, so the four loads of a
+// fragment hit 32 banks), B from SsT (row stride 132: 32 banks).  Each step's
+// operands are loaded while the step before issues its MMAs.
+__device__ __forceinline__ void g1_mma(const ScanBuf& b, ScanSmem& sm) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int mt = warp & 3, ng = warp >> 2;
+    const unsigned char* xa = reinterpret_cast<const unsigned char*>(mt < 2 ? &b.K[0][0][0] : &b.Q[0][0][0]) +
+                              (16 * (mt & 1) + g) * 128 + 4 * t;
+    const float* sb = &sm.SsT[24 * ng + g][t];
+    auto load = [&](const int j, float (&av)[4], float (&bv)[6]) {
+        const unsigned char* xr = xa + (j >> 2) * (C * 128);
+        const int ca = ((2 * (j & 3)) ^ g) << 4, cb = ((2 * (j & 3) + 1) ^ g) << 4;
+        av[0] = ldsf(xr + ca);
+        av[1] = ldsf(xr + 1024 + ca);
+        av[2] = ldsf(xr + cb);
+        av[3] = ldsf(xr + 1024 + cb);
+#pragma unroll
+        for (int n = 0; n < 3; ++n) {
+            bv[2 * n] = sb[8 * n * SST + 8 * j];
+            bv[2 * n + 1] = sb[8 * n * SST + 8 * j + 4];
+        }
+    };
+    float acc[3][4], accx[3][4];
+#pragma unroll
+    for (int n = 0; n < 3; ++n)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[n][i] = accx[n][i] = 0.f;
+    float av[2][4], bv[2][6];
+    load(0, av[0], bv[0]);
+#pragma unroll 4
+    for (int j = 0; j < D / 8; ++j) {  // key dims 8j .. 8j + 7
+        const int cur = j & 1;
+        if (j + 1 < D / 8) load(j + 1, av[cur ^ 1], bv[cur ^ 1]);
+        uint32_t ah[4], al[4], bh[3][2], bl[3][2];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) split_tf32(av[cur][i], ah[i], al[i]);
+#pragma unroll
+        for (int i = 0; i < 6; ++i) split_tf32(bv[cur][i], bh[i >> 1][i & 1], bl[i >> 1][i & 1]);
+        // grouped by term, so that no MMA waits on the one just before it
+#pragma unroll
+        for (int n = 0; n < 3; ++n) mma_tf32(acc[n], ah, bh[n]);
+#pragma unroll
+        for (int n = 0; n < 3; ++n) mma_tf32(accx[n], ah, bl[n]);
+#pragma unroll
+        for (int n = 0; n < 3; ++n) mma_tf32(accx[n], al, bh[n]);
+    }
+#pragma unroll
+    for (int n = 0; n < 3; ++n) {
+        const int col = 24 * ng + 8 * n + 2 * t, m = col >> 4, jc = col & 15;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            const int tk = 16 * (mt & 1) + g + 8 * hf;
+            const float x0 = acc[n][2 * hf] + accx[n][2 * hf];
+            const float x1 = acc[n][2 * hf + 1] + accx[n][2 * hf + 1];
+            const float eg = b.rec[m][REC_EG + tk];
+            if (mt < 2) {
+                const float2 v = *reinterpret_cast<const float2*>(&b.V[m][tk][jc]);
+                *reinterpret_cast<float2*>(&sm.W[tk][col]) = make_float2(v.x - eg * x0, v.y - eg * x1);
+            } else {
+                *reinterpret_cast<float2*>(&sm.W[C + tk][col]) = make_float2(eg * x0, eg * x1);
+            }
+        }
+    }
+}
+
+// ---- P2 / P3 on the tensor cores: the chunk's two small products per head, in
+// transposed form (rows = the head's 16 columns, columns = tokens), so that the
+// A operands (U', D) come from W / Dm with 32-bank fragment loads:
+//     D^T = U'^T T'^T,   O^T = (e^gamma Q S0)^T + D^T P^T.
+// T' and P are lower triangular (the records hold their zeros), so token tile nn
+// needs only the k steps kk <= nn: 10 of 16.  Warp w < 6 takes head w / 2 and the
+// token tiles {w % 2, 3 - w % 2}, four k steps per warp in all.
+__device__ __forceinline__ void load_a_cols(const float (*x)[WST], const int kk, const int col0, const int g,
+                                            const int t, uint32_t (&ah)[4], uint32_t (&al)[4]) {
+    split_tf32(x[8 * kk + t][col0 + g], ah[0], al[0]);
+    split_tf32(x[8 * kk + t][col0 + g + 8], ah[1], al[1]);
+    split_tf32(x[8 * kk + t + 4][col0 + g], ah[2], al[2]);
+    split_tf32(x[8 * kk + t + 4][col0 + g + 8], ah[3], al[3]);
+}
+__device__ __forceinline__ void load_b_rec(const float* r, const int kk, const int nn, const int g, const int t,
+                                           uint32_t (&bh)[2], uint32_t (&bl)[2]) {
+    split_tf32(r[(8 * kk + t) * C + 8 * nn + g], bh[0], bl[0]);
+    split_tf32(r[(8 * kk + t + 4) * C + 8 * nn + g], bh[1], bl[1]);
+}
+
+// D^T tiles of head w / 2 -> Dm (D) and Dp (e^(gamma_last - gamma) D), [token][column]
+__device__ __forceinline__ void p2_mma(const ScanBuf& b, ScanSmem& sm) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int m = warp >> 1, na = warp & 1, nb = 3 - na;
+    const float* tp = &b.rec[m][REC_TP];
+    float acc[2][4], accx[2][4];
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[i][e] = accx[i][e] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < C / 8; ++kk) {
+        if (kk > nb) break;
+        uint32_t ah[4], al[4], bh[2][2], bl[2][2];
+        load_a_cols(sm.W, kk, m * NC, g, t, ah, al);
+        const bool both = kk <= na;  // tile nb (> na) takes every k step up to nb
+        load_b_rec(tp, kk, nb, g, t, bh[1], bl[1]);
+        if (both) load_b_rec(tp, kk, na, g, t, bh[0], bl[0]);
+        mma_tf32(acc[1], ah, bh[1]);
+        if (both) mma_tf32(acc[0], ah, bh[0]);
+        mma_tf32(accx[1], ah, bl[1]);
+        if (both) mma_tf32(accx[0], ah, bl[0]);
+        mma_tf32(accx[1], al, bh[1]);
+        if (both) mma_tf32(accx[0], al, bh[0]);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int nn = i ? nb : na;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int col = m * NC + g + 8 * (e >> 1), tok = 8 * nn + 2 * t + (e & 1);
+            const float d = acc[i][e] + accx[i][e];
+            sm.Dm[tok][col] = d;
+            sm.Dp[tok][col] = b.rec[m][REC_ER + tok] * d;
+        }
+    }
+}
+
+// O^T tiles of head w / 2 -> out (tokens < nt)
+__device__ __forceinline__ void p3_mma(const ChunkScanParams& p, const ScanBuf& b, const ScanSmem& sm, const int kh,
+                                       const int c0, const int c, const int nt) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int m = warp >> 1, na = warp & 1, nb = 3 - na;
+    const float* pt = &b.rec[m][REC_PT];
+    float acc[2][4], accx[2][4];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int nn = i ? nb : na;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            acc[i][e] = sm.W[C + 8 * nn + 2 * t + (e & 1)][m * NC + g + 8 * (e >> 1)];
+            accx[i][e] = 0.f;
+        }
+    }
+#pragma unroll
+    for (int kk = 0; kk < C / 8; ++kk) {
+        if (kk > nb) break;
+        uint32_t ah[4], al[4], bh[2][2], bl[2][2];
+        load_a_cols(sm.Dm, kk, m * NC, g, t, ah, al);
+        const bool both = kk <= na;  // tile nb (> na) takes every k step up to nb
+        load_b_rec(pt, kk, nb, g, t, bh[1], bl[1]);
+        if (both) load_b_rec(pt, kk, na, g, t, bh[0], bl[0]);
+        mma_tf32(acc[1], ah, bh[1]);
+        if (both) mma_tf32(acc[0], ah, bh[0]);
+        mma_tf32(accx[1], ah, bl[1]);
+        if (both) mma_tf32(accx[0], ah, bl[0]);
+        mma_tf32(accx[1], al, bh[1]);
+        if (both) mma_tf32(accx[0], al, bh[0]);
+    }
+    const int h = kh + m * p.n_kh;
+    float* o = p.out + ((p.t_begin + static_cast<int64_t>(c) * C) * p.n_vh + h) * D + c0;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int nn = i ? nb : na;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int tok = 8 * nn + 2 * t + (e & 1);
+            if (tok < nt) o[static_cast<int64_t>(tok) * p.n_vh * D + g + 8 * (e >> 1)] = acc[i][e] + accx[i][e];
+        }
+    }
+}
+
+// ---- G4: S_end = e^gamma_last S0 + K^T (e^(gamma_last-gamma) D), and its transposed copy ----
+
+// FMA form: packed over key-dim pairs, 8 key dims x 3 columns per thread.
+__device__ __forceinline__ void g4_fma(const ScanBuf& b, ScanSmem& sm, ScanState<false>& S) {
+    const int tid = threadIdx.x, it = tid >> 4, jj = tid & 15;
+    const unsigned char* kb = reinterpret_cast<const unsigned char*>(&b.K[it >> 2][0][0]);
+    const int cc0 = 2 * (it & 3);
+    float2 acc[kHeadsPerKey][4];
+#pragma unroll
+    for (int m = 0; m < kHeadsPerKey; ++m) {
+        const float el = b.rec[m][REC_EG + C - 1];
+        const float2 el2 = make_float2(el, el);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[m][q] = fmul2(el2, S.v[m][q]);
+    }
+#pragma unroll 8
+    for (int t = 0; t < C; ++t) {
+        const float4 klo = *reinterpret_cast<const float4*>(kb + swz(t, cc0));
+        const float4 khi = *reinterpret_cast<const float4*>(kb + swz(t, cc0 + 1));
+#pragma unroll
+        for (int m = 0; m < kHeadsPerKey; ++m) {
+            const float dv = sm.Dp[t][m * NC + jj];
+            const float2 d2 = make_float2(dv, dv);
+            acc[m][0] = ffma2(make_float2(klo.x, klo.y), d2, acc[m][0]);
+            acc[m][1] = ffma2(make_float2(klo.z, klo.w), d2, acc[m][1]);
+            acc[m][2] = ffma2(make_float2(khi.x, khi.y), d2, acc[m][2]);
+            acc[m][3] = ffma2(make_float2(khi.z, khi.w), d2, acc[m][3]);
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < kHeadsPerKey; ++m) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) S.v[m][q] = acc[m][q];
+#pragma unroll
+        for (int h4 = 0; h4 < 2; ++h4)
+            *reinterpret_cast<float4*>(&sm.SsT[m * NC + jj][8 * it + 4 * h4]) =
+                make_float4(acc[m][2 * h4].x, acc[m][2 * h4].y, acc[m][2 * h4 + 1].x, acc[m][2 * h4 + 1].y);
+    }
+}
+
+// MMA form: warp w updates its 16 key dims (mma_key) of all 48 columns, K^T from
+// the swizzled k box (A: key dims x tokens), D' from Dp (B: tokens x columns, row
+// stride 56: 32 banks), the state itself the accumulator; each step's operands
+// are loaded while the step before issues its MMAs.
+__device__ __forceinline__ void g4_mma(const ScanBuf& b, ScanSmem& sm, ScanState<true>& S) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int ch = 2 * (warp & 1) + 4 * (g >> 2);  // 16-byte chunk of key row g; row g + 8: ch + 1
+    const unsigned char* ka = reinterpret_cast<const unsigned char*>(&b.K[warp >> 1][0][0]) + 4 * (g & 3);
+    auto load = [&](const int j, float (&av)[4], float (&bv)[2 * NCC / 8]) {
+        const unsigned char* r0 = ka + (8 * j + t) * 128;  // token 8j + t: row & 7 == t
+        const unsigned char* r1 = r0 + 4 * 128;            // token 8j + t + 4: row & 7 == t + 4
+        av[0] = ldsf(r0 + ((ch ^ t) << 4));
+        av[1] = ldsf(r0 + (((ch + 1) ^ t) << 4));
+        av[2] = ldsf(r1 + ((ch ^ (t + 4)) << 4));
+        av[3] = ldsf(r1 + (((ch + 1) ^ (t + 4)) << 4));
+#pragma unroll
+        for (int n = 0; n < NCC / 8; ++n) {
+            bv[2 * n] = sm.Dp[8 * j + t][8 * n + g];
+            bv[2 * n + 1] = sm.Dp[8 * j + t + 4][8 * n + g];
+        }
+    };
+    float av[2][4], bv[2][2 * NCC / 8];
+    load(0, av[0], bv[0]);
+    float sx[NCC / 8][4];
+#pragma unroll
+    for (int n = 0; n < NCC / 8; ++n) {
+        const float el = b.rec[n >> 1][REC_EG + C - 1];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            S.v[n][i] *= el;
+            sx[n][i] = 0.f;
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < C / 8; ++j) {  // tokens 8j .. 8j + 7
+        const int cur = j & 1;
+        if (j + 1 < C / 8) load(j + 1, av[cur ^ 1], bv[cur ^ 1]);
+        uint32_t ah[4], al[4], bh[NCC / 8][2], bl[NCC / 8][2];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) split_tf32(av[cur][i], ah[i], al[i]);
+#pragma unroll
+        for (int i = 0; i < 2 * NCC / 8; ++i) split_tf32(bv[cur][i], bh[i >> 1][i & 1], bl[i >> 1][i & 1]);
+#pragma unroll
+        for (int n = 0; n < NCC / 8; ++n) mma_tf32(S.v[n], ah, bh[n]);
+#pragma unroll
+        for (int n = 0; n < NCC / 8; ++n) mma_tf32(sx[n], ah, bl[n]);
+#pragma unroll
+        for (int n = 0; n < NCC / 8; ++n) mma_tf32(sx[n], al, bh[n]);
+    }
+    const int key = mma_key(warp, g);
+#pragma unroll
+    for (int n = 0; n < NCC / 8; ++n) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) S.v[n][i] += sx[n][i];
+        const int col = 8 * n + 2 * t;
+        sm.SsT[col][key] = S.v[n][0];
+        sm.SsT[col + 1][key] = S.v[n][1];
+        sm.SsT[col][key + 4] = S.v[n][2];
+        sm.SsT[col + 1][key + 4] = S.v[n][3];
+    }
+}
+
 // The scan of key head `kh`, value columns c0..c0+15 of its three heads, over the
-// super-block's chunks.  With `flags` set, chunk c's prep records are read only
-// once flags[c * n_kh + kh] == gen (records written by other CTAs of the same
-// launch); a flag wait that runs out records the flag's index, its last value and
-// `gen` in diag[0..2].  A wait that runs out is reported in the status word and
-// the state is left as it was; every thread still takes the same path through
-// the chunk loop (a thread that gave up computes on whatever landed), so the
-// CTA's barriers stay matched and the CTA ends.
+// super-block's chunks, with the two large products as FP32 FMAs (kMma false) or
+// split-TF32 tensor-core MMAs (kMma true).  With `flags` set, chunk c's prep
+// records are read only once flags[c * n_kh + kh] == gen (records written by
+// other CTAs of the same launch); a flag wait that runs out records the flag's
+// index, its last value and `gen` in diag[0..2].  A wait that runs out is
+// reported in the status word and the state is left as it was; every thread still
+// takes the same path through the chunk loop (a thread that gave up computes on
+// whatever landed), so the CTA's barriers stay matched and the CTA ends.
+template <bool kMma>
 __device__ __forceinline__ void scan_body(const ChunkScanParams& p, ScanSmem& sm, const int kh, const int c0,
                                           const uint32_t* flags, uint32_t* diag, const uint32_t gen,
                                           uint32_t* out_flags = nullptr) {
@@ -250,19 +752,8 @@ __device__ __forceinline__ void scan_body(const ChunkScanParams& p, ScanSmem& sm
         sm.flag_gave_up = 0;
     }
 
-    // state slice -> registers (G4 tile: rows 8*it..8*it+7, column c0+j of each head)
-    const int it = tid >> 4, jj = tid & 15;
-    float2 Sreg[kHeadsPerKey][4];
-#pragma unroll
-    for (int m = 0; m < kHeadsPerKey; ++m) {
-        const float* sh = p.state + (static_cast<int64_t>(kh + m * n_kh) * D + 8 * it) * D + c0 + jj;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) Sreg[m][q] = make_float2(sh[(2 * q) * D], sh[(2 * q + 1) * D]);
-#pragma unroll
-        for (int h4 = 0; h4 < 2; ++h4)
-            *reinterpret_cast<float4*>(&sm.SsT[m * NC + jj][8 * it + 4 * h4]) =
-                make_float4(Sreg[m][2 * h4].x, Sreg[m][2 * h4].y, Sreg[m][2 * h4 + 1].x, Sreg[m][2 * h4 + 1].y);
-    }
+    ScanState<kMma> S;
+    state_load(p, sm, S, kh, c0);
     __syncthreads();
 
     // k, q and v tiles of chunk c (TMA), on the chunk's buffer barrier, which expects
@@ -315,11 +806,6 @@ __device__ __forceinline__ void scan_body(const ChunkScanParams& p, ScanSmem& sm
         __syncwarp();
     }
 
-    // G1 tile: warp tg takes X rows 8*(tg&3)..+7 of K (tg < 4) or Q (tg >= 4); lane
-    // bit 4 picks the key-dim half kgrp (dims 0..63 or 64..127) and the low four bits
-    // the column jw of each head.  Each quarter-warp shares its rows and half, so the
-    // X loads are broadcasts; the halves' partial sums meet by a shuffle.
-    const int tg = warp, kgrp = (lane >> 4) & 1, jw = lane & 15;
     // P2 / P3 tile: head pm, rows 4*pti..+3, columns 2*pjp, 2*pjp+1
     const int pm = tid >> 6, pti = (tid >> 3) & 7, pjp = tid & 7;
 
@@ -333,55 +819,10 @@ __device__ __forceinline__ void scan_body(const ChunkScanParams& p, ScanSmem& sm
         const ScanBuf& b = sm.buf[c & 1];
         const int nt = min(C, p.n_tokens - c * C);
 
-        // ---- G1: W = [K; Q] S0 (64 x 48), packed over even/odd key dims, the key dims
-        //      split over the two half-warps and their partial sums added once ----
-        {
-            const unsigned char* xb = reinterpret_cast<const unsigned char*>(tg < 4 ? &b.K[0][0][0] : &b.Q[0][0][0]) +
-                                      (8 * (tg & 3)) * 128;
-            float2 acc[8][kHeadsPerKey];
-#pragma unroll
-            for (int r = 0; r < 8; ++r)
-#pragma unroll
-                for (int m = 0; m < kHeadsPerKey; ++m) acc[r][m] = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int bh = 0; bh < 2; ++bh) {
-                const int bx = 2 * kgrp + bh;
-#pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
-                    float4 s4[kHeadsPerKey];
-#pragma unroll
-                    for (int m = 0; m < kHeadsPerKey; ++m)
-                        s4[m] = *reinterpret_cast<const float4*>(&sm.SsT[m * NC + jw][32 * bx + 4 * cc]);
-#pragma unroll
-                    for (int r = 0; r < 8; ++r) {  // row 8*(tg&3) + r has (row & 7) == r
-                        const float4 a = *reinterpret_cast<const float4*>(xb + bx * (C * 128) + r * 128 + ((cc ^ r) << 4));
-#pragma unroll
-                        for (int m = 0; m < kHeadsPerKey; ++m) {
-                            acc[r][m] = ffma2(make_float2(a.x, a.y), make_float2(s4[m].x, s4[m].y), acc[r][m]);
-                            acc[r][m] = ffma2(make_float2(a.z, a.w), make_float2(s4[m].z, s4[m].w), acc[r][m]);
-                        }
-                    }
-                }
-            }
-            // reduce-scatter with lane ^ 16: kgrp 0 finishes the even rows, kgrp 1 the odd
-            // ones, each as (dims 0..63) + (dims 64..127)
-#pragma unroll
-            for (int r2 = 0; r2 < 4; ++r2) {
-                const int t = 8 * (tg & 3) + 2 * r2 + kgrp;
-#pragma unroll
-                for (int m = 0; m < kHeadsPerKey; ++m) {
-                    const float ev = acc[2 * r2][m].x + acc[2 * r2][m].y;
-                    const float od = acc[2 * r2 + 1][m].x + acc[2 * r2 + 1][m].y;
-                    const float other = __shfl_xor_sync(0xffffffffu, kgrp ? ev : od, 16);
-                    const float x = kgrp ? other + od : ev + other;
-                    const float eg = b.rec[m][REC_EG + t];
-                    if (tg < 4)
-                        sm.W[t][m * NC + jw] = b.V[m][t][jw] - eg * x;
-                    else
-                        sm.W[C + t][m * NC + jw] = eg * x;
-                }
-            }
-        }
+        if constexpr (kMma)
+            g1_mma(b, sm);
+        else
+            g1_fma(b, sm);
         __syncthreads();
 
         // ---- P2: D = T' U' per head (32x32 by 32x16); warp 7, idle here, loads the next
@@ -397,7 +838,9 @@ __device__ __forceinline__ void scan_body(const ChunkScanParams& p, ScanSmem& sm
             if (lane == 0 && out_flags && c > 0) st_release_gpu(out_flags + ((c - 1) * n_kh + kh) * 8 + c0 / NC, gen);
             __syncwarp();
         }
-        if (tid < kHeadsPerKey * 64) {
+        if constexpr (kMma) {
+            if (warp < 2 * kHeadsPerKey) p2_mma(b, sm);
+        } else if (tid < kHeadsPerKey * 64) {
             const float* tp = &b.rec[pm][REC_TP];
             float acc[4][2];
 #pragma unroll
@@ -430,7 +873,9 @@ __device__ __forceinline__ void scan_body(const ChunkScanParams& p, ScanSmem& sm
         __syncthreads();
 
         // ---- P3: O = e^gamma Q S0 + P D per head -> out ----
-        if (tid < kHeadsPerKey * 64) {
+        if (kMma && warp < 2 * kHeadsPerKey) {
+            p3_mma(p, b, sm, kh, c0, c, nt);
+        } else if (!kMma && tid < kHeadsPerKey * 64) {
             const float* pt = &b.rec[pm][REC_PT];
             float acc[4][2];
 #pragma unroll
@@ -467,42 +912,10 @@ __device__ __forceinline__ void scan_body(const ChunkScanParams& p, ScanSmem& sm
             __syncwarp();
         }
 
-        // ---- G4: S_end = e^gamma_last S0 + K^T (e^(gamma_last-gamma) D), packed over key-dim pairs ----
-        {
-            const unsigned char* kb = reinterpret_cast<const unsigned char*>(&b.K[it >> 2][0][0]);
-            const int cc0 = 2 * (it & 3);
-            float2 acc[kHeadsPerKey][4];
-#pragma unroll
-            for (int m = 0; m < kHeadsPerKey; ++m) {
-                const float el = b.rec[m][REC_EG + C - 1];
-                const float2 el2 = make_float2(el, el);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) acc[m][q] = fmul2(el2, Sreg[m][q]);
-            }
-#pragma unroll 8
-            for (int t = 0; t < C; ++t) {
-                const float4 klo = *reinterpret_cast<const float4*>(kb + swz(t, cc0));
-                const float4 khi = *reinterpret_cast<const float4*>(kb + swz(t, cc0 + 1));
-#pragma unroll
-                for (int m = 0; m < kHeadsPerKey; ++m) {
-                    const float dv = sm.Dp[t][m * NC + jj];
-                    const float2 d2 = make_float2(dv, dv);
-                    acc[m][0] = ffma2(make_float2(klo.x, klo.y), d2, acc[m][0]);
-                    acc[m][1] = ffma2(make_float2(klo.z, klo.w), d2, acc[m][1]);
-                    acc[m][2] = ffma2(make_float2(khi.x, khi.y), d2, acc[m][2]);
-                    acc[m][3] = ffma2(make_float2(khi.z, khi.w), d2, acc[m][3]);
-                }
-            }
-#pragma unroll
-            for (int m = 0; m < kHeadsPerKey; ++m) {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) Sreg[m][q] = acc[m][q];
-#pragma unroll
-                for (int h4 = 0; h4 < 2; ++h4)
-                    *reinterpret_cast<float4*>(&sm.SsT[m * NC + jj][8 * it + 4 * h4]) =
-                        make_float4(acc[m][2 * h4].x, acc[m][2 * h4].y, acc[m][2 * h4 + 1].x, acc[m][2 * h4 + 1].y);
-            }
-        }
+        if constexpr (kMma)
+            g4_mma(b, sm, S);
+        else
+            g4_fma(b, sm, S);
         __syncthreads();
     }
 
@@ -514,20 +927,13 @@ __device__ __forceinline__ void scan_body(const ChunkScanParams& p, ScanSmem& sm
         return;
     }
     if (sm.flag_gave_up) return;
-#pragma unroll
-    for (int m = 0; m < kHeadsPerKey; ++m) {
-        float* sh = p.state + (static_cast<int64_t>(kh + m * n_kh) * D + 8 * it) * D + c0 + jj;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            sh[(2 * q) * D] = Sreg[m][q].x;
-            sh[(2 * q + 1) * D] = Sreg[m][q].y;
-        }
-    }
+    state_store(p, S, kh, c0);
 }
 
 // One CTA per (key head, 16 value columns); the prep kernel has run before.
+template <bool kMma>
 __global__ void __launch_bounds__(SCAN_THREADS, 1) gdn_chunk_scan_kernel(const __grid_constant__ ChunkScanParams p) {
-    scan_body(p, *aligned_dynamic_smem<ScanSmem, 1024>(), blockIdx.x, blockIdx.y * NC, nullptr, nullptr, 0u);
+    scan_body<kMma>(p, *aligned_dynamic_smem<ScanSmem, 1024>(), blockIdx.x, blockIdx.y * NC, nullptr, nullptr, 0u);
 }
 
 // 16-byte load through L2 only: out is written by other CTAs of the same launch.
@@ -594,6 +1000,7 @@ __device__ __forceinline__ void norm_units(const ChunkFusedParams& p, const int 
 // resident (a cooperative launch guarantees it).  The generation number lives in
 // device memory and the last CTA to finish advances it, so a replayed CUDA graph
 // of this launch never matches a stale flag.
+template <bool kMma>
 __global__ void __launch_bounds__(SCAN_THREADS, 1) gdn_chunk_fused_kernel(const __grid_constant__ ChunkFusedParams p) {
     __shared__ uint32_t s_gen;
     const int tid = threadIdx.x;
@@ -624,7 +1031,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) gdn_chunk_fused_kernel(const 
         if (p.y) norm_units(p, b, gen);
     } else {
         const int s = b - p.n_prep, n_kh = p.scan.n_kh;
-        scan_body(p.scan, *aligned_dynamic_smem<ScanSmem, 1024>(), s % n_kh, (s / n_kh) * NC, p.flags, p.sync + 2,
+        scan_body<kMma>(p.scan, *aligned_dynamic_smem<ScanSmem, 1024>(), s % n_kh, (s / n_kh) * NC, p.flags, p.sync + 2,
                   gen, p.y ? p.out_flags : nullptr);
     }
     __syncthreads();
@@ -655,10 +1062,11 @@ int chunk_fused_prep_ctas(int n_kh, int sm_count) {
     return n_prep >= n_kh ? n_prep : 0;
 }
 
-cudaError_t launch_chunk_fused(const ChunkFusedParams& p, cudaStream_t s) {
+cudaError_t launch_chunk_fused(const ChunkFusedParams& p, const bool mma, cudaStream_t s) {
     constexpr size_t body = sizeof(ScanSmem) > sizeof(PrepSmemT<2>) ? sizeof(ScanSmem) : sizeof(PrepSmemT<2>);
     const size_t smem = body + 1024;
-    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(gdn_chunk_fused_kernel), static_cast<int>(smem));
+    const auto kernel = mma ? gdn_chunk_fused_kernel<true> : gdn_chunk_fused_kernel<false>;
+    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kernel), static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.n_prep + (D / NC) * p.scan.n_kh);
@@ -670,15 +1078,16 @@ cudaError_t launch_chunk_fused(const ChunkFusedParams& p, cudaStream_t s) {
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gdn_chunk_fused_kernel, p);
+    return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
-cudaError_t launch_chunk_scan(const ChunkScanParams& p, cudaStream_t s) {
+cudaError_t launch_chunk_scan(const ChunkScanParams& p, const bool mma, cudaStream_t s) {
     const size_t smem = sizeof(ScanSmem) + 1024;
-    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(gdn_chunk_scan_kernel), static_cast<int>(smem));
+    const auto kernel = mma ? gdn_chunk_scan_kernel<true> : gdn_chunk_scan_kernel<false>;
+    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kernel), static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     dim3 grid(p.n_kh, D / NC);
-    gdn_chunk_scan_kernel<<<grid, SCAN_THREADS, smem, s>>>(p);
+    kernel<<<grid, SCAN_THREADS, smem, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -387,12 +387,16 @@ cudaError_t launch_chunk_scan_tc(const ChunkScanParams& p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+ScanKind chunk_scan_kind() {
+    const char* v = std::getenv("GDN_CHUNK_SCAN");
+    if (v && std::strcmp(v, "fma") == 0) return ScanKind::kFma;
+    if (v && std::strcmp(v, "tc") == 0) return ScanKind::kTcgen05;
+    return ScanKind::kMma;
+}
+
 cudaError_t launch_chunk_scan_default(const ChunkScanParams& p, cudaStream_t s) {
-    static const bool use_tc = [] {
-        const char* v = std::getenv("GDN_CHUNK_SCAN");
-        return v && std::strcmp(v, "tc") == 0;
-    }();
-    return use_tc ? launch_chunk_scan_tc(p, s) : launch_chunk_scan(p, s);
+    const ScanKind k = chunk_scan_kind();
+    return k == ScanKind::kTcgen05 ? launch_chunk_scan_tc(p, s) : launch_chunk_scan(p, k == ScanKind::kMma, s);
 }
 
 }  // namespace gdn

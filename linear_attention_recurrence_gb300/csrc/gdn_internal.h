@@ -134,15 +134,20 @@ struct ChunkFusedParams {
 int chunk_fused_prep_ctas(int n_kh, int sm_count);
 constexpr int kSyncWords = 8;  // words of ChunkFusedParams::sync
 // Fails (cudaErrorCooperativeLaunchTooLarge) when the grid cannot be resident at once.
-cudaError_t launch_chunk_fused(const ChunkFusedParams& p, cudaStream_t s);
-cudaError_t launch_chunk_scan(const ChunkScanParams& p, cudaStream_t s);
-// The same scan with the chunk's large products (K S0, Q S0, K^T D) on the tensor
-// cores as split-TF32 (3 passes); same parameters and results within tolerance.
+// `mma`: the scan's large products (K S0, Q S0, K^T D) as split-TF32 warp-level
+// tensor-core MMAs; else as packed FP32 FMAs.  Both meet the same tolerance.
+cudaError_t launch_chunk_fused(const ChunkFusedParams& p, bool mma, cudaStream_t s);
+cudaError_t launch_chunk_scan(const ChunkScanParams& p, bool mma, cudaStream_t s);
+// The same scan with the large products as split-TF32 tcgen05 MMAs (accumulators
+// in tensor memory); same parameters and results within tolerance.
 cudaError_t launch_chunk_scan_tc(const ChunkScanParams& p, cudaStream_t s);
-// The scan the entry points use: the CUDA-core scan, or the tensor-core scan when
-// the environment variable GDN_CHUNK_SCAN is "tc" (for A/B measurements: at 48
-// columns per CTA each tcgen05.mma costs a near-fixed ~80 cycles, so the two run
-// at the same speed).
+// Which scan the entry points run, from the environment variable GDN_CHUNK_SCAN
+// (read on every call, for A/B measurements): "fma" the CUDA-core products, "tc"
+// the tcgen05 scan (two launches only: at 48 columns per CTA each tcgen05.mma
+// costs a near-fixed ~80 cycles), anything else the warp-level MMA scan.
+enum class ScanKind { kFma, kMma, kTcgen05 };
+ScanKind chunk_scan_kind();
+// The two-launch scan of the selected kind.
 cudaError_t launch_chunk_scan_default(const ChunkScanParams& p, cudaStream_t s);
 int chunk_scan_box_cols();
 

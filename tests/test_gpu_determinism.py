@@ -119,27 +119,29 @@ def _sm_count():
     return torch.cuda.get_device_properties(0).multi_processor_count
 
 
+@pytest.mark.parametrize("kind", ["mma", "fma"])
 @pytest.mark.parametrize("T", [1, 130, 2048, 4099])
-def test_one_launch_chunked_matches_two_launch_bits(T):
+def test_one_launch_chunked_matches_two_launch_bits(T, kind):
     """Prep and scan in one cooperative launch (prep on the SMs the scan leaves
     free, handing records over through flags) give the same bits as the prep
     kernel followed by the scan kernel, with one launch per super-block instead
-    of two."""
+    of two; for either form of the scan's large products."""
     if _sm_count() < 9 * 16:
         pytest.skip("too few SMs for the one-launch form at 16 key heads")
     t = to_dev(make_inputs(T, seed=14, norm=False))
     n_sb = (T + 2047) // 2048
-    with _env("GDN_CHUNK_OVERLAP", "0"):
-        n0 = gdn.gdn_launch_count()
-        o2, s2 = _run(t, "chunked", [T])
-        assert gdn.gdn_launch_count() - n0 == 2 * n_sb
-    for i in range(3):
-        gdn.gdn_poison_scratch(0x7FC00000 if i % 2 == 0 else 0xFF800000)
-        n0 = gdn.gdn_launch_count()
-        o1, s1 = _run(t, "chunked", [T])
-        assert gdn.gdn_launch_count() - n0 == n_sb
-        assert np.array_equal(o1.view(np.uint32), o2.view(np.uint32))
-        assert np.array_equal(s1.view(np.uint32), s2.view(np.uint32))
+    with _env("GDN_CHUNK_SCAN", kind):
+        with _env("GDN_CHUNK_OVERLAP", "0"):
+            n0 = gdn.gdn_launch_count()
+            o2, s2 = _run(t, "chunked", [T])
+            assert gdn.gdn_launch_count() - n0 == 2 * n_sb
+        for i in range(3):
+            gdn.gdn_poison_scratch(0x7FC00000 if i % 2 == 0 else 0xFF800000)
+            n0 = gdn.gdn_launch_count()
+            o1, s1 = _run(t, "chunked", [T])
+            assert gdn.gdn_launch_count() - n0 == n_sb
+            assert np.array_equal(o1.view(np.uint32), o2.view(np.uint32))
+            assert np.array_equal(s1.view(np.uint32), s2.view(np.uint32))
 
 
 def test_one_launch_chunked_under_graph_replay():

@@ -4,6 +4,9 @@ Bar: max|diff| / max|value| <= 2e-6 for the FP32 output and the final state
 (both modes); the FP16 norm within 1 ulp of the oracle's norm of the same FP32
 input, and end to end within 1 ulp plus the propagated output tolerance.
 """
+import contextlib
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -16,8 +19,26 @@ from linear_attention_recurrence_gb300.inputs import make_inputs
 
 pytestmark = pytest.mark.gpu
 
-MODES = ("sequential", "chunked")
+# "chunked" runs the default scan (large products as split-TF32 warp-level MMAs),
+# "chunked:fma" the same scan with them as FP32 FMAs (GDN_CHUNK_SCAN=fma)
+MODES = ("sequential", "chunked", "chunked:fma")
 NAN = float("nan")
+
+
+@contextlib.contextmanager
+def _scan_env(mode):
+    """Base mode of `mode`, with GDN_CHUNK_SCAN set to its ':' suffix meanwhile."""
+    base, _, kind = mode.partition(":")
+    old = os.environ.get("GDN_CHUNK_SCAN")
+    if kind:
+        os.environ["GDN_CHUNK_SCAN"] = kind
+    try:
+        yield base
+    finally:
+        if old is None:
+            os.environ.pop("GDN_CHUNK_SCAN", None)
+        else:
+            os.environ["GDN_CHUNK_SCAN"] = old
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -35,9 +56,10 @@ def _run(t, mode, splits=None, state=None):
     out = torch.full((T,) + tuple(t["v"].shape[1:]), NAN, device=t["q"].device)
     bounds = [0] + list(np.cumsum(splits if splits else [T]))
     assert bounds[-1] == T
-    for a, b in zip(bounds[:-1], bounds[1:]):
-        gdn.gdn_recurrence(t["q"][a:b], t["k"][a:b], t["v"][a:b], t["g"][a:b], t["beta"][a:b], st,
-                           out=out[a:b], mode=mode)
+    with _scan_env(mode) as base:
+        for a, b in zip(bounds[:-1], bounds[1:]):
+            gdn.gdn_recurrence(t["q"][a:b], t["k"][a:b], t["v"][a:b], t["g"][a:b], t["beta"][a:b], st,
+                               out=out[a:b], mode=base)
     torch.cuda.synchronize()
     assert gdn.gdn_device_status() == gdn.GDN_OK
     return out, st
@@ -118,8 +140,9 @@ def test_T32768_superblocks_carried(mode):
     out = torch.full((T, 48, 128), NAN, device="cuda")
     for i in range(T // SB):
         a, b = i * SB, (i + 1) * SB
-        gdn.gdn_recurrence(t["q"][a:b], t["k"][a:b], t["v"][a:b], t["g"][a:b], t["beta"][a:b], st,
-                           out=out[a:b], mode=mode)
+        with _scan_env(mode) as base:
+            gdn.gdn_recurrence(t["q"][a:b], t["k"][a:b], t["v"][a:b], t["g"][a:b], t["beta"][a:b], st,
+                               out=out[a:b], mode=base)
         o_ref, s_ref = oracle.recurrence(x["q"][a:b], x["k"][a:b], x["v"][a:b], x["g"][a:b], x["beta"][a:b],
                                          s_ref)
         es = rel_err(st.cpu().numpy(), s_ref)
@@ -160,7 +183,8 @@ def test_T0_is_noop(mode):
     t = to_dev(x)
     st = t["S0"].clone()
     out = torch.full((0, 48, 128), NAN, device="cuda")
-    gdn.gdn_recurrence(t["q"][:0], t["k"][:0], t["v"][:0], t["g"][:0], t["beta"][:0], st, out=out, mode=mode)
+    with _scan_env(mode) as base:
+        gdn.gdn_recurrence(t["q"][:0], t["k"][:0], t["v"][:0], t["g"][:0], t["beta"][:0], st, out=out, mode=base)
     torch.cuda.synchronize()
     assert torch.equal(st, t["S0"])
 
