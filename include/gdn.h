@@ -65,7 +65,7 @@ typedef enum gdn_mode {
 
 /* Token count from which GDN_AUTO takes the chunked form: the measured crossover
  * of the two modes' GPU time per call on GB300 (48 value heads, d = 128). */
-#define GDN_AUTO_CHUNKED_MIN_T 128
+#define GDN_AUTO_CHUNKED_MIN_T 64
 
 typedef enum gdn_status {
     GDN_OK = 0,

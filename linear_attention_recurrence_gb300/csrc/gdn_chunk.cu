@@ -548,11 +548,11 @@ __device__ __forceinline__ void p2_mma(const ScanBuf& b, ScanSmem& sm) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     const int m = warp >> 1, na = warp & 1, nb = 3 - na;
     const float* tp = &b.rec[m][REC_TP];
-    float acc[2][4], accx[2][4];
+    float acc[2][4], accx[2][4], accy[2][4];
 #pragma unroll
     for (int i = 0; i < 2; ++i)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[i][e] = accx[i][e] = 0.f;
+        for (int e = 0; e < 4; ++e) acc[i][e] = accx[i][e] = accy[i][e] = 0.f;
 #pragma unroll
     for (int kk = 0; kk < C / 8; ++kk) {
         if (kk > nb) break;
@@ -565,8 +565,8 @@ __device__ __forceinline__ void p2_mma(const ScanBuf& b, ScanSmem& sm) {
         if (both) mma_tf32(acc[0], ah, bh[0]);
         mma_tf32(accx[1], ah, bl[1]);
         if (both) mma_tf32(accx[0], ah, bl[0]);
-        mma_tf32(accx[1], al, bh[1]);
-        if (both) mma_tf32(accx[0], al, bh[0]);
+        mma_tf32(accy[1], al, bh[1]);
+        if (both) mma_tf32(accy[0], al, bh[0]);
     }
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
@@ -574,7 +574,7 @@ __device__ __forceinline__ void p2_mma(const ScanBuf& b, ScanSmem& sm) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int col = m * NC + g + 8 * (e >> 1), tok = 8 * nn + 2 * t + (e & 1);
-            const float d = acc[i][e] + accx[i][e];
+            const float d = acc[i][e] + (accx[i][e] + accy[i][e]);
             sm.Dm[tok][col] = d;
             sm.Dp[tok][col] = b.rec[m][REC_ER + tok] * d;
         }
@@ -587,14 +587,14 @@ __device__ __forceinline__ void p3_mma(const ChunkScanParams& p, const ScanBuf& 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     const int m = warp >> 1, na = warp & 1, nb = 3 - na;
     const float* pt = &b.rec[m][REC_PT];
-    float acc[2][4], accx[2][4];
+    float acc[2][4], accx[2][4], accy[2][4];
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
         const int nn = i ? nb : na;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             acc[i][e] = sm.W[C + 8 * nn + 2 * t + (e & 1)][m * NC + g + 8 * (e >> 1)];
-            accx[i][e] = 0.f;
+            accx[i][e] = accy[i][e] = 0.f;
         }
     }
 #pragma unroll
@@ -609,8 +609,8 @@ __device__ __forceinline__ void p3_mma(const ChunkScanParams& p, const ScanBuf& 
         if (both) mma_tf32(acc[0], ah, bh[0]);
         mma_tf32(accx[1], ah, bl[1]);
         if (both) mma_tf32(accx[0], ah, bl[0]);
-        mma_tf32(accx[1], al, bh[1]);
-        if (both) mma_tf32(accx[0], al, bh[0]);
+        mma_tf32(accy[1], al, bh[1]);
+        if (both) mma_tf32(accy[0], al, bh[0]);
     }
     const int h = kh + m * p.n_kh;
     float* o = p.out + ((p.t_begin + static_cast<int64_t>(c) * C) * p.n_vh + h) * D + c0;
@@ -620,7 +620,7 @@ __device__ __forceinline__ void p3_mma(const ChunkScanParams& p, const ScanBuf& 
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int tok = 8 * nn + 2 * t + (e & 1);
-            if (tok < nt) o[static_cast<int64_t>(tok) * p.n_vh * D + g + 8 * (e >> 1)] = acc[i][e] + accx[i][e];
+            if (tok < nt) o[static_cast<int64_t>(tok) * p.n_vh * D + g + 8 * (e >> 1)] = acc[i][e] + (accx[i][e] + accy[i][e]);
         }
     }
 }
@@ -688,15 +688,20 @@ __device__ __forceinline__ void g4_mma(const ScanBuf& b, ScanSmem& sm, ScanState
     };
     float av[2][4], bv[2][2 * NCC / 8];
     load(0, av[0], bv[0]);
+    // the state from its transposed copy (the values the registers held: left dead
+    // through the phases before, they free 24 registers there)
+    const int key = mma_key(warp, g);
     float sx[NCC / 8][4];
 #pragma unroll
     for (int n = 0; n < NCC / 8; ++n) {
         const float el = b.rec[n >> 1][REC_EG + C - 1];
+        const int col = 8 * n + 2 * t;
+        S.v[n][0] = sm.SsT[col][key] * el;
+        S.v[n][1] = sm.SsT[col + 1][key] * el;
+        S.v[n][2] = sm.SsT[col][key + 4] * el;
+        S.v[n][3] = sm.SsT[col + 1][key + 4] * el;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            S.v[n][i] *= el;
-            sx[n][i] = 0.f;
-        }
+        for (int i = 0; i < 4; ++i) sx[n][i] = 0.f;
     }
 #pragma unroll
     for (int j = 0; j < C / 8; ++j) {  // tokens 8j .. 8j + 7
@@ -714,7 +719,6 @@ __device__ __forceinline__ void g4_mma(const ScanBuf& b, ScanSmem& sm, ScanState
 #pragma unroll
         for (int n = 0; n < NCC / 8; ++n) mma_tf32(sx[n], al, bh[n]);
     }
-    const int key = mma_key(warp, g);
 #pragma unroll
     for (int n = 0; n < NCC / 8; ++n) {
 #pragma unroll

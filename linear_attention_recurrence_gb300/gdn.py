@@ -22,7 +22,7 @@ LIB_PATH = os.path.join(_PKG, "libgdn.so")
 GDN_SEQUENTIAL = 0
 GDN_CHUNKED = 1
 GDN_AUTO = 2
-GDN_AUTO_CHUNKED_MIN_T = 128
+GDN_AUTO_CHUNKED_MIN_T = 64
 GDN_OK = 0
 GDN_ERR_INVALID_ARG = -1
 GDN_ERR_UNSUPPORTED = -2

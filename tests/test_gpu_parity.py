@@ -19,9 +19,10 @@ from linear_attention_recurrence_gb300.inputs import make_inputs
 
 pytestmark = pytest.mark.gpu
 
-# "chunked" runs the default scan (large products as split-TF32 warp-level MMAs),
-# "chunked:fma" the same scan with them as FP32 FMAs (GDN_CHUNK_SCAN=fma)
-MODES = ("sequential", "chunked", "chunked:fma")
+# "chunked" runs the default scan (its products as split-TF32 warp-level MMAs),
+# "chunked:fma" the same scan with them as FP32 FMAs (GDN_CHUNK_SCAN=fma), "chunked:tc"
+# the two-launch scan with its S0 products as split-TF32 tcgen05 MMAs (GDN_CHUNK_SCAN=tc)
+MODES = ("sequential", "chunked", "chunked:fma", "chunked:tc")
 NAN = float("nan")
 
 
