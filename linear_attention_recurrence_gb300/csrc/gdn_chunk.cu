@@ -24,9 +24,12 @@
 // When the SMs the scan leaves free number at least n_kh, one cooperative launch
 // runs both: the prep on those SMs, chunk by chunk ahead of the scan, which waits
 // on a per-(chunk, key head) flag instead of a kernel boundary (gdn_chunk_fused_kernel).
-// The large products (K S0, Q S0, K^T D) run as register-tiled packed FP32x2 FMAs;
-// the tolerance the path is held to (2e-6 relative to FP64) leaves no room for
-// TF32 tensor-core inputs there.
+// By default every product (K K^T and Q K^T in the prep; K S0, Q S0, T'U', P D and
+// K^T D' in the scan) runs on the tensor cores as warp-level m16n8k8 TF32 MMAs on
+// split operands (three MMAs per FP32 product, see "products on the tensor cores"
+// below): plain TF32 inputs would miss the 2e-6 tolerance (relative to FP64) the
+// path is held to by three orders of magnitude.  The scan's products as
+// register-tiled packed FP32x2 FMAs remain selectable (the FMA form).
 #include "gdn_device.cuh"
 #include "gdn_internal.h"
 #include "gdn_norm_row.cuh"
