@@ -706,8 +706,14 @@ def main():
     flop = FLOP_SEQ if args.mode == "sequential" else FLOP_CHUNKED
     achieved = flop * CT / (kern["rec_call_ms"] * 1e-3) / 1e12
     per_call = (kern["launches"] / args.steps - 1) / ncalls  # the norm is one launch per step
-    chunk_label = ("gdn_chunk_fused_kernel (prep and scan in one launch) per 2048-token call" if per_call < 1.5
-                   else "gdn_chunk_prep_kernel + gdn_chunk_scan_kernel per 2048-token call")
+    scan_kind = os.environ.get("GDN_CHUNK_SCAN", "")
+    products = {"fma": "products as packed FP32 FMAs",
+                "tc": "S0 products as split-TF32 tcgen05 MMAs"}.get(scan_kind, "products as split-TF32 mma.sync MMAs")
+    one_launch = per_call < 1.5
+    chunk_label = (("gdn_chunk_fused_kernel (prep and scan in one launch) per 2048-token call" if one_launch
+                    else "gdn_chunk_prep_kernel + gdn_chunk_scan_kernel per 2048-token call") + ", " + products)
+    # the capture in profiles/dram_traffic.md is of the default one-launch kernel
+    chunk_traffic = captured_traffic("gdn_chunk.cu") if one_launch and scan_kind not in ("fma", "tc") else None
     norm_gbs = BYTES_NORM * T / (kern["norm_ms"] * 1e-3) / 1e9
     value = main_res["ms_per_step"] * 1e3 / (T * ws)  # already the max over ranks
     line = {
@@ -723,7 +729,7 @@ def main():
         "gpu_launches": main_res["launches"],
         "roofline": {"bound": "alu", "achieved": achieved, "peak": alu_peak_tflops, "unit": "TFLOP/s",
                      "frac": achieved / alu_peak_tflops,
-                     "traffic": captured_traffic("gdn_chunk.cu" if args.mode == "chunked" else "gdn_seq.cu"),
+                     "traffic": chunk_traffic if args.mode == "chunked" else captured_traffic("gdn_seq.cu"),
                      "kernel": chunk_label if args.mode == "chunked" else "gdn_seq_kernel per 2048-token call",
                      "peak_basis": f"{sms} SMs x 128 FP32 lanes x 2 x {sm_mhz_max:.0f} MHz ({peak_src} max clock)",
                      "frac_at_observed_clock": (achieved / (sms * FP32_LANES_PER_SM * 2 * clocks["sm_mhz"] * 1e6
