@@ -490,7 +490,7 @@ __device__ __forceinline__ void g1_mma(const ScanBuf& b, ScanSmem& sm) {
         for (int i = 0; i < 4; ++i) acc[n][i] = accx[n][i] = 0.f;
     float av[2][4], bv[2][6];
     load(0, av[0], bv[0]);
-#pragma unroll 4
+#pragma unroll
     for (int j = 0; j < D / 8; ++j) {  // key dims 8j .. 8j + 7
         const int cur = j & 1;
         if (j + 1 < D / 8) load(j + 1, av[cur ^ 1], bv[cur ^ 1]);

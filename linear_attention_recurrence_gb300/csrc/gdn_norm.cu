@@ -6,7 +6,7 @@
 //
 // HBM-bound (per row: 512 B of o, 512 B of z read, 256 B of y written).  One warp
 // per row, one float4 of o and of z per lane, streamed past L1; two rows in flight
-// per warp and a grid of 4 CTAs of 256 threads per SM, grid-striding.
+// per warp and a grid of 8 CTAs of 128 threads per SM, grid-striding.
 #include <cuda_fp16.h>
 
 #include "gdn_device.cuh"
@@ -16,11 +16,12 @@
 namespace gdn {
 namespace {
 
-// 256-thread CTAs (4 per SM): small enough (threads, registers, no shared memory)
-// to run beside a one-launch chunked recurrence CTA, so a norm on a second stream
-// overlaps the next recurrence call instead of delaying its launch.
-constexpr int kThreads = 256;
-constexpr int kCtasPerSm = 4;
+// 128-thread CTAs (8 per SM): small enough (threads, registers, no shared memory)
+// for one to run beside a one-launch chunked recurrence CTA (256 threads of up to
+// 208 registers), so a norm on a second stream overlaps the next recurrence call
+// instead of delaying its launch.
+constexpr int kThreads = 128;
+constexpr int kCtasPerSm = 8;
 constexpr int kRowsInFlight = 2;
 
 __device__ __forceinline__ float4 ld_stream(const float* p) {
