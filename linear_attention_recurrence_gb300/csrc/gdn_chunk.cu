@@ -308,6 +308,10 @@ struct ScanSmem {
 };
 static_assert(sizeof(ScanSmem) + 1024 <= 227 * 1024, "scan shared memory");
 static_assert(kHeadsPerKey * C * C % 256 == 0, "prep A / P loop");
+// g1_mma's exchange of partial sums: 8 warps x 12 floats x 32 lanes in Dm, Dp
+static_assert(offsetof(ScanSmem, Dp) == offsetof(ScanSmem, Dm) + sizeof(float) * C * WST &&
+                  2 * C * WST >= 8 * 12 * 32,
+              "g1_mma exchange space");
 
 // byte offset of float4 chunk `cc` (0..7) of row `r` in a 128-byte-swizzled box
 __device__ __forceinline__ int swz(int r, int cc) { return r * 128 + ((cc ^ (r & 7)) << 4); }
@@ -459,68 +463,96 @@ __device__ __forceinline__ void g1_fma(const ScanBuf& b, ScanSmem& sm) {
     }
 }
 
-// MMA form: warp w computes rows 16*(w&3)..+15 of [K; Q] (K for w&3 < 2) times
-// the CTA's columns 24*(w>>2)..+23 (three n8 tiles), over the 16 k8 steps of the
-// key dims; A from the swizzled k / q box (row & 7 == g, so the four loads of a
-// fragment hit 32 banks), B from SsT (row stride 132: 32 banks).  Each step's
-// operands are loaded while the step before issues its MMAs.
+// MMA form: warp w sums key dims 64 (w >> 2) .. +63 (8 k8 steps) for the 32 rows of
+// K (w & 1 == 0) or Q times the CTA's columns 24 ((w >> 1) & 1) .. +23: two m16
+// tiles x three n8 tiles, so each split fragment feeds two or three MMAs (0.78
+// splits per MMA instead of 1.11 with one m16 tile over all key dims; the splits'
+// integer work bounds the issue rate).  A from the swizzled k / q box (row & 7 ==
+// g: the fragment loads hit 32 banks), B from SsT (row stride 132: 32 banks); each
+// step's operands load while the step before issues its MMAs.  The two key-dim
+// halves meet through shared memory (the Dm / Dp space, free until P2): warp w
+// finishes row tile w >> 2 and hands the other to warp w ^ 4, so the result is the
+// same sum in the same order for every element.
 __device__ __forceinline__ void g1_mma(const ScanBuf& b, ScanSmem& sm) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const int mt = warp & 3, ng = warp >> 2;
-    const unsigned char* xa = reinterpret_cast<const unsigned char*>(mt < 2 ? &b.K[0][0][0] : &b.Q[0][0][0]) +
-                              (16 * (mt & 1) + g) * 128 + 4 * t;
+    const int h = warp >> 2, xq = warp & 1, ng = (warp >> 1) & 1;  // key-dim half, K or Q, column group
+    const unsigned char* xa = reinterpret_cast<const unsigned char*>(xq ? &b.Q[0][0][0] : &b.K[0][0][0]) +
+                              g * 128 + 4 * t;
     const float* sb = &sm.SsT[24 * ng + g][t];
-    auto load = [&](const int j, float (&av)[4], float (&bv)[6]) {
+    auto load = [&](const int j, float (&av)[8], float (&bv)[6]) {
         const unsigned char* xr = xa + (j >> 2) * (C * 128);
         const int ca = ((2 * (j & 3)) ^ g) << 4, cb = ((2 * (j & 3) + 1) ^ g) << 4;
-        av[0] = ldsf(xr + ca);
-        av[1] = ldsf(xr + 1024 + ca);
-        av[2] = ldsf(xr + cb);
-        av[3] = ldsf(xr + 1024 + cb);
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            av[4 * r + 0] = ldsf(xr + 2048 * r + ca);
+            av[4 * r + 1] = ldsf(xr + 2048 * r + 1024 + ca);
+            av[4 * r + 2] = ldsf(xr + 2048 * r + cb);
+            av[4 * r + 3] = ldsf(xr + 2048 * r + 1024 + cb);
+        }
 #pragma unroll
         for (int n = 0; n < 3; ++n) {
             bv[2 * n] = sb[8 * n * SST + 8 * j];
             bv[2 * n + 1] = sb[8 * n * SST + 8 * j + 4];
         }
     };
-    float acc[3][4], accx[3][4];
+    float acc[2][3][4], accx[2][3][4];
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int n = 0; n < 3; ++n)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[r][n][i] = accx[r][n][i] = 0.f;
+    float av[2][8], bv[2][6];
+    load(8 * h, av[0], bv[0]);
+#pragma unroll
+    for (int jj = 0; jj < D / 16; ++jj) {
+        const int j = 8 * h + jj, cur = jj & 1;
+        if (jj + 1 < D / 16) load(j + 1, av[cur ^ 1], bv[cur ^ 1]);
+        uint32_t ah[2][4], al[2][4], bh[3][2], bl[3][2];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) split_tf32(av[cur][i], ah[i >> 2][i & 3], al[i >> 2][i & 3]);
+#pragma unroll
+        for (int i = 0; i < 6; ++i) split_tf32(bv[cur][i], bh[i >> 1][i & 1], bl[i >> 1][i & 1]);
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+            for (int n = 0; n < 3; ++n) mma_tf32(acc[r][n], ah[r], bh[n]);
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+            for (int n = 0; n < 3; ++n) mma_tf32(accx[r][n], ah[r], bl[n]);
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+            for (int n = 0; n < 3; ++n) mma_tf32(accx[r][n], al[r], bh[n]);
+    }
+    // the partner's row tile (1 - h) out, then this warp's row tile h in (half 0 + half 1)
+    float* xchg = &sm.Dm[0][0];
 #pragma unroll
     for (int n = 0; n < 3; ++n)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) acc[n][i] = accx[n][i] = 0.f;
-    float av[2][4], bv[2][6];
-    load(0, av[0], bv[0]);
-#pragma unroll
-    for (int j = 0; j < D / 8; ++j) {  // key dims 8j .. 8j + 7
-        const int cur = j & 1;
-        if (j + 1 < D / 8) load(j + 1, av[cur ^ 1], bv[cur ^ 1]);
-        uint32_t ah[4], al[4], bh[3][2], bl[3][2];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) split_tf32(av[cur][i], ah[i], al[i]);
-#pragma unroll
-        for (int i = 0; i < 6; ++i) split_tf32(bv[cur][i], bh[i >> 1][i & 1], bl[i >> 1][i & 1]);
-        // grouped by term, so that no MMA waits on the one just before it
-#pragma unroll
-        for (int n = 0; n < 3; ++n) mma_tf32(acc[n], ah, bh[n]);
-#pragma unroll
-        for (int n = 0; n < 3; ++n) mma_tf32(accx[n], ah, bl[n]);
-#pragma unroll
-        for (int n = 0; n < 3; ++n) mma_tf32(accx[n], al, bh[n]);
-    }
+        for (int i = 0; i < 4; ++i)
+            xchg[(warp * 12 + 4 * n + i) * 32 + lane] = h ? acc[0][n][i] + accx[0][n][i] : acc[1][n][i] + accx[1][n][i];
+    __syncthreads();
 #pragma unroll
     for (int n = 0; n < 3; ++n) {
         const int col = 24 * ng + 8 * n + 2 * t, m = col >> 4, jc = col & 15;
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
-            const int tk = 16 * (mt & 1) + g + 8 * hf;
-            const float x0 = acc[n][2 * hf] + accx[n][2 * hf];
-            const float x1 = acc[n][2 * hf + 1] + accx[n][2 * hf + 1];
+            const int tk = 16 * h + g + 8 * hf;
+            float x[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int i = 2 * hf + e;
+                const float own = h ? acc[1][n][i] + accx[1][n][i] : acc[0][n][i] + accx[0][n][i];
+                x[e] = own + xchg[((warp ^ 4) * 12 + 4 * n + i) * 32 + lane];
+            }
             const float eg = b.rec[m][REC_EG + tk];
-            if (mt < 2) {
+            if (!xq) {
                 const float2 v = *reinterpret_cast<const float2*>(&b.V[m][tk][jc]);
-                *reinterpret_cast<float2*>(&sm.W[tk][col]) = make_float2(v.x - eg * x0, v.y - eg * x1);
+                *reinterpret_cast<float2*>(&sm.W[tk][col]) = make_float2(v.x - eg * x[0], v.y - eg * x[1]);
             } else {
-                *reinterpret_cast<float2*>(&sm.W[C + tk][col]) = make_float2(eg * x0, eg * x1);
+                *reinterpret_cast<float2*>(&sm.W[C + tk][col]) = make_float2(eg * x[0], eg * x[1]);
             }
         }
     }
