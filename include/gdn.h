@@ -91,6 +91,11 @@ typedef enum gdn_status {
  * chunks (other FP32 rounding; within 2e-6 of the FP64 result, relative to
  * the largest magnitude).  GDN_AUTO picks one of the two by T per call (so a
  * sequence split into calls of different lengths may mix the two roundings).
+ * GDN_CHUNKED computes the chunk's products on the tensor cores as three TF32
+ * MMAs per FP32 product (split operands; same 2e-6 bound).  Environment
+ * variables read on every call, for A/B measurements: GDN_CHUNK_SCAN=fma (the
+ * products as FP32 FMAs) or =tc (tcgen05 for the state products, two launches);
+ * GDN_CHUNK_OVERLAP=0 (prep and scan as two launches instead of one).
  *
  * Supported shapes: d == 128 and n_vh == 3 * n_kh (n_kh >= 1).  T == 0 is a
  * no-op returning GDN_OK.  The first GDN_CHUNKED call on a device allocates the
