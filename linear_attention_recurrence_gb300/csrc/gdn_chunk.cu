@@ -323,7 +323,8 @@ __device__ __forceinline__ float ldsf(const unsigned char* p) { return *reinterp
 //  * FMA: thread (it = tid / 16, jj = tid % 16) holds key dims 8 it .. 8 it + 7 of
 //    column jj of each head, as pairs of consecutive key dims;
 //  * MMA: warp w holds 16 key dims (mma_key) of all 48 columns as six m16n8
-//    accumulator tiles (rows = key dims, columns = the CTA's columns 8n .. 8n + 7).
+//    accumulator tiles (rows = key dims, columns = the CTA's columns 8n .. 8n + 7);
+//    the update reloads them from SsT, so between updates they are dead.
 template <bool kMma>
 struct ScanState;
 template <>
@@ -534,9 +535,25 @@ __device__ __forceinline__ void g1_mma(const ScanBuf& b, ScanSmem& sm) {
         for (int i = 0; i < 4; ++i)
             xchg[(warp * 12 + 4 * n + i) * 32 + lane] = h ? acc[0][n][i] + accx[0][n][i] : acc[1][n][i] + accx[1][n][i];
     __syncthreads();
+    // every load of the epilogue first, then the stores (the compiler cannot tell
+    // the stores into W from the loads of xchg, V and the records apart)
+    float xo[3][4], eg[3][2];
+    float2 vv[3][2];
 #pragma unroll
     for (int n = 0; n < 3; ++n) {
         const int col = 24 * ng + 8 * n + 2 * t, m = col >> 4, jc = col & 15;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) xo[n][i] = xchg[((warp ^ 4) * 12 + 4 * n + i) * 32 + lane];
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            const int tk = 16 * h + g + 8 * hf;
+            eg[n][hf] = b.rec[m][REC_EG + tk];
+            vv[n][hf] = xq ? make_float2(0.f, 0.f) : *reinterpret_cast<const float2*>(&b.V[m][tk][jc]);
+        }
+    }
+#pragma unroll
+    for (int n = 0; n < 3; ++n) {
+        const int col = 24 * ng + 8 * n + 2 * t;
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
             const int tk = 16 * h + g + 8 * hf;
@@ -545,14 +562,13 @@ __device__ __forceinline__ void g1_mma(const ScanBuf& b, ScanSmem& sm) {
             for (int e = 0; e < 2; ++e) {
                 const int i = 2 * hf + e;
                 const float own = h ? acc[1][n][i] + accx[1][n][i] : acc[0][n][i] + accx[0][n][i];
-                x[e] = own + xchg[((warp ^ 4) * 12 + 4 * n + i) * 32 + lane];
+                x[e] = own + xo[n][i];
             }
-            const float eg = b.rec[m][REC_EG + tk];
             if (!xq) {
-                const float2 v = *reinterpret_cast<const float2*>(&b.V[m][tk][jc]);
-                *reinterpret_cast<float2*>(&sm.W[tk][col]) = make_float2(v.x - eg * x[0], v.y - eg * x[1]);
+                *reinterpret_cast<float2*>(&sm.W[tk][col]) =
+                    make_float2(vv[n][hf].x - eg[n][hf] * x[0], vv[n][hf].y - eg[n][hf] * x[1]);
             } else {
-                *reinterpret_cast<float2*>(&sm.W[C + tk][col]) = make_float2(eg * x[0], eg * x[1]);
+                *reinterpret_cast<float2*>(&sm.W[C + tk][col]) = make_float2(eg[n][hf] * x[0], eg[n][hf] * x[1]);
             }
         }
     }
@@ -564,7 +580,7 @@ __device__ __forceinline__ void g1_mma(const ScanBuf& b, ScanSmem& sm) {
 //     D^T = U'^T T'^T,   O^T = (e^gamma Q S0)^T + D^T P^T.
 // T' and P are lower triangular (the records hold their zeros), so token tile nn
 // needs only the k steps kk <= nn: 10 of 16.  Warp w < 6 takes head w / 2 and the
-// token tiles {w % 2, 3 - w % 2}, four k steps per warp in all.
+// token tiles {w % 2, 3 - w % 2}: five k steps per warp.
 __device__ __forceinline__ void load_a_cols(const float (*x)[WST], const int kk, const int col0, const int g,
                                             const int t, uint32_t (&ah)[4], uint32_t (&al)[4]) {
     split_tf32(x[8 * kk + t][col0 + g], ah[0], al[0]);
@@ -603,6 +619,12 @@ __device__ __forceinline__ void p2_mma(const ScanBuf& b, ScanSmem& sm) {
         mma_tf32(accy[1], al, bh[1]);
         if (both) mma_tf32(accy[0], al, bh[0]);
     }
+    // the records' e^(gamma_last - gamma) first, then the stores
+    float er[2][2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) er[i][e] = b.rec[m][REC_ER + 8 * (i ? nb : na) + 2 * t + e];
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
         const int nn = i ? nb : na;
@@ -611,7 +633,7 @@ __device__ __forceinline__ void p2_mma(const ScanBuf& b, ScanSmem& sm) {
             const int col = m * NC + g + 8 * (e >> 1), tok = 8 * nn + 2 * t + (e & 1);
             const float d = acc[i][e] + (accx[i][e] + accy[i][e]);
             sm.Dm[tok][col] = d;
-            sm.Dp[tok][col] = b.rec[m][REC_ER + tok] * d;
+            sm.Dp[tok][col] = er[i][e & 1] * d;
         }
     }
 }
@@ -767,8 +789,8 @@ __device__ __forceinline__ void g4_mma(const ScanBuf& b, ScanSmem& sm, ScanState
 }
 
 // The scan of key head `kh`, value columns c0..c0+15 of its three heads, over the
-// super-block's chunks, with the two large products as FP32 FMAs (kMma false) or
-// split-TF32 tensor-core MMAs (kMma true).  With `flags` set, chunk c's prep
+// super-block's chunks, with the products as FP32 FMAs (kMma false) or all of them
+// as split-TF32 tensor-core MMAs (kMma true).  With `flags` set, chunk c's prep
 // records are read only once flags[c * n_kh + kh] == gen (records written by
 // other CTAs of the same launch); a flag wait that runs out records the flag's
 // index, its last value and `gen` in diag[0..2].  A wait that runs out is
