@@ -220,17 +220,30 @@ __device__ __forceinline__ void prep_task(const ChunkPrepParams& p, PrepSmem& sm
     }
     __syncthreads();
 
-    // A (shared memory) and P^T, e^gamma, e^(gamma_last - gamma) (records).
-#pragma unroll 4
-    for (int r = 0; r < kHeadsPerKey * C * C / PREP_THREADS; ++r) {
-        const int idx = tid + r * PREP_THREADS;
-        const int m = idx / (C * C), i = (idx / C) % C, t = idx % C;
-        float* rec = p.prep + (static_cast<int64_t>(ci) * p.n_vh + kh + m * p.n_kh) * REC;
-        const bool lower = i <= t;
-        const float e = lower ? expf(sm.gam[m][t] - sm.gam[m][i]) : 0.f;
-        const float kk = sm.KK[0][t][i] + sm.KK[1][t][i], qk = sm.QK[0][t][i] + sm.QK[1][t][i];
-        sm.A[m][t][i] = (i < t) ? sm.bet[m][t] * e * kk : 0.f;
-        rec[REC_PT + i * C + t] = lower ? e * qk : 0.f;
+    // A (shared memory) and P^T, e^gamma, e^(gamma_last - gamma) (records), four
+    // entries per thread at a time: their shared loads first, then the stores (the
+    // compiler cannot tell the stores into A from the loads apart)
+#pragma unroll 1
+    for (int r0 = 0; r0 < kHeadsPerKey * C * C / PREP_THREADS; r0 += 4) {
+        float av[4], pv[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int idx = tid + (r0 + r) * PREP_THREADS;
+            const int m = idx / (C * C), i = (idx / C) % C, t = idx % C;
+            const bool lower = i <= t;
+            const float e = lower ? expf(sm.gam[m][t] - sm.gam[m][i]) : 0.f;
+            const float kk = sm.KK[0][t][i] + sm.KK[1][t][i], qk = sm.QK[0][t][i] + sm.QK[1][t][i];
+            av[r] = (i < t) ? sm.bet[m][t] * e * kk : 0.f;
+            pv[r] = lower ? e * qk : 0.f;
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int idx = tid + (r0 + r) * PREP_THREADS;
+            const int m = idx / (C * C), i = (idx / C) % C, t = idx % C;
+            float* rec = p.prep + (static_cast<int64_t>(ci) * p.n_vh + kh + m * p.n_kh) * REC;
+            sm.A[m][t][i] = av[r];
+            rec[REC_PT + i * C + t] = pv[r];
+        }
     }
     if (tid < kHeadsPerKey * C) {
         const int m = tid / C, t = tid % C;
