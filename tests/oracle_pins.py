@@ -204,6 +204,14 @@ def pin_chunked_equals_sequential(orc):
             oc, STc = orc.chunked(q, k, v, g, beta, S0, 32, nthreads=1)
             assert _rel(oc, o) < 1e-12, ("out", shape, T, _rel(oc, o))
             assert _rel(STc, ST) < 1e-12, ("state", shape, T, _rel(STc, ST))
+    # the algebra holds for any chunk size (only rounding depends on it): 16 and 64,
+    # across their chunk edges and with partial last chunks
+    for C, Ts in ((16, (15, 16, 17, 50)), (64, (63, 64, 65, 130))):
+        for T in Ts:
+            q, k, v, g, beta, S0 = _rand_inputs(rng, T, **SMALL)
+            o, ST = orc.recurrence(q, k, v, g, beta, S0, nthreads=1)
+            oc, STc = orc.chunked(q, k, v, g, beta, S0, C, nthreads=1)
+            assert _rel(oc, o) < 1e-12 and _rel(STc, ST) < 1e-12, (C, T, _rel(oc, o), _rel(STc, ST))
     # a chunk size of 1 is the sequential recurrence token by token
     q, k, v, g, beta, S0 = _rand_inputs(rng, 9, **SMALL)
     o, ST = orc.recurrence(q, k, v, g, beta, S0, nthreads=1)
