@@ -106,11 +106,12 @@ class Clocks:
         self.index = index
         self.proc = None
         self.window = None
+        self.windows = []
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -119,6 +120,11 @@ class Clocks:
     def mark(self, t_begin: float, t_end: float):
         """Wall-clock bounds of the timed region (time.time())."""
         self.window = (t_begin, t_end)
+        self.windows.append((t_begin, t_end))
+
+    def add_window(self, t_begin: float, t_end: float):
+        """Wall-clock bounds of another GPU-timed pass (per-kernel, other mode, C3, C5)."""
+        self.windows.append((t_begin, t_end))
 
     def __exit__(self, *a):
         self.out = ""
@@ -130,9 +136,12 @@ class Clocks:
                 self.proc.kill()
                 self.out, _ = self.proc.communicate()
 
-    def summary(self):
+    def summary(self, all_windows: bool = False):
+        """Clocks and throttle reasons in the timed region (or, with all_windows, in
+        every GPU-timed pass marked)."""
         import datetime
 
+        wins = self.windows if all_windows else ([self.window] if self.window else [])
         rows = []
         for ln in (self.out or "").splitlines():
             parts = [p.strip() for p in ln.split(",")]
@@ -141,7 +150,7 @@ class Clocks:
                     ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
                 except ValueError:
                     continue
-                if self.window is None or self.window[0] <= ts <= self.window[1]:
+                if not wins or any(a <= ts <= b for a, b in wins):
                     rows.append(parts)
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
@@ -177,6 +186,44 @@ def cpu_baseline(tokens_target_s: float = 10.0, seed: int = 0):
     return {"value": dt / T * 1e6, "unit": "µs/token/layer", "cores": nt, "kind": "oracle",
             "sample": f"first {T} tokens of the T=32768 workload, 48 value heads, FP64 recurrence + norm, "
                       f"{nt} OpenMP threads, {dt:.1f} s"}
+
+
+def oracle_t8192(seed: int = 0):
+    """The FP64 oracle (unchanged) at the T = 8192 configuration (recurrence + norm,
+    one layer): single-thread and all-core wall times.  The all-core run is the
+    cpu_baseline of the headline line."""
+    import oracle
+    from linear_attention_recurrence_gb300.inputs import make_inputs
+
+    T = 8192
+    nt = oracle.max_threads()
+    x = make_inputs(T, seed=seed)
+    res = {}
+    for threads in (nt, 1):
+        t0 = time.perf_counter()
+        o, _ = oracle.recurrence(x["q"], x["k"], x["v"], x["g"], x["beta"], x["S0"], nthreads=threads)
+        oracle.out_norm(o, x["z"], x["w"], 1e-6, nthreads=threads)
+        res[threads] = time.perf_counter() - t0
+    return {"value": res[nt] / T * 1e6, "unit": "µs/token/layer", "cores": nt, "kind": "oracle",
+            "sample": f"T=8192 (the first 8192 tokens of the workload), 48 value heads, FP64 recurrence + norm, "
+                      f"{nt} OpenMP threads: {res[nt]:.2f} s; 1 thread: {res[1]:.2f} s",
+            "t8192_all_cores_s": res[nt], "t8192_one_thread_s": res[1],
+            "one_thread_us_per_token_layer": res[1] / T * 1e6}
+
+
+def _stack_layer_inputs(layer: int):
+    from linear_attention_recurrence_gb300.inputs import make_inputs
+
+    return make_inputs(2048, seed=0, layer=layer)
+
+
+def stack_inputs_async(n_layers: int):
+    """Start drawing the stack's per-layer inputs (2048 tokens each, each layer its
+    own seed) on the host cores in a spawn pool; returns (pool, async result)."""
+    import multiprocessing as mp
+
+    pool = mp.get_context("spawn").Pool(processes=max(1, min(16, os.cpu_count() or 1)))
+    return pool, pool.map_async(_stack_layer_inputs, range(n_layers))
 
 
 def run_reference(args):
@@ -248,28 +295,18 @@ def run_sweep(args):
     return 0
 
 
-def run_stack(args):
-    """A stack of L independent layers, 2048 tokens each (every layer its own seeded
-    q/k/v/g/beta/S0/z/w), recurrence in the selected mode then the FP16 norm per
-    layer: the whole-stack prefill time of one 2048-token prompt chunk."""
-    import torch
-
-    from linear_attention_recurrence_gb300 import build, gdn
-    from linear_attention_recurrence_gb300.inputs import make_inputs
-
-    build.build()
-    dev = torch.device("cuda", torch.cuda.current_device())
-    L, T = args.stack, 2048
-    layers = [{k: torch.from_numpy(v).to(dev) for k, v in make_inputs(T, seed=0, layer=i).items()} for i in range(L)]
+def make_stack_step(gdn, torch, dev, layers, mode):
+    """One prefill step of a stack of independent layers (2048 tokens each):
+    layer i's recurrence on the main stream, its FP16 norm on a second stream
+    beside layer i+1's recurrence (two output buffers alternate, and a layer's
+    recurrence waits for the norm that last read its buffer).  Returns step()."""
+    T = layers[0]["q"].shape[0]
     states = [torch.empty_like(x["S0"]) for x in layers]
     outs = [torch.empty((T, N_VH, D), device=dev) for _ in range(2)]
     y = torch.empty((T, N_VH, D), device=dev, dtype=torch.float16)
     main, side = torch.cuda.current_stream(), torch.cuda.Stream(dev)
 
     def step():
-        """Layer i's recurrence on the main stream, its norm on a second stream beside
-        layer i+1's recurrence; the two output buffers alternate, and a layer's
-        recurrence waits for the norm that last read its buffer."""
         side.wait_stream(main)
         norm_done = [None, None]
         for i, (x, st) in enumerate(zip(layers, states)):
@@ -277,7 +314,7 @@ def run_stack(args):
             if norm_done[i % 2] is not None:
                 main.wait_event(norm_done[i % 2])
             st.copy_(x["S0"])
-            gdn.gdn_recurrence(x["q"], x["k"], x["v"], x["g"], x["beta"], st, out=o, mode=args.mode, stream=main)
+            gdn.gdn_recurrence(x["q"], x["k"], x["v"], x["g"], x["beta"], st, out=o, mode=mode, stream=main)
             rec_done = torch.cuda.Event()
             rec_done.record(main)
             side.wait_event(rec_done)
@@ -286,6 +323,24 @@ def run_stack(args):
             norm_done[i % 2].record(side)
         main.wait_stream(side)
 
+    return step
+
+
+def run_stack(args):
+    """A stack of L independent layers, 2048 tokens each (every layer its own seeded
+    q/k/v/g/beta/S0/z/w), recurrence in the selected mode then the FP16 norm per
+    layer: the whole-stack prefill time of one 2048-token prompt chunk."""
+    import torch
+
+    from linear_attention_recurrence_gb300 import build, gdn
+
+    pool, pending = stack_inputs_async(args.stack)
+    build.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    L, T = args.stack, 2048
+    layers = [{k: torch.from_numpy(v).to(dev) for k, v in x.items()} for x in pending.get()]
+    pool.close()
+    step = make_stack_step(gdn, torch, dev, layers, args.mode)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -452,6 +507,10 @@ def main():
     ap.add_argument("--prestage", action="store_true",
                     help="time the pre-stage (conv + norms + gates) over --tokens tokens in one call")
     ap.add_argument("--skip-other-mode", action="store_true")
+    ap.add_argument("--skip-extra", action="store_true",
+                    help="skip the T=8192 (both modes) and 36-layer stack measurements")
+    ap.add_argument("--chunk-products", default="mma", choices=["mma", "fma", "tc"],
+                    help="how the chunked form computes its products (library option chunk_products)")
     ap.add_argument("--ref-seconds", type=float, default=10.0)
     ap.add_argument("--sweep", action="store_true",
                     help="time one call of each mode for T = 1 .. 32768 (one JSON line) instead of the step")
@@ -479,6 +538,8 @@ def main():
     from linear_attention_recurrence_gb300.inputs import make_inputs
 
     ws, rank, local = _dist()
+    want_extra = ws == 1 and not args.skip_extra
+    stack_pool = stack_inputs_async(36) if want_extra else None
     if ws > 1:
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
@@ -488,6 +549,7 @@ def main():
     if ws > 1:
         dist.barrier()
     gdn.load_library()
+    gdn.gdn_set_option("chunk_products", args.chunk_products)
 
     T, CT = args.tokens, args.call_tokens
     ncalls = T // CT
@@ -584,16 +646,79 @@ def main():
             res["norm_ms"] = statistics.mean(nrm)
         return res
 
+    def timed_alternating(modes, rounds):
+        """Per-call CUDA-event times of the recurrence and of the norm for each mode,
+        the modes' steps alternating (the last one of each round is modes[-1]);
+        medians over the rounds."""
+        for mode in modes:
+            step(mode)
+        torch.cuda.synchronize()
+        per = {m: {"rec": [], "step": [], "norm": [], "launches": 0} for m in modes}
+        for _ in range(rounds):
+            for mode in modes:
+                ev = ([], [], [], [])
+                n0 = gdn.gdn_launch_count()
+                step(mode, ev)
+                torch.cuda.synchronize()
+                per[mode]["launches"] += gdn.gdn_launch_count() - n0
+                rec = [a.elapsed_time(b) for a, b in zip(ev[0], ev[1])]
+                per[mode]["rec"] += rec
+                per[mode]["step"].append(sum(rec))
+                per[mode]["norm"] += [a.elapsed_time(b) for a, b in zip(ev[2], ev[3])]
+        return {m: {"rec_call_ms": statistics.median(r["rec"]), "rec_ms_per_step": statistics.median(r["step"]),
+                    "norm_ms": statistics.median(r["norm"]), "launches": r["launches"] / rounds * args.steps}
+                for m, r in per.items()}
+
+    def time_c3(rounds=20):
+        """The T = 8192 configuration: one call per mode (then the norm of its 8192
+        rows), the modes alternating, L2 flushed before every call (the 8192-token
+        inputs would fit in it); medians over `rounds` after one warm-up round."""
+        T3 = 8192
+        flush = torch.empty(64 << 20, dtype=torch.float32, device=dev)  # 256 MB, twice the L2
+        st = torch.empty_like(t["S0"])
+        res = {m: {"rec": [], "norm": []} for m in ("sequential", "chunked")}
+        for r in range(rounds + 1):
+            for mode in ("sequential", "chunked"):
+                st.copy_(t["S0"])
+                flush.zero_()
+                e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                e[0].record(stream)
+                gdn.gdn_recurrence(t["q"][:T3], t["k"][:T3], t["v"][:T3], t["g"][:T3], t["beta"][:T3], st,
+                                   out=out[:T3], mode=mode, stream=stream)
+                e[1].record(stream)
+                gdn.gdn_out_norm(out[:T3], t["z"][:T3], t["w"], 1e-6, y=y[:T3], stream=stream)
+                e[2].record(stream)
+                torch.cuda.synchronize()
+                if r > 0:
+                    res[mode]["rec"].append(e[0].elapsed_time(e[1]))
+                    res[mode]["norm"].append(e[1].elapsed_time(e[2]))
+        out_c3 = {}
+        for mode, r in res.items():
+            rec, nrm = statistics.median(r["rec"]), statistics.median(r["norm"])
+            flop = FLOP_SEQ if mode == "sequential" else FLOP_CHUNKED
+            out_c3[mode] = {"recurrence_ms": rec, "norm_ms": nrm, "us_per_token_layer": (rec + nrm) * 1e3 / T3,
+                            "recurrence_us_per_token_layer": rec * 1e3 / T3,
+                            "alu_tflops": flop * T3 / (rec * 1e-3) / 1e12}
+        return out_c3
+
     other = "sequential" if args.mode == "chunked" else "chunked"
-    with Clocks(dev.index) as clk:
-        time.sleep(0.5)  # nvidia-smi's first samples
-        main_res = timed(args.mode, args.steps, args.warmup, per_kernel=False, clk=clk)
-        time.sleep(0.1)
+    clk = Clocks(dev.index).__enter__()
+    time.sleep(0.5)  # nvidia-smi's first samples
+    main_res = timed(args.mode, args.steps, args.warmup, per_kernel=False, clk=clk)
+    time.sleep(0.1)
     y_main = y.clone()
-    kern = timed(args.mode, args.steps, 1, per_kernel=True)
+    wall0 = time.time()
+    alt = timed_alternating(([] if args.skip_other_mode else [other]) + [args.mode], args.steps)
+    clk.add_window(wall0, time.time())
+    kern = alt[args.mode]
+    other_res = alt.get(other)
     torch.cuda.synchronize()
     assert torch.equal(y_main, y), "the overlapped step's output differs from the plain step's"
-    other_res = None if args.skip_other_mode else timed(other, args.steps, 1, per_kernel=True)
+    c3 = None
+    if want_extra:
+        wall0 = time.time()
+        c3 = time_c3()
+        clk.add_window(wall0, time.time())
     assert gdn.gdn_device_status() == gdn.GDN_OK
 
     # end to end through the public API with host buffers: every step copies its inputs
@@ -682,6 +807,35 @@ def main():
         assert torch.equal(y_last, y), "pipelined end-to-end step differs from the plain step"
         assert torch.equal(hy, y.cpu()) and torch.equal(hs, state.cpu())
 
+    # the 36-layer stack (36 independent layers x 2048 tokens, recurrence + norm per
+    # layer, each layer's own seeded inputs, drawn on the host cores meanwhile)
+    c5 = None
+    if stack_pool is not None:
+        pool, pending = stack_pool
+        layers = [{k: torch.from_numpy(v).to(dev) for k, v in xl.items()} for xl in pending.get()]
+        pool.close()
+        stack_step = make_stack_step(gdn, torch, dev, layers, args.mode)
+        for _ in range(2):
+            stack_step()
+        torch.cuda.synchronize()
+        wall0 = time.time()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_stack = 5
+        e0.record()
+        for _ in range(n_stack):
+            stack_step()
+        e1.record()
+        torch.cuda.synchronize()
+        clk.add_window(wall0, time.time())
+        ms5 = e0.elapsed_time(e1) / n_stack
+        c5 = {"ms": ms5, "us_per_token_layer": ms5 * 1e3 / (36 * 2048), "mode": args.mode, "steps": n_stack,
+              "workload": "36 independent layers x 2048 tokens, recurrence + FP16 norm per layer (each layer its "
+                          "own seeded inputs; layer i's norm on a second stream beside layer i+1's recurrence)"}
+        del layers
+        assert gdn.gdn_device_status() == gdn.GDN_OK
+    time.sleep(0.1)
+    clk.__exit__(None, None, None)
+
     if rank != 0:
         if ws > 1:
             dist.destroy_process_group()
@@ -706,7 +860,7 @@ def main():
     flop = FLOP_SEQ if args.mode == "sequential" else FLOP_CHUNKED
     achieved = flop * CT / (kern["rec_call_ms"] * 1e-3) / 1e12
     per_call = (kern["launches"] / args.steps - 1) / ncalls  # the norm is one launch per step
-    scan_kind = os.environ.get("GDN_CHUNK_SCAN", "")
+    scan_kind = args.chunk_products
     products = {"fma": "products as packed FP32 FMAs",
                 "tc": "S0 products as split-TF32 tcgen05 MMAs"}.get(scan_kind, "products as split-TF32 mma.sync MMAs")
     one_launch = per_call < 1.5
@@ -737,12 +891,22 @@ def main():
         "norm_roofline": {"bound": "hbm", "achieved": norm_gbs, "peak": hbm_gbs, "unit": "GB/s",
                           "frac": norm_gbs / hbm_gbs, "peak_basis": f"{peak_src} copy bandwidth"},
         "modes": modes,
+        "modes_timing": "per-call CUDA events on the launching stream, the two modes' steps alternating, medians "
+                        f"over {args.steps} steps",
         "clocks": clocks,
+        "clocks_all_passes": clk.summary(all_windows=True),
     }
+    if c3 is not None:
+        for mode, r in c3.items():
+            r["alu_frac"] = r["alu_tflops"] / alu_peak_tflops
+        line["c3_t8192"] = dict(c3, timing="one 8192-token call per mode then the norm of its rows, modes "
+                                           "alternating, L2 flushed before each call, medians over 20 runs")
+    if c5 is not None:
+        line["c5_stack36"] = c5
     if e2e is not None:
         line["e2e"] = e2e
     if not args.skip_cpu and ws == 1:
-        line["cpu_baseline"] = cpu_baseline()
+        line["cpu_baseline"] = oracle_t8192()
     print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()

@@ -29,11 +29,12 @@
  *
  * Ownership: every pointer is a DEVICE pointer owned by the caller, on the
  * current CUDA device.  The library allocates only (a) a 4-byte status word per
- * device and (b) the chunked mode's per-device scratch (one 2048-token
- * super-block of prep results, about 25.9 MB, plus 12 KB of hand-off flags),
- * both on first use and kept until gdn_release_scratch() or process exit.
- * Chunked calls on one device share that scratch: enqueue them on one stream
- * (or otherwise order them); two in flight at once would corrupt each other.
+ * device, (b) the chunked mode's per-device scratch (one 2048-token super-block
+ * of prep results, about 25.9 MB, plus 12 KB of hand-off flags) and (c) the
+ * sequential mode's fused-norm scratch (about 100 KB for 16 key heads), each on
+ * first use and kept until gdn_release_scratch() or process exit.  Calls on one
+ * device share that scratch: enqueue them on one stream (or otherwise order
+ * them); two in flight at once would corrupt each other.
  *
  * Asynchrony: every compute call only validates its arguments on the host and
  * enqueues kernels on `cuda_stream` (a cudaStream_t; NULL = the legacy default
@@ -92,10 +93,10 @@ typedef enum gdn_status {
  * the largest magnitude).  GDN_AUTO picks one of the two by T per call (so a
  * sequence split into calls of different lengths may mix the two roundings).
  * GDN_CHUNKED computes the chunk's products on the tensor cores as three TF32
- * MMAs per FP32 product (split operands; same 2e-6 bound).  Environment
- * variables read on every call, for A/B measurements: GDN_CHUNK_SCAN=fma (the
- * products as FP32 FMAs) or =tc (tcgen05 for the state products, two launches);
- * GDN_CHUNK_OVERLAP=0 (prep and scan as two launches instead of one).
+ * MMAs per FP32 product (split operands; same 2e-6 bound).  Other forms of the
+ * chunked kernels, for A/B measurements, are chosen with gdn_set_option()
+ * (GDN_OPT_CHUNK_PRODUCTS, GDN_OPT_CHUNK_ONE_LAUNCH); the library reads no
+ * environment variable.
  *
  * Supported shapes: d == 128 and n_vh == 3 * n_kh (n_kh >= 1).  T == 0 is a
  * no-op returning GDN_OK.  The first GDN_CHUNKED call on a device allocates the
@@ -171,13 +172,24 @@ int gdn_out_norm(const float* out, const float* z, const float* w, float eps,
 /*
  * gdn_recurrence_norm - gdn_recurrence followed by gdn_out_norm of its output, in
  * one call: out (FP32, written as by gdn_recurrence) and y_fp16 (the same bits
- * gdn_out_norm would give for that out).  The norm of each 2048-token
- * super-block is launched after its recurrence.  With the environment variable
- * GDN_FUSED_NORM=1 and the one-launch chunked form, the norm instead runs inside
- * that launch, on the SMs that prepare the chunks, as the scan finishes each
- * (chunk, key head), reading the output back from L2 (same bits; on GB300 slower,
- * those SMs cannot stream the norm's traffic as fast as the scan produces it).
- * Arguments as the two calls'; y_fp16 may overlap no other argument.
+ * gdn_out_norm would give for that out).
+ *
+ * GDN_SEQUENTIAL: the norm is fused into the scan's epilogue ([P413] "What
+ * changes": the FP32 output is only the norm's input): one cooperative launch
+ * whose CTAs exchange each row's partial sums of squares through global memory,
+ * so y comes from the outputs while they are still on chip.  There `out` may be
+ * NULL: the FP32 output is then not written at all.  If the 8 n_kh CTAs cannot
+ * be resident at once (n_kh > SMs / 8), the scan and the norm are two launches
+ * and `out` is required.
+ * GDN_CHUNKED: the norm of each 2048-token super-block is launched after its
+ * recurrence.  With the option GDN_OPT_NORM_IN_LAUNCH set to 1 and the one-launch
+ * chunked form, the norm instead runs inside that launch, on the SMs that
+ * prepare the chunks, as the scan finishes each (chunk, key head), reading the
+ * output back from L2 (same bits; on GB300 slower, those SMs cannot stream the
+ * norm's traffic as fast as the scan produces it).
+ *
+ * Arguments as the two calls'; z, w and y_fp16 16-byte aligned; y_fp16 may
+ * overlap no other argument.
  */
 int gdn_recurrence_norm(const float* q, const float* k, const float* v,
                         const float* g, const float* beta,
@@ -197,19 +209,30 @@ int gdn_recurrence_norm(const float* q, const float* k, const float* v,
  * synchronisation.  The caller passes inputs and outputs exactly as for
  * gdn_recurrence (same layouts, same alignment rules, device pointers it owns).
  *
- * Scratch: a fixed 12,976,128-byte array in the library's static device memory
- * (one 512-token super-block of prep records for up to 96 value heads), which
- * every GPU that loads the library holds until the process exits.  Calls with
- * n_vh > 96 are rejected with GDN_ERR_UNSUPPORTED and a message saying so.
- * The first call on each device looks up that array's device address (with the
- * device current); make that first call before any stream capture.  Every call
- * in the process shares the one array per device and leaves its last contents
- * there; each call writes every scratch word it reads before reading it, so no
- * clearing is needed, but two calls whose kernels overlap on a GPU (different
- * streams, or different host threads) race on the array and corrupt each
- * other's results: serialise them.  This call has no status word:
- * gdn_device_status() does not report a bounded wait that gives up here.
- * Results equal gdn_recurrence's chunked mode for the same inputs.
+ * Scratch: a fixed 12,976,128-byte array (one 512-token super-block of prep
+ * records for up to 96 value heads) and a 4-byte status word, both in the
+ * library's static device memory.  Calls with n_vh > 96 are rejected with
+ * GDN_ERR_UNSUPPORTED and a message saying so.
+ *
+ * Set-up: the CUDA runtime places that static memory on a GPU when it loads the
+ * library's device code there.  Under its default lazy module loading
+ * (CUDA_MODULE_LOADING=LAZY) that happens at this entry point's first call on
+ * each device, which looks up the array's and the status word's device
+ * addresses and has the runtime load the kernels it launches (about 13 MB of
+ * device memory in all, kept until the process exits).  So make the first call
+ * on each device, with that device current, before the caller reserves its
+ * arena (or run with CUDA_MODULE_LOADING=EAGER, which loads everything when the
+ * library is loaded) and before any stream capture.  A call with T == 0 does
+ * that set-up and nothing else (the pointers are not used and may be NULL).
+ *
+ * Every call in the process shares the one array per device and leaves its last
+ * contents there; each call writes every scratch word it reads before reading
+ * it, so no clearing is needed, but two calls whose kernels overlap on a GPU
+ * (different streams, or different host threads) race on the array and corrupt
+ * each other's results: serialise them.  A bounded wait that gives up in these
+ * kernels sets the status word, which gdn_device_status() reads and clears
+ * (without allocating anything).  Results are bit-identical to gdn_recurrence's
+ * chunked mode for the same inputs.
  */
 int gdn_recurrence_chunked_noalloc(const float* q, const float* k, const float* v,
                                    const float* g, const float* beta,
@@ -217,20 +240,63 @@ int gdn_recurrence_chunked_noalloc(const float* q, const float* k, const float* 
                                    int64_t T, int n_kh, int n_vh, int d,
                                    void* cuda_stream);
 
+/*
+ * Process-wide options.  The library reads no environment variable: the A/B
+ * forms of its kernels and its failure-path test hooks are chosen here.  A value
+ * applies to every call that starts after gdn_set_option returns; do not change
+ * an option while another thread is inside a call of this library.  The defaults
+ * are the production forms.  The pages have no counterpart to these options.
+ */
+typedef enum gdn_option {
+    /* How GDN_CHUNKED computes the chunk's products: GDN_PRODUCTS_MMA (default,
+     * split-TF32 warp-level MMAs), GDN_PRODUCTS_FMA (packed FP32 FMAs) or
+     * GDN_PRODUCTS_TCGEN05 (the state products as split-TF32 tcgen05 MMAs; always
+     * two launches per super-block).  All meet the same 2e-6 bound. */
+    GDN_OPT_CHUNK_PRODUCTS = 1,
+    /* 1 (default): the chunk prep runs beside the scan in one cooperative launch
+     * when the device has SMs to spare for it; 0: a prep launch, then a scan
+     * launch.  Same bits either way. */
+    GDN_OPT_CHUNK_ONE_LAUNCH = 2,
+    /* gdn_recurrence_norm in GDN_CHUNKED: 0 (default) launches the norm after each
+     * super-block; 1 norms on the prep SMs inside the one launch.  Same bits. */
+    GDN_OPT_NORM_IN_LAUNCH = 3,
+    /* GDN_SEQUENTIAL: state rows per thread, 16 (default) or 8.  Same bits. */
+    GDN_OPT_SEQ_ROWS_PER_THREAD = 4,
+    /* Failure-path test hook: the prep task (chunk * n_kh + key head, in every
+     * super-block) whose hand-off flag the one-launch chunked kernel never
+     * publishes, so the scan CTAs waiting for it give up their bounded wait and
+     * gdn_device_status() returns GDN_ERR_TIMEOUT; -1 (default) withholds none. */
+    GDN_OPT_TEST_WITHHOLD_PREP_TASK = 101,
+    /* Failure-path test hook: 1 makes the chunked scratch allocation fail as a
+     * failed cudaMalloc would (GDN_ERR_ALLOC, nothing launched); 0 (default). */
+    GDN_OPT_TEST_FAIL_SCRATCH_ALLOC = 102
+} gdn_option;
+
+enum { GDN_PRODUCTS_MMA = 0, GDN_PRODUCTS_FMA = 1, GDN_PRODUCTS_TCGEN05 = 2 };
+
+/* Sets `option` to `value`: GDN_OK, or GDN_ERR_INVALID_ARG for an unknown option
+ * or a value it does not allow (the option is then unchanged). */
+int gdn_set_option(int option, int value);
+
+/* Stores the current value of `option` in *value: GDN_OK or GDN_ERR_INVALID_ARG. */
+int gdn_get_option(int option, int* value);
+
 /* Message for the calling thread's last non-OK status ("" if none). */
 const char* gdn_last_error(void);
 
 /*
  * Synchronises `cuda_stream`, then reads and clears the current device's
- * status word: GDN_OK, or GDN_ERR_TIMEOUT if a kernel gave up a bounded wait
- * since the last read, or GDN_ERR_CUDA if the stream reports an error.
+ * status words (the allocating entry points' and gdn_recurrence_chunked_noalloc's):
+ * GDN_OK, or GDN_ERR_TIMEOUT if a kernel gave up a bounded wait since the last
+ * read, or GDN_ERR_CUDA if the stream reports an error.  Allocates nothing.
  */
 int gdn_device_status(void* cuda_stream);
 
 /*
- * Frees the chunked-mode scratch of `device` (a CUDA device ordinal).  The
- * caller must ensure no chunked call is still running on it.  The next chunked
- * call allocates it again.  Returns GDN_OK (also if nothing was allocated).
+ * Frees the chunked-mode scratch and the fused-norm scratch of `device` (a CUDA
+ * device ordinal).  The caller must ensure no call is still running on it.  The
+ * next call that needs them allocates them again.  Returns GDN_OK (also if
+ * nothing was allocated).
  */
 int gdn_release_scratch(int device);
 

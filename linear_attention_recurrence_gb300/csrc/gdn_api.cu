@@ -5,7 +5,6 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
-#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -30,8 +29,29 @@ struct DeviceState {
     uint32_t* flags = nullptr; // one-launch chunked form: per-(chunk, key head) flags, then 2 sync words
     uint32_t* sync = nullptr;
     uint32_t* out_flags = nullptr;
+    void* seqnorm = nullptr;   // the sequential scan's fused norm: exchange buffer, counters, generation
+    int seqnorm_n_kh = 0;
 };
 DeviceState g_dev[kMaxDevices];
+
+// Process-wide options (gdn_set_option): A/B choices of the chunked form and the
+// failure-path test hooks.  Plain atomics; every call reads the values current
+// when it starts.  Nothing is read from the environment.
+constexpr int kOptSlots = 8;
+// constant-initialised defaults, in slot order (see opt_slot)
+std::atomic<int> g_opt[kOptSlots] = {GDN_PRODUCTS_MMA, 1, 0, 16, -1, 0, 0, 0};
+int opt_slot(int option) {
+    switch (option) {
+        case GDN_OPT_CHUNK_PRODUCTS: return 0;
+        case GDN_OPT_CHUNK_ONE_LAUNCH: return 1;
+        case GDN_OPT_NORM_IN_LAUNCH: return 2;
+        case GDN_OPT_SEQ_ROWS_PER_THREAD: return 3;
+        case GDN_OPT_TEST_WITHHOLD_PREP_TASK: return 4;
+        case GDN_OPT_TEST_FAIL_SCRATCH_ALLOC: return 5;
+        default: return -1;
+    }
+}
+int opt(int option) { return g_opt[opt_slot(option)].load(std::memory_order_relaxed); }
 
 int fail(int code, const std::string& msg) {
     t_last_error = msg;
@@ -56,8 +76,9 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// 2-D FP32 tensor map over a row-major [rows][width] array; out-of-range rows read as 0.
-int make_map(CUtensorMap* map, const float* base, uint64_t width, uint64_t rows, uint32_t box_w, uint32_t box_h,
+// 2-D FP32 tensor map over a row-major [rows][width] array; out-of-range rows
+// read as 0 and are not written.
+int make_map(CUtensorMap* map, const void* base, uint64_t width, uint64_t rows, uint32_t box_w, uint32_t box_h,
              CUtensorMapSwizzle swizzle) {
     auto enc = tensor_map_encoder();
     if (!enc) return fail(GDN_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
@@ -65,7 +86,7 @@ int make_map(CUtensorMap* map, const float* base, uint64_t width, uint64_t rows,
     cuuint64_t strides[1] = {width * sizeof(float)};
     cuuint32_t box[2] = {box_w, box_h};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, estr,
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(GDN_ERR_CUDA, "cuTensorMapEncodeTiled failed: " + std::to_string(r));
@@ -101,6 +122,40 @@ size_t scratch_bytes_for(int n_vh) {
     return static_cast<size_t>(gdn::kChunksPerSuperBlock) * n_vh * gdn::kPrepRecordFloats * sizeof(float);
 }
 
+// The fused sequential norm's scratch for n_kh key heads (zeroed once; its counters
+// carry a generation number, so it is never cleared again).
+int ensure_seqnorm(DeviceState* d, int n_kh) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (d->seqnorm && d->seqnorm_n_kh >= n_kh) return GDN_OK;
+    if (opt(GDN_OPT_TEST_FAIL_SCRATCH_ALLOC) == 1)
+        return fail(GDN_ERR_ALLOC, "sequential norm scratch allocation failed (simulated by GDN_OPT_TEST_FAIL_SCRATCH_ALLOC)");
+    cudaError_t e;
+    if (d->seqnorm) {
+        e = cudaDeviceSynchronize();  // the old buffer may still be in use by queued work
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+        cudaFree(d->seqnorm);
+        d->seqnorm = nullptr;
+        d->seqnorm_n_kh = 0;
+    }
+    const size_t bytes = gdn::seq_norm_scratch_bytes(n_kh);
+    void* p = nullptr;
+    e = cudaMalloc(&p, bytes);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(GDN_ERR_ALLOC, "sequential norm scratch allocation of " + std::to_string(bytes) +
+                                       " bytes failed: " + cudaGetErrorString(e));
+    }
+    e = cudaMemset(p, 0, bytes);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        cudaFree(p);
+        return cuda_fail(e, "sequential norm scratch initialisation");
+    }
+    d->seqnorm = p;
+    d->seqnorm_n_kh = n_kh;
+    return GDN_OK;
+}
+
 // Flag words of the one-launch chunked form for up to n_vh key heads (n_kh <= n_vh).
 size_t flag_words_for(int n_vh) { return static_cast<size_t>(gdn::kChunksPerSuperBlock) * n_vh; }
 // Output flags of the one-launch form with the norm: [chunk][key head][8 scan CTAs] (n_kh <= n_vh).
@@ -118,8 +173,8 @@ int ensure_scratch(DeviceState* d, int n_vh) {
     const size_t need = scratch_bytes_for(n_vh);
     std::lock_guard<std::mutex> lk(g_mu);
     if (d->scratch && d->scratch_bytes >= need) return GDN_OK;
-    const char* sim = std::getenv("GDN_SIMULATE_ALLOC_FAILURE");
-    if (sim && sim[0] == '1') return fail(GDN_ERR_ALLOC, "chunked scratch allocation failed (simulated)");
+    if (opt(GDN_OPT_TEST_FAIL_SCRATCH_ALLOC) == 1)
+        return fail(GDN_ERR_ALLOC, "chunked scratch allocation failed (simulated by GDN_OPT_TEST_FAIL_SCRATCH_ALLOC)");
     if (d->scratch) {
         // a larger head count than before: the old buffer may still be in use by queued work
         cudaError_t e = cudaDeviceSynchronize();
@@ -154,31 +209,21 @@ int ensure_scratch(DeviceState* d, int n_vh) {
     return GDN_OK;
 }
 
-// The chunked form runs prep and scan in one launch unless the environment sets
-// GDN_CHUNK_OVERLAP=0 or selects the tensor-core scan (GDN_CHUNK_SCAN=tc), both
-// for A/B measurements; read on every call.
 // gdn_recurrence_norm runs the norm inside the one-launch chunked kernel (on the
-// prep CTAs, as the scan finishes each chunk) only when GDN_FUSED_NORM=1: on GB300
-// those 24 SMs cannot stream the norm's traffic as fast as the scan produces it
-// (measured 562 vs 362 us per 2048-token call), so by default the norm is a
-// launch of its own after the recurrence.  Read on every call.
-bool fused_norm_enabled() {
-    const char* v = std::getenv("GDN_FUSED_NORM");
-    return v && std::strcmp(v, "1") == 0;
-}
+// prep CTAs, as the scan finishes each chunk) only when GDN_OPT_NORM_IN_LAUNCH is
+// 1: on GB300 those 24 SMs cannot stream the norm's traffic as fast as the scan
+// produces it (measured 562 vs 362 us per 2048-token call), so by default the
+// norm is a launch of its own after the recurrence.
+bool fused_norm_enabled() { return opt(GDN_OPT_NORM_IN_LAUNCH) == 1; }
 
-// Failure-path test hook: GDN_TEST_WITHHOLD_PREP_FLAG=<task> keeps that prep task
-// (chunk * n_kh + key head of each super-block) from publishing its flag, so the
-// scan CTAs that wait for it run out their bounded wait and report
-// GDN_ERR_TIMEOUT (nothing faults or hangs; the next call runs normally).
-int withheld_prep_task() {
-    const char* v = std::getenv("GDN_TEST_WITHHOLD_PREP_FLAG");
-    return v ? std::atoi(v) : -1;
-}
+// Failure-path test hook (GDN_OPT_TEST_WITHHOLD_PREP_TASK): that prep task (chunk
+// * n_kh + key head of each super-block) never publishes its flag, so the scan
+// CTAs that wait for it run out their bounded wait and report GDN_ERR_TIMEOUT
+// (nothing faults or hangs; the next call runs normally).
+int withheld_prep_task() { return opt(GDN_OPT_TEST_WITHHOLD_PREP_TASK); }
 
 bool fused_chunk_launch_enabled() {
-    const char* o = std::getenv("GDN_CHUNK_OVERLAP");
-    if (o && std::strcmp(o, "0") == 0) return false;
+    if (opt(GDN_OPT_CHUNK_ONE_LAUNCH) == 0) return false;
     return gdn::chunk_scan_kind() != gdn::ScanKind::kTcgen05;
 }
 
@@ -195,13 +240,7 @@ bool overlap(const void* a, size_t an, const void* b, size_t bn) {
     return a0 < b0 + bn && b0 < a0 + an;
 }
 
-int seq_rows_per_thread() {
-    static int v = [] {
-        const char* s = std::getenv("GDN_SEQ_ROWS_PER_THREAD");
-        return (s && std::atoi(s) == 8) ? 8 : 16;
-    }();
-    return v;
-}
+int seq_rows_per_thread() { return opt(GDN_OPT_SEQ_ROWS_PER_THREAD); }
 
 }  // namespace
 
@@ -226,6 +265,13 @@ cudaError_t set_smem_once(const void* kernel, int bytes) {
     return e;
 }
 int internal_fail(int code, const std::string& msg) { return fail(code, msg); }
+ScanKind chunk_scan_kind() {
+    switch (opt(GDN_OPT_CHUNK_PRODUCTS)) {
+        case GDN_PRODUCTS_FMA: return ScanKind::kFma;
+        case GDN_PRODUCTS_TCGEN05: return ScanKind::kTcgen05;
+        default: return ScanKind::kMma;
+    }
+}
 void internal_count_launch() { g_launches.fetch_add(1); }
 }  // namespace gdn
 
@@ -252,18 +298,23 @@ int run_recurrence(const float* q, const float* k, const float* v, const float* 
     if (n_vh != kHeadsPerKey * n_kh) return fail(GDN_ERR_UNSUPPORTED, "only n_vh == 3 * n_kh is supported");
     if (T > INT32_MAX - 4096) return fail(GDN_ERR_UNSUPPORTED, "T too large for 32-bit TMA coordinates");
     if (T == 0) return GDN_OK;
-    if (!q || !k || !v || !g || !beta || !state_inout || !out) return fail(GDN_ERR_INVALID_ARG, "null pointer");
-    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(state_inout, 16))
+    // the fused sequential norm may leave the FP32 output unwritten
+    const bool out_optional = norm && mode == GDN_SEQUENTIAL;
+    if (!q || !k || !v || !g || !beta || !state_inout || (!out && !out_optional))
+        return fail(GDN_ERR_INVALID_ARG, "null pointer");
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || (out && !aligned(out, 16)) ||
+        !aligned(state_inout, 16))
         return fail(GDN_ERR_INVALID_ARG, "q, k, v, out and state_inout must be 16-byte aligned");
     if (!aligned(g, 4) || !aligned(beta, 4)) return fail(GDN_ERR_INVALID_ARG, "g and beta must be 4-byte aligned");
     const size_t qk_bytes = static_cast<size_t>(T) * n_kh * d * 4, v_bytes = static_cast<size_t>(T) * n_vh * d * 4;
     const size_t gb_bytes = static_cast<size_t>(T) * n_vh * 4, s_bytes = static_cast<size_t>(n_vh) * d * d * 4;
     const void* ins[5] = {q, k, v, g, beta};
     const size_t in_bytes[5] = {qk_bytes, qk_bytes, v_bytes, gb_bytes, gb_bytes};
+    const size_t o_bytes = out ? v_bytes : 0;
     for (int i = 0; i < 5; ++i)
-        if (overlap(out, v_bytes, ins[i], in_bytes[i]) || overlap(state_inout, s_bytes, ins[i], in_bytes[i]))
+        if (overlap(out, o_bytes, ins[i], in_bytes[i]) || overlap(state_inout, s_bytes, ins[i], in_bytes[i]))
             return fail(GDN_ERR_INVALID_ARG, "out / state_inout overlap an input");
-    if (overlap(out, v_bytes, state_inout, s_bytes)) return fail(GDN_ERR_INVALID_ARG, "out overlaps state_inout");
+    if (overlap(out, o_bytes, state_inout, s_bytes)) return fail(GDN_ERR_INVALID_ARG, "out overlaps state_inout");
 
     DeviceState* dev = nullptr;
     int rc = device_state(&dev);
@@ -281,6 +332,9 @@ int run_recurrence(const float* q, const float* k, const float* v, const float* 
         if ((rc = make_map(&p.tm_v, v, static_cast<uint64_t>(n_vh) * d, T, seq_box_cols(), B,
                            CU_TENSOR_MAP_SWIZZLE_NONE)))
             return rc;
+        if (out && (rc = make_map(&p.tm_o, out, static_cast<uint64_t>(n_vh) * d, T, seq_box_cols(), B,
+                                  CU_TENSOR_MAP_SWIZZLE_NONE)))
+            return rc;
         p.g = g;
         p.beta = beta;
         p.state = state_inout;
@@ -289,6 +343,31 @@ int run_recurrence(const float* q, const float* k, const float* v, const float* 
         p.n_kh = n_kh;
         p.n_vh = n_vh;
         p.status = dev->status;
+        // The norm fused into the scan (z loaded and y stored by TMA, one cooperative
+        // launch) when all 8 n_kh CTAs fit on the device at once; else the scan, then
+        // the norm's own launch (out is required then).
+        if (norm != nullptr && kSeqSlices * n_kh <= dev->sm_count) {
+            if ((rc = ensure_seqnorm(dev, n_kh)) != GDN_OK) return rc;
+            if ((rc = make_map(&p.tm_z, norm->z, static_cast<uint64_t>(n_vh) * d, T, seq_box_cols(), B,
+                               CU_TENSOR_MAP_SWIZZLE_NONE)))
+                return rc;
+            const size_t cnt = static_cast<size_t>(seq_norm_counters(n_kh));
+            p.xflags = static_cast<unsigned long long*>(dev->seqnorm);
+            p.sync = reinterpret_cast<uint32_t*>(p.xflags + cnt);
+            p.xg = reinterpret_cast<float*>(reinterpret_cast<char*>(p.sync) + 16);
+            p.w = norm->w;
+            p.y = norm->y;
+            p.eps = norm->eps;
+            cudaError_t e = launch_seq(p, seq_rows_per_thread(), s);
+            if (e == cudaSuccess) {
+                g_launches.fetch_add(1);
+                return GDN_OK;
+            }
+            if (e != cudaErrorCooperativeLaunchTooLarge) return cuda_fail(e, "sequential scan + norm launch");
+            cudaGetLastError();  // fewer SMs available than the device has: two launches instead
+            p.y = nullptr;
+        }
+        if (norm && !out) return fail(GDN_ERR_INVALID_ARG, "out is required when the norm cannot be fused");
         cudaError_t e = launch_seq(p, seq_rows_per_thread(), s);
         if (e != cudaSuccess) return cuda_fail(e, "sequential scan launch");
         g_launches.fetch_add(1);
@@ -392,18 +471,19 @@ int gdn_recurrence_norm(const float* q, const float* k, const float* v, const fl
     if (!(eps >= 0.0f) || eps != eps) return fail(GDN_ERR_INVALID_ARG, "eps must be a non-negative number");
     if (T > 0 && n_vh > 0 && d > 0) {
         if (!z || !w || !y_fp16) return fail(GDN_ERR_INVALID_ARG, "null pointer");
-        if (!aligned(z, 16) || !aligned(w, 16) || !aligned(y_fp16, 8))
-            return fail(GDN_ERR_INVALID_ARG, "z, w must be 16-byte and y_fp16 8-byte aligned");
+        if (!aligned(z, 16) || !aligned(w, 16) || !aligned(y_fp16, 16))
+            return fail(GDN_ERR_INVALID_ARG, "z, w and y_fp16 must be 16-byte aligned");
         const size_t nb = static_cast<size_t>(T) * n_vh * d;
         const size_t qk_b = static_cast<size_t>(T) * (n_kh > 0 ? n_kh : 0) * d * 4, gb_b = static_cast<size_t>(T) * n_vh * 4;
-        const void* reads[] = {q, k, v, g, beta, z, w, out, state_inout};
+        const void* reads[] = {q, k, v, g, beta, z, w, out, state_inout};  // null entries are skipped
         const size_t rb[] = {qk_b, qk_b, nb * 4, gb_b, gb_b, nb * 4, static_cast<size_t>(d) * 4, nb * 4,
                              static_cast<size_t>(n_vh) * d * d * 4};
         for (int i = 0; i < 9; ++i)
             if (reads[i] && overlap(y_fp16, nb * 2, reads[i], rb[i]))
                 return fail(GDN_ERR_INVALID_ARG, "y_fp16 overlaps another argument");
-        if (overlap(z, nb * 4, out, nb * 4) || overlap(z, nb * 4, state_inout, static_cast<size_t>(n_vh) * d * d * 4) ||
-            overlap(w, static_cast<size_t>(d) * 4, out, nb * 4))
+        const size_t ob = out ? nb * 4 : 0;
+        if (overlap(z, nb * 4, out, ob) || overlap(z, nb * 4, state_inout, static_cast<size_t>(n_vh) * d * d * 4) ||
+            overlap(w, static_cast<size_t>(d) * 4, out, ob))
             return fail(GDN_ERR_INVALID_ARG, "out / state_inout overlap an input");
     }
     const NormArgs na{z, w, eps, y_fp16};
@@ -516,38 +596,57 @@ int gdn_out_norm(const float* out, const float* z, const float* w, float eps, ui
 const char* gdn_last_error(void) { return t_last_error.c_str(); }
 
 int gdn_device_status(void* cuda_stream) {
-    DeviceState* dev = nullptr;
-    int rc = device_state(&dev);
-    if (rc != GDN_OK) return rc;
-    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream));
+    // Allocates nothing: a device whose status word was never allocated has run no
+    // kernel of the allocating entry points.
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(GDN_ERR_UNSUPPORTED, "device ordinal out of range");
+    e = cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream));
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-    int word = 0;
-    e = cudaMemcpy(&word, dev->status, sizeof(int), cudaMemcpyDeviceToHost);
-    if (e != cudaSuccess) return cuda_fail(e, "status read");
-    if (word != 0) {
-        e = cudaMemset(dev->status, 0, sizeof(int));
-        if (e != cudaSuccess) return cuda_fail(e, "status reset");
-        std::string msg = "a kernel gave up a bounded wait (status word " + std::to_string(word) + ")";
-        uint32_t diag[3] = {0, 0, 0};
-        if ((word & gdn::kDevErrFlagTimeout) && dev->sync &&
-            cudaMemcpy(diag, dev->sync + 2, sizeof(diag), cudaMemcpyDeviceToHost) == cudaSuccess)
-            msg += ": prep flag " + std::to_string(diag[0]) + " held " + std::to_string(diag[1]) + ", awaited " +
-                   std::to_string(diag[2]);
-        return fail(GDN_ERR_TIMEOUT, msg);
+    DeviceState* d = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (g_dev[dev].init) d = &g_dev[dev];
     }
-    return GDN_OK;
+    int word = 0;
+    if (d) {
+        e = cudaMemcpy(&word, d->status, sizeof(int), cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess) return cuda_fail(e, "status read");
+        if (word != 0) {
+            e = cudaMemset(d->status, 0, sizeof(int));
+            if (e != cudaSuccess) return cuda_fail(e, "status reset");
+        }
+    }
+    int na_word = 0;
+    e = gdn::noalloc_take_status(dev, &na_word);
+    if (e != cudaSuccess) return cuda_fail(e, "status read (non-allocating entry point)");
+    if (word == 0 && na_word == 0) return GDN_OK;
+    std::string msg = "a kernel gave up a bounded wait (status word " + std::to_string(word | na_word) + ")";
+    if (na_word != 0) msg += " in gdn_recurrence_chunked_noalloc";
+    uint32_t diag[3] = {0, 0, 0};
+    if ((word & gdn::kDevErrFlagTimeout) && d && d->sync &&
+        cudaMemcpy(diag, d->sync + 2, sizeof(diag), cudaMemcpyDeviceToHost) == cudaSuccess)
+        msg += ": prep flag " + std::to_string(diag[0]) + " held " + std::to_string(diag[1]) + ", awaited " +
+               std::to_string(diag[2]);
+    return fail(GDN_ERR_TIMEOUT, msg);
 }
 
 int gdn_release_scratch(int device) {
     if (device < 0 || device >= kMaxDevices) return fail(GDN_ERR_INVALID_ARG, "device ordinal out of range");
     std::lock_guard<std::mutex> lk(g_mu);
     DeviceState& d = g_dev[device];
-    if (!d.scratch) return GDN_OK;
+    if (!d.scratch && !d.seqnorm) return GDN_OK;
     int cur = 0;
     cudaGetDevice(&cur);
     cudaSetDevice(device);
     cudaError_t e = cudaFree(d.scratch);
     cudaError_t e2 = cudaFree(d.flags);
+    if (d.seqnorm) {
+        cudaFree(d.seqnorm);
+        d.seqnorm = nullptr;
+        d.seqnorm_n_kh = 0;
+    }
     cudaSetDevice(cur);
     d.scratch = nullptr;
     d.flags = d.sync = d.out_flags = nullptr;
@@ -569,6 +668,35 @@ int gdn_poison_scratch(uint32_t bits, int n_vh, void* cuda_stream) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "scratch fill launch");
     g_launches.fetch_add(1);
+    return GDN_OK;
+}
+
+int gdn_set_option(int option, int value) {
+    const int slot = opt_slot(option);
+    if (slot < 0) return fail(GDN_ERR_INVALID_ARG, "unknown option " + std::to_string(option));
+    bool ok = true;
+    switch (option) {
+        case GDN_OPT_CHUNK_PRODUCTS:
+            ok = value == GDN_PRODUCTS_MMA || value == GDN_PRODUCTS_FMA || value == GDN_PRODUCTS_TCGEN05;
+            break;
+        case GDN_OPT_CHUNK_ONE_LAUNCH:
+        case GDN_OPT_NORM_IN_LAUNCH:
+        case GDN_OPT_TEST_FAIL_SCRATCH_ALLOC: ok = value == 0 || value == 1; break;
+        case GDN_OPT_SEQ_ROWS_PER_THREAD: ok = value == 8 || value == 16; break;
+        case GDN_OPT_TEST_WITHHOLD_PREP_TASK: ok = value >= -1; break;
+        default: break;
+    }
+    if (!ok) return fail(GDN_ERR_INVALID_ARG, "value " + std::to_string(value) + " not allowed for option " +
+                                                  std::to_string(option));
+    g_opt[slot].store(value);
+    return GDN_OK;
+}
+
+int gdn_get_option(int option, int* value) {
+    const int slot = opt_slot(option);
+    if (slot < 0) return fail(GDN_ERR_INVALID_ARG, "unknown option " + std::to_string(option));
+    if (!value) return fail(GDN_ERR_INVALID_ARG, "null pointer");
+    *value = g_opt[slot].load();
     return GDN_OK;
 }
 

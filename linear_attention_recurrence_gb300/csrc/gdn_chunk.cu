@@ -1155,6 +1155,16 @@ cudaError_t launch_chunk_fused(const ChunkFusedParams& p, const bool mma, cudaSt
     return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
+cudaError_t preload_two_launch_chunk_kernels() {
+    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(gdn_chunk_prep_kernel),
+                                  static_cast<int>(sizeof(PrepSmemT<1>) + 16));
+    if (e != cudaSuccess) return e;
+    const int smem = static_cast<int>(sizeof(ScanSmem) + 1024);
+    e = set_smem_once(reinterpret_cast<const void*>(gdn_chunk_scan_kernel<true>), smem);
+    if (e != cudaSuccess) return e;
+    return set_smem_once(reinterpret_cast<const void*>(gdn_chunk_scan_kernel<false>), smem);
+}
+
 cudaError_t launch_chunk_scan(const ChunkScanParams& p, const bool mma, cudaStream_t s) {
     const size_t smem = sizeof(ScanSmem) + 1024;
     const auto kernel = mma ? gdn_chunk_scan_kernel<true> : gdn_chunk_scan_kernel<false>;

@@ -21,8 +21,6 @@
 // live in shared memory in the K-major 128-byte-swizzled layout both TMA and the
 // MMA descriptors use; k/q tiles, v columns and prep records for the next chunk are
 // loaded as soon as their buffers are free.
-#include <cstdlib>
-#include <cstring>
 
 #include "gdn_device.cuh"
 #include "gdn_internal.h"
@@ -378,6 +376,10 @@ __global__ void __launch_bounds__(THREADS, 1) gdn_chunk_scan_tc_kernel(const __g
 
 }  // namespace
 
+cudaError_t preload_chunk_scan_tc() {
+    return set_smem_once(reinterpret_cast<const void*>(gdn_chunk_scan_tc_kernel), static_cast<int>(SMEM_BYTES + 1024));
+}
+
 cudaError_t launch_chunk_scan_tc(const ChunkScanParams& p, cudaStream_t s) {
     const size_t smem = SMEM_BYTES + 1024;
     cudaError_t e = set_smem_once(reinterpret_cast<const void*>(gdn_chunk_scan_tc_kernel), static_cast<int>(smem));
@@ -385,13 +387,6 @@ cudaError_t launch_chunk_scan_tc(const ChunkScanParams& p, cudaStream_t s) {
     dim3 grid(p.n_kh, D / NC);
     gdn_chunk_scan_tc_kernel<<<grid, THREADS, smem, s>>>(p);
     return cudaGetLastError();
-}
-
-ScanKind chunk_scan_kind() {
-    const char* v = std::getenv("GDN_CHUNK_SCAN");
-    if (v && std::strcmp(v, "fma") == 0) return ScanKind::kFma;
-    if (v && std::strcmp(v, "tc") == 0) return ScanKind::kTcgen05;
-    return ScanKind::kMma;
 }
 
 cudaError_t launch_chunk_scan_default(const ChunkScanParams& p, cudaStream_t s) {

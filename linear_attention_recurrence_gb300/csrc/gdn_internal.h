@@ -26,18 +26,35 @@ struct SeqParams {
     CUtensorMap tm_k;  // k viewed as [T][n_kh*128] FP32, box {128, B}
     CUtensorMap tm_q;  // q, same
     CUtensorMap tm_v;  // v viewed as [T][n_vh*128] FP32, box {16, B}
+    CUtensorMap tm_o;  // out viewed as [T][n_vh*128] FP32, box {16, B} (TMA stores)
+    CUtensorMap tm_z;  // fused norm: z viewed as [T][n_vh*128] FP32, box {16, B}
     const float* g;
     const float* beta;
     float* state;
-    float* out;
+    float* out;        // nullptr: the FP32 output is not stored (fused norm only)
+    const float* w;    // fused norm: weight [128]
+    uint16_t* y;       // fused norm: y, or nullptr for the recurrence alone
+    float eps;
+    // fused norm, device scratch of seq_norm_scratch_bytes(n_kh): the exchange of
+    // the group sums between the 8 CTAs of a key head, its counters, and the
+    // launch generation (sync[0]) with a count of finished CTAs (sync[1])
+    float* xg;
+    unsigned long long* xflags;  // [2][n_kh][8][4]: stages published, stages consumed
+    uint32_t* sync;
     int64_t T;
     int n_kh;
     int n_vh;
     int* status;
 };
 int seq_tokens_per_stage();
+constexpr int kSeqSlices = 8;  // CTAs (16-column slices) of a key head in the sequential scan
 int seq_box_cols();
-// rows_per_thread: 8 or 16.  Returns the CUDA error of the launch.
+// rows_per_thread: 8 or 16.  With p.y set, the gated RMSNorm of the output is
+// fused in (a cooperative launch; it fails with cudaErrorCooperativeLaunchTooLarge
+// when the 8 n_kh CTAs cannot be resident at once).  Returns the CUDA error of the
+// launch.
+size_t seq_norm_scratch_bytes(int n_kh);
+int seq_norm_counters(int n_kh);  // 64-bit counters at the start of that scratch
 cudaError_t launch_seq(const SeqParams& p, int rows_per_thread, cudaStream_t s);
 
 // ---- batched decode (one token per sequence) ----
@@ -141,15 +158,26 @@ cudaError_t launch_chunk_scan(const ChunkScanParams& p, bool mma, cudaStream_t s
 // The same scan with the large products as split-TF32 tcgen05 MMAs (accumulators
 // in tensor memory); same parameters and results within tolerance.
 cudaError_t launch_chunk_scan_tc(const ChunkScanParams& p, cudaStream_t s);
-// Which scan the entry points run, from the environment variable GDN_CHUNK_SCAN
-// (read on every call, for A/B measurements): "fma" the CUDA-core products, "tc"
-// the tcgen05 scan (two launches only: at 48 columns per CTA each tcgen05.mma
-// costs a near-fixed ~80 cycles), anything else the warp-level MMA scan.
+// Which scan the entry points run, from the option GDN_OPT_CHUNK_PRODUCTS (set by
+// gdn_set_option, for A/B measurements): GDN_PRODUCTS_FMA the CUDA-core products,
+// GDN_PRODUCTS_TCGEN05 the tcgen05 scan (two launches only: at 48 columns per CTA
+// each tcgen05.mma costs a near-fixed ~80 cycles), else the warp-level MMA scan.
+// Implemented in gdn_api.cu.
 enum class ScanKind { kFma, kMma, kTcgen05 };
 ScanKind chunk_scan_kind();
 // The two-launch scan of the selected kind.
 cudaError_t launch_chunk_scan_default(const ChunkScanParams& p, cudaStream_t s);
 int chunk_scan_box_cols();
+// Make the runtime load the two-launch chunk kernels (prep, both forms of the
+// scan; the tcgen05 scan) on the current device now, without launching them.
+// Under lazy module loading this is otherwise done by their first launch.
+cudaError_t preload_two_launch_chunk_kernels();
+cudaError_t preload_chunk_scan_tc();
+
+// The non-allocating entry point's status word on `device` (gdn_noalloc.cu): if
+// that entry point has been set up on the device, copies the word to *word and
+// clears it; else sets *word to 0.  Returns the CUDA error of the copies.
+cudaError_t noalloc_take_status(int device, int* word);
 
 // Raises a kernel's dynamic shared-memory limit to `bytes` on the current device,
 // once per (kernel, device); later calls return at once (implemented in gdn_api.cu).

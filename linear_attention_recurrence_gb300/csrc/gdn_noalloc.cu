@@ -8,8 +8,13 @@
 // fragments what the arena manages; or a latency-critical path that must not
 // take cudaMalloc's implicit device synchronisation.  This entry point runs the
 // same prep and scan kernels with their scratch in a fixed-size array that lives
-// in this file's static device memory, which the CUDA runtime sets aside when it
-// loads the library's device code on a GPU and keeps until the process exits.
+// in this file's static device memory, and reports a bounded wait that gave up in
+// a status word that is static device memory too.  The CUDA runtime sets both
+// aside when it loads this file's device code on a GPU and keeps them until the
+// process exits.  With the runtime's default lazy module loading, that load (and
+// the load of the kernels) happens at this entry point's first call on each
+// device, in its set-up step; a call with T == 0 does only that set-up, so a
+// caller can make it at start-up, before it reserves its arena.
 //
 // Limits: at most kNoAllocMaxHeads value heads.  The scratch holds the records of
 // one 512-token super-block (instead of the allocating path's 2048), so it is
@@ -37,11 +42,15 @@ constexpr size_t kNoAllocScratchFloats =
 // Shared by every call in the process on a given device; see the header for the
 // rules that follow from that.
 static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchFloats];
+// Bounded waits of this entry point's kernels that gave up (bits as in the
+// allocating path's status word); read and cleared by gdn_device_status().
+static __device__ int g_noalloc_status;
 
 constexpr int kMaxDev = 64;
 struct NoAllocDevice {
     bool ready = false;
     float* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+    int* status = nullptr;     // device address of g_noalloc_status on this device
 };
 NoAllocDevice g_nd[kMaxDev];
 std::mutex g_nd_mu;
@@ -76,7 +85,8 @@ int map2d(CUtensorMap* map, const float* base, uint64_t width, uint64_t rows, ui
 }
 
 // Once per device, with that device current: look up where the runtime placed
-// the static array on it.  Nothing is allocated.
+// the static array and the status word on it, and have it load the kernels this
+// entry point launches.  Nothing is allocated by this code.
 int noalloc_device(NoAllocDevice** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -89,7 +99,16 @@ int noalloc_device(NoAllocDevice** out) {
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess)
             return internal_fail(GDN_ERR_CUDA, std::string("cudaGetSymbolAddress(scratch): ") + cudaGetErrorString(e));
+        void* st = nullptr;
+        e = cudaGetSymbolAddress(&st, g_noalloc_status);
+        if (e != cudaSuccess)
+            return internal_fail(GDN_ERR_CUDA, std::string("cudaGetSymbolAddress(status): ") + cudaGetErrorString(e));
+        e = preload_two_launch_chunk_kernels();
+        if (e == cudaSuccess) e = preload_chunk_scan_tc();
+        if (e != cudaSuccess)
+            return internal_fail(GDN_ERR_CUDA, std::string("loading the chunk kernels: ") + cudaGetErrorString(e));
         d.scratch = static_cast<float*>(p);
+        d.status = static_cast<int*>(st);
         d.ready = true;
     }
     *out = &d;
@@ -99,6 +118,20 @@ int noalloc_device(NoAllocDevice** out) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 }  // namespace
+
+cudaError_t noalloc_take_status(int device, int* word) {
+    *word = 0;
+    if (device < 0 || device >= kMaxDev) return cudaSuccess;
+    int* st = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_nd_mu);
+        if (!g_nd[device].ready) return cudaSuccess;
+        st = g_nd[device].status;
+    }
+    cudaError_t e = cudaMemcpy(word, st, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && *word != 0) e = cudaMemset(st, 0, sizeof(int));
+    return e;
+}
 }  // namespace gdn
 
 extern "C" int gdn_recurrence_chunked_noalloc(const float* q, const float* k, const float* v, const float* g,
@@ -117,12 +150,12 @@ extern "C" int gdn_recurrence_chunked_noalloc(const float* q, const float* k, co
                                  std::to_string(kNoAllocMaxHeads) + " value heads (its fixed scratch holds " +
                                  std::to_string(kNoAllocScratchFloats * sizeof(float)) + " bytes)");
     if (T > INT32_MAX - 4096) return internal_fail(GDN_ERR_UNSUPPORTED, "T too large for 32-bit TMA coordinates");
-    if (T == 0) return GDN_OK;
+    NoAllocDevice* dev = nullptr;
+    if (T == 0) return noalloc_device(&dev);  // the set-up alone; pointers are not used
     if (!q || !k || !v || !g || !beta || !state_inout || !out) return internal_fail(GDN_ERR_INVALID_ARG, "null pointer");
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(state_inout))
         return internal_fail(GDN_ERR_INVALID_ARG, "q, k, v, out and state_inout must be 16-byte aligned");
 
-    NoAllocDevice* dev = nullptr;
     int rc = noalloc_device(&dev);
     if (rc != GDN_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
@@ -141,7 +174,7 @@ extern "C" int gdn_recurrence_chunked_noalloc(const float* q, const float* k, co
     sp.out = out;
     sp.n_kh = n_kh;
     sp.n_vh = n_vh;
-    sp.status = nullptr;  // no status word: a bounded wait that runs out here still ends the kernel
+    sp.status = dev->status;
     ChunkPrepParams pp;
     pp.q = q;
     pp.k = k;

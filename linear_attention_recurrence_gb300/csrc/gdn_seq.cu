@@ -20,12 +20,31 @@
 // of the column ends with bit-identical sums and no CTA barrier is needed per
 // token.  The state slice lives in registers for the whole call.  A producer warp
 // stages B-token blocks of k, q and v with TMA into a 4-deep ring and fills in
-// e^g, beta and k.q for each token; consumer warps run ahead of each other
-// within the ring.  Per token every lane does its arithmetic in the same order,
-// independent of the token's position in the block or the call, so a sequence
-// split over calls gives the same bits as one call.
+// e^g, beta and k.q for each token; consumer warps run ahead of each other within
+// the ring.
+//
+// With the gated RMSNorm fused in (gdn_recurrence_norm, "#413 ..." section "What
+// changes": the FP32 output is only the norm's input), the consumers write each
+// block's outputs to shared memory and four more warps per CTA (one per SM
+// sub-partition, each a quarter of the block's rows) norm them: per (token,
+// head) row a norm warp publishes the sums of squares of its CTA's four 4-column
+// groups in global memory (release counter per block), gathers the other seven
+// CTAs' of the key head (acquire), adds the row's 32 group sums in the order
+// gdn_out_norm's warp does (so y has that kernel's bits), and writes y (FP16);
+// the producer loads z and stores the FP32 output by TMA, or not at all.  That form is a
+// cooperative launch, so the eight CTAs of a key head are resident together and
+// their waits end.  (Eight-CTA clusters with distributed shared memory would
+// avoid the global round trip, but at one CTA per SM a GB300 holds only 15 such
+// clusters at once, one short of 16 key heads.)
+//
+// Per token every lane does its arithmetic in the same order, independent of
+// the token's position in the block or the call, so a sequence split over calls
+// gives the same bits as one call.
+#include <cstddef>
+
 #include "gdn_device.cuh"
 #include "gdn_internal.h"
+#include "gdn_norm_row.cuh"
 
 namespace gdn {
 namespace {
@@ -35,14 +54,22 @@ constexpr int NCOL = 16;  // value columns per CTA (per head)
 constexpr int B = 16;     // tokens per stage (the producer's k.q reduce-scatter assumes 16)
 static_assert(B == 16, "k.q reduce-scatter layout");
 constexpr int NS = 4;     // stages in the ring
+constexpr int SLICES = D / NCOL;           // CTAs (column slices) of a key head
+constexpr int ROWS = kHeadsPerKey * B;     // (head, token) rows of a stage
+constexpr int NSX = 2;                     // slots of the exchange between the CTAs of a key head
+constexpr int kNormWarps = 4;              // norm warps per CTA (one per SM sub-partition)
+constexpr int NROWS = ROWS / kNormWarps;   // rows of a stage each norm warp norms
+static_assert(NROWS <= 32 && NROWS * kNormWarps == ROWS, "rows per norm warp");
 
-template <int R>
+template <int R, bool NORM>
 struct SeqShape {
     static_assert(R % 4 == 0 && D % R == 0, "rows per lane");
     static constexpr int G = D / R;          // lanes per column
     static constexpr int CPW = 32 / G;       // columns per warp
     static constexpr int NCW = NCOL / CPW;   // consumer warps
-    static constexpr int THREADS = (NCW + 1) * 32;
+    static constexpr int PRODUCER = NCW;     // warp index of the producer
+    static constexpr int NORM0 = NCW + 1;    // warp index of the first norm warp (NORM only)
+    static constexpr int THREADS = (NCW + 1 + (NORM ? kNormWarps : 0)) * 32;
     static constexpr int P4 = R / 4;         // float4 row groups per lane
 };
 
@@ -56,115 +83,173 @@ struct __align__(128) Stage {
 };
 constexpr uint32_t kStageTxBytes = 2 * B * D * 4 + kHeadsPerKey * B * NCOL * 4;
 
+// The fused norm's buffers.
+struct __align__(128) NormBufs {
+    float z[NS][kHeadsPerKey][B][NCOL];       // TMA: the gate z of the stage's rows and columns
+    float r[kNormWarps][NROWS];               // per row: 1 / sqrt(mean o^2 + eps)
+};
+constexpr uint32_t kZTxBytes = kHeadsPerKey * B * NCOL * 4;
+
+// The plain scan uses the members up to `o` only, and is launched with that much.
 struct SeqSmem {
     Stage st[NS];
-    uint64_t full[NS];   // TMA bytes landed
-    uint64_t ready[NS];  // producer's per-token scalars written
-    uint64_t empty[NS];  // every consumer warp is done with the stage
+    uint64_t full[NS];    // TMA bytes landed
+    uint64_t ready[NS];   // producer's per-token scalars written (and the stage's output tiles free)
+    uint64_t empty[NS];   // every consumer warp is done with the stage's inputs and has written its outputs
+    uint64_t zfull[NS];   // norm: z tile landed
+    uint64_t normed[NS];  // norm: every norm warp is done with the stage's output and z tiles
+    alignas(128) float o[NS][kHeadsPerKey][B][NCOL];  // norm: each stage's outputs
+    NormBufs nb;                                      // norm
 };
 
-template <int R>
-__global__ void __launch_bounds__(SeqShape<R>::THREADS, 1) gdn_seq_kernel(const __grid_constant__ SeqParams p) {
-    using Sh = SeqShape<R>;
-    SeqSmem& sm = *aligned_dynamic_smem<SeqSmem, 1024>();
-    const int kh = blockIdx.x;
-    const int c0 = blockIdx.y * NCOL;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+// ---------------- producer warp ----------------
+template <int R, bool NORM>
+__device__ void producer_role(const SeqParams& p, SeqSmem& sm, int kh, int c0, int lane) {
+    // parameters read once into registers (see consumer_role)
     const int64_t T = p.T;
     const int n_kh = p.n_kh, n_vh = p.n_vh;
+    const float* const gp = p.g;
+    const float* const betap = p.beta;
+    const bool store_out = NORM && p.out != nullptr;
+    int* const status = p.status;
     const int64_t nst = (T + B - 1) / B;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(&sm.full[s], 1);
-            mbar_init(&sm.ready[s], 1);
-            mbar_init(&sm.empty[s], Sh::NCW);
-        }
-        mbar_init_fence();
-    }
-    __syncthreads();
-
-    if (warp == Sh::NCW) {
-        // ---------------- producer warp ----------------
-        auto issue = [&](int64_t s) {
-            Stage& st = sm.st[s % NS];
-            uint64_t* bar = &sm.full[s % NS];
-            const int y = static_cast<int>(s * B);
-            mbar_arrive_expect_tx(bar, kStageTxBytes);
-            tma_load_2d(st.k, &p.tm_k, bar, kh * D, y);
-            tma_load_2d(st.q, &p.tm_q, bar, kh * D, y);
+    auto issue = [&](int64_t s) {
+        Stage& st = sm.st[s % NS];
+        uint64_t* bar = &sm.full[s % NS];
+        const int y = static_cast<int>(s * B);
+        mbar_arrive_expect_tx(bar, kStageTxBytes);
+        tma_load_2d(st.k, &p.tm_k, bar, kh * D, y);
+        tma_load_2d(st.q, &p.tm_q, bar, kh * D, y);
+#pragma unroll
+        for (int m = 0; m < kHeadsPerKey; ++m) tma_load_2d(st.v[m], &p.tm_v, bar, (kh + m * n_kh) * D + c0, y);
+    };
+    auto issue_z = [&](int64_t s) {  // with the norm: the gate z of stage s
+        uint64_t* bar = &sm.zfull[s % NS];
+        mbar_arrive_expect_tx(bar, kZTxBytes);
+#pragma unroll
+        for (int m = 0; m < kHeadsPerKey; ++m)
+            tma_load_2d(&sm.nb.z[s % NS][m][0][0], &p.tm_z, bar, (kh + m * n_kh) * D + c0, static_cast<int>(s * B));
+    };
+    auto store_outputs = [&](int64_t r) {  // with the norm (else the consumers store their outputs)
+        if (store_out) {
 #pragma unroll
             for (int m = 0; m < kHeadsPerKey; ++m)
-                tma_load_2d(st.v[m], &p.tm_v, bar, (kh + m * n_kh) * D + c0, y);
-        };
-        int64_t issued = nst < NS ? nst : NS;
-        if (lane == 0)
-            for (int64_t s = 0; s < issued; ++s) issue(s);
-        __syncwarp();  // lanes 1..31 must not spin on a barrier while lane 0 still has copies to issue
-        int64_t landed = 0;  // stages whose full barrier this warp has observed
-        bool ok = true;
-        for (int64_t s = 0; s < nst && ok; ++s) {
-            const int buf = static_cast<int>(s % NS);
-            Stage& st = sm.st[buf];
-            for (int idx = lane; idx < kHeadsPerKey * B; idx += 32) {
-                const int tt = idx / kHeadsPerKey, m = idx % kHeadsPerKey;
-                const int64_t t = s * B + tt;
-                float gv = 0.f, bv = 0.f;
-                if (t < T) {
-                    gv = __ldg(p.g + t * n_vh + kh + m * n_kh);
-                    bv = __ldg(p.beta + t * n_vh + kh + m * n_kh);
-                }
-                st.a[tt][m] = expf(gv);
-                st.b[tt][m] = bv;
+                tma_store_2d(&p.tm_o, &sm.o[r % NS][m][0][0], (kh + m * n_kh) * D + c0, static_cast<int>(r * B));
+            bulk_commit_group();
+        }
+    };
+    int64_t issued = nst < NS ? nst : NS;
+    if (lane == 0)
+        for (int64_t s = 0; s < issued; ++s) {
+            issue(s);
+            if (NORM) issue_z(s);
+        }
+    __syncwarp();  // lanes 1..31 must not spin on a barrier while lane 0 still has copies to issue
+    int64_t z_issued = NORM ? issued : 0;
+    int64_t landed = 0;  // stages whose full barrier this warp has observed
+    bool ok = true;
+    for (int64_t s = 0; s < nst && ok; ++s) {
+        const int buf = static_cast<int>(s % NS);
+        Stage& st = sm.st[buf];
+        for (int idx = lane; idx < kHeadsPerKey * B; idx += 32) {
+            const int tt = idx / kHeadsPerKey, m = idx % kHeadsPerKey;
+            const int64_t t = s * B + tt;
+            float gv = 0.f, bv = 0.f;
+            if (t < T) {
+                gv = __ldg(gp + t * n_vh + kh + m * n_kh);
+                bv = __ldg(betap + t * n_vh + kh + m * n_kh);
             }
-            if (!mbar_wait(&sm.full[buf], static_cast<uint32_t>((s / NS) & 1))) { ok = false; break; }
-            landed = s + 1;
-            // k.q of the block's 16 tokens: lane partials over dims 4*lane..4*lane+3, then
-            // a reduce-scatter over the warp (keep half the tokens at each xor level),
-            // so lanes 2u and 2u+1 end with token 8*b4 + 4*b3 + 2*b2 + b1 of lane 2u.
-            float kqv[B];
+            st.a[tt][m] = expf(gv);
+            st.b[tt][m] = bv;
+        }
+        if (!mbar_wait(&sm.full[buf], static_cast<uint32_t>((s / NS) & 1))) { ok = false; break; }
+        landed = s + 1;
+        // k.q of the block's 16 tokens: lane partials over dims 4*lane..4*lane+3, then
+        // a reduce-scatter over the warp (keep half the tokens at each xor level),
+        // so lanes 2u and 2u+1 end with token 8*b4 + 4*b3 + 2*b2 + b1 of lane 2u.
+        float kqv[B];
 #pragma unroll
-            for (int tt = 0; tt < B; ++tt) {
-                const float4 k4 = reinterpret_cast<const float4*>(st.k[tt])[lane];
-                const float4 q4 = reinterpret_cast<const float4*>(st.q[tt])[lane];
-                kqv[tt] = fmaf(k4.w, q4.w, fmaf(k4.z, q4.z, fmaf(k4.y, q4.y, k4.x * q4.x)));
+        for (int tt = 0; tt < B; ++tt) {
+            const float4 k4 = reinterpret_cast<const float4*>(st.k[tt])[lane];
+            const float4 q4 = reinterpret_cast<const float4*>(st.q[tt])[lane];
+            kqv[tt] = fmaf(k4.w, q4.w, fmaf(k4.z, q4.z, fmaf(k4.y, q4.y, k4.x * q4.x)));
+        }
+#pragma unroll
+        for (int lvl = 0; lvl < 4; ++lvl) {
+            const int off = 16 >> lvl, half = B >> (lvl + 1);
+            const bool upper = (lane & off) != 0;
+#pragma unroll
+            for (int i = 0; i < half; ++i) {
+                const float send = upper ? kqv[i] : kqv[i + half];
+                const float keep = upper ? kqv[i + half] : kqv[i];
+                kqv[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
             }
-#pragma unroll
-            for (int lvl = 0; lvl < 4; ++lvl) {
-                const int off = 16 >> lvl, half = B >> (lvl + 1);
-                const bool upper = (lane & off) != 0;
-#pragma unroll
-                for (int i = 0; i < half; ++i) {
-                    const float send = upper ? kqv[i] : kqv[i + half];
-                    const float keep = upper ? kqv[i + half] : kqv[i];
-                    kqv[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-                }
+        }
+        kqv[0] += __shfl_xor_sync(0xffffffffu, kqv[0], 1);
+        if ((lane & 1) == 0)
+            st.kq[((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1)] = kqv[0];
+        __threadfence_block();
+        __syncwarp();
+        // With the norm the consumers write this stage's output tile once 'ready'
+        // arrives; it was last read by the TMA store of stage s - NS (the stores
+        // committed so far are those of stages <= s - 2) and by the epilogue.
+        if (NORM && lane == 0) bulk_wait_group_read<NS - 2>();
+        if (NORM && s >= NS) {
+            if (!mbar_wait(&sm.normed[buf], static_cast<uint32_t>(((s - NS) / NS) & 1))) {
+                ok = false;
+                break;
             }
-            kqv[0] += __shfl_xor_sync(0xffffffffu, kqv[0], 1);
-            if ((lane & 1) == 0)
-                st.kq[((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1)] = kqv[0];
-            __threadfence_block();
+            if (lane == 0) issue_z(s);  // stage s - NS's z tile is read
+            z_issued = s + 1;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.ready[buf]);
+        // Store the outputs of the stage the consumers finished last, then refill its buffer.
+        if (s >= 1) {
+            const int64_t r = s - 1;
+            if (!mbar_wait(&sm.empty[r % NS], static_cast<uint32_t>((r / NS) & 1))) { ok = false; break; }
+            if (lane == 0) {
+                store_outputs(r);
+                if (r + NS < nst) issue(r + NS);
+            }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.ready[buf]);
-            // Refill the buffer the consumers finished last.
-            if (s >= 1 && s - 1 + NS < nst) {
-                const int64_t r = s - 1;
-                if (!mbar_wait(&sm.empty[r % NS], static_cast<uint32_t>((r / NS) & 1))) { ok = false; break; }
-                if (lane == 0) issue(r + NS);
-                __syncwarp();
-                issued = r + NS + 1;
-            }
+            if (r + NS < nst) issued = r + NS + 1;
         }
-        if (!ok) {
-            // Record the failure, then let every issued copy land before the CTA exits.
-            if (lane == 0) report_timeout(p.status);
-            for (int64_t s = landed; s < issued; ++s)
-                mbar_wait(&sm.full[s % NS], static_cast<uint32_t>((s / NS) & 1));
-        }
-        return;
     }
+    if (ok) {
+        const int64_t r = nst - 1;
+        if (!mbar_wait(&sm.empty[r % NS], static_cast<uint32_t>((r / NS) & 1)))
+            ok = false;
+        else if (lane == 0)
+            store_outputs(r);
+    }
+    if (NORM && lane == 0) bulk_wait_group_all();  // every output store has landed before the CTA exits
+    __syncwarp();
+    if (!ok) {
+        // Record the failure, then let every issued copy land before the CTA exits.
+        if (lane == 0) report_timeout(status);
+        for (int64_t s = landed; s < issued; ++s) mbar_wait(&sm.full[s % NS], static_cast<uint32_t>((s / NS) & 1));
+    }
+    if (NORM) {
+        // z tiles nobody waited for (the norm warps stopped early) land before the CTA exits
+        for (int64_t s = (z_issued > NS ? z_issued - NS : 0); s < z_issued; ++s)
+            mbar_wait(&sm.zfull[s % NS], static_cast<uint32_t>((s / NS) & 1));
+    }
+}
 
-    // ---------------- consumer warps ----------------
+// ---------------- consumer warps ----------------
+template <int R, bool NORM>
+__device__ void consumer_role(const SeqParams& p, SeqSmem& sm, int kh, int c0, int warp, int lane) {
+    using Sh = SeqShape<R, NORM>;
+    // parameters read once into registers (p is the kernel's parameter block, seen
+    // here through a reference; reads of it inside the loop could not be hoisted
+    // past the output stores)
+    const int64_t T = p.T;
+    const int n_kh = p.n_kh;
+    const int64_t out_stride = static_cast<int64_t>(p.n_vh) * D;
+    float* const state = p.state;
+    int* const status = p.status;
+    const int64_t nst = (T + B - 1) / B;
     const int colw = lane / Sh::G;
     const int rg = lane % Sh::G;
     const int cl = warp * Sh::CPW + colw;  // column within the CTA
@@ -173,7 +258,7 @@ __global__ void __launch_bounds__(SeqShape<R>::THREADS, 1) gdn_seq_kernel(const 
     float2 S[kHeadsPerKey][Sh::P4][2];
 #pragma unroll
     for (int m = 0; m < kHeadsPerKey; ++m) {
-        const float* sh = p.state + static_cast<int64_t>(kh + m * n_kh) * D * D + c;
+        const float* sh = state + static_cast<int64_t>(kh + m * n_kh) * D * D + c;
 #pragma unroll
         for (int pp = 0; pp < Sh::P4; ++pp) {
             const int row = 4 * rg + 4 * Sh::G * pp;
@@ -181,7 +266,6 @@ __global__ void __launch_bounds__(SeqShape<R>::THREADS, 1) gdn_seq_kernel(const 
             S[m][pp][1] = make_float2(sh[(row + 2) * D], sh[(row + 3) * D]);
         }
     }
-    float* out_col = p.out + static_cast<int64_t>(kh + (rg < kHeadsPerKey ? rg : 0) * n_kh) * D + c;
 
     // One token's operands, loaded from the stage one token ahead of use.
     struct Ops {
@@ -204,15 +288,21 @@ __global__ void __launch_bounds__(SeqShape<R>::THREADS, 1) gdn_seq_kernel(const 
         }
         o.kq = st.kq[tt];
     };
+    // Output destination of token tt of a stage (lanes rg < 3): with the norm the
+    // shared output tile (indexing the shared array itself keeps the store a
+    // shared-memory store that the compiler can tell apart from the operand
+    // loads), else out.
+    float* const o_all = &sm.o[0][0][0][0];
+    float* const out_col = NORM ? nullptr : p.out + static_cast<int64_t>(kh + (rg < kHeadsPerKey ? rg : 0) * n_kh) * D + c;
+    const int my_m = rg < kHeadsPerKey ? rg : 0;
     // One token: both column sums from one pass over the state (12 independent
     // packed accumulator chains), the k-sum reduction first (it gates delta), the
     // decay product a*S formed while the shuffles are in flight, then the update;
     // the q-sum reduction and the output come last, off the state's critical path.
-    auto token = [&](const Ops& o, int64_t t) {
+    auto token = [&](const Ops& o, int64_t dst) {
         float2 ak[kHeadsPerKey][2], aq[kHeadsPerKey][2];
 #pragma unroll
-        for (int m = 0; m < kHeadsPerKey; ++m)
-            ak[m][0] = ak[m][1] = aq[m][0] = aq[m][1] = make_float2(0.f, 0.f);
+        for (int m = 0; m < kHeadsPerKey; ++m) ak[m][0] = ak[m][1] = aq[m][0] = aq[m][1] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int pp = 0; pp < Sh::P4; ++pp) {
             const float2 k01 = make_float2(o.k[pp].x, o.k[pp].y), k23 = make_float2(o.k[pp].z, o.k[pp].w);
@@ -268,38 +358,51 @@ __global__ void __launch_bounds__(SeqShape<R>::THREADS, 1) gdn_seq_kernel(const 
             const float out = fmaf(o.kq, delta[m], o.a[m] * sq[m]);
             if (rg == m) o_mine = out;
         }
-        if (rg < kHeadsPerKey) out_col[t * static_cast<int64_t>(n_vh) * D] = o_mine;
+        if (rg < kHeadsPerKey) {
+            if (NORM)
+                o_all[dst] = o_mine;
+            else
+                out_col[dst * out_stride] = o_mine;
+        }
     };
 
+    bool ok = true;
     for (int64_t s = 0; s < nst; ++s) {
         const int buf = static_cast<int>(s % NS);
         const uint32_t par = static_cast<uint32_t>((s / NS) & 1);
         if (!mbar_wait(&sm.full[buf], par) || !mbar_wait(&sm.ready[buf], par)) {
-            if (lane == 0) report_timeout(p.status);
-            return;
+            if (lane == 0) report_timeout(status);
+            ok = false;
+            break;
         }
         const Stage& st = sm.st[buf];
+        // destination of token tt's output: o_base + tt * o_step
+        const int64_t o_base = NORM ? ((buf * kHeadsPerKey + my_m) * B) * NCOL + cl : s * B;
+        const int64_t o_step = NORM ? NCOL : 1;
         const int64_t rem = T - s * B;
         const int nt = rem < B ? static_cast<int>(rem) : B;
-        const int64_t t0 = s * B;
         Ops x0, x1;
         load(x0, st, 0);
         int tt = 0;
 #pragma unroll 1
         for (; tt + 1 < nt; tt += 2) {
             load(x1, st, tt + 1);
-            token(x0, t0 + tt);
+            token(x0, o_base + tt * o_step);
             if (tt + 2 < nt) load(x0, st, tt + 2);
-            token(x1, t0 + tt + 1);
+            token(x1, o_base + (tt + 1) * o_step);
         }
-        if (tt < nt) token(x0, t0 + tt);
+        if (tt < nt) token(x0, o_base + tt * o_step);
+        // The stage's inputs are read and its outputs written: hand it back (with the
+        // norm, after making the output tile visible to the TMA store's async proxy).
+        if (NORM) fence_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.empty[buf]);
     }
+    if (!ok) return;  // the state is left as it was
 
 #pragma unroll
     for (int m = 0; m < kHeadsPerKey; ++m) {
-        float* sh = p.state + static_cast<int64_t>(kh + m * n_kh) * D * D + c;
+        float* sh = state + static_cast<int64_t>(kh + m * n_kh) * D * D + c;
 #pragma unroll
         for (int pp = 0; pp < Sh::P4; ++pp) {
             const int row = 4 * rg + 4 * Sh::G * pp;
@@ -311,25 +414,221 @@ __global__ void __launch_bounds__(SeqShape<R>::THREADS, 1) gdn_seq_kernel(const 
     }
 }
 
-template <int R>
+// ---------------- norm warps ----------------
+// Norm warp i of a CTA norms rows 12 i .. 12 i + 11 of every stage ((head, token)
+// row m * 16 + tt).  Per stage: wait for the output tile; per row compute the sums
+// of squares of the CTA's four 4-column groups (each as gdn_out_norm's lane does
+// for its 4 columns) and publish them in global memory at [key head][slot][slice];
+// gather all eight slices' once their publication counters show the stage; add a
+// row's 32 group sums in the order of gdn_out_norm's xor tree (offsets 16, 8, 4,
+// 2, 1); form r and write y for the CTA's 16 columns with the row code's
+// expression.  The gather and the norm of a stage run one stage after its
+// publication, so the round trip through L2 overlaps the next stage's work.  The
+// counters hold (generation << 32 | stages), so a replayed launch never takes an
+// earlier launch's values for its own.
+__device__ void norm_role(const SeqParams& p, SeqSmem& sm, int kh, int c0, int slice, int wi, int lane,
+                          unsigned long long gen) {
+    // parameters read once into registers (see consumer_role)
+    const int64_t T = p.T;
+    const int n_kh = p.n_kh;
+    const int64_t y_stride = static_cast<int64_t>(p.n_vh) * D;
+    const float eps = p.eps;
+    float* const xg = p.xg;
+    uint16_t* const yp = p.y;
+    int* const status = p.status;
+    const int64_t nst = (T + B - 1) / B;
+    NormBufs& nb = sm.nb;
+    const int row0 = wi * NROWS;
+    const int q = lane & 3;  // 4-column group of this lane in the y phase
+    const float4 wq = *reinterpret_cast<const float4*>(p.w + c0 + 4 * q);
+    // publication counters of (key head, slice, norm warp): stages published / consumed
+    unsigned long long* pub = p.xflags + static_cast<int64_t>(kh) * SLICES * kNormWarps + wi;
+    unsigned long long* con = p.xflags + static_cast<int64_t>(n_kh + kh) * SLICES * kNormWarps + wi;
+    auto xslot = [&](int64_t s, int sl) {  // slice sl's group sums of this warp's rows, in the stage's slot
+        return reinterpret_cast<float4*>(xg) + ((static_cast<int64_t>(kh) * NSX + s % NSX) * SLICES + sl) * ROWS + row0;
+    };
+    bool ok = true;
+    for (int64_t s = 0; s <= nst; ++s) {
+        if (s < nst) {
+            const int slot = static_cast<int>(s % NS);
+            // (1) the stage's outputs are in the tile
+            if (!mbar_wait(&sm.empty[slot], static_cast<uint32_t>((s / NS) & 1))) ok = false;
+            if (!__all_sync(0xffffffffu, ok)) break;
+            // (2) group sums of row row0 + lane
+            float4 part = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (lane < NROWS) {
+                const int row = row0 + lane;
+                const float4* orow = reinterpret_cast<const float4*>(&sm.o[slot][row / B][row % B][0]);
+                float g4[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float4 o4 = orow[u];
+                    float ss = o4.x * o4.x;
+                    ss = fmaf(o4.y, o4.y, ss);
+                    ss = fmaf(o4.z, o4.z, ss);
+                    ss = fmaf(o4.w, o4.w, ss);
+                    g4[u] = ss;
+                }
+                part = make_float4(g4[0], g4[1], g4[2], g4[3]);
+            }
+            // (3) the slot is free once every slice has consumed stage s - NSX: lanes 0..7 watch one slice each
+            if (s >= NSX && lane < SLICES &&
+                !wait_counter(con + lane * kNormWarps, (gen << 32) | static_cast<uint64_t>(s - NSX + 1)))
+                ok = false;
+            if (!__all_sync(0xffffffffu, ok)) break;
+            __syncwarp();  // the other lanes' stores below come after lanes 0..7 saw the counters
+            // (4) publish
+            if (lane < NROWS) xslot(s, slice)[lane] = part;
+            __threadfence();
+            __syncwarp();
+            if (lane == 0)
+                st_release_gpu_u64(pub + slice * kNormWarps, (gen << 32) | static_cast<uint64_t>(s + 1));
+        }
+        if (s == 0) continue;
+        const int64_t u = s - 1;  // the stage normed in this iteration
+        const int slot = static_cast<int>(u % NS);
+        // (5) gather: every slice has published stage u
+        if (lane < SLICES && !wait_counter(pub + lane * kNormWarps, (gen << 32) | static_cast<uint64_t>(u + 1)))
+            ok = false;
+        if (!__all_sync(0xffffffffu, ok)) break;
+        __syncwarp();  // every lane's loads below come after lanes 0..7 saw the counters
+        __threadfence();
+        if (lane < NROWS) {
+            float g[32];
+#pragma unroll
+            for (int sl = 0; sl < SLICES; ++sl) {
+                const float4 v = __ldcg(xslot(u, sl) + lane);
+                g[4 * sl] = v.x;
+                g[4 * sl + 1] = v.y;
+                g[4 * sl + 2] = v.z;
+                g[4 * sl + 3] = v.w;
+            }
+            // lane 0's view of the xor tree: level 16, 8, 4, 2, 1
+#pragma unroll
+            for (int j = 0; j < 16; ++j) g[j] = g[j] + g[j + 16];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) g[j] = g[j] + g[j + 8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) g[j] = g[j] + g[j + 4];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) g[j] = g[j] + g[j + 2];
+            const float ss = g[0] + g[1];
+            nb.r[wi][lane] = rsqrtf(fmaf(ss, 1.0f / 128.0f, eps));
+        }
+        // (6) this warp has read stage u's slot
+        __syncwarp();
+        if (lane == 0) st_release_gpu_u64(con + slice * kNormWarps, (gen << 32) | static_cast<uint64_t>(u + 1));
+        // (7) z landed
+        if (!mbar_wait(&sm.zfull[slot], static_cast<uint32_t>((u / NS) & 1))) ok = false;
+        if (!__all_sync(0xffffffffu, ok)) break;
+        // (8) y of the CTA's columns: lane = 4-column group q of rows row0 + (lane >> 2) + 8 j
+#pragma unroll
+        for (int j = 0; j < (NROWS + 7) / 8; ++j) {
+            const int rl = (lane >> 2) + 8 * j;
+            if (rl < NROWS) {
+                const int row = row0 + rl;
+                const int m = row / B, tt = row % B;
+                const int64_t t = u * B + tt;
+                if (t < T) {
+                    const float4 o4 = *reinterpret_cast<const float4*>(&sm.o[slot][m][tt][4 * q]);
+                    const float4 z4 = *reinterpret_cast<const float4*>(&nb.z[slot][m][tt][4 * q]);
+                    const float r = nb.r[wi][rl];
+                    const __half2 lo =
+                        __floats2half2_rn(o4.x * r * wq.x * norm_silu(z4.x), o4.y * r * wq.y * norm_silu(z4.y));
+                    const __half2 hi =
+                        __floats2half2_rn(o4.z * r * wq.z * norm_silu(z4.z), o4.w * r * wq.w * norm_silu(z4.w));
+                    uint2 pkd;
+                    pkd.x = *reinterpret_cast<const uint32_t*>(&lo);
+                    pkd.y = *reinterpret_cast<const uint32_t*>(&hi);
+                    *reinterpret_cast<uint2*>(yp + t * y_stride + static_cast<int64_t>(kh + m * n_kh) * D + c0 +
+                                              4 * q) = pkd;
+                }
+            }
+        }
+        // (9) done with stage u's output and z tiles
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.normed[slot]);
+    }
+    if (!ok && lane == 0) report_error(status, kDevErrFlagTimeout);
+}
+
+template <int R, bool NORM>
+__global__ void __launch_bounds__(SeqShape<R, NORM>::THREADS, 1) gdn_seq_kernel(const __grid_constant__ SeqParams p) {
+    using Sh = SeqShape<R, NORM>;
+    SeqSmem& sm = *aligned_dynamic_smem<SeqSmem, 1024>();
+    const int kh = blockIdx.x;
+    const int c0 = blockIdx.y * NCOL;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __shared__ uint32_t s_gen;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.ready[s], 1);
+            mbar_init(&sm.empty[s], Sh::NCW);
+            mbar_init(&sm.zfull[s], 1);
+            mbar_init(&sm.normed[s], kNormWarps);
+        }
+        mbar_init_fence();
+        // this launch's generation: one more than the last finished launch's
+        if (NORM) s_gen = ld_acquire_gpu(p.sync) + 1u;
+    }
+    __syncthreads();
+
+    if (warp == Sh::PRODUCER)
+        producer_role<R, NORM>(p, sm, kh, c0, lane);
+    else if (NORM && warp >= Sh::NORM0)
+        norm_role(p, sm, kh, c0, blockIdx.y, warp - Sh::NORM0, lane, s_gen);
+    else
+        consumer_role<R, NORM>(p, sm, kh, c0, warp, lane);
+    if (NORM) {
+        // the last CTA to finish advances the generation
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            __threadfence();
+            if (atomicAdd(p.sync + 1, 1u) == gridDim.x * gridDim.y - 1) {
+                p.sync[1] = 0u;
+                st_release_gpu(p.sync, s_gen);
+            }
+        }
+    }
+}
+
+template <int R, bool NORM>
 cudaError_t launch_seq_t(const SeqParams& p, cudaStream_t s) {
-    using Sh = SeqShape<R>;
-    const size_t smem = sizeof(SeqSmem) + 1024;
-    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(gdn_seq_kernel<R>), static_cast<int>(smem));
+    using Sh = SeqShape<R, NORM>;
+    const size_t smem = (NORM ? sizeof(SeqSmem) : offsetof(SeqSmem, o)) + 1024;
+    const auto kernel = gdn_seq_kernel<R, NORM>;
+    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kernel), static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    dim3 grid(p.n_kh, D / NCOL);
-    gdn_seq_kernel<R><<<grid, Sh::THREADS, smem, s>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.n_kh, SLICES);
+    cfg.blockDim = dim3(Sh::THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;  // the fused norm's CTAs wait for each other
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = NORM ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
 }  // namespace
 
 int seq_tokens_per_stage() { return B; }
+size_t seq_norm_scratch_bytes(int n_kh) {
+    // counters first (8-byte aligned), then sync words, then the group sums (16-byte aligned)
+    return static_cast<size_t>(seq_norm_counters(n_kh)) * 8 + 16 +
+           static_cast<size_t>(n_kh) * NSX * SLICES * ROWS * 16;
+}
+int seq_norm_counters(int n_kh) { return 2 * n_kh * SLICES * kNormWarps; }
 int seq_box_cols() { return NCOL; }
 
 cudaError_t launch_seq(const SeqParams& p, int rows_per_thread, cudaStream_t s) {
-    if (rows_per_thread == 8) return launch_seq_t<8>(p, s);
-    return launch_seq_t<16>(p, s);
+    const bool norm = p.y != nullptr;
+    if (rows_per_thread == 8) return norm ? launch_seq_t<8, true>(p, s) : launch_seq_t<8, false>(p, s);
+    return norm ? launch_seq_t<16, true>(p, s) : launch_seq_t<16, false>(p, s);
 }
 
 }  // namespace gdn

@@ -29,6 +29,22 @@ GDN_ERR_UNSUPPORTED = -2
 GDN_ERR_ALLOC = -3
 GDN_ERR_CUDA = -4
 GDN_ERR_TIMEOUT = -5
+# options (gdn_set_option)
+GDN_OPT_CHUNK_PRODUCTS = 1
+GDN_OPT_CHUNK_ONE_LAUNCH = 2
+GDN_OPT_NORM_IN_LAUNCH = 3
+GDN_OPT_SEQ_ROWS_PER_THREAD = 4
+GDN_OPT_TEST_WITHHOLD_PREP_TASK = 101
+GDN_OPT_TEST_FAIL_SCRATCH_ALLOC = 102
+GDN_PRODUCTS_MMA = 0
+GDN_PRODUCTS_FMA = 1
+GDN_PRODUCTS_TCGEN05 = 2
+_OPTIONS = {"chunk_products": GDN_OPT_CHUNK_PRODUCTS, "chunk_one_launch": GDN_OPT_CHUNK_ONE_LAUNCH,
+            "norm_in_launch": GDN_OPT_NORM_IN_LAUNCH, "seq_rows_per_thread": GDN_OPT_SEQ_ROWS_PER_THREAD,
+            "test_withhold_prep_task": GDN_OPT_TEST_WITHHOLD_PREP_TASK,
+            "test_fail_scratch_alloc": GDN_OPT_TEST_FAIL_SCRATCH_ALLOC}
+_PRODUCTS = {"mma": GDN_PRODUCTS_MMA, "fma": GDN_PRODUCTS_FMA, "tc": GDN_PRODUCTS_TCGEN05,
+             "tcgen05": GDN_PRODUCTS_TCGEN05}
 
 _MODES = {"sequential": GDN_SEQUENTIAL, "seq": GDN_SEQUENTIAL, "chunked": GDN_CHUNKED, "auto": GDN_AUTO,
           GDN_SEQUENTIAL: GDN_SEQUENTIAL, GDN_CHUNKED: GDN_CHUNKED, GDN_AUTO: GDN_AUTO}
@@ -38,7 +54,8 @@ _lib = None
 
 EXPORTS = ("gdn_recurrence", "gdn_out_norm", "gdn_last_error", "gdn_device_status",
            "gdn_release_scratch", "gdn_poison_scratch", "gdn_chunked_scratch_bytes", "gdn_launch_count",
-           "gdn_recurrence_chunked_noalloc", "gdn_decode", "gdn_prestage", "gdn_recurrence_norm")
+           "gdn_recurrence_chunked_noalloc", "gdn_decode", "gdn_prestage", "gdn_recurrence_norm",
+           "gdn_set_option", "gdn_get_option")
 
 
 class GDNError(RuntimeError):
@@ -82,6 +99,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gdn_poison_scratch.restype = i32
         lib.gdn_chunked_scratch_bytes.argtypes = [i32]
         lib.gdn_chunked_scratch_bytes.restype = ctypes.c_size_t
+        lib.gdn_set_option.argtypes = [i32, i32]
+        lib.gdn_set_option.restype = i32
+        lib.gdn_get_option.argtypes = [i32, ctypes.POINTER(ctypes.c_int)]
+        lib.gdn_get_option.restype = i32
         lib.gdn_launch_count.argtypes = []
         lib.gdn_launch_count.restype = ctypes.c_uint64
         if path == LIB_PATH:
@@ -144,12 +165,13 @@ def gdn_recurrence(q, k, v, g, beta, state, out=None, mode="sequential", stream=
 
 
 def gdn_recurrence_norm(q, k, v, g, beta, state, z, w, eps: float = 1e-6, out=None, y=None, mode="chunked",
-                        stream=None):
+                        stream=None, store_out=True):
     """gdn_recurrence and gdn_out_norm of its output in one call; returns (out, y).
 
     ``out`` ([T][n_vh][d] FP32) and ``y`` ([T][n_vh][d] float16) are allocated if
-    None.  In chunked mode the norm runs inside the recurrence's launch when the
-    one-launch form applies.
+    None.  In sequential mode the norm is fused into the scan (one launch), and
+    with ``store_out=False`` the FP32 output is not written at all (``out`` is
+    returned as None).
     """
     T, n_kh, d = q.shape
     n_vh = v.shape[1]
@@ -161,11 +183,14 @@ def gdn_recurrence_norm(q, k, v, g, beta, state, z, w, eps: float = 1e-6, out=No
     _want(state, "state", (n_vh, d, d))
     _want(z, "z", (T, n_vh, d))
     _want(w, "w", (d,))
-    if out is None:
+    if not store_out:
+        out = None
+    elif out is None:
         out = torch.empty((T, n_vh, d), dtype=torch.float32, device=q.device)
     if y is None:
         y = torch.empty((T, n_vh, d), dtype=torch.float16, device=q.device)
-    _want(out, "out", (T, n_vh, d))
+    if out is not None:
+        _want(out, "out", (T, n_vh, d))
     _want(y, "y", (T, n_vh, d), dtype=torch.float16)
     if mode not in _MODES:
         raise ValueError(f"unknown mode {mode!r}")
@@ -296,6 +321,47 @@ def gdn_poison_scratch(bits: int = 0x7FC00000, n_vh: int = 48, stream=None):
 
 def gdn_chunked_scratch_bytes(n_vh: int = 48) -> int:
     return int(load_library().gdn_chunked_scratch_bytes(int(n_vh)))
+
+
+def _option_id(option) -> int:
+    return _OPTIONS[option] if isinstance(option, str) else int(option)
+
+
+def gdn_set_option(option, value):
+    """Set a process-wide option of the library (``option``: a GDN_OPT_* number or
+    its lower-case name without the prefix, e.g. "chunk_products"; for that one
+    ``value`` may also be "mma", "fma" or "tc")."""
+    if isinstance(value, str):
+        value = _PRODUCTS[value]
+    _check(load_library().gdn_set_option(_option_id(option), int(value)))
+
+
+def gdn_get_option(option) -> int:
+    v = ctypes.c_int(0)
+    _check(load_library().gdn_get_option(_option_id(option), ctypes.byref(v)))
+    return int(v.value)
+
+
+class options:
+    """Context manager: set options for the duration of a block, then restore them.
+
+    >>> with gdn.options(chunk_products="fma", chunk_one_launch=0): ...
+    """
+
+    def __init__(self, **kw):
+        self.kw = kw
+        self.saved = {}
+
+    def __enter__(self):
+        for name, value in self.kw.items():
+            self.saved[name] = gdn_get_option(name)
+            gdn_set_option(name, value)
+        return self
+
+    def __exit__(self, *exc):
+        for name, value in self.saved.items():
+            gdn_set_option(name, value)
+        return False
 
 
 def gdn_launch_count() -> int:

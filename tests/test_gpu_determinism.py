@@ -95,26 +95,6 @@ def test_auto_mode_is_the_chosen_mode_bit_for_bit(T):
     assert np.array_equal(sa.view(np.uint32), sc.view(np.uint32))
 
 
-def _env(name, value):
-    """Context manager setting one environment variable (read by the library per call)."""
-    import contextlib
-    import os
-
-    @contextlib.contextmanager
-    def cm():
-        old = os.environ.get(name)
-        os.environ[name] = value
-        try:
-            yield
-        finally:
-            if old is None:
-                del os.environ[name]
-            else:
-                os.environ[name] = old
-
-    return cm()
-
-
 def _sm_count():
     return torch.cuda.get_device_properties(0).multi_processor_count
 
@@ -130,8 +110,8 @@ def test_one_launch_chunked_matches_two_launch_bits(T, kind):
         pytest.skip("too few SMs for the one-launch form at 16 key heads")
     t = to_dev(make_inputs(T, seed=14, norm=False))
     n_sb = (T + 2047) // 2048
-    with _env("GDN_CHUNK_SCAN", kind):
-        with _env("GDN_CHUNK_OVERLAP", "0"):
+    with gdn.options(chunk_products=kind):
+        with gdn.options(chunk_one_launch=0):
             n0 = gdn.gdn_launch_count()
             o2, s2 = _run(t, "chunked", [T])
             assert gdn.gdn_launch_count() - n0 == 2 * n_sb
@@ -170,3 +150,22 @@ def test_one_launch_chunked_under_graph_replay():
         assert gdn.gdn_device_status() == gdn.GDN_OK
         assert np.array_equal(out.cpu().numpy().view(np.uint32), o_ref.view(np.uint32)), i
         assert np.array_equal(st.cpu().numpy().view(np.uint32), s_ref.view(np.uint32)), i
+
+
+def test_chunked_reruns_at_engine_shapes_with_poisoned_scratch():
+    """Chunked mode gives the same bits on 20 reruns at each of seven token counts
+    from 130 to 8192, with the scratch filled with NaN (or -inf) before every other
+    run ("#1372 DeltaNet recurrence: STRATA_GDN_CHUNKED=1", section "Measured": the
+    pages ran 199 reruns at each of 7 engine shapes between 130 and 8192 tokens,
+    NaN-filling the scratch between runs)."""
+    x = make_inputs(8192, seed=16, norm=False)  # each shape takes a prefix of this draw
+    t_all = to_dev(x)
+    for T in (130, 257, 1000, 2047, 2049, 4099, 8192):
+        t = {k: (v[:T] if k != "S0" else v) for k, v in t_all.items()}
+        o_ref, s_ref = _run(t, "chunked", [T])
+        for i in range(20):
+            if i % 2 == 0:
+                gdn.gdn_poison_scratch(0x7FC00000 if i % 4 == 0 else 0xFF800000)
+            o, s = _run(t, "chunked", [T])
+            assert np.array_equal(o.view(np.uint32), o_ref.view(np.uint32)), (T, i)
+            assert np.array_equal(s.view(np.uint32), s_ref.view(np.uint32)), (T, i)

@@ -22,6 +22,7 @@ from linear_attention_recurrence_gb300.inputs import make_inputs
 x = make_inputs(64, seed=0, norm=False)
 t = {{k: torch.from_numpy(v).cuda() for k, v in x.items()}}
 st = t["S0"].clone()
+gdn.gdn_set_option("test_fail_scratch_alloc", 1)
 n0 = gdn.gdn_launch_count()
 try:
     gdn.gdn_recurrence(t["q"], t["k"], t["v"], t["g"], t["beta"], st, mode="chunked")
@@ -38,8 +39,9 @@ print("SEQ-OK", gdn.gdn_device_status())
 
 
 def test_simulated_scratch_allocation_failure():
-    env = dict(os.environ, GDN_SIMULATE_ALLOC_FAILURE="1")
-    r = subprocess.run([sys.executable, "-c", CHILD.format(root=ROOT)], env=env, capture_output=True, text=True,
+    """In a fresh process (so the scratch has not been allocated yet), the test
+    option makes the scratch allocation fail: GDN_ERR_ALLOC, nothing launched."""
+    r = subprocess.run([sys.executable, "-c", CHILD.format(root=ROOT)], capture_output=True, text=True,
                        timeout=300)
     assert r.returncode == 0, r.stderr
     assert f"STATUS {gdn.GDN_ERR_ALLOC} LAUNCHES 0 STATE-UNCHANGED True" in r.stdout, r.stdout
@@ -96,14 +98,11 @@ def test_bounded_flag_wait_runs_out_and_reports():
     x = make_inputs(64, seed=31, norm=False)
     t = to_dev(x)
     st = t["S0"].clone()
-    os.environ["GDN_TEST_WITHHOLD_PREP_FLAG"] = "5"  # chunk 0, key head 5
-    try:
+    with gdn.options(test_withhold_prep_task=5):  # chunk 0, key head 5
         t0 = time.time()
         gdn.gdn_recurrence(t["q"], t["k"], t["v"], t["g"], t["beta"], st, mode="chunked")
         rc = gdn.gdn_device_status()
         elapsed = time.time() - t0
-    finally:
-        del os.environ["GDN_TEST_WITHHOLD_PREP_FLAG"]
     assert rc == gdn.GDN_ERR_TIMEOUT
     msg = gdn.gdn_last_error()
     assert "prep flag 5" in msg, msg

@@ -33,16 +33,8 @@ def _built():
 
 @contextlib.contextmanager
 def _scan(kind):
-    old = os.environ.get("GDN_CHUNK_SCAN")
-    if kind:
-        os.environ["GDN_CHUNK_SCAN"] = kind
-    try:
+    with gdn.options(chunk_products=kind or "mma"):
         yield
-    finally:
-        if old is None:
-            os.environ.pop("GDN_CHUNK_SCAN", None)
-        else:
-            os.environ["GDN_CHUNK_SCAN"] = old
 
 
 def _run(t, v, s0, mode, kind):

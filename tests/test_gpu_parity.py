@@ -20,26 +20,19 @@ from linear_attention_recurrence_gb300.inputs import make_inputs
 pytestmark = pytest.mark.gpu
 
 # "chunked" runs the default scan (its products as split-TF32 warp-level MMAs),
-# "chunked:fma" the same scan with them as FP32 FMAs (GDN_CHUNK_SCAN=fma), "chunked:tc"
-# the two-launch scan with its S0 products as split-TF32 tcgen05 MMAs (GDN_CHUNK_SCAN=tc)
+# "chunked:fma" the same scan with them as FP32 FMAs (option chunk_products=fma),
+# "chunked:tc" the two-launch scan with its S0 products as split-TF32 tcgen05 MMAs
+# (chunk_products=tc)
 MODES = ("sequential", "chunked", "chunked:fma", "chunked:tc")
 NAN = float("nan")
 
 
 @contextlib.contextmanager
 def _scan_env(mode):
-    """Base mode of `mode`, with GDN_CHUNK_SCAN set to its ':' suffix meanwhile."""
+    """Base mode of `mode`, with the chunk_products option set to its ':' suffix meanwhile."""
     base, _, kind = mode.partition(":")
-    old = os.environ.get("GDN_CHUNK_SCAN")
-    if kind:
-        os.environ["GDN_CHUNK_SCAN"] = kind
-    try:
+    with gdn.options(chunk_products=kind or "mma"):
         yield base
-    finally:
-        if old is None:
-            os.environ.pop("GDN_CHUNK_SCAN", None)
-        else:
-            os.environ["GDN_CHUNK_SCAN"] = old
 
 
 @pytest.fixture(scope="module", autouse=True)

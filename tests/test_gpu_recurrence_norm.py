@@ -5,8 +5,6 @@ the bits gdn_out_norm gives for that output, whichever way the call runs the nor
 a launch after the recurrence); and the FP16 output within 1 ulp of the FP64 norm
 of the same FP32 output ("#413 prefill: DeltaNet recurrence with the three value
 heads of a key head in one thread", section "What changes")."""
-import os
-
 import numpy as np
 import pytest
 import torch
@@ -61,28 +59,19 @@ def test_recurrence_norm_matches_the_two_calls(mode, T):
     chunked = mode == "chunked" or (mode == "auto" and T >= gdn.GDN_AUTO_CHUNKED_MIN_T)
     if chunked and _one_launch_available():
         assert launches == 2 * ((T + 2047) // 2048)  # one launch and its norm per super-block
-
-
-def _with_env(name, value, fn):
-    old = os.environ.get(name)
-    os.environ[name] = value
-    try:
-        return fn()
-    finally:
-        if old is None:
-            del os.environ[name]
-        else:
-            os.environ[name] = old
+    if not chunked:
+        assert launches == 1  # the norm fused into the sequential scan
 
 
 @pytest.mark.parametrize("T", [1, 33, 130, 2048, 4099])
 def test_norm_inside_the_one_launch_same_bits(T):
-    """GDN_FUSED_NORM=1: the prep CTAs norm each (chunk, key head) once its 8 scan
-    CTAs have published it, inside the one launch; same bits as the two calls."""
+    """Option norm_in_launch=1: the prep CTAs norm each (chunk, key head) once its 8
+    scan CTAs have published it, inside the one launch; same bits as the two calls."""
     if not _one_launch_available():
         pytest.skip("too few SMs for the one-launch form")
     t = to_dev(make_inputs(T, seed=25))
-    (o1, y1, s1), (o2, y2, s2), launches = _with_env("GDN_FUSED_NORM", "1", lambda: _pair(t, T, "chunked"))
+    with gdn.options(norm_in_launch=1):
+        (o1, y1, s1), (o2, y2, s2), launches = _pair(t, T, "chunked")
     assert launches == (T + 2047) // 2048
     assert np.array_equal(_bits(o1), _bits(o2)) and np.array_equal(_bits(s1), _bits(s2))
     assert np.array_equal(_bits(y1), _bits(y2))
@@ -107,28 +96,25 @@ def test_recurrence_norm_two_launch_form_same_bits():
     st = t["S0"].clone()
     o1, y1 = gdn.gdn_recurrence_norm(t["q"], t["k"], t["v"], t["g"], t["beta"], st, t["z"], t["w"], 1e-6)
     torch.cuda.synchronize()
-    old = os.environ.get("GDN_CHUNK_OVERLAP")
-    os.environ["GDN_CHUNK_OVERLAP"] = "0"
-    try:
+    with gdn.options(chunk_one_launch=0):
         st2 = t["S0"].clone()
         n0 = gdn.gdn_launch_count()
         o2, y2 = gdn.gdn_recurrence_norm(t["q"], t["k"], t["v"], t["g"], t["beta"], st2, t["z"], t["w"], 1e-6)
         torch.cuda.synchronize()
         assert gdn.gdn_launch_count() - n0 == 3 * 3  # prep, scan, norm per super-block
-    finally:
-        if old is None:
-            del os.environ["GDN_CHUNK_OVERLAP"]
-        else:
-            os.environ["GDN_CHUNK_OVERLAP"] = old
     assert np.array_equal(_bits(o1), _bits(o2)) and np.array_equal(_bits(y1), _bits(y2))
 
 
-@pytest.mark.parametrize("fused", ["0", "1"])
-def test_recurrence_norm_graph_replay_with_poisoned_outputs(fused, monkeypatch):
+@pytest.mark.parametrize("fused", [0, 1])
+def test_recurrence_norm_graph_replay_with_poisoned_outputs(fused):
     """Captured once, replayed with out and y poisoned with NaN and the scratch
     poisoned in between: every replay gives the eager bits (the output flags
     carry the launch's generation number, so no replay norms stale rows)."""
-    monkeypatch.setenv("GDN_FUSED_NORM", fused)
+    with gdn.options(norm_in_launch=fused):
+        _graph_replay_case()
+
+
+def _graph_replay_case():
     T = 4099
     t = to_dev(make_inputs(T, seed=24))
     st = t["S0"].clone()
@@ -154,3 +140,73 @@ def test_recurrence_norm_graph_replay_with_poisoned_outputs(fused, monkeypatch):
         torch.cuda.synchronize()
         assert gdn.gdn_device_status() == gdn.GDN_OK
         assert np.array_equal(_bits(out), o_ref) and np.array_equal(_bits(y), y_ref)
+
+
+@pytest.mark.parametrize("T,splits", [(1, [1]), (17, [17]), (4099, [4099]), (4099, [1000, 3099]), (2048, [5, 2043])])
+def test_sequential_norm_fused_without_fp32_output(T, splits):
+    """Sequential mode fuses the norm into the scan (the 8 CTAs of a key head as
+    one cluster, one launch per call) and, asked not to, writes no FP32 output:
+    y and the state have the bits of gdn_recurrence followed by gdn_out_norm, also
+    when the sequence is split over calls."""
+    t = to_dev(make_inputs(T, seed=26))
+    st = t["S0"].clone()
+    y = torch.full((T, 48, 128), float("nan"), device="cuda", dtype=torch.float16)
+    a = 0
+    n0 = gdn.gdn_launch_count()
+    for n in splits:
+        b = a + n
+        out, _ = gdn.gdn_recurrence_norm(t["q"][a:b], t["k"][a:b], t["v"][a:b], t["g"][a:b], t["beta"][a:b], st,
+                                         t["z"][a:b], t["w"], 1e-6, y=y[a:b], mode="sequential", store_out=False)
+        assert out is None
+        a = b
+    assert gdn.gdn_launch_count() - n0 == len(splits)
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_status() == gdn.GDN_OK
+    st2 = t["S0"].clone()
+    out2 = gdn.gdn_recurrence(t["q"], t["k"], t["v"], t["g"], t["beta"], st2, mode="sequential")
+    y2 = gdn.gdn_out_norm(out2, t["z"], t["w"], 1e-6)
+    torch.cuda.synchronize()
+    assert np.array_equal(_bits(y), _bits(y2))
+    assert np.array_equal(_bits(st), _bits(st2))
+
+
+@pytest.mark.parametrize("n_kh,T", [(1, 50), (5, 777)])
+def test_sequential_norm_fused_other_head_counts(n_kh, T):
+    """Other cluster counts (one cluster of 8 CTAs per key head)."""
+    t = to_dev(make_inputs(T, seed=27, n_kh=n_kh, n_vh=3 * n_kh))
+    (o1, y1, s1), (o2, y2, s2), launches = _pair(t, T, "sequential")
+    assert launches == 1
+    assert np.array_equal(_bits(o1), _bits(o2)) and np.array_equal(_bits(s1), _bits(s2))
+    assert np.array_equal(_bits(y1), _bits(y2))
+
+
+def test_sequential_norm_fused_graph_replay():
+    """The fused sequential call captured once and replayed with y and out poisoned:
+    every replay gives the eager bits."""
+    T = 1000
+    t = to_dev(make_inputs(T, seed=28))
+    st = t["S0"].clone()
+    o_ref, y_ref = gdn.gdn_recurrence_norm(t["q"], t["k"], t["v"], t["g"], t["beta"], st, t["z"], t["w"], 1e-6,
+                                           mode="sequential")
+    torch.cuda.synchronize()
+    o_ref, y_ref, s_ref = _bits(o_ref), _bits(y_ref), _bits(st)
+    st = t["S0"].clone()
+    out = torch.empty((T, 48, 128), device="cuda")
+    y = torch.empty((T, 48, 128), device="cuda", dtype=torch.float16)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            gdn.gdn_recurrence_norm(t["q"], t["k"], t["v"], t["g"], t["beta"], st, t["z"], t["w"], 1e-6, out=out,
+                                    y=y, mode="sequential")
+    torch.cuda.synchronize()
+    for _ in range(3):
+        st.copy_(t["S0"])
+        out.fill_(float("nan"))
+        y.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert gdn.gdn_device_status() == gdn.GDN_OK
+        assert np.array_equal(_bits(out), o_ref) and np.array_equal(_bits(y), y_ref)
+        assert np.array_equal(_bits(st), s_ref)
