@@ -174,13 +174,15 @@ int gdn_out_norm(const float* out, const float* z, const float* w, float eps,
  * one call: out (FP32, written as by gdn_recurrence) and y_fp16 (the same bits
  * gdn_out_norm would give for that out).
  *
- * GDN_SEQUENTIAL: the norm is fused into the scan's epilogue ([P413] "What
- * changes": the FP32 output is only the norm's input): one cooperative launch
- * whose CTAs exchange each row's partial sums of squares through global memory,
- * so y comes from the outputs while they are still on chip.  There `out` may be
- * NULL: the FP32 output is then not written at all.  If the 8 n_kh CTAs cannot
- * be resident at once (n_kh > SMs / 8), the scan and the norm are two launches
- * and `out` is required.
+ * GDN_SEQUENTIAL: with `out` NULL (or the option GDN_OPT_NORM_IN_LAUNCH set to
+ * 1) the norm is fused into the scan's epilogue ([P413] "What changes": the FP32
+ * output is only the norm's input): one cooperative launch whose CTAs exchange
+ * each row's partial sums of squares through global memory, so y comes from the
+ * outputs while they are still on chip and, with `out` NULL, the FP32 output is
+ * never written.  Otherwise the scan and the norm are two launches, which on
+ * GB300 take less time (the scan is ALU-bound; the fused form saves the FP32
+ * output's HBM traffic, not time).  The fused form needs the 8 n_kh CTAs
+ * resident at once (n_kh <= SMs / 8); beyond that `out` is required.
  * GDN_CHUNKED: the norm of each 2048-token super-block is launched after its
  * recurrence.  With the option GDN_OPT_NORM_IN_LAUNCH set to 1 and the one-launch
  * chunked form, the norm instead runs inside that launch, on the SMs that
@@ -257,8 +259,11 @@ typedef enum gdn_option {
      * when the device has SMs to spare for it; 0: a prep launch, then a scan
      * launch.  Same bits either way. */
     GDN_OPT_CHUNK_ONE_LAUNCH = 2,
-    /* gdn_recurrence_norm in GDN_CHUNKED: 0 (default) launches the norm after each
-     * super-block; 1 norms on the prep SMs inside the one launch.  Same bits. */
+    /* gdn_recurrence_norm: 0 (default) launches the norm after the recurrence
+     * (after each super-block in GDN_CHUNKED; in GDN_SEQUENTIAL only when `out` is
+     * given); 1 norms inside the recurrence's launch (GDN_CHUNKED: on the prep
+     * SMs of the one-launch form; GDN_SEQUENTIAL: in the scan's epilogue).  Same
+     * bits either way. */
     GDN_OPT_NORM_IN_LAUNCH = 3,
     /* GDN_SEQUENTIAL: state rows per thread, 16 (default) or 8.  Same bits. */
     GDN_OPT_SEQ_ROWS_PER_THREAD = 4,

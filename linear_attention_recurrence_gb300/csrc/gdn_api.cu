@@ -209,11 +209,12 @@ int ensure_scratch(DeviceState* d, int n_vh) {
     return GDN_OK;
 }
 
-// gdn_recurrence_norm runs the norm inside the one-launch chunked kernel (on the
-// prep CTAs, as the scan finishes each chunk) only when GDN_OPT_NORM_IN_LAUNCH is
-// 1: on GB300 those 24 SMs cannot stream the norm's traffic as fast as the scan
-// produces it (measured 562 vs 362 us per 2048-token call), so by default the
-// norm is a launch of its own after the recurrence.
+// gdn_recurrence_norm runs the norm inside the recurrence's launch only when
+// GDN_OPT_NORM_IN_LAUNCH is 1 (or, in sequential mode, when no FP32 output is
+// wanted): in the one-launch chunked kernel the prep CTAs cannot stream the
+// norm's traffic as fast as the scan produces it (measured 562 vs 362 us per
+// 2048-token call), and the sequential scan's fused epilogue costs more than the
+// norm's own launch, so by default the norm is a launch of its own.
 bool fused_norm_enabled() { return opt(GDN_OPT_NORM_IN_LAUNCH) == 1; }
 
 // Failure-path test hook (GDN_OPT_TEST_WITHHOLD_PREP_TASK): that prep task (chunk
@@ -343,10 +344,15 @@ int run_recurrence(const float* q, const float* k, const float* v, const float* 
         p.n_kh = n_kh;
         p.n_vh = n_vh;
         p.status = dev->status;
-        // The norm fused into the scan (z loaded and y stored by TMA, one cooperative
-        // launch) when all 8 n_kh CTAs fit on the device at once; else the scan, then
-        // the norm's own launch (out is required then).
-        if (norm != nullptr && kSeqSlices * n_kh <= dev->sm_count) {
+        // The norm fused into the scan (one cooperative launch, the FP32 output only
+        // optionally stored) when the caller asks for no FP32 output or for the
+        // in-launch norm, and all 8 n_kh CTAs fit on the device at once; else the
+        // scan, then the norm's own launch (out is required then).  On GB300 the
+        // two launches are faster at every T (5.6 vs 9.6 us at T = 1, 537 vs 666 us
+        // at T = 2048): the scan is ALU-bound, so the fused form saves the output's
+        // HBM traffic but not time.
+        const bool want_fused = norm != nullptr && (out == nullptr || fused_norm_enabled());
+        if (want_fused && kSeqSlices * n_kh <= dev->sm_count) {
             if ((rc = ensure_seqnorm(dev, n_kh)) != GDN_OK) return rc;
             if ((rc = make_map(&p.tm_z, norm->z, static_cast<uint64_t>(n_vh) * d, T, seq_box_cols(), B,
                                CU_TENSOR_MAP_SWIZZLE_NONE)))

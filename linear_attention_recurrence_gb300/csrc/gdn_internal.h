@@ -39,7 +39,7 @@ struct SeqParams {
     // the group sums between the 8 CTAs of a key head, its counters, and the
     // launch generation (sync[0]) with a count of finished CTAs (sync[1])
     float* xg;
-    unsigned long long* xflags;  // [2][n_kh][8][4]: stages published, stages consumed
+    unsigned long long* xflags;  // [n_kh][8][48] stages published per row, [n_kh][8][norm warps] gathered
     uint32_t* sync;
     int64_t T;
     int n_kh;

@@ -28,7 +28,7 @@
 // block's outputs to shared memory and four more warps per CTA (one per SM
 // sub-partition, each a quarter of the block's rows) norm them: per (token,
 // head) row a norm warp publishes the sums of squares of its CTA's four 4-column
-// groups in global memory (release counter per block), gathers the other seven
+// groups in global memory (a release counter per row), gathers the other seven
 // CTAs' of the key head (acquire), adds the row's 32 group sums in the order
 // gdn_out_norm's warp does (so y has that kernel's bits), and writes y (FP16);
 // the producer loads z and stores the FP32 output by TMA, or not at all.  That form is a
@@ -57,7 +57,7 @@ constexpr int NS = 4;     // stages in the ring
 constexpr int SLICES = D / NCOL;           // CTAs (column slices) of a key head
 constexpr int ROWS = kHeadsPerKey * B;     // (head, token) rows of a stage
 constexpr int NSX = 2;                     // slots of the exchange between the CTAs of a key head
-constexpr int kNormWarps = 4;              // norm warps per CTA (one per SM sub-partition)
+constexpr int kNormWarps = 2;              // norm warps per CTA (one per SM sub-partition)
 constexpr int NROWS = ROWS / kNormWarps;   // rows of a stage each norm warp norms
 static_assert(NROWS <= 32 && NROWS * kNormWarps == ROWS, "rows per norm warp");
 
@@ -419,10 +419,10 @@ __device__ void consumer_role(const SeqParams& p, SeqSmem& sm, int kh, int c0, i
 // row m * 16 + tt).  Per stage: wait for the output tile; per row compute the sums
 // of squares of the CTA's four 4-column groups (each as gdn_out_norm's lane does
 // for its 4 columns) and publish them in global memory at [key head][slot][slice];
-// gather all eight slices' once their publication counters show the stage; add a
-// row's 32 group sums in the order of gdn_out_norm's xor tree (offsets 16, 8, 4,
-// 2, 1); form r and write y for the CTA's 16 columns with the row code's
-// expression.  The gather and the norm of a stage run one stage after its
+// gather all eight slices' once their per-row publication counters show the
+// stage; add a row's 32 group sums in the order of gdn_out_norm's xor tree
+// (offsets 16, 8, 4, 2, 1); form r and write y for the CTA's 16 columns with the
+// row code's expression.  The gather and the norm of a stage run one stage after its
 // publication, so the round trip through L2 overlaps the next stage's work.  The
 // counters hold (generation << 32 | stages), so a replayed launch never takes an
 // earlier launch's values for its own.
@@ -441,9 +441,16 @@ __device__ void norm_role(const SeqParams& p, SeqSmem& sm, int kh, int c0, int s
     const int row0 = wi * NROWS;
     const int q = lane & 3;  // 4-column group of this lane in the y phase
     const float4 wq = *reinterpret_cast<const float4*>(p.w + c0 + 4 * q);
-    // publication counters of (key head, slice, norm warp): stages published / consumed
-    unsigned long long* pub = p.xflags + static_cast<int64_t>(kh) * SLICES * kNormWarps + wi;
-    unsigned long long* con = p.xflags + static_cast<int64_t>(n_kh + kh) * SLICES * kNormWarps + wi;
+    // Counters (stages, tagged with the generation): per (key head, slice, row) the
+    // stages whose group sums of that row are published, and per (key head, slice,
+    // norm warp) the stages that warp has gathered.  A lane releases its own row's
+    // counter after storing the row's sums (release orders its own earlier store),
+    // and a lane that gathers a row acquires that row's counters itself, so no
+    // fence is needed.
+    unsigned long long* const pub = p.xflags;
+    unsigned long long* const con = p.xflags + static_cast<int64_t>(n_kh) * SLICES * ROWS;
+    auto pub_at = [&](int sl, int row) { return pub + (static_cast<int64_t>(kh) * SLICES + sl) * ROWS + row; };
+    auto con_at = [&](int sl) { return con + (static_cast<int64_t>(kh) * SLICES + sl) * kNormWarps + wi; };
     auto xslot = [&](int64_t s, int sl) {  // slice sl's group sums of this warp's rows, in the stage's slot
         return reinterpret_cast<float4*>(xg) + ((static_cast<int64_t>(kh) * NSX + s % NSX) * SLICES + sl) * ROWS + row0;
     };
@@ -471,28 +478,30 @@ __device__ void norm_role(const SeqParams& p, SeqSmem& sm, int kh, int c0, int s
                 }
                 part = make_float4(g4[0], g4[1], g4[2], g4[3]);
             }
-            // (3) the slot is free once every slice has consumed stage s - NSX: lanes 0..7 watch one slice each
-            if (s >= NSX && lane < SLICES &&
-                !wait_counter(con + lane * kNormWarps, (gen << 32) | static_cast<uint64_t>(s - NSX + 1)))
+            // (3) the slot is free once the same warp of every slice has gathered stage
+            // s - NSX: lanes 0..7 watch one slice each; the warp barrier orders the other
+            // lanes' stores after what they saw
+            if (s >= NSX && lane < SLICES && !wait_counter(con_at(lane), (gen << 32) | static_cast<uint64_t>(s - NSX + 1)))
                 ok = false;
             if (!__all_sync(0xffffffffu, ok)) break;
-            __syncwarp();  // the other lanes' stores below come after lanes 0..7 saw the counters
-            // (4) publish
-            if (lane < NROWS) xslot(s, slice)[lane] = part;
-            __threadfence();
             __syncwarp();
-            if (lane == 0)
-                st_release_gpu_u64(pub + slice * kNormWarps, (gen << 32) | static_cast<uint64_t>(s + 1));
+            // (4) publish: each lane its row's sums, then that row's counter
+            if (lane < NROWS) {
+                xslot(s, slice)[lane] = part;
+                st_release_gpu_u64(pub_at(slice, row0 + lane), (gen << 32) | static_cast<uint64_t>(s + 1));
+            }
         }
         if (s == 0) continue;
         const int64_t u = s - 1;  // the stage normed in this iteration
         const int slot = static_cast<int>(u % NS);
-        // (5) gather: every slice has published stage u
-        if (lane < SLICES && !wait_counter(pub + lane * kNormWarps, (gen << 32) | static_cast<uint64_t>(u + 1)))
-            ok = false;
+        // (5) gather: lane = row row0 + lane; acquire its 8 counters, then load
+        if (lane < NROWS) {
+            const unsigned long long want = (gen << 32) | static_cast<uint64_t>(u + 1);
+#pragma unroll 1
+            for (int sl = 0; sl < SLICES && ok; ++sl)
+                if (!wait_counter(pub_at(sl, row0 + lane), want)) ok = false;
+        }
         if (!__all_sync(0xffffffffu, ok)) break;
-        __syncwarp();  // every lane's loads below come after lanes 0..7 saw the counters
-        __threadfence();
         if (lane < NROWS) {
             float g[32];
 #pragma unroll
@@ -515,9 +524,10 @@ __device__ void norm_role(const SeqParams& p, SeqSmem& sm, int kh, int c0, int s
             const float ss = g[0] + g[1];
             nb.r[wi][lane] = rsqrtf(fmaf(ss, 1.0f / 128.0f, eps));
         }
-        // (6) this warp has read stage u's slot
+        // (6) this warp has read stage u's slot (its loads are complete: their values
+        // are in r); the warp barrier orders them before lane 0's release
         __syncwarp();
-        if (lane == 0) st_release_gpu_u64(con + slice * kNormWarps, (gen << 32) | static_cast<uint64_t>(u + 1));
+        if (lane == 0) st_release_gpu_u64(con_at(slice), (gen << 32) | static_cast<uint64_t>(u + 1));
         // (7) z landed
         if (!mbar_wait(&sm.zfull[slot], static_cast<uint32_t>((u / NS) & 1))) ok = false;
         if (!__all_sync(0xffffffffu, ok)) break;
@@ -622,7 +632,7 @@ size_t seq_norm_scratch_bytes(int n_kh) {
     return static_cast<size_t>(seq_norm_counters(n_kh)) * 8 + 16 +
            static_cast<size_t>(n_kh) * NSX * SLICES * ROWS * 16;
 }
-int seq_norm_counters(int n_kh) { return 2 * n_kh * SLICES * kNormWarps; }
+int seq_norm_counters(int n_kh) { return n_kh * SLICES * (ROWS + kNormWarps); }
 int seq_box_cols() { return NCOL; }
 
 cudaError_t launch_seq(const SeqParams& p, int rows_per_thread, cudaStream_t s) {
