@@ -88,6 +88,30 @@ def captured_traffic(source_file: str):
     return None
 
 
+def captured_counts(source_file: str):
+    """Instruction counts of one launch from profiles/flop_counts.md for the kernel
+    whose source is `source_file` (None when that file changed since the capture):
+    {"fp32_flop": FFMA x 2 + FFMA2 x 4 + FADD + FADD2 x 2 + FMUL + FMUL2 x 2 (thread
+    instructions), "tensor_flop": mma.sync m16n8k8 warp instructions x 2048}."""
+    import hashlib
+    import re
+
+    table = os.path.join(ROOT, "profiles", "flop_counts.md")
+    src = os.path.join(ROOT, "linear_attention_recurrence_gb300", "csrc", source_file)
+    if not (os.path.exists(table) and os.path.exists(src)):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    for line in open(table):
+        cells = [c.strip() for c in line.strip().strip("|").split("|")]
+        if len(cells) >= 10 and cells[1] == "csrc/" + source_file and re.fullmatch(r"[0-9a-f]{16}", cells[2]):
+            if cells[2] != sha:
+                return None
+            ffma, ffma2, fadd, fadd2, fmul, fmul2, hmma = (int(c) for c in cells[3:10])
+            return {"fp32_flop": 2 * ffma + 4 * ffma2 + fadd + 2 * fadd2 + fmul + 2 * fmul2,
+                    "tensor_flop": hmma * 2048}
+    return None
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -869,6 +893,17 @@ def main():
     # the capture in profiles/dram_traffic.md is of the default one-launch kernel
     chunk_traffic = captured_traffic("gdn_chunk.cu") if one_launch and scan_kind not in ("fma", "tc") else None
     norm_gbs = BYTES_NORM * T / (kern["norm_ms"] * 1e-3) / 1e9
+    counts = captured_counts("gdn_chunk.cu" if args.mode == "chunked" else "gdn_seq.cu")
+    if args.mode == "chunked" and not (one_launch and scan_kind == "mma"):
+        counts = None  # the capture is of the default one-launch kernel
+    counted = None
+    if counts is not None:
+        call_s = kern["rec_call_ms"] * 1e-3
+        counted = {"fp32_flop_per_call": counts["fp32_flop"], "tensor_flop_per_call": counts["tensor_flop"],
+                   "fp32_tflops": counts["fp32_flop"] / call_s / 1e12,
+                   "tensor_tflops": counts["tensor_flop"] / call_s / 1e12,
+                   "source": "ncu thread-instruction counts of one 2048-token launch (profiles/flop_counts.md) "
+                             "at this run's median call time"}
     value = main_res["ms_per_step"] * 1e3 / (T * ws)  # already the max over ranks
     line = {
         "metric": METRIC, "value": value, "unit": "µs/token/layer", "n_gpus": ws, "steps": args.steps,
@@ -887,7 +922,8 @@ def main():
                      "kernel": chunk_label if args.mode == "chunked" else "gdn_seq_kernel per 2048-token call",
                      "peak_basis": f"{sms} SMs x 128 FP32 lanes x 2 x {sm_mhz_max:.0f} MHz ({peak_src} max clock)",
                      "frac_at_observed_clock": (achieved / (sms * FP32_LANES_PER_SM * 2 * clocks["sm_mhz"] * 1e6
-                                                            / 1e12)) if clocks.get("sm_mhz") else None},
+                                                            / 1e12)) if clocks.get("sm_mhz") else None,
+                     "counted": counted},
         "norm_roofline": {"bound": "hbm", "achieved": norm_gbs, "peak": hbm_gbs, "unit": "GB/s",
                           "frac": norm_gbs / hbm_gbs, "peak_basis": f"{peak_src} copy bandwidth"},
         "modes": modes,
