@@ -53,6 +53,19 @@ def _peaks():
     return 6800.0, SM_MAX_MHZ, "fallback"
 
 
+def _tf32_peak():
+    """Dense TF32 tensor peak: the measured bf16 GEMM rate x the nominal TF32:BF16
+    ratio (1.1 : 2.25 PFLOP/s dense), with its basis."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            bf16 = float(json.load(f).get("bf16_tflops", 1900.0))
+        src = "measured"
+    else:
+        bf16, src = 1900.0, "fallback"
+    return bf16 * 1.1 / 2.25, f"{src} bf16 GEMM {bf16:.0f} TFLOP/s x 1.1/2.25 (nominal TF32:BF16 dense)"
+
+
 def aggregate(local_ms: float, tokens_per_rank: int, world_size: int, device=None):
     """Whole-job figures for `world_size` independent replicas: the slowest rank's
     time (max over ranks) and the tokens of all ranks.  Returns (max_ms,
@@ -899,9 +912,12 @@ def main():
     counted = None
     if counts is not None:
         call_s = kern["rec_call_ms"] * 1e-3
+        tf32_peak, tf32_basis = _tf32_peak()
         counted = {"fp32_flop_per_call": counts["fp32_flop"], "tensor_flop_per_call": counts["tensor_flop"],
                    "fp32_tflops": counts["fp32_flop"] / call_s / 1e12,
                    "tensor_tflops": counts["tensor_flop"] / call_s / 1e12,
+                   "tensor_frac_of_tf32_peak": counts["tensor_flop"] / call_s / 1e12 / tf32_peak,
+                   "tf32_peak_tflops": tf32_peak, "tf32_peak_basis": tf32_basis,
                    "source": "ncu thread-instruction counts of one 2048-token launch (profiles/flop_counts.md) "
                              "at this run's median call time"}
     value = main_res["ms_per_step"] * 1e3 / (T * ws)  # already the max over ranks
