@@ -548,6 +548,9 @@ def main():
                     help="skip the T=8192 (both modes) and 36-layer stack measurements")
     ap.add_argument("--chunk-products", default="mma", choices=["mma", "fma", "tc"],
                     help="how the chunked form computes its products (library option chunk_products)")
+    ap.add_argument("--norm-in-launch", action="store_true",
+                    help="with --step-api fused: the norm inside the recurrence's launch (library option "
+                         "norm_in_launch; sequential mode: the scan's fused epilogue)")
     ap.add_argument("--ref-seconds", type=float, default=10.0)
     ap.add_argument("--sweep", action="store_true",
                     help="time one call of each mode for T = 1 .. 32768 (one JSON line) instead of the step")
@@ -587,6 +590,7 @@ def main():
         dist.barrier()
     gdn.load_library()
     gdn.gdn_set_option("chunk_products", args.chunk_products)
+    gdn.gdn_set_option("norm_in_launch", 1 if args.norm_in_launch else 0)
 
     T, CT = args.tokens, args.call_tokens
     ncalls = T // CT

@@ -25,12 +25,12 @@ constexpr int kGateRows = 64;   // tokens per gate warp
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 
-// x sigmoid(x) as x times the correctly rounded reciprocal of 1 + e^-x (for
-// x -> -inf the reciprocal of +inf is 0 and the product -0).  The exponential is
-// the hardware approximation (__expf; a few ulp at these arguments): the kernel
-// is issue-bound, and the outputs stay within a few 1e-7 of the FP64 values
-// relative to their largest magnitude (the tests hold them to 2e-6).
-__device__ __forceinline__ float silu(float x) { return x * __frcp_rn(1.f + __expf(-x)); }
+// x sigmoid(x) = x / (1 + e^-x) with the hardware exponential and the fast
+// division (a few FP32 ulp each at these arguments; for x -> -inf the quotient
+// is -0): the kernel is issue-bound, and the outputs stay within a few 1e-7 of
+// the FP64 values relative to their largest magnitude (the tests hold them to
+// 2e-6).
+__device__ __forceinline__ float silu(float x) { return __fdividef(x, 1.f + __expf(-x)); }
 
 __device__ __forceinline__ float softplus(float x) { return fmaxf(x, 0.f) + log1pf(expf(-fabsf(x))); }
 
