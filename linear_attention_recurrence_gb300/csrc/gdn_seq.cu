@@ -559,7 +559,7 @@ __device__ void norm_role(const SeqParams& p, SeqSmem& sm, int kh, int c0, int s
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.normed[slot]);
     }
-    if (!ok && lane == 0) report_error(status, kDevErrFlagTimeout);
+    if (!ok && lane == 0) report_error(status, kDevErrNormTimeout);
 }
 
 template <int R, bool NORM>
