@@ -289,6 +289,17 @@ def gdn_recurrence_chunked_noalloc(q, k, v, g, beta, state, out, stream=None):
     return out
 
 
+def gdn_noalloc_setup(n_kh: int = 16, n_vh: int = 48, d: int = 128, stream=None):
+    """The non-allocating entry point's set-up on the current device (a call with
+    T = 0): the runtime loads its static scratch, status word and kernels now, so
+    a caller can do this at start-up, before it reserves its memory arena and
+    before any stream capture."""
+    nil = ctypes.c_void_p(0)
+    lib = load_library()
+    _check(lib.gdn_recurrence_chunked_noalloc(nil, nil, nil, nil, nil, nil, nil, 0, int(n_kh), int(n_vh), int(d),
+                                              _stream_ptr(stream)))
+
+
 def gdn_out_norm(out, z, w, eps: float = 1e-6, y=None, stream=None):
     """Gated RMSNorm of ``out`` ([T][n_vh][d] FP32) with gate ``z`` and weight ``w``
     ([d]) to FP16; returns ``y`` ([T][n_vh][d] float16, allocated if None)."""
