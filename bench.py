@@ -546,7 +546,7 @@ def main():
     ap.add_argument("--skip-other-mode", action="store_true")
     ap.add_argument("--skip-extra", action="store_true",
                     help="skip the T=8192 (both modes) and 36-layer stack measurements")
-    ap.add_argument("--chunk-products", default="mma", choices=["mma", "fma", "tc"],
+    ap.add_argument("--chunk-products", default="mma", choices=["mma", "fma", "tc", "tmem"],
                     help="how the chunked form computes its products (library option chunk_products)")
     ap.add_argument("--norm-in-launch", action="store_true",
                     help="with --step-api fused: the norm inside the recurrence's launch (library option "

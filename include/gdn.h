@@ -251,9 +251,13 @@ int gdn_recurrence_chunked_noalloc(const float* q, const float* k, const float* 
  */
 typedef enum gdn_option {
     /* How GDN_CHUNKED computes the chunk's products: GDN_PRODUCTS_MMA (default,
-     * split-TF32 warp-level MMAs), GDN_PRODUCTS_FMA (packed FP32 FMAs) or
+     * split-TF32 warp-level MMAs), GDN_PRODUCTS_FMA (packed FP32 FMAs),
      * GDN_PRODUCTS_TCGEN05 (the state products as split-TF32 tcgen05 MMAs; always
-     * two launches per super-block).  All meet the same 2e-6 bound. */
+     * two launches per super-block) or GDN_PRODUCTS_TMEM (one CTA per value head
+     * keeps the state in tensor memory and every product is a split-TF32 tcgen05
+     * MMA; one cooperative launch per super-block with the prep beside it, when the
+     * value heads leave at least n_kh SMs, else the GDN_PRODUCTS_MMA form; its
+     * scratch is about 152 MB for 48 value heads).  All meet the same 2e-6 bound. */
     GDN_OPT_CHUNK_PRODUCTS = 1,
     /* 1 (default): the chunk prep runs beside the scan in one cooperative launch
      * when the device has SMs to spare for it; 0: a prep launch, then a scan
@@ -277,7 +281,7 @@ typedef enum gdn_option {
     GDN_OPT_TEST_FAIL_SCRATCH_ALLOC = 102
 } gdn_option;
 
-enum { GDN_PRODUCTS_MMA = 0, GDN_PRODUCTS_FMA = 1, GDN_PRODUCTS_TCGEN05 = 2 };
+enum { GDN_PRODUCTS_MMA = 0, GDN_PRODUCTS_FMA = 1, GDN_PRODUCTS_TCGEN05 = 2, GDN_PRODUCTS_TMEM = 3 };
 
 /* Sets `option` to `value`: GDN_OK, or GDN_ERR_INVALID_ARG for an unknown option
  * or a value it does not allow (the option is then unchanged). */

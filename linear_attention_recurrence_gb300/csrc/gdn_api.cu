@@ -118,8 +118,14 @@ int device_state(DeviceState** out) {
     return GDN_OK;
 }
 
+// Chunked scratch for n_vh value heads: the prep records of one super-block, or,
+// when the tensor-memory form is selected, its tiles (the larger of the two, so a
+// fallback to the other forms finds room too).
 size_t scratch_bytes_for(int n_vh) {
-    return static_cast<size_t>(gdn::kChunksPerSuperBlock) * n_vh * gdn::kPrepRecordFloats * sizeof(float);
+    const size_t rec = static_cast<size_t>(gdn::kChunksPerSuperBlock) * n_vh * gdn::kPrepRecordFloats * sizeof(float);
+    if (gdn::chunk_scan_kind() != gdn::ScanKind::kTmem) return rec;
+    const size_t tiles = gdn::tile_scratch_floats((n_vh + gdn::kHeadsPerKey - 1) / gdn::kHeadsPerKey, n_vh) * sizeof(float);
+    return tiles > rec ? tiles : rec;
 }
 
 // The fused sequential norm's scratch for n_kh key heads (zeroed once; its counters
@@ -270,6 +276,7 @@ ScanKind chunk_scan_kind() {
     switch (opt(GDN_OPT_CHUNK_PRODUCTS)) {
         case GDN_PRODUCTS_FMA: return ScanKind::kFma;
         case GDN_PRODUCTS_TCGEN05: return ScanKind::kTcgen05;
+        case GDN_PRODUCTS_TMEM: return ScanKind::kTmem;
         default: return ScanKind::kMma;
     }
 }
@@ -410,12 +417,48 @@ int run_recurrence(const float* q, const float* k, const float* v, const float* 
     pp.n_kh = n_kh;
     pp.n_vh = n_vh;
     int n_prep = fused_chunk_launch_enabled() ? chunk_fused_prep_ctas(n_kh, dev->sm_count) : 0;
+    // The tensor-memory form: the prep and one scan CTA per value head in one
+    // cooperative launch, when the value heads leave at least n_kh SMs for the prep
+    // (else, or if fewer SMs are free than the device has, the forms below).
+    int n_prep_tm = 0;
+    ChunkTmemParams tp;
+    std::memset(&tp, 0, sizeof(tp));
+    if (chunk_scan_kind() == ScanKind::kTmem && opt(GDN_OPT_CHUNK_ONE_LAUNCH) != 0 && !(norm && fused_norm_enabled()))
+        n_prep_tm = chunk_tmem_prep_ctas(n_kh, n_vh, dev->sm_count);
+    if (n_prep_tm > 0) {
+        if ((rc = make_map(&tp.tm_v, v, static_cast<uint64_t>(n_vh) * d, T, d, kChunk, CU_TENSOR_MAP_SWIZZLE_NONE)))
+            return rc;
+        tp.state = state_inout;
+        tp.out = out;
+        tp.status = dev->status;
+        tp.flags = dev->flags;
+        tp.sync = dev->sync;
+        tp.n_prep = n_prep_tm;
+        tp.withhold_task = withheld_prep_task();
+    }
     for (int64_t t0 = 0; t0 < T; t0 += kSuperBlock) {
         const int n = static_cast<int>((T - t0) < kSuperBlock ? (T - t0) : kSuperBlock);
         pp.t_begin = t0;
         pp.n_tokens = n;
         sp.t_begin = t0;
         sp.n_tokens = n;
+        if (n_prep_tm > 0) {
+            tp.prep = pp;
+            cudaError_t e = launch_chunk_tmem(tp, s);
+            if (e == cudaSuccess) {
+                g_launches.fetch_add(1);
+                if (norm) {  // the norm of this super-block's rows after it
+                    e = launch_out_norm(out + t0 * n_vh * d, norm->z + t0 * n_vh * d, norm->w, norm->eps,
+                                        norm->y + t0 * n_vh * d, static_cast<int64_t>(n) * n_vh, dev->sm_count, s);
+                    if (e != cudaSuccess) return cuda_fail(e, "output norm launch");
+                    g_launches.fetch_add(1);
+                }
+                continue;
+            }
+            if (e != cudaErrorCooperativeLaunchTooLarge) return cuda_fail(e, "chunk prep+scan (tensor memory) launch");
+            cudaGetLastError();  // fewer SMs available than the device has: the forms below
+            n_prep_tm = 0;
+        }
         if (n_prep > 0) {
             ChunkFusedParams fp;
             fp.scan = sp;
@@ -430,7 +473,7 @@ int run_recurrence(const float* q, const float* k, const float* v, const float* 
             fp.eps = in_launch ? norm->eps : 0.f;
             fp.out_flags = dev->out_flags;
             fp.withhold_task = withheld_prep_task();
-            cudaError_t e = launch_chunk_fused(fp, chunk_scan_kind() == ScanKind::kMma, s);
+            cudaError_t e = launch_chunk_fused(fp, chunk_scan_kind() != ScanKind::kFma, s);
             if (e == cudaSuccess) {
                 g_launches.fetch_add(1);
                 if (norm && !in_launch) {  // the norm of this super-block's rows after it
@@ -684,7 +727,8 @@ int gdn_set_option(int option, int value) {
     bool ok = true;
     switch (option) {
         case GDN_OPT_CHUNK_PRODUCTS:
-            ok = value == GDN_PRODUCTS_MMA || value == GDN_PRODUCTS_FMA || value == GDN_PRODUCTS_TCGEN05;
+            ok = value == GDN_PRODUCTS_MMA || value == GDN_PRODUCTS_FMA || value == GDN_PRODUCTS_TCGEN05 ||
+                 value == GDN_PRODUCTS_TMEM;
             break;
         case GDN_OPT_CHUNK_ONE_LAUNCH:
         case GDN_OPT_NORM_IN_LAUNCH:

@@ -391,7 +391,7 @@ cudaError_t launch_chunk_scan_tc(const ChunkScanParams& p, cudaStream_t s) {
 
 cudaError_t launch_chunk_scan_default(const ChunkScanParams& p, cudaStream_t s) {
     const ScanKind k = chunk_scan_kind();
-    return k == ScanKind::kTcgen05 ? launch_chunk_scan_tc(p, s) : launch_chunk_scan(p, k == ScanKind::kMma, s);
+    return k == ScanKind::kTcgen05 ? launch_chunk_scan_tc(p, s) : launch_chunk_scan(p, k != ScanKind::kFma, s);
 }
 
 }  // namespace gdn

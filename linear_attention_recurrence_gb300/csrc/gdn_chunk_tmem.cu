@@ -1,0 +1,492 @@
+// Chunked Gated DeltaNet recurrence with the state in tensor memory (sm_103a).
+//
+// Same math as gdn_chunk.cu ("#1372 DeltaNet recurrence: STRATA_GDN_CHUNKED=1 - the
+// prompt's recurrence in 32-token chunks", section "What it does"); per value head
+// and chunk, with gamma the running gate sum inside the chunk and S0 the state
+// before it, in transposed form (value columns first):
+//     X^T   = S0^T [K; Q]^T                          128 x 64, K = 128 key dims
+//     U'^T  = V^T - X_K^T diag(e^gamma)              (epilogue)
+//     D^T   = U'^T T'^T                               128 x 32, K = 32
+//     O^T   = X_Q^T diag(e^gamma) + D^T P^T           128 x 32, K = 32 (+ epilogue)
+//     S^T   = e^gamma_last S0^T + D'^T K,  D' = diag(e^(gamma_last - gamma)) D
+//                                                     128 x 128, K = 32
+// One CTA per value head keeps S^T in tensor memory (value column j = lane j, key
+// dim i = column i) as the FP32 accumulator of the update.  Every product is a
+// tcgen05.mma with M = 128 over those lanes: its A operand (S0^T, U'^T, D^T, D'^T)
+// comes from tensor memory, its B operand ([K; Q], T', P, K^T) from shared memory,
+// where the prep's swizzled tiles land by bulk copies.  Products are split TF32:
+// x = hi + lo with hi = x rounded to TF32 and lo = x - hi, and a.b is accumulated
+// in FP32 as hi_a lo_b + lo_a hi_b + hi_a hi_b (small terms first); plain TF32
+// would miss the 2e-6 tolerance against FP64 by three orders of magnitude.  The
+// gate scalings act in the epilogues, so one key head's tiles serve its three
+// value heads unchanged.
+//
+// Warp roles (320 threads): warps 0-7 move values between tensor memory and
+// registers (warp w: lanes 32 (w % 4) .. +31, half w / 4 of each step's columns);
+// lane 0 of warp 8 issues the copies; lane 0 of warp 9 issues the MMAs.  Per chunk:
+//   epilogue: split S (hi, lo; S <- e^gamma_last S) -> MMA: X -> epilogue: U'
+//   -> MMA: D -> epilogue: D, D' -> MMA: the state update, then P D
+//   -> epilogue, during the next chunk: O -> out.
+// The CTAs before the scan CTAs run the prep of the same super-block (one task per
+// (chunk, key head), in chunk order) and publish a flag per task, as the one-launch
+// kernel of gdn_chunk.cu does; the cooperative launch keeps every CTA resident.
+#include "gdn_chunk_prep.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int TM_THREADS = 320;
+constexpr int kEpiWarps = 8;
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr uint32_t TMEM_COLS = 512;
+
+// tensor-memory columns
+constexpr uint32_t TM_S = 0;    // S^T, the update's accumulator (128 key dims)
+constexpr uint32_t TM_H = 128;  // S0^T TF32 hi; once X is done: U' hi [0,32), U' lo [32,64),
+                                // D' hi [64,96), D' lo [96,128)
+constexpr uint32_t TM_L = 256;  // S0^T TF32 lo
+constexpr uint32_t TM_X = 384;  // chunk parity p: X at TM_X + 64 p (X_K [0,32), which then takes D and
+                                // then P D; X_Q [32,64)); the other parity's 64 columns take D hi
+                                // [0,32) and D lo [32,64) once that chunk's O is out
+
+// shared memory (bytes from a 1024-aligned base)
+constexpr uint32_t OFF_KQ = 0;        // [2 buffers][hi 32 KB | lo 32 KB]: [4 key-dim blocks][64 rows][128 B]
+constexpr uint32_t OFF_KT = 131072;   // K^T hi 16 KB | lo 16 KB: [128 key dims][128 B]
+constexpr uint32_t OFF_TP = 163840;   // T' hi 4 KB | lo 4 KB: [32 rows][128 B]
+constexpr uint32_t OFF_P = 172032;    // P hi 4 KB | lo 4 KB
+constexpr uint32_t OFF_V = 180224;    // [2 buffers][32 tokens][128 columns] floats (TMA)
+constexpr uint32_t OFF_G = 212992;    // [2 buffers][e^gamma 32 | e^(gamma_last - gamma) 32] floats
+constexpr uint32_t OFF_BAR = 213504;  // mbarriers, then the tensor-memory address and the abort word
+constexpr uint32_t SCAN_SMEM = OFF_BAR + 256;
+enum {
+    B_KQ0, B_KQ1, B_TP, B_KTP, B_VG0, B_VG1,  // copies landed
+    B_MX0, B_MX1, B_MD, B_MS, B_MO, B_FIN,    // MMA groups done (tcgen05.commit)
+    B_ES, B_EU, B_ED, B_EO,                   // epilogue steps done (one arrival per epilogue warp)
+    NBAR
+};
+static_assert(NBAR * 8 + 8 <= 256, "barrier space");
+constexpr uint32_t TX_KQ = 2 * 2 * C * D * 4, TX_TP = 2 * C * C * 4, TX_KTP = 2 * D * C * 4 + 2 * C * C * 4;
+constexpr uint32_t TX_VG = C * D * 4 + 2 * C * 4;
+
+constexpr uint32_t IDESC_N32 = umma_idesc_tf32(128, 32);
+constexpr uint32_t IDESC_N64 = umma_idesc_tf32(128, 64);
+constexpr uint32_t IDESC_N128 = umma_idesc_tf32(128, 128);
+
+struct TmemShared {
+    uint64_t* bar;
+    volatile int* abort_flag;  // set once a wait gave up: every later wait returns at once
+    int* status;
+};
+
+// Waits for the phase of `bar` with the given parity.  Returns false when the
+// wait gives up (poll limit: the abort word is set and the status reported) or
+// when another role already gave up.
+__device__ __forceinline__ bool wait_ab(const TmemShared& sh, int b, uint32_t parity) {
+    for (uint32_t i = 0;; ++i) {
+        if (mbar_try_wait(&sh.bar[b], parity)) return true;
+        if ((i & 255u) == 255u) {
+            if (*sh.abort_flag) return false;
+            if (i >= kWaitPolls) {
+                *sh.abort_flag = 1;
+                report_timeout(sh.status);
+                return false;
+            }
+        }
+    }
+}
+
+// The same for a whole warp.  Every lane waits: only a thread that observes the
+// phase completing is guaranteed to see the copies' data (lanes that learnt of it
+// from another lane by a shuffle read stale shared memory on GB300).  The warp
+// agrees on the outcome, so its .sync.aligned tensor-memory accesses stay converged.
+__device__ __forceinline__ bool warp_wait_ab(const TmemShared& sh, int b, uint32_t parity) {
+    const bool ok = wait_ab(sh, b, parity);
+    return __all_sync(0xffffffffu, ok) != 0;
+}
+
+// Tell the MMA issuer that this warp's tensor-memory stores have landed.
+__device__ __forceinline__ void epi_arrive(const TmemShared& sh, int b) {
+    tmem_wait_st();
+    tc_fence_before_sync();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&sh.bar[b]);
+}
+
+__device__ __forceinline__ void split16(const float (&x)[16], float (&hi)[16], float (&lo)[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) split_f(x[i], hi[i], lo[i]);
+}
+
+// ---- the scan of value head vh ----
+__device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned char* sm, const int vh,
+                                          const uint32_t gen) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int n_kh = p.prep.n_kh, n_vh = p.prep.n_vh;
+    const int kh = vh % n_kh;
+    const int n_tokens = p.prep.n_tokens;
+    const int nch = (n_tokens + C - 1) / C;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + NBAR * 8);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + OFF_BAR + NBAR * 8 + 4);
+    const TmemShared sh{bar, abort_flag, p.status};
+
+    if (tid == 0) {
+        for (int b = 0; b < B_ES; ++b) mbar_init(&bar[b], 1);
+        for (int b = B_ES; b < NBAR; ++b) mbar_init(&bar[b], kEpiWarps);
+        *abort_flag = 0;
+        mbar_init_fence();
+    }
+    if (warp == kMmaWarp) tmem_alloc(tslot, TMEM_COLS);
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tbase = *tslot;
+
+    if (warp == kProducerWarp) {
+        // ---------------- copies ----------------
+        if (lane == 0) {
+            int armed[B_VG1 + 1];  // last chunk whose copies each load barrier was armed for (-1: none)
+#pragma unroll
+            for (int b = 0; b <= B_VG1; ++b) armed[b] = -1;
+            float* tiles = p.prep.prep;
+            for (int c = 0; c < nch && !*abort_flag; ++c) {
+                // the prep task of (c, kh) has published its tiles
+                uint32_t seen = 0;
+                if (!wait_flag(p.flags + c * n_kh + kh, gen, &seen)) {
+                    *abort_flag = 1;
+                    report_error(p.status, kDevErrFlagTimeout);
+                    p.sync[2] = static_cast<uint32_t>(c * n_kh + kh);
+                    p.sync[3] = seen;
+                    p.sync[4] = gen;
+                    break;
+                }
+                fence_proxy_async_global();
+                const float* kt = key_tiles(tiles, n_kh, c, kh);
+                const float* ht = head_tiles(tiles, n_kh, n_vh, c, vh);
+                const int s = c & 1;
+                // v and the gates of chunk c: the buffer's chunk c-2 is out (O epilogue done)
+                if (c >= 2 && !wait_ab(sh, B_EO, static_cast<uint32_t>(c & 1))) break;
+                mbar_arrive_expect_tx(&bar[B_VG0 + s], TX_VG);
+                tma_load_2d(sm + OFF_V + s * (C * D * 4), &p.tm_v, &bar[B_VG0 + s], vh * D,
+                            static_cast<int>(p.prep.t_begin + static_cast<int64_t>(c) * C));
+                bulk_load(sm + OFF_G + s * 256, ht + kTileEG, 2 * C * 4, &bar[B_VG0 + s]);
+                if (s) armed[B_VG1] = c; else armed[B_VG0] = c;
+                // [K; Q] of chunk c: the buffer's chunk c-2 has been read by its X product
+                if (c >= 2 && !wait_ab(sh, B_MX0 + s, static_cast<uint32_t>(((c - 2) >> 1) & 1))) break;
+                mbar_arrive_expect_tx(&bar[B_KQ0 + s], TX_KQ);
+                bulk_load(sm + OFF_KQ + s * 65536, kt + kTileKQH, TX_KQ, &bar[B_KQ0 + s]);
+                if (s) armed[B_KQ1] = c; else armed[B_KQ0] = c;
+                // T' of chunk c: chunk c-1's D product is done
+                if (c >= 1 && !wait_ab(sh, B_MD, static_cast<uint32_t>((c - 1) & 1))) break;
+                mbar_arrive_expect_tx(&bar[B_TP], TX_TP);
+                bulk_load(sm + OFF_TP, ht + kTileTPH, TX_TP, &bar[B_TP]);
+                armed[B_TP] = c;
+                // K^T and P of chunk c: chunk c-1's update and P D are done
+                if (c >= 1 && !wait_ab(sh, B_MO, static_cast<uint32_t>((c - 1) & 1))) break;
+                mbar_arrive_expect_tx(&bar[B_KTP], TX_KTP);
+                bulk_load(sm + OFF_KT, kt + kTileKTH, 2 * D * C * 4, &bar[B_KTP]);
+                bulk_load(sm + OFF_P, ht + kTilePH, 2 * C * C * 4, &bar[B_KTP]);
+                armed[B_KTP] = c;
+            }
+            // before the CTA ends: every copy issued has landed (bounded waits; normally
+            // these phases completed long ago and the waits return at once)
+#pragma unroll
+            for (int b = 0; b <= B_VG1; ++b) {
+                if (armed[b] < 0) continue;
+                const bool two = (b == B_KQ0 || b == B_KQ1 || b == B_VG0 || b == B_VG1);
+                mbar_wait(&bar[b], static_cast<uint32_t>((two ? armed[b] >> 1 : armed[b]) & 1));
+            }
+        }
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        // ---------------- MMAs ----------------
+        if (lane == 0) {
+            const uint64_t kq_desc = umma_desc_sw128(sm + OFF_KQ);
+            const uint64_t kt_desc = umma_desc_sw128(sm + OFF_KT);
+            const uint64_t tp_desc = umma_desc_sw128(sm + OFF_TP);
+            const uint64_t p_desc = umma_desc_sw128(sm + OFF_P);
+            // descriptor start addresses count 16-byte units: +2 per 8-float k step
+            for (int c = 0; c < nch; ++c) {
+                const uint32_t pp = static_cast<uint32_t>(c & 1);
+                const uint32_t tX = tbase + TM_X + 64 * pp, tXo = tbase + TM_X + 64 * (pp ^ 1);
+                if (!wait_ab(sh, B_ES, pp)) break;
+                if (!wait_ab(sh, B_KQ0 + (c & 1), static_cast<uint32_t>((c >> 1) & 1))) break;
+                if (c >= 1 && !wait_ab(sh, B_MO, pp ^ 1)) break;
+                tc_fence_after_sync();
+                // X = S0^T [K; Q]^T: 16 k steps of 8 key dims, N = 64 tokens (k then q)
+                const uint64_t xb = kq_desc + static_cast<uint64_t>(((c & 1) * 65536) >> 4);
+                // the cross terms of every k step first, while the accumulator is small
+                // (each tcgen05.mma adds to it with FP32 rounding), then the hi.hi terms
+#pragma unroll
+                for (int ks = 0; ks < D / 8; ++ks) {
+                    const uint64_t bh = xb + static_cast<uint64_t>((((ks >> 2) * 8192) + (ks & 3) * 32) >> 4);
+                    const uint64_t bl = bh + (32768 >> 4);
+                    umma_tf32_ts(tX, tbase + TM_H + 8 * ks, bl, IDESC_N64, ks > 0);
+                    umma_tf32_ts(tX, tbase + TM_L + 8 * ks, bh, IDESC_N64, true);
+                }
+#pragma unroll
+                for (int ks = 0; ks < D / 8; ++ks) {
+                    const uint64_t bh = xb + static_cast<uint64_t>((((ks >> 2) * 8192) + (ks & 3) * 32) >> 4);
+                    umma_tf32_ts(tX, tbase + TM_H + 8 * ks, bh, IDESC_N64, true);
+                }
+                umma_commit(&bar[B_MX0 + (c & 1)]);
+                // D^T = U'^T T'^T: K = 32 tokens, N = 32
+                if (!wait_ab(sh, B_EU, pp)) break;
+                if (!wait_ab(sh, B_TP, pp)) break;
+                tc_fence_after_sync();
+#pragma unroll
+                for (int ks = 0; ks < C / 8; ++ks) {
+                    const uint64_t bh = tp_desc + static_cast<uint64_t>((ks * 32) >> 4);
+                    const uint64_t bl = bh + (4096 >> 4);
+                    umma_tf32_ts(tX, tbase + TM_H + 8 * ks, bl, IDESC_N32, ks > 0);
+                    umma_tf32_ts(tX, tbase + TM_H + 32 + 8 * ks, bh, IDESC_N32, true);
+                }
+#pragma unroll
+                for (int ks = 0; ks < C / 8; ++ks)
+                    umma_tf32_ts(tX, tbase + TM_H + 8 * ks, tp_desc + static_cast<uint64_t>((ks * 32) >> 4), IDESC_N32,
+                                 true);
+                umma_commit(&bar[B_MD]);
+                // S^T += D'^T K (N = 128 key dims), then P D^T into X_K's columns
+                if (!wait_ab(sh, B_ED, pp)) break;
+                if (!wait_ab(sh, B_KTP, pp)) break;
+                tc_fence_after_sync();
+#pragma unroll
+                for (int ks = 0; ks < C / 8; ++ks) {
+                    const uint64_t bh = kt_desc + static_cast<uint64_t>((ks * 32) >> 4);
+                    const uint64_t bl = bh + (16384 >> 4);
+                    umma_tf32_ts(tbase + TM_S, tbase + TM_H + 64 + 8 * ks, bl, IDESC_N128, true);
+                    umma_tf32_ts(tbase + TM_S, tbase + TM_H + 96 + 8 * ks, bh, IDESC_N128, true);
+                    umma_tf32_ts(tbase + TM_S, tbase + TM_H + 64 + 8 * ks, bh, IDESC_N128, true);
+                }
+                umma_commit(&bar[B_MS]);
+#pragma unroll
+                for (int ks = 0; ks < C / 8; ++ks) {
+                    const uint64_t bh = p_desc + static_cast<uint64_t>((ks * 32) >> 4);
+                    const uint64_t bl = bh + (4096 >> 4);
+                    umma_tf32_ts(tX, tXo + 8 * ks, bl, IDESC_N32, ks > 0);
+                    umma_tf32_ts(tX, tXo + 32 + 8 * ks, bh, IDESC_N32, true);
+                }
+#pragma unroll
+                for (int ks = 0; ks < C / 8; ++ks)
+                    umma_tf32_ts(tX, tXo + 8 * ks, p_desc + static_cast<uint64_t>((ks * 32) >> 4), IDESC_N32, true);
+                umma_commit(&bar[B_MO]);
+            }
+            // every MMA issued has completed before the tensor memory is freed
+            umma_commit(&bar[B_FIN]);
+            mbar_wait(&bar[B_FIN], 0);
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue warps 0-7 ----------------
+        const int q = warp & 3, hc = warp >> 2;
+        const int j = 32 * q + lane;                        // value column = tensor-memory lane
+        const uint32_t tl = tbase + (static_cast<uint32_t>(32 * q) << 16);  // this warp's lanes
+        const float* Vb = reinterpret_cast<const float*>(sm + OFF_V);
+        const float* Gb = reinterpret_cast<const float*>(sm + OFF_G);
+        float* state = p.state + static_cast<int64_t>(vh) * D * D;
+        bool ok = true;
+
+        // split of 32 key dims (columns col .. col+31) of the state S: hi, lo for X;
+        // e^gamma_last S for the update
+        auto split_state = [&](float (&s)[32], const uint32_t col, const float el) {
+            float h[32], l[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                split_f(s[i], h[i], l[i]);
+                s[i] *= el;
+            }
+            tmem_st32(tl + TM_H + col, h);
+            tmem_st32(tl + TM_L + col, l);
+            tmem_st32(tl + TM_S + col, s);
+        };
+        // O of chunk cc (its X_Q and P D in parity cc & 1's columns) -> out
+        auto o_out = [&](int cc) {
+            const uint32_t tX = tl + TM_X + 64 * static_cast<uint32_t>(cc & 1);
+            float y[16], xq[16];
+            tmem_ld16x2(tX + 16 * hc, tX + 32 + 16 * hc, y, xq);
+            const float* eg = Gb + (cc & 1) * 64;
+            const int nt = min(C, n_tokens - cc * C);
+            float* o = p.out + ((p.prep.t_begin + static_cast<int64_t>(cc) * C) * n_vh + vh) * D + j;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int t = 16 * hc + i;
+                if (t < nt) o[static_cast<int64_t>(t) * n_vh * D] = fmaf(eg[t], xq[i], y[i]);
+            }
+        };
+
+        // the starting state, split (its gates come with chunk 0's v)
+        {
+            ok = warp_wait_ab(sh, B_VG0, 0);
+            const float el = Gb[C - 1];
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                float s[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) s[i] = state[static_cast<int64_t>(64 * hc + 32 * b + i) * D + j];
+                split_state(s, 64 * hc + 32 * b, el);
+            }
+            epi_arrive(sh, B_ES);
+        }
+        for (int c = 0; c < nch && ok; ++c) {
+            const uint32_t pp = static_cast<uint32_t>(c & 1);
+            const uint32_t tX = tl + TM_X + 64 * pp, tXo = tl + TM_X + 64 * (pp ^ 1);
+            const float* V = Vb + (c & 1) * (C * D);
+            const float* eg = Gb + (c & 1) * 64;
+            const float* er = eg + C;
+            if (c >= 1) {
+                // split of the state after chunk c-1 (needs chunk c's e^gamma_last)
+                if (!(ok = warp_wait_ab(sh, B_MS, pp ^ 1))) break;
+                if (!(ok = warp_wait_ab(sh, B_VG0 + (c & 1), static_cast<uint32_t>((c >> 1) & 1)))) break;
+                tc_fence_after_sync();
+                const float el = eg[C - 1];
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {
+                    float s[32];
+                    tmem_ld32(tl + TM_S + 64 * hc + 32 * b, s);
+                    split_state(s, 64 * hc + 32 * b, el);
+                }
+                epi_arrive(sh, B_ES);
+                // O of chunk c-1
+                if (!(ok = warp_wait_ab(sh, B_MO, pp ^ 1))) break;
+                tc_fence_after_sync();
+                o_out(c - 1);
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar[B_EO]);
+            }
+            // U' = V - e^gamma X_K (tokens 16 hc .. +15), split -> U' hi / lo
+            if (!(ok = warp_wait_ab(sh, B_MX0 + (c & 1), static_cast<uint32_t>((c >> 1) & 1)))) break;
+            tc_fence_after_sync();
+            {
+                float x[16], h[16], l[16];
+                tmem_ld16(tX + 16 * hc, x);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int t = 16 * hc + i;
+                    x[i] = fmaf(-eg[t], x[i], V[t * D + j]);
+                }
+                split16(x, h, l);
+                tmem_st16(tl + TM_H + 16 * hc, h);
+                tmem_st16(tl + TM_H + 32 + 16 * hc, l);
+            }
+            epi_arrive(sh, B_EU);
+            // D -> D hi / lo (for P D) and D' = e^(gamma_last - gamma) D -> hi / lo (for the update)
+            if (!(ok = warp_wait_ab(sh, B_MD, pp))) break;
+            tc_fence_after_sync();
+            {
+                float d[16], h[16], l[16];
+                tmem_ld16(tX + 16 * hc, d);
+                split16(d, h, l);
+                tmem_st16(tXo + 16 * hc, h);
+                tmem_st16(tXo + 32 + 16 * hc, l);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) d[i] *= er[16 * hc + i];
+                split16(d, h, l);
+                tmem_st16(tl + TM_H + 64 + 16 * hc, h);
+                tmem_st16(tl + TM_H + 96 + 16 * hc, l);
+            }
+            epi_arrive(sh, B_ED);
+        }
+        if (ok) {
+            // the state after the last chunk, then its outputs
+            ok = warp_wait_ab(sh, B_MS, static_cast<uint32_t>((nch - 1) & 1));
+            if (ok) {
+                tc_fence_after_sync();
+                float a[32], b2[32];
+                tmem_ld32(tl + TM_S + 64 * hc, a);
+                tmem_ld32(tl + TM_S + 64 * hc + 32, b2);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    state[static_cast<int64_t>(64 * hc + i) * D + j] = a[i];
+                    state[static_cast<int64_t>(64 * hc + 32 + i) * D + j] = b2[i];
+                }
+                ok = warp_wait_ab(sh, B_MO, static_cast<uint32_t>((nch - 1) & 1));
+            }
+            if (ok) {
+                tc_fence_after_sync();
+                o_out(nch - 1);
+            }
+        }
+        tc_fence_before_sync();
+    }
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after_sync();
+        tmem_dealloc(tbase, TMEM_COLS);
+    }
+}
+
+__global__ void __launch_bounds__(TM_THREADS, 1) gdn_chunk_tmem_kernel(const __grid_constant__ ChunkTmemParams p) {
+    __shared__ uint32_t s_gen;
+    const int tid = threadIdx.x;
+    if (tid == 0) s_gen = ld_acquire_gpu(p.sync) + 1u;
+    __syncthreads();
+    const uint32_t gen = s_gen;
+    const int b = static_cast<int>(blockIdx.x);
+    if (b < p.n_prep) {
+        // prep CTA: tasks (chunk, key head) = b, b + n_prep, ... on threads 0-255
+        if (tid < PREP_THREADS) {
+            PrepSmemT<2>& sm = *aligned_dynamic_smem<PrepSmemT<2>, 1024>();
+            const int n_kh = p.prep.n_kh;
+            const int tasks = ((p.prep.n_tokens + C - 1) / C) * n_kh;
+            if (b < tasks) prep_load(p.prep, sm, 0, b / n_kh, b % n_kh);
+            for (int task = b, i = 0; task < tasks; task += p.n_prep, ++i) {
+                const int next = task + p.n_prep;
+                if (next < tasks) {
+                    prep_load(p.prep, sm, (i + 1) & 1, next / n_kh, next % n_kh);
+                    cp_async_wait<1>();
+                } else {
+                    cp_async_wait<0>();
+                }
+                PrepSyncNamed::sync();
+                prep_task<PrepOut::kTiles, PrepSyncNamed>(p.prep, sm, i & 1, task / n_kh, task % n_kh);
+                fence_proxy_async_global();
+                PrepSyncNamed::sync();
+                if (tid == 0 && task != p.withhold_task) st_release_gpu(p.flags + task, gen);
+            }
+        }
+    } else {
+        tmem_scan(p, aligned_dynamic_smem<unsigned char, 1024>(), b - p.n_prep, gen);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();
+        if (atomicAdd(p.sync + 1, 1u) == gridDim.x - 1) {
+            p.sync[1] = 0u;
+            st_release_gpu(p.sync, gen);
+        }
+    }
+}
+
+constexpr size_t kTmemSmem =
+    (SCAN_SMEM > sizeof(PrepSmemT<2>) ? SCAN_SMEM : sizeof(PrepSmemT<2>)) + 1024;
+static_assert(kTmemSmem <= 227 * 1024, "tensor-memory kernel shared memory");
+
+}  // namespace
+
+int chunk_tmem_prep_ctas(int n_kh, int n_vh, int sm_count) {
+    const int n_prep = sm_count - n_vh;
+    return n_prep >= n_kh ? n_prep : 0;
+}
+
+cudaError_t preload_chunk_tmem() {
+    return set_smem_once(reinterpret_cast<const void*>(gdn_chunk_tmem_kernel), static_cast<int>(kTmemSmem));
+}
+
+cudaError_t launch_chunk_tmem(const ChunkTmemParams& p, cudaStream_t s) {
+    cudaError_t e = preload_chunk_tmem();
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.n_prep + p.prep.n_vh);
+    cfg.blockDim = dim3(TM_THREADS);
+    cfg.dynamicSmemBytes = kTmemSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gdn_chunk_tmem_kernel, p);
+}
+
+}  // namespace gdn

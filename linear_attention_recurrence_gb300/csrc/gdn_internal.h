@@ -21,6 +21,33 @@ constexpr int kRecPT = kChunk * kChunk;              // P^T  [s][t]
 constexpr int kRecEG = 2 * kChunk * kChunk;          // e^gamma_t
 constexpr int kRecER = 2 * kChunk * kChunk + kChunk;  // e^(gamma_last - gamma_t)
 
+// Tiles of the tensor-memory scan (gdn_chunk_tmem.cu), written by its prep and
+// read by bulk copies into shared memory, where the MMA descriptors read them as
+// K-major operands: every 32-float row is 128-byte swizzled (16-byte chunk index
+// XOR row % 8), so a tile copied to a 1024-byte-aligned address is in the layout
+// the descriptors expect.  Each FP32 value is stored as TF32 hi and lo (x = hi + lo).
+// Per (chunk, key head), kKeyTileFloats floats:
+//   [K; Q] hi, lo: [4 blocks of 32 key dims][64 rows: k tokens 0-31, q tokens 0-31][32]
+//   K^T hi, lo:    [128 key dims][32 tokens]
+constexpr int kTileKQH = 0, kTileKQL = 8192, kTileKTH = 16384, kTileKTL = 20480, kKeyTileFloats = 24576;
+// Per (chunk, value head), kHeadTileFloats floats: T' hi, lo and P hi, lo, each
+// [32 rows t][32 columns s], then e^gamma_t [32] and e^(gamma_last - gamma_t) [32].
+constexpr int kTileTPH = 0, kTileTPL = 1024, kTilePH = 2048, kTilePL = 3072, kTileEG = 4096, kTileER = 4128;
+constexpr int kHeadTileFloats = 4160;
+// One super-block's tiles: key tiles [kChunksPerSuperBlock][n_kh], then head tiles
+// [kChunksPerSuperBlock][n_vh].
+inline size_t tile_scratch_floats(int n_kh, int n_vh) {
+    return static_cast<size_t>(kChunksPerSuperBlock) *
+           (static_cast<size_t>(n_kh) * kKeyTileFloats + static_cast<size_t>(n_vh) * kHeadTileFloats);
+}
+__host__ __device__ inline float* key_tiles(float* base, int n_kh, int ci, int kh) {
+    return base + (static_cast<int64_t>(ci) * n_kh + kh) * kKeyTileFloats;
+}
+__host__ __device__ inline float* head_tiles(float* base, int n_kh, int n_vh, int ci, int vh) {
+    return base + static_cast<int64_t>(kChunksPerSuperBlock) * n_kh * kKeyTileFloats +
+           (static_cast<int64_t>(ci) * n_vh + vh) * kHeadTileFloats;
+}
+
 // ---- sequential scan ----
 struct SeqParams {
     CUtensorMap tm_k;  // k viewed as [T][n_kh*128] FP32, box {128, B}
@@ -155,6 +182,29 @@ constexpr int kSyncWords = 8;  // words of ChunkFusedParams::sync
 // tensor-core MMAs; else as packed FP32 FMAs.  Both meet the same tolerance.
 cudaError_t launch_chunk_fused(const ChunkFusedParams& p, bool mma, cudaStream_t s);
 cudaError_t launch_chunk_scan(const ChunkScanParams& p, bool mma, cudaStream_t s);
+// Prep and the tensor-memory scan of one super-block in one cooperative launch
+// (gdn_chunk_tmem.cu): CTAs 0..n_prep-1 run the prep tasks, writing tiles
+// (kKeyTileFloats / kHeadTileFloats above) into prep.prep; the next n_vh CTAs scan,
+// one per value head.
+struct ChunkTmemParams {
+    ChunkPrepParams prep;  // the prep's inputs, super-block and head counts; prep.prep: the tiles
+    CUtensorMap tm_v;      // v viewed as [T][n_vh*128], box {128, 32}, no swizzle
+    float* state;
+    float* out;
+    int* status;
+    uint32_t* flags;       // as ChunkFusedParams::flags
+    uint32_t* sync;        // as ChunkFusedParams::sync
+    int n_prep;
+    int withhold_task;     // failure-path test: this prep task's flag is never published (-1: none)
+};
+// Prep CTAs of the tensor-memory form on a device with sm_count SMs (one CTA per
+// SM: the scan CTAs hold all 512 tensor-memory columns), or 0 when fewer than
+// n_kh SMs would be left for the prep.
+int chunk_tmem_prep_ctas(int n_kh, int n_vh, int sm_count);
+// Fails (cudaErrorCooperativeLaunchTooLarge) when the grid cannot be resident at once.
+cudaError_t launch_chunk_tmem(const ChunkTmemParams& p, cudaStream_t s);
+// Make the runtime load the tensor-memory kernel on the current device now.
+cudaError_t preload_chunk_tmem();
 // The same scan with the large products as split-TF32 tcgen05 MMAs (accumulators
 // in tensor memory); same parameters and results within tolerance.
 cudaError_t launch_chunk_scan_tc(const ChunkScanParams& p, cudaStream_t s);
@@ -163,7 +213,7 @@ cudaError_t launch_chunk_scan_tc(const ChunkScanParams& p, cudaStream_t s);
 // GDN_PRODUCTS_TCGEN05 the tcgen05 scan (two launches only: at 48 columns per CTA
 // each tcgen05.mma costs a near-fixed ~80 cycles), else the warp-level MMA scan.
 // Implemented in gdn_api.cu.
-enum class ScanKind { kFma, kMma, kTcgen05 };
+enum class ScanKind { kFma, kMma, kTcgen05, kTmem };
 ScanKind chunk_scan_kind();
 // The two-launch scan of the selected kind.
 cudaError_t launch_chunk_scan_default(const ChunkScanParams& p, cudaStream_t s);

@@ -39,12 +39,13 @@ GDN_OPT_TEST_FAIL_SCRATCH_ALLOC = 102
 GDN_PRODUCTS_MMA = 0
 GDN_PRODUCTS_FMA = 1
 GDN_PRODUCTS_TCGEN05 = 2
+GDN_PRODUCTS_TMEM = 3
 _OPTIONS = {"chunk_products": GDN_OPT_CHUNK_PRODUCTS, "chunk_one_launch": GDN_OPT_CHUNK_ONE_LAUNCH,
             "norm_in_launch": GDN_OPT_NORM_IN_LAUNCH, "seq_rows_per_thread": GDN_OPT_SEQ_ROWS_PER_THREAD,
             "test_withhold_prep_task": GDN_OPT_TEST_WITHHOLD_PREP_TASK,
             "test_fail_scratch_alloc": GDN_OPT_TEST_FAIL_SCRATCH_ALLOC}
 _PRODUCTS = {"mma": GDN_PRODUCTS_MMA, "fma": GDN_PRODUCTS_FMA, "tc": GDN_PRODUCTS_TCGEN05,
-             "tcgen05": GDN_PRODUCTS_TCGEN05}
+             "tcgen05": GDN_PRODUCTS_TCGEN05, "tmem": GDN_PRODUCTS_TMEM}
 
 _MODES = {"sequential": GDN_SEQUENTIAL, "seq": GDN_SEQUENTIAL, "chunked": GDN_CHUNKED, "auto": GDN_AUTO,
           GDN_SEQUENTIAL: GDN_SEQUENTIAL, GDN_CHUNKED: GDN_CHUNKED, GDN_AUTO: GDN_AUTO}

@@ -19,11 +19,12 @@ from linear_attention_recurrence_gb300.inputs import make_inputs
 
 pytestmark = pytest.mark.gpu
 
-# "chunked" runs the default scan (its products as split-TF32 warp-level MMAs),
-# "chunked:fma" the same scan with them as FP32 FMAs (option chunk_products=fma),
-# "chunked:tc" the two-launch scan with its S0 products as split-TF32 tcgen05 MMAs
-# (chunk_products=tc)
-MODES = ("sequential", "chunked", "chunked:fma", "chunked:tc")
+# "chunked" runs the default scan, "chunked:mma" the scan with its products as
+# split-TF32 warp-level MMAs (option chunk_products=mma), "chunked:fma" the same scan
+# with them as FP32 FMAs, "chunked:tc" the two-launch scan with its S0 products as
+# split-TF32 tcgen05 MMAs, "chunked:tmem" the scan with the state in tensor memory
+# and every product a split-TF32 tcgen05 MMA
+MODES = ("sequential", "chunked", "chunked:mma", "chunked:fma", "chunked:tc", "chunked:tmem")
 NAN = float("nan")
 
 
@@ -31,7 +32,10 @@ NAN = float("nan")
 def _scan_env(mode):
     """Base mode of `mode`, with the chunk_products option set to its ':' suffix meanwhile."""
     base, _, kind = mode.partition(":")
-    with gdn.options(chunk_products=kind or "mma"):
+    if not kind:
+        yield base
+        return
+    with gdn.options(chunk_products=kind):
         yield base
 
 
