@@ -42,18 +42,19 @@ constexpr uint32_t TMEM_COLS = 512;
 
 // tensor-memory columns
 constexpr uint32_t TM_S = 0;    // S^T, the update's accumulator (128 key dims)
-constexpr uint32_t TM_H = 128;  // S0^T TF32 hi; once X is done: U' hi [0,32), U' lo [32,64),
-                                // D' hi [64,96), D' lo [96,128)
+constexpr uint32_t TM_H = 128;  // S0^T TF32 hi; once X is done: U' hi [0,32), U' lo [32,64); the D product
+                                // [64,128) (hi.hi [64,96), cross terms [96,128)), then D' hi [64,96), lo [96,128)
 constexpr uint32_t TM_L = 256;  // S0^T TF32 lo
-constexpr uint32_t TM_X = 384;  // chunk parity p: X at TM_X + 64 p (X_K [0,32), which then takes D and
-                                // then P D; X_Q [32,64)); the other parity's 64 columns take D hi
-                                // [0,32) and D lo [32,64) once that chunk's O is out
+constexpr uint32_t TM_X = 384;  // chunk parity p: 64 columns at TM_X + 64 p: X_K [0,32), X_Q [32,64); then
+                                // e^gamma X_Q [0,32) and zeros [32,64), on which P D accumulates (hi.hi terms
+                                // onto the first half, cross terms onto the second); the other parity's 64
+                                // columns take D hi [0,32), D lo [32,64) once that chunk's O is out
 
 // shared memory (bytes from a 1024-aligned base)
 constexpr uint32_t OFF_KQ = 0;        // [2 buffers][hi 32 KB | lo 32 KB]: [4 key-dim blocks][64 rows][128 B]
 constexpr uint32_t OFF_KT = 131072;   // K^T hi 16 KB | lo 16 KB: [128 key dims][128 B]
-constexpr uint32_t OFF_TP = 163840;   // T' hi 4 KB | lo 4 KB: [32 rows][128 B]
-constexpr uint32_t OFF_P = 172032;    // P hi 4 KB | lo 4 KB
+constexpr uint32_t OFF_TP = 163840;   // T' hi 4 KB | lo 4 KB: [32 rows][128 B] (one 64-row operand [hi; lo])
+constexpr uint32_t OFF_P = 172032;    // P hi 4 KB | lo 4 KB, the same
 constexpr uint32_t OFF_V = 180224;    // [2 buffers][32 tokens][128 columns] floats (TMA)
 constexpr uint32_t OFF_G = 212992;    // [2 buffers][e^gamma 32 | e^(gamma_last - gamma) 32] floats
 constexpr uint32_t OFF_BAR = 213504;  // mbarriers, then the tensor-memory address and the abort word
@@ -61,7 +62,7 @@ constexpr uint32_t SCAN_SMEM = OFF_BAR + 256;
 enum {
     B_KQ0, B_KQ1, B_TP, B_KTP, B_VG0, B_VG1,  // copies landed
     B_MX0, B_MX1, B_MD, B_MS, B_MO, B_FIN,    // MMA groups done (tcgen05.commit)
-    B_ES, B_EU, B_ED, B_EO,                   // epilogue steps done (one arrival per epilogue warp)
+    B_ESA, B_ESB, B_EU, B_ED, B_EO,           // epilogue steps done (one arrival per epilogue warp)
     NBAR
 };
 static_assert(NBAR * 8 + 8 <= 256, "barrier space");
@@ -112,9 +113,18 @@ __device__ __forceinline__ void epi_arrive(const TmemShared& sh, int b) {
     if ((threadIdx.x & 31) == 0) mbar_arrive(&sh.bar[b]);
 }
 
+// TF32 hi (to nearest, ties away: integer operations on the bits) and lo = x - hi
+// (exact; one packed FMA per pair).
+__device__ __forceinline__ void split_pair(const float x0, const float x1, float& h0, float& h1, float& l0, float& l1) {
+    h0 = __uint_as_float((__float_as_uint(x0) + 0x1000u) & 0xFFFFE000u);
+    h1 = __uint_as_float((__float_as_uint(x1) + 0x1000u) & 0xFFFFE000u);
+    const float2 l = ffma2(make_float2(h0, h1), make_float2(-1.f, -1.f), make_float2(x0, x1));
+    l0 = l.x;
+    l1 = l.y;
+}
 __device__ __forceinline__ void split16(const float (&x)[16], float (&hi)[16], float (&lo)[16]) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) split_f(x[i], hi[i], lo[i]);
+    for (int i = 0; i < 16; i += 2) split_pair(x[i], x[i + 1], hi[i], hi[i + 1], lo[i], lo[i + 1]);
 }
 
 // ---- the scan of value head vh ----
@@ -131,8 +141,8 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
     const TmemShared sh{bar, abort_flag, p.status};
 
     if (tid == 0) {
-        for (int b = 0; b < B_ES; ++b) mbar_init(&bar[b], 1);
-        for (int b = B_ES; b < NBAR; ++b) mbar_init(&bar[b], kEpiWarps);
+        for (int b = 0; b < B_ESA; ++b) mbar_init(&bar[b], 1);
+        for (int b = B_ESA; b < NBAR; ++b) mbar_init(&bar[b], kEpiWarps);
         *abort_flag = 0;
         mbar_init_fence();
     }
@@ -164,7 +174,8 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
                 const float* kt = key_tiles(tiles, n_kh, c, kh);
                 const float* ht = head_tiles(tiles, n_kh, n_vh, c, vh);
                 const int s = c & 1;
-                // v and the gates of chunk c: the buffer's chunk c-2 is out (O epilogue done)
+                // v and the gates of chunk c: the buffer's chunk c-2 is out (its O epilogue,
+                // which follows its last use of them, is done)
                 if (c >= 2 && !wait_ab(sh, B_EO, static_cast<uint32_t>(c & 1))) break;
                 mbar_arrive_expect_tx(&bar[B_VG0 + s], TX_VG);
                 tma_load_2d(sm + OFF_V + s * (C * D * 4), &p.tm_v, &bar[B_VG0 + s], vh * D,
@@ -209,19 +220,31 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
             for (int c = 0; c < nch; ++c) {
                 const uint32_t pp = static_cast<uint32_t>(c & 1);
                 const uint32_t tX = tbase + TM_X + 64 * pp, tXo = tbase + TM_X + 64 * (pp ^ 1);
-                if (!wait_ab(sh, B_ES, pp)) break;
+                const uint64_t xb = kq_desc + static_cast<uint64_t>(((c & 1) * 65536) >> 4);
                 if (!wait_ab(sh, B_KQ0 + (c & 1), static_cast<uint32_t>((c >> 1) & 1))) break;
                 if (c >= 1 && !wait_ab(sh, B_MO, pp ^ 1)) break;
+                // X = S0^T [K; Q]^T, N = 64 tokens (k then q), 16 k steps of 8 key dims: the
+                // cross terms of every k step first, while the accumulator is small (each
+                // tcgen05.mma adds to it with FP32 rounding), then the hi.hi terms.  The
+                // state's split lands in two halves (key dims 0-31 and 64-95 first).
+                if (!wait_ab(sh, B_ESA, pp)) break;
                 tc_fence_after_sync();
-                // X = S0^T [K; Q]^T: 16 k steps of 8 key dims, N = 64 tokens (k then q)
-                const uint64_t xb = kq_desc + static_cast<uint64_t>(((c & 1) * 65536) >> 4);
-                // the cross terms of every k step first, while the accumulator is small
-                // (each tcgen05.mma adds to it with FP32 rounding), then the hi.hi terms
 #pragma unroll
-                for (int ks = 0; ks < D / 8; ++ks) {
+                for (int i = 0; i < 8; ++i) {
+                    const int ks = (i & 3) + 8 * (i >> 2);  // 0-3, 8-11
                     const uint64_t bh = xb + static_cast<uint64_t>((((ks >> 2) * 8192) + (ks & 3) * 32) >> 4);
                     const uint64_t bl = bh + (32768 >> 4);
-                    umma_tf32_ts(tX, tbase + TM_H + 8 * ks, bl, IDESC_N64, ks > 0);
+                    umma_tf32_ts(tX, tbase + TM_H + 8 * ks, bl, IDESC_N64, i > 0);
+                    umma_tf32_ts(tX, tbase + TM_L + 8 * ks, bh, IDESC_N64, true);
+                }
+                if (!wait_ab(sh, B_ESB, pp)) break;
+                tc_fence_after_sync();
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int ks = 4 + (i & 3) + 8 * (i >> 2);  // 4-7, 12-15
+                    const uint64_t bh = xb + static_cast<uint64_t>((((ks >> 2) * 8192) + (ks & 3) * 32) >> 4);
+                    const uint64_t bl = bh + (32768 >> 4);
+                    umma_tf32_ts(tX, tbase + TM_H + 8 * ks, bl, IDESC_N64, true);
                     umma_tf32_ts(tX, tbase + TM_L + 8 * ks, bh, IDESC_N64, true);
                 }
 #pragma unroll
@@ -230,23 +253,19 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
                     umma_tf32_ts(tX, tbase + TM_H + 8 * ks, bh, IDESC_N64, true);
                 }
                 umma_commit(&bar[B_MX0 + (c & 1)]);
-                // D^T = U'^T T'^T: K = 32 tokens, N = 32
+                // D^T = U'^T T'^T (K = 32 tokens): per k step U' hi . [T' hi; T' lo] (N = 64: hi.hi
+                // terms to columns 64-95 of H, hi.lo to 96-127) and U' lo . T' hi (N = 32, to 96-127)
                 if (!wait_ab(sh, B_EU, pp)) break;
                 if (!wait_ab(sh, B_TP, pp)) break;
                 tc_fence_after_sync();
 #pragma unroll
                 for (int ks = 0; ks < C / 8; ++ks) {
-                    const uint64_t bh = tp_desc + static_cast<uint64_t>((ks * 32) >> 4);
-                    const uint64_t bl = bh + (4096 >> 4);
-                    umma_tf32_ts(tX, tbase + TM_H + 8 * ks, bl, IDESC_N32, ks > 0);
-                    umma_tf32_ts(tX, tbase + TM_H + 32 + 8 * ks, bh, IDESC_N32, true);
+                    const uint64_t b = tp_desc + static_cast<uint64_t>((ks * 32) >> 4);
+                    umma_tf32_ts(tbase + TM_H + 64, tbase + TM_H + 8 * ks, b, IDESC_N64, ks > 0);
+                    umma_tf32_ts(tbase + TM_H + 96, tbase + TM_H + 32 + 8 * ks, b, IDESC_N32, true);
                 }
-#pragma unroll
-                for (int ks = 0; ks < C / 8; ++ks)
-                    umma_tf32_ts(tX, tbase + TM_H + 8 * ks, tp_desc + static_cast<uint64_t>((ks * 32) >> 4), IDESC_N32,
-                                 true);
                 umma_commit(&bar[B_MD]);
-                // S^T += D'^T K (N = 128 key dims), then P D^T into X_K's columns
+                // S^T += D'^T K (N = 128 key dims, cross terms first), then P D^T onto e^gamma X_Q
                 if (!wait_ab(sh, B_ED, pp)) break;
                 if (!wait_ab(sh, B_KTP, pp)) break;
                 tc_fence_after_sync();
@@ -256,19 +275,18 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
                     const uint64_t bl = bh + (16384 >> 4);
                     umma_tf32_ts(tbase + TM_S, tbase + TM_H + 64 + 8 * ks, bl, IDESC_N128, true);
                     umma_tf32_ts(tbase + TM_S, tbase + TM_H + 96 + 8 * ks, bh, IDESC_N128, true);
-                    umma_tf32_ts(tbase + TM_S, tbase + TM_H + 64 + 8 * ks, bh, IDESC_N128, true);
-                }
-                umma_commit(&bar[B_MS]);
-#pragma unroll
-                for (int ks = 0; ks < C / 8; ++ks) {
-                    const uint64_t bh = p_desc + static_cast<uint64_t>((ks * 32) >> 4);
-                    const uint64_t bl = bh + (4096 >> 4);
-                    umma_tf32_ts(tX, tXo + 8 * ks, bl, IDESC_N32, ks > 0);
-                    umma_tf32_ts(tX, tXo + 32 + 8 * ks, bh, IDESC_N32, true);
                 }
 #pragma unroll
                 for (int ks = 0; ks < C / 8; ++ks)
-                    umma_tf32_ts(tX, tXo + 8 * ks, p_desc + static_cast<uint64_t>((ks * 32) >> 4), IDESC_N32, true);
+                    umma_tf32_ts(tbase + TM_S, tbase + TM_H + 64 + 8 * ks, kt_desc + static_cast<uint64_t>((ks * 32) >> 4),
+                                 IDESC_N128, true);
+                umma_commit(&bar[B_MS]);
+#pragma unroll
+                for (int ks = 0; ks < C / 8; ++ks) {
+                    const uint64_t b = p_desc + static_cast<uint64_t>((ks * 32) >> 4);
+                    umma_tf32_ts(tX, tXo + 8 * ks, b, IDESC_N64, true);
+                    umma_tf32_ts(tX + 32, tXo + 32 + 8 * ks, b, IDESC_N32, true);
+                }
                 umma_commit(&bar[B_MO]);
             }
             // every MMA issued has completed before the tensor memory is freed
@@ -286,31 +304,31 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
         float* state = p.state + static_cast<int64_t>(vh) * D * D;
         bool ok = true;
 
-        // split of 32 key dims (columns col .. col+31) of the state S: hi, lo for X;
-        // e^gamma_last S for the update
+        // split of key dims col .. col+31 of the state S: hi, lo for X; e^gamma_last S for the update
         auto split_state = [&](float (&s)[32], const uint32_t col, const float el) {
             float h[32], l[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                split_f(s[i], h[i], l[i]);
-                s[i] *= el;
+            for (int i = 0; i < 32; i += 2) {
+                split_pair(s[i], s[i + 1], h[i], h[i + 1], l[i], l[i + 1]);
+                const float2 e = fmul2(make_float2(s[i], s[i + 1]), make_float2(el, el));
+                s[i] = e.x;
+                s[i + 1] = e.y;
             }
             tmem_st32(tl + TM_H + col, h);
             tmem_st32(tl + TM_L + col, l);
             tmem_st32(tl + TM_S + col, s);
         };
-        // O of chunk cc (its X_Q and P D in parity cc & 1's columns) -> out
+        // O of chunk cc (e^gamma X_Q + P D: its two accumulators) -> out
         auto o_out = [&](int cc) {
             const uint32_t tX = tl + TM_X + 64 * static_cast<uint32_t>(cc & 1);
-            float y[16], xq[16];
-            tmem_ld16x2(tX + 16 * hc, tX + 32 + 16 * hc, y, xq);
-            const float* eg = Gb + (cc & 1) * 64;
+            float a[16], b2[16];
+            tmem_ld16x2(tX + 16 * hc, tX + 32 + 16 * hc, a, b2);
             const int nt = min(C, n_tokens - cc * C);
             float* o = p.out + ((p.prep.t_begin + static_cast<int64_t>(cc) * C) * n_vh + vh) * D + j;
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const int t = 16 * hc + i;
-                if (t < nt) o[static_cast<int64_t>(t) * n_vh * D] = fmaf(eg[t], xq[i], y[i]);
+                if (t < nt) o[static_cast<int64_t>(t) * n_vh * D] = a[i] + b2[i];
             }
         };
 
@@ -324,8 +342,8 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
 #pragma unroll
                 for (int i = 0; i < 32; ++i) s[i] = state[static_cast<int64_t>(64 * hc + 32 * b + i) * D + j];
                 split_state(s, 64 * hc + 32 * b, el);
+                epi_arrive(sh, b ? B_ESB : B_ESA);
             }
-            epi_arrive(sh, B_ES);
         }
         for (int c = 0; c < nch && ok; ++c) {
             const uint32_t pp = static_cast<uint32_t>(c & 1);
@@ -334,18 +352,18 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
             const float* eg = Gb + (c & 1) * 64;
             const float* er = eg + C;
             if (c >= 1) {
-                // split of the state after chunk c-1 (needs chunk c's e^gamma_last)
-                if (!(ok = warp_wait_ab(sh, B_MS, pp ^ 1))) break;
+                // split of the state after chunk c-1 (with chunk c's e^gamma_last)
                 if (!(ok = warp_wait_ab(sh, B_VG0 + (c & 1), static_cast<uint32_t>((c >> 1) & 1)))) break;
-                tc_fence_after_sync();
                 const float el = eg[C - 1];
+                if (!(ok = warp_wait_ab(sh, B_MS, pp ^ 1))) break;
+                tc_fence_after_sync();
 #pragma unroll
                 for (int b = 0; b < 2; ++b) {
                     float s[32];
                     tmem_ld32(tl + TM_S + 64 * hc + 32 * b, s);
                     split_state(s, 64 * hc + 32 * b, el);
+                    epi_arrive(sh, b ? B_ESB : B_ESA);
                 }
-                epi_arrive(sh, B_ES);
                 // O of chunk c-1
                 if (!(ok = warp_wait_ab(sh, B_MO, pp ^ 1))) break;
                 tc_fence_after_sync();
@@ -354,33 +372,58 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar[B_EO]);
             }
-            // U' = V - e^gamma X_K (tokens 16 hc .. +15), split -> U' hi / lo
+            // U' = V - e^gamma X_K (tokens 16 hc .. +15), split -> U' hi / lo; e^gamma X_Q and
+            // zeros, the start of O's two accumulators, in X's place
+            float vv[16], ev[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                vv[i] = V[(16 * hc + i) * D + j];
+                ev[i] = eg[16 * hc + i];
+            }
             if (!(ok = warp_wait_ab(sh, B_MX0 + (c & 1), static_cast<uint32_t>((c >> 1) & 1)))) break;
             tc_fence_after_sync();
             {
-                float x[16], h[16], l[16];
-                tmem_ld16(tX + 16 * hc, x);
+                float xk[16], xq[16], h[16], l[16];
+                tmem_ld16x2(tX + 16 * hc, tX + 32 + 16 * hc, xk, xq);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int t = 16 * hc + i;
-                    x[i] = fmaf(-eg[t], x[i], V[t * D + j]);
+                for (int i = 0; i < 16; i += 2) {
+                    const float2 u = ffma2(make_float2(-ev[i], -ev[i + 1]), make_float2(xk[i], xk[i + 1]),
+                                           make_float2(vv[i], vv[i + 1]));
+                    xk[i] = u.x;
+                    xk[i + 1] = u.y;
+                    const float2 o = fmul2(make_float2(ev[i], ev[i + 1]), make_float2(xq[i], xq[i + 1]));
+                    xq[i] = o.x;
+                    xq[i + 1] = o.y;
                 }
-                split16(x, h, l);
+                split16(xk, h, l);
                 tmem_st16(tl + TM_H + 16 * hc, h);
                 tmem_st16(tl + TM_H + 32 + 16 * hc, l);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) l[i] = 0.f;
+                tmem_st16(tX + 16 * hc, xq);
+                tmem_st16(tX + 32 + 16 * hc, l);
             }
             epi_arrive(sh, B_EU);
-            // D -> D hi / lo (for P D) and D' = e^(gamma_last - gamma) D -> hi / lo (for the update)
+            // D (its two accumulators) -> D hi / lo (for P D), D' = e^(gamma_last - gamma) D -> hi / lo
+            float rv[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) rv[i] = er[16 * hc + i];
             if (!(ok = warp_wait_ab(sh, B_MD, pp))) break;
             tc_fence_after_sync();
             {
-                float d[16], h[16], l[16];
-                tmem_ld16(tX + 16 * hc, d);
+                float d[16], x[16], h[16], l[16];
+                tmem_ld16x2(tl + TM_H + 64 + 16 * hc, tl + TM_H + 96 + 16 * hc, d, x);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) d[i] += x[i];
                 split16(d, h, l);
                 tmem_st16(tXo + 16 * hc, h);
                 tmem_st16(tXo + 32 + 16 * hc, l);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) d[i] *= er[16 * hc + i];
+                for (int i = 0; i < 16; i += 2) {
+                    const float2 e = fmul2(make_float2(d[i], d[i + 1]), make_float2(rv[i], rv[i + 1]));
+                    d[i] = e.x;
+                    d[i + 1] = e.y;
+                }
                 split16(d, h, l);
                 tmem_st16(tl + TM_H + 64 + 16 * hc, h);
                 tmem_st16(tl + TM_H + 96 + 16 * hc, l);
