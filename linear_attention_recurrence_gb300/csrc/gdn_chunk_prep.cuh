@@ -162,17 +162,18 @@ __device__ __forceinline__ void prep_task(const ChunkPrepParams& p, PrepSmem& sm
         sm.bet[warp][lane] = bv;
     }
     if constexpr (OUT == PrepOut::kTiles) {
-        // [K; Q] (64 rows x 128 key dims, 4 blocks of 32 key dims) and K^T (128 key
-        // dims x 32 tokens), split into TF32 hi / lo, in the swizzled tile layout
+        // [K; Q] (64 rows x 128 key dims, 4 blocks of 32 key dims; per block the 64 hi
+        // rows, then the 64 lo rows) and K^T (128 key dims x 32 tokens), split into TF32
+        // hi / lo, in the swizzled tile layout
         float* kt = key_tiles(p.prep, p.n_kh, ci, kh);
         for (int it = tid; it < 2 * C * (D / 4); it += PREP_THREADS) {
             const int n = it >> 5, c4 = it & 31;  // row, 16-byte chunk along the key dims
             const float4 x = *reinterpret_cast<const float4*>(&(n < C ? K[n] : Q[n - C])[4 * c4]);
             float4 h, l;
             split_f4(x, h, l);
-            const int off = (c4 >> 3) * (2 * C * 32) + swf(n, 4 * (c4 & 7));
-            *reinterpret_cast<float4*>(kt + kTileKQH + off) = h;
-            *reinterpret_cast<float4*>(kt + kTileKQL + off) = l;
+            float* blk = kt + kTileKQ + (c4 >> 3) * (4 * C * 32);
+            *reinterpret_cast<float4*>(blk + swf(n, 4 * (c4 & 7))) = h;
+            *reinterpret_cast<float4*>(blk + swf(kTileKQLoRow + n, 4 * (c4 & 7))) = l;
         }
         for (int it = tid; it < D * (C / 4); it += PREP_THREADS) {
             const int r = it & (D - 1), j4 = it >> 7;  // key dim, 4 tokens

@@ -15,18 +15,25 @@
 // tcgen05.mma with M = 128 over those lanes: its A operand (S0^T, U'^T, D^T, D'^T)
 // comes from tensor memory, its B operand ([K; Q], T', P, K^T) from shared memory,
 // where the prep's swizzled tiles land by bulk copies.  Products are split TF32:
-// x = hi + lo with hi = x rounded to TF32 and lo = x - hi, and a.b is accumulated
-// in FP32 as hi_a lo_b + lo_a hi_b + hi_a hi_b (small terms first); plain TF32
-// would miss the 2e-6 tolerance against FP64 by three orders of magnitude.  The
-// gate scalings act in the epilogues, so one key head's tiles serve its three
+// x = hi + lo, and a.b is accumulated in FP32 as hi_a hi_b in one accumulator and
+// hi_a lo_b + lo_a hi_b in another (joined in the epilogue); plain TF32 would miss
+// the 2e-6 tolerance against FP64 by three orders of magnitude.  The tensor cores
+// read an FP32 operand as TF32 by dropping its low 13 bits (measured on GB300 for
+// both operand sources), so the state's hi part is the accumulator itself and
+// only its lo part, x - hi rounded to TF32, is written out; the B operands and the
+// chunk's intermediates are split with hi rounded to nearest.  Where one MMA can
+// take both, hi_a (hi_b, lo_b) is a single MMA over the stacked [hi; lo] operand.
+// The gate scalings act in the epilogues, so one key head's tiles serve its three
 // value heads unchanged.
 //
 // Warp roles (320 threads): warps 0-7 move values between tensor memory and
 // registers (warp w: lanes 32 (w % 4) .. +31, half w / 4 of each step's columns);
 // lane 0 of warp 8 issues the copies; lane 0 of warp 9 issues the MMAs.  Per chunk:
-//   epilogue: split S (hi, lo; S <- e^gamma_last S) -> MMA: X -> epilogue: U'
-//   -> MMA: D -> epilogue: D, D' -> MMA: the state update, then P D
-//   -> epilogue, during the next chunk: O -> out.
+//   MMA: X's hi.(hi, lo) terms from the state as it stands, while the epilogue
+//   writes the state's lo part (in two halves); MMA: X's lo.hi terms, then the
+//   chunk before's P D -> epilogue: U', then e^gamma_last S in place -> MMA: D ->
+//   epilogue: D', then D -> MMA: the state update, while the epilogue writes the
+//   chunk before's O to out.
 // The CTAs before the scan CTAs run the prep of the same super-block (one task per
 // (chunk, key head), in chunk order) and publish a flag per task, as the one-launch
 // kernel of gdn_chunk.cu does; the cooperative launch keeps every CTA resident.
@@ -41,32 +48,32 @@ constexpr int kProducerWarp = 8, kMmaWarp = 9;
 constexpr uint32_t TMEM_COLS = 512;
 
 // tensor-memory columns
-constexpr uint32_t TM_S = 0;    // S^T, the update's accumulator (128 key dims)
-constexpr uint32_t TM_H = 128;  // S0^T TF32 hi; once X is done: U' hi [0,32), U' lo [32,64); the D product
-                                // [64,128) (hi.hi [64,96), cross terms [96,128)), then D' hi [64,96), lo [96,128)
-constexpr uint32_t TM_L = 256;  // S0^T TF32 lo
-constexpr uint32_t TM_X = 384;  // chunk parity p: 64 columns at TM_X + 64 p: X_K [0,32), X_Q [32,64); then
-                                // e^gamma X_Q [0,32) and zeros [32,64), on which P D accumulates (hi.hi terms
-                                // onto the first half, cross terms onto the second); the other parity's 64
-                                // columns take D hi [0,32), D lo [32,64) once that chunk's O is out
+constexpr uint32_t TM_S = 0;    // S^T, the update's accumulator (128 key dims); also X's TF32 hi operand
+constexpr uint32_t TM_L = 128;  // S^T's TF32 lo part; once X is done: U' hi [0,32), U' lo [32,64); the D
+                                // product [64,128) (hi.hi [64,96), cross terms [96,128)), then D' hi
+                                // [64,96), D' lo [96,128)
+constexpr uint32_t TM_X = 256;  // chunk parity p: 128 columns at TM_X + 128 p: X's hi.hi terms [0,64)
+                                // (k tokens, then q) and cross terms [64,128); then O's accumulators,
+                                // e^gamma X_Q [0,32) and zeros [32,64), and D hi [64,96), D lo [96,128)
 
 // shared memory (bytes from a 1024-aligned base)
-constexpr uint32_t OFF_KQ = 0;        // [2 buffers][hi 32 KB | lo 32 KB]: [4 key-dim blocks][64 rows][128 B]
+constexpr uint32_t OFF_KQ = 0;        // [2 buffers][4 key-dim blocks][128 rows: hi 64, lo 64][128 B]
 constexpr uint32_t OFF_KT = 131072;   // K^T hi 16 KB | lo 16 KB: [128 key dims][128 B]
 constexpr uint32_t OFF_TP = 163840;   // T' hi 4 KB | lo 4 KB: [32 rows][128 B] (one 64-row operand [hi; lo])
-constexpr uint32_t OFF_P = 172032;    // P hi 4 KB | lo 4 KB, the same
-constexpr uint32_t OFF_V = 180224;    // [2 buffers][32 tokens][128 columns] floats (TMA)
-constexpr uint32_t OFF_G = 212992;    // [2 buffers][e^gamma 32 | e^(gamma_last - gamma) 32] floats
-constexpr uint32_t OFF_BAR = 213504;  // mbarriers, then the tensor-memory address and the abort word
+constexpr uint32_t OFF_P = 172032;    // [2 buffers][P hi 4 KB | lo 4 KB], the same
+constexpr uint32_t OFF_V = 188416;    // [2 buffers][32 tokens][128 columns] floats (TMA)
+constexpr uint32_t OFF_G = 221184;    // [2 buffers][e^gamma 32 | e^(gamma_last - gamma) 32] floats
+constexpr uint32_t OFF_BAR = 221696;  // mbarriers, then the tensor-memory address and the abort word
 constexpr uint32_t SCAN_SMEM = OFF_BAR + 256;
 enum {
-    B_KQ0, B_KQ1, B_TP, B_KTP, B_VG0, B_VG1,  // copies landed
-    B_MX0, B_MX1, B_MD, B_MS, B_MO, B_FIN,    // MMA groups done (tcgen05.commit)
-    B_ESA, B_ESB, B_EU, B_ED, B_EO,           // epilogue steps done (one arrival per epilogue warp)
+    B_KQ0, B_KQ1, B_P0, B_P1, B_VG0, B_VG1, B_TP, B_KT,  // copies landed
+    B_MX0, B_MX1, B_MD, B_MS, B_MO, B_FIN,               // MMA groups done (tcgen05.commit)
+    B_ESA, B_ESB, B_EU, B_ED, B_EDO, B_EO,               // epilogue steps done (one arrival per epilogue warp)
+    B_VF0, B_VF1,                                        // v / gates buffer read for the last time (the same)
     NBAR
 };
 static_assert(NBAR * 8 + 8 <= 256, "barrier space");
-constexpr uint32_t TX_KQ = 2 * 2 * C * D * 4, TX_TP = 2 * C * C * 4, TX_KTP = 2 * D * C * 4 + 2 * C * C * 4;
+constexpr uint32_t TX_KQ = 2 * 2 * C * D * 4, TX_TP = 2 * C * C * 4, TX_P = 2 * C * C * 4, TX_KT = 2 * D * C * 4;
 constexpr uint32_t TX_VG = C * D * 4 + 2 * C * 4;
 
 constexpr uint32_t IDESC_N32 = umma_idesc_tf32(128, 32);
@@ -113,11 +120,14 @@ __device__ __forceinline__ void epi_arrive(const TmemShared& sh, int b) {
     if ((threadIdx.x & 31) == 0) mbar_arrive(&sh.bar[b]);
 }
 
+__device__ __forceinline__ float rna_tf32(const float x) {
+    return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xFFFFE000u);
+}
 // TF32 hi (to nearest, ties away: integer operations on the bits) and lo = x - hi
 // (exact; one packed FMA per pair).
 __device__ __forceinline__ void split_pair(const float x0, const float x1, float& h0, float& h1, float& l0, float& l1) {
-    h0 = __uint_as_float((__float_as_uint(x0) + 0x1000u) & 0xFFFFE000u);
-    h1 = __uint_as_float((__float_as_uint(x1) + 0x1000u) & 0xFFFFE000u);
+    h0 = rna_tf32(x0);
+    h1 = rna_tf32(x1);
     const float2 l = ffma2(make_float2(h0, h1), make_float2(-1.f, -1.f), make_float2(x0, x1));
     l0 = l.x;
     l1 = l.y;
@@ -125,6 +135,18 @@ __device__ __forceinline__ void split_pair(const float x0, const float x1, float
 __device__ __forceinline__ void split16(const float (&x)[16], float (&hi)[16], float (&lo)[16]) {
 #pragma unroll
     for (int i = 0; i < 16; i += 2) split_pair(x[i], x[i + 1], hi[i], hi[i + 1], lo[i], lo[i + 1]);
+}
+// The state's lo part: x - (x with its low 13 bits cleared, which the tensor cores
+// take as its TF32 hi), rounded to TF32.
+__device__ __forceinline__ void state_lo32(const float (&s)[32], float (&lo)[32]) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+        const float t0 = __uint_as_float(__float_as_uint(s[i]) & 0xFFFFE000u);
+        const float t1 = __uint_as_float(__float_as_uint(s[i + 1]) & 0xFFFFE000u);
+        const float2 d = ffma2(make_float2(t0, t1), make_float2(-1.f, -1.f), make_float2(s[i], s[i + 1]));
+        lo[i] = rna_tf32(d.x);
+        lo[i + 1] = rna_tf32(d.y);
+    }
 }
 
 // ---- the scan of value head vh ----
@@ -154,10 +176,14 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
 
     if (warp == kProducerWarp) {
         // ---------------- copies ----------------
+        // Each buffer is refilled once the MMA group or epilogue step that last reads it
+        // has finished.  The order below also keeps every wait at most one phase behind
+        // its barrier: the phase after the awaited one depends on a copy issued later in
+        // the same iteration.
         if (lane == 0) {
-            int armed[B_VG1 + 1];  // last chunk whose copies each load barrier was armed for (-1: none)
+            int armed[B_KT + 1];  // last chunk whose copies each load barrier was armed for (-1: none)
 #pragma unroll
-            for (int b = 0; b <= B_VG1; ++b) armed[b] = -1;
+            for (int b = 0; b <= B_KT; ++b) armed[b] = -1;
             float* tiles = p.prep.prep;
             for (int c = 0; c < nch && !*abort_flag; ++c) {
                 // the prep task of (c, kh) has published its tiles
@@ -174,37 +200,41 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
                 const float* kt = key_tiles(tiles, n_kh, c, kh);
                 const float* ht = head_tiles(tiles, n_kh, n_vh, c, vh);
                 const int s = c & 1;
-                // v and the gates of chunk c: the buffer's chunk c-2 is out (its O epilogue,
-                // which follows its last use of them, is done)
-                if (c >= 2 && !wait_ab(sh, B_EO, static_cast<uint32_t>(c & 1))) break;
+                const uint32_t par2 = static_cast<uint32_t>(((c - 2) >> 1) & 1);
+                // v and the gates of chunk c: the buffer's chunk c-2 has been read for the last time
+                if (c >= 2 && !wait_ab(sh, B_VF0 + s, par2)) break;
                 mbar_arrive_expect_tx(&bar[B_VG0 + s], TX_VG);
                 tma_load_2d(sm + OFF_V + s * (C * D * 4), &p.tm_v, &bar[B_VG0 + s], vh * D,
                             static_cast<int>(p.prep.t_begin + static_cast<int64_t>(c) * C));
                 bulk_load(sm + OFF_G + s * 256, ht + kTileEG, 2 * C * 4, &bar[B_VG0 + s]);
                 if (s) armed[B_VG1] = c; else armed[B_VG0] = c;
-                // [K; Q] of chunk c: the buffer's chunk c-2 has been read by its X product
-                if (c >= 2 && !wait_ab(sh, B_MX0 + s, static_cast<uint32_t>(((c - 2) >> 1) & 1))) break;
+                // P of chunk c: the buffer's chunk c-2 P D is done
+                if (c >= 2 && !wait_ab(sh, B_MO, static_cast<uint32_t>(c & 1))) break;
+                mbar_arrive_expect_tx(&bar[B_P0 + s], TX_P);
+                bulk_load(sm + OFF_P + s * TX_P, ht + kTilePH, TX_P, &bar[B_P0 + s]);
+                if (s) armed[B_P1] = c; else armed[B_P0] = c;
+                // [K; Q] of chunk c: the buffer's chunk c-2 X product is done
+                if (c >= 2 && !wait_ab(sh, B_MX0 + s, par2)) break;
                 mbar_arrive_expect_tx(&bar[B_KQ0 + s], TX_KQ);
-                bulk_load(sm + OFF_KQ + s * 65536, kt + kTileKQH, TX_KQ, &bar[B_KQ0 + s]);
+                bulk_load(sm + OFF_KQ + s * 65536, kt + kTileKQ, TX_KQ, &bar[B_KQ0 + s]);
                 if (s) armed[B_KQ1] = c; else armed[B_KQ0] = c;
                 // T' of chunk c: chunk c-1's D product is done
                 if (c >= 1 && !wait_ab(sh, B_MD, static_cast<uint32_t>((c - 1) & 1))) break;
                 mbar_arrive_expect_tx(&bar[B_TP], TX_TP);
                 bulk_load(sm + OFF_TP, ht + kTileTPH, TX_TP, &bar[B_TP]);
                 armed[B_TP] = c;
-                // K^T and P of chunk c: chunk c-1's update and P D are done
-                if (c >= 1 && !wait_ab(sh, B_MO, static_cast<uint32_t>((c - 1) & 1))) break;
-                mbar_arrive_expect_tx(&bar[B_KTP], TX_KTP);
-                bulk_load(sm + OFF_KT, kt + kTileKTH, 2 * D * C * 4, &bar[B_KTP]);
-                bulk_load(sm + OFF_P, ht + kTilePH, 2 * C * C * 4, &bar[B_KTP]);
-                armed[B_KTP] = c;
+                // K^T of chunk c: chunk c-1's update is done
+                if (c >= 1 && !wait_ab(sh, B_MS, static_cast<uint32_t>((c - 1) & 1))) break;
+                mbar_arrive_expect_tx(&bar[B_KT], TX_KT);
+                bulk_load(sm + OFF_KT, kt + kTileKTH, TX_KT, &bar[B_KT]);
+                armed[B_KT] = c;
             }
             // before the CTA ends: every copy issued has landed (bounded waits; normally
             // these phases completed long ago and the waits return at once)
 #pragma unroll
-            for (int b = 0; b <= B_VG1; ++b) {
+            for (int b = 0; b <= B_KT; ++b) {
                 if (armed[b] < 0) continue;
-                const bool two = (b == B_KQ0 || b == B_KQ1 || b == B_VG0 || b == B_VG1);
+                const bool two = b < B_TP;  // double-buffered: one phase per two chunks
                 mbar_wait(&bar[b], static_cast<uint32_t>((two ? armed[b] >> 1 : armed[b]) & 1));
             }
         }
@@ -217,78 +247,92 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
             const uint64_t tp_desc = umma_desc_sw128(sm + OFF_TP);
             const uint64_t p_desc = umma_desc_sw128(sm + OFF_P);
             // descriptor start addresses count 16-byte units: +2 per 8-float k step
-            for (int c = 0; c < nch; ++c) {
+            auto kq_b = [&](int c, int ks) {  // [K; Q] block of k step ks: 128 rows [hi; lo]
+                return kq_desc + static_cast<uint64_t>(((c & 1) * 65536 + (ks >> 2) * 16384 + (ks & 3) * 32) >> 4);
+            };
+            // P D of chunk cc, once its D and O's accumulators are in place and its P has
+            // landed: per k step D hi . [P hi; P lo] (N = 64: hi.hi onto e^gamma X_Q, hi.lo
+            // onto the zeros) and D lo . P hi (N = 32, onto the second half)
+            auto issue_o = [&](int cc) {
+                if (!wait_ab(sh, B_EDO, static_cast<uint32_t>(cc & 1))) return false;
+                if (!wait_ab(sh, B_P0 + (cc & 1), static_cast<uint32_t>((cc >> 1) & 1))) return false;
+                tc_fence_after_sync();
+                const uint32_t tXc = tbase + TM_X + 128 * static_cast<uint32_t>(cc & 1);
+                const uint64_t pb = p_desc + static_cast<uint64_t>(((cc & 1) * TX_P) >> 4);
+#pragma unroll
+                for (int ks = 0; ks < C / 8; ++ks) {
+                    const uint64_t b = pb + static_cast<uint64_t>((ks * 32) >> 4);
+                    umma_tf32_ts(tXc, tXc + 64 + 8 * ks, b, IDESC_N64, true);
+                    umma_tf32_ts(tXc + 32, tXc + 96 + 8 * ks, b, IDESC_N32, true);
+                }
+                umma_commit(&bar[B_MO]);
+                return true;
+            };
+            bool alive = true;
+            for (int c = 0; c < nch && alive; ++c) {
                 const uint32_t pp = static_cast<uint32_t>(c & 1);
-                const uint32_t tX = tbase + TM_X + 64 * pp, tXo = tbase + TM_X + 64 * (pp ^ 1);
-                const uint64_t xb = kq_desc + static_cast<uint64_t>(((c & 1) * 65536) >> 4);
+                const uint32_t tX = tbase + TM_X + 128 * pp;
+                alive = false;
+                // [K; Q] has landed and X's buffer is free (chunk c-2's O is out); then the
+                // state after chunk c-1 is final (chunk 0: the starting state is in place)
                 if (!wait_ab(sh, B_KQ0 + (c & 1), static_cast<uint32_t>((c >> 1) & 1))) break;
-                if (c >= 1 && !wait_ab(sh, B_MO, pp ^ 1)) break;
-                // X = S0^T [K; Q]^T, N = 64 tokens (k then q), 16 k steps of 8 key dims: the
-                // cross terms of every k step first, while the accumulator is small (each
-                // tcgen05.mma adds to it with FP32 rounding), then the hi.hi terms.  The
-                // state's split lands in two halves (key dims 0-31 and 64-95 first).
+                if (c >= 2 && !wait_ab(sh, B_EO, pp)) break;
+                if (!wait_ab(sh, c == 0 ? B_ESB : B_MS, c == 0 ? 0u : pp ^ 1)) break;
+                tc_fence_after_sync();
+                // X = S0^T [K; Q]^T, N = 64 tokens (k then q), 16 k steps of 8 key dims:
+                // hi . [hi; lo] (N = 128) from the state itself
+#pragma unroll
+                for (int ks = 0; ks < D / 8; ++ks)
+                    umma_tf32_ts(tX, tbase + TM_S + 8 * ks, kq_b(c, ks), IDESC_N128, ks > 0);
+                // lo . hi (N = 64, onto the cross terms): key dims 0-31 and 64-95 first
                 if (!wait_ab(sh, B_ESA, pp)) break;
                 tc_fence_after_sync();
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const int ks = (i & 3) + 8 * (i >> 2);  // 0-3, 8-11
-                    const uint64_t bh = xb + static_cast<uint64_t>((((ks >> 2) * 8192) + (ks & 3) * 32) >> 4);
-                    const uint64_t bl = bh + (32768 >> 4);
-                    umma_tf32_ts(tX, tbase + TM_H + 8 * ks, bl, IDESC_N64, i > 0);
-                    umma_tf32_ts(tX, tbase + TM_L + 8 * ks, bh, IDESC_N64, true);
+                    umma_tf32_ts(tX + 64, tbase + TM_L + 8 * ks, kq_b(c, ks), IDESC_N64, true);
                 }
                 if (!wait_ab(sh, B_ESB, pp)) break;
                 tc_fence_after_sync();
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const int ks = 4 + (i & 3) + 8 * (i >> 2);  // 4-7, 12-15
-                    const uint64_t bh = xb + static_cast<uint64_t>((((ks >> 2) * 8192) + (ks & 3) * 32) >> 4);
-                    const uint64_t bl = bh + (32768 >> 4);
-                    umma_tf32_ts(tX, tbase + TM_H + 8 * ks, bl, IDESC_N64, true);
-                    umma_tf32_ts(tX, tbase + TM_L + 8 * ks, bh, IDESC_N64, true);
-                }
-#pragma unroll
-                for (int ks = 0; ks < D / 8; ++ks) {
-                    const uint64_t bh = xb + static_cast<uint64_t>((((ks >> 2) * 8192) + (ks & 3) * 32) >> 4);
-                    umma_tf32_ts(tX, tbase + TM_H + 8 * ks, bh, IDESC_N64, true);
+                    umma_tf32_ts(tX + 64, tbase + TM_L + 8 * ks, kq_b(c, ks), IDESC_N64, true);
                 }
                 umma_commit(&bar[B_MX0 + (c & 1)]);
+                // the chunk before's P D fills the tensor pipe while the epilogue forms U'
+                if (c >= 1 && !issue_o(c - 1)) break;
                 // D^T = U'^T T'^T (K = 32 tokens): per k step U' hi . [T' hi; T' lo] (N = 64: hi.hi
-                // terms to columns 64-95 of H, hi.lo to 96-127) and U' lo . T' hi (N = 32, to 96-127)
-                if (!wait_ab(sh, B_EU, pp)) break;
+                // terms to columns 64-95 of L, hi.lo to 96-127) and U' lo . T' hi (N = 32, to 96-127)
                 if (!wait_ab(sh, B_TP, pp)) break;
+                if (!wait_ab(sh, B_EU, pp)) break;
                 tc_fence_after_sync();
 #pragma unroll
                 for (int ks = 0; ks < C / 8; ++ks) {
                     const uint64_t b = tp_desc + static_cast<uint64_t>((ks * 32) >> 4);
-                    umma_tf32_ts(tbase + TM_H + 64, tbase + TM_H + 8 * ks, b, IDESC_N64, ks > 0);
-                    umma_tf32_ts(tbase + TM_H + 96, tbase + TM_H + 32 + 8 * ks, b, IDESC_N32, true);
+                    umma_tf32_ts(tbase + TM_L + 64, tbase + TM_L + 8 * ks, b, IDESC_N64, ks > 0);
+                    umma_tf32_ts(tbase + TM_L + 96, tbase + TM_L + 32 + 8 * ks, b, IDESC_N32, true);
                 }
                 umma_commit(&bar[B_MD]);
-                // S^T += D'^T K (N = 128 key dims, cross terms first), then P D^T onto e^gamma X_Q
+                // S^T += D'^T K (N = 128 key dims; the accumulator holds e^gamma_last S0^T)
+                if (!wait_ab(sh, B_KT, pp)) break;
                 if (!wait_ab(sh, B_ED, pp)) break;
-                if (!wait_ab(sh, B_KTP, pp)) break;
                 tc_fence_after_sync();
 #pragma unroll
                 for (int ks = 0; ks < C / 8; ++ks) {
                     const uint64_t bh = kt_desc + static_cast<uint64_t>((ks * 32) >> 4);
                     const uint64_t bl = bh + (16384 >> 4);
-                    umma_tf32_ts(tbase + TM_S, tbase + TM_H + 64 + 8 * ks, bl, IDESC_N128, true);
-                    umma_tf32_ts(tbase + TM_S, tbase + TM_H + 96 + 8 * ks, bh, IDESC_N128, true);
+                    umma_tf32_ts(tbase + TM_S, tbase + TM_L + 64 + 8 * ks, bl, IDESC_N128, true);
+                    umma_tf32_ts(tbase + TM_S, tbase + TM_L + 96 + 8 * ks, bh, IDESC_N128, true);
                 }
 #pragma unroll
                 for (int ks = 0; ks < C / 8; ++ks)
-                    umma_tf32_ts(tbase + TM_S, tbase + TM_H + 64 + 8 * ks, kt_desc + static_cast<uint64_t>((ks * 32) >> 4),
+                    umma_tf32_ts(tbase + TM_S, tbase + TM_L + 64 + 8 * ks, kt_desc + static_cast<uint64_t>((ks * 32) >> 4),
                                  IDESC_N128, true);
                 umma_commit(&bar[B_MS]);
-#pragma unroll
-                for (int ks = 0; ks < C / 8; ++ks) {
-                    const uint64_t b = p_desc + static_cast<uint64_t>((ks * 32) >> 4);
-                    umma_tf32_ts(tX, tXo + 8 * ks, b, IDESC_N64, true);
-                    umma_tf32_ts(tX + 32, tXo + 32 + 8 * ks, b, IDESC_N32, true);
-                }
-                umma_commit(&bar[B_MO]);
+                alive = true;
             }
+            if (alive) issue_o(nch - 1);  // the last chunk's P D
             // every MMA issued has completed before the tensor memory is freed
             umma_commit(&bar[B_FIN]);
             mbar_wait(&bar[B_FIN], 0);
@@ -304,23 +348,9 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
         float* state = p.state + static_cast<int64_t>(vh) * D * D;
         bool ok = true;
 
-        // split of key dims col .. col+31 of the state S: hi, lo for X; e^gamma_last S for the update
-        auto split_state = [&](float (&s)[32], const uint32_t col, const float el) {
-            float h[32], l[32];
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-                split_pair(s[i], s[i + 1], h[i], h[i + 1], l[i], l[i + 1]);
-                const float2 e = fmul2(make_float2(s[i], s[i + 1]), make_float2(el, el));
-                s[i] = e.x;
-                s[i + 1] = e.y;
-            }
-            tmem_st32(tl + TM_H + col, h);
-            tmem_st32(tl + TM_L + col, l);
-            tmem_st32(tl + TM_S + col, s);
-        };
-        // O of chunk cc (e^gamma X_Q + P D: its two accumulators) -> out
+        // O of chunk cc (its two accumulators) -> out
         auto o_out = [&](int cc) {
-            const uint32_t tX = tl + TM_X + 64 * static_cast<uint32_t>(cc & 1);
+            const uint32_t tX = tl + TM_X + 128 * static_cast<uint32_t>(cc & 1);
             float a[16], b2[16];
             tmem_ld16x2(tX + 16 * hc, tX + 32 + 16 * hc, a, b2);
             const int nt = min(C, n_tokens - cc * C);
@@ -332,78 +362,86 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
             }
         };
 
-        // the starting state, split (its gates come with chunk 0's v)
-        {
-            ok = warp_wait_ab(sh, B_VG0, 0);
-            const float el = Gb[C - 1];
+        // the starting state and its lo part (key dims 64 hc + 32 b .. +31)
 #pragma unroll
-            for (int b = 0; b < 2; ++b) {
-                float s[32];
+        for (int b = 0; b < 2; ++b) {
+            float s[32], lo[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) s[i] = state[static_cast<int64_t>(64 * hc + 32 * b + i) * D + j];
-                split_state(s, 64 * hc + 32 * b, el);
-                epi_arrive(sh, b ? B_ESB : B_ESA);
-            }
+            for (int i = 0; i < 32; ++i) s[i] = state[static_cast<int64_t>(64 * hc + 32 * b + i) * D + j];
+            state_lo32(s, lo);
+            tmem_st32(tl + TM_S + 64 * hc + 32 * b, s);
+            tmem_st32(tl + TM_L + 64 * hc + 32 * b, lo);
+            epi_arrive(sh, b ? B_ESB : B_ESA);
         }
         for (int c = 0; c < nch && ok; ++c) {
             const uint32_t pp = static_cast<uint32_t>(c & 1);
-            const uint32_t tX = tl + TM_X + 64 * pp, tXo = tl + TM_X + 64 * (pp ^ 1);
+            const uint32_t tX = tl + TM_X + 128 * pp;
             const float* V = Vb + (c & 1) * (C * D);
             const float* eg = Gb + (c & 1) * 64;
             const float* er = eg + C;
             if (c >= 1) {
-                // split of the state after chunk c-1 (with chunk c's e^gamma_last)
-                if (!(ok = warp_wait_ab(sh, B_VG0 + (c & 1), static_cast<uint32_t>((c >> 1) & 1)))) break;
-                const float el = eg[C - 1];
+                // the lo part of the state after chunk c-1, in two halves
                 if (!(ok = warp_wait_ab(sh, B_MS, pp ^ 1))) break;
                 tc_fence_after_sync();
 #pragma unroll
                 for (int b = 0; b < 2; ++b) {
-                    float s[32];
+                    float s[32], lo[32];
                     tmem_ld32(tl + TM_S + 64 * hc + 32 * b, s);
-                    split_state(s, 64 * hc + 32 * b, el);
+                    state_lo32(s, lo);
+                    tmem_st32(tl + TM_L + 64 * hc + 32 * b, lo);
                     epi_arrive(sh, b ? B_ESB : B_ESA);
                 }
-                // O of chunk c-1
-                if (!(ok = warp_wait_ab(sh, B_MO, pp ^ 1))) break;
-                tc_fence_after_sync();
-                o_out(c - 1);
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bar[B_EO]);
             }
             // U' = V - e^gamma X_K (tokens 16 hc .. +15), split -> U' hi / lo; e^gamma X_Q and
             // zeros, the start of O's two accumulators, in X's place
+            if (!(ok = warp_wait_ab(sh, B_VG0 + (c & 1), static_cast<uint32_t>((c >> 1) & 1)))) break;
             float vv[16], ev[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 vv[i] = V[(16 * hc + i) * D + j];
                 ev[i] = eg[16 * hc + i];
             }
+            const float el = eg[C - 1];
             if (!(ok = warp_wait_ab(sh, B_MX0 + (c & 1), static_cast<uint32_t>((c >> 1) & 1)))) break;
             tc_fence_after_sync();
             {
-                float xk[16], xq[16], h[16], l[16];
+                float xk[16], xq[16], ck[16], cq[16], h[16], l[16];
                 tmem_ld16x2(tX + 16 * hc, tX + 32 + 16 * hc, xk, xq);
+                tmem_ld16x2(tX + 64 + 16 * hc, tX + 96 + 16 * hc, ck, cq);
 #pragma unroll
                 for (int i = 0; i < 16; i += 2) {
-                    const float2 u = ffma2(make_float2(-ev[i], -ev[i + 1]), make_float2(xk[i], xk[i + 1]),
-                                           make_float2(vv[i], vv[i + 1]));
+                    const float2 k2 = make_float2(xk[i] + ck[i], xk[i + 1] + ck[i + 1]);
+                    const float2 q2 = make_float2(xq[i] + cq[i], xq[i + 1] + cq[i + 1]);
+                    const float2 u = ffma2(make_float2(-ev[i], -ev[i + 1]), k2, make_float2(vv[i], vv[i + 1]));
                     xk[i] = u.x;
                     xk[i + 1] = u.y;
-                    const float2 o = fmul2(make_float2(ev[i], ev[i + 1]), make_float2(xq[i], xq[i + 1]));
+                    const float2 o = fmul2(make_float2(ev[i], ev[i + 1]), q2);
                     xq[i] = o.x;
                     xq[i + 1] = o.y;
                 }
                 split16(xk, h, l);
-                tmem_st16(tl + TM_H + 16 * hc, h);
-                tmem_st16(tl + TM_H + 32 + 16 * hc, l);
+                tmem_st16(tl + TM_L + 16 * hc, h);
+                tmem_st16(tl + TM_L + 32 + 16 * hc, l);
+                epi_arrive(sh, B_EU);
+                // (O's accumulators are next needed by P D, after the D step below)
 #pragma unroll
                 for (int i = 0; i < 16; ++i) l[i] = 0.f;
                 tmem_st16(tX + 16 * hc, xq);
                 tmem_st16(tX + 32 + 16 * hc, l);
             }
-            epi_arrive(sh, B_EU);
+            // the update's accumulator: S0 -> e^gamma_last S0 (X has read S0)
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                float s[32];
+                tmem_ld32(tl + TM_S + 64 * hc + 32 * b, s);
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    const float2 e = fmul2(make_float2(s[i], s[i + 1]), make_float2(el, el));
+                    s[i] = e.x;
+                    s[i + 1] = e.y;
+                }
+                tmem_st32(tl + TM_S + 64 * hc + 32 * b, s);
+            }
             // D (its two accumulators) -> D hi / lo (for P D), D' = e^(gamma_last - gamma) D -> hi / lo
             float rv[16];
 #pragma unroll
@@ -411,24 +449,36 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
             if (!(ok = warp_wait_ab(sh, B_MD, pp))) break;
             tc_fence_after_sync();
             {
-                float d[16], x[16], h[16], l[16];
-                tmem_ld16x2(tl + TM_H + 64 + 16 * hc, tl + TM_H + 96 + 16 * hc, d, x);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) d[i] += x[i];
-                split16(d, h, l);
-                tmem_st16(tXo + 16 * hc, h);
-                tmem_st16(tXo + 32 + 16 * hc, l);
+                float d[16], x[16], e[16], h[16], l[16];
+                tmem_ld16x2(tl + TM_L + 64 + 16 * hc, tl + TM_L + 96 + 16 * hc, d, x);
 #pragma unroll
                 for (int i = 0; i < 16; i += 2) {
-                    const float2 e = fmul2(make_float2(d[i], d[i + 1]), make_float2(rv[i], rv[i + 1]));
-                    d[i] = e.x;
-                    d[i + 1] = e.y;
+                    d[i] += x[i];
+                    d[i + 1] += x[i + 1];
+                    const float2 f = fmul2(make_float2(d[i], d[i + 1]), make_float2(rv[i], rv[i + 1]));
+                    e[i] = f.x;
+                    e[i + 1] = f.y;
                 }
+                // D' first (the update waits for it), then D (for P D)
+                split16(e, h, l);
+                tmem_st16(tl + TM_L + 64 + 16 * hc, h);
+                tmem_st16(tl + TM_L + 96 + 16 * hc, l);
+                epi_arrive(sh, B_ED);
+                if (lane == 0) mbar_arrive(&bar[B_VF0 + (c & 1)]);  // chunk c's v and gates are read
                 split16(d, h, l);
-                tmem_st16(tl + TM_H + 64 + 16 * hc, h);
-                tmem_st16(tl + TM_H + 96 + 16 * hc, l);
+                tmem_st16(tX + 64 + 16 * hc, h);
+                tmem_st16(tX + 96 + 16 * hc, l);
+                epi_arrive(sh, B_EDO);
             }
-            epi_arrive(sh, B_ED);
+            // O of chunk c-1, while the tensor pipe runs the update
+            if (c >= 1) {
+                if (!(ok = warp_wait_ab(sh, B_MO, pp ^ 1))) break;
+                tc_fence_after_sync();
+                o_out(c - 1);
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar[B_EO]);
+            }
         }
         if (ok) {
             // the state after the last chunk, then its outputs

@@ -27,9 +27,10 @@ constexpr int kRecER = 2 * kChunk * kChunk + kChunk;  // e^(gamma_last - gamma_t
 // XOR row % 8), so a tile copied to a 1024-byte-aligned address is in the layout
 // the descriptors expect.  Each FP32 value is stored as TF32 hi and lo (x = hi + lo).
 // Per (chunk, key head), kKeyTileFloats floats:
-//   [K; Q] hi, lo: [4 blocks of 32 key dims][64 rows: k tokens 0-31, q tokens 0-31][32]
-//   K^T hi, lo:    [128 key dims][32 tokens]
-constexpr int kTileKQH = 0, kTileKQL = 8192, kTileKTH = 16384, kTileKTL = 20480, kKeyTileFloats = 24576;
+//   [K; Q]:     [4 blocks of 32 key dims][128 rows: hi of k tokens 0-31, q tokens 0-31,
+//               then lo of the same 64][32] (one 128-row operand [hi; lo] per block)
+//   K^T hi, lo: [128 key dims][32 tokens]
+constexpr int kTileKQ = 0, kTileKQLoRow = 64, kTileKTH = 16384, kTileKTL = 20480, kKeyTileFloats = 24576;
 // Per (chunk, value head), kHeadTileFloats floats: T' hi, lo and P hi, lo, each
 // [32 rows t][32 columns s], then e^gamma_t [32] and e^(gamma_last - gamma_t) [32].
 constexpr int kTileTPH = 0, kTileTPL = 1024, kTilePH = 2048, kTilePL = 3072, kTileEG = 4096, kTileER = 4128;
