@@ -26,9 +26,11 @@
 // The gate scalings act in the epilogues, so one key head's tiles serve its three
 // value heads unchanged.
 //
-// Warp roles (320 threads): warps 0-7 move values between tensor memory and
+// Warp roles (352 threads): warps 0-7 move values between tensor memory and
 // registers (warp w: lanes 32 (w % 4) .. +31, half w / 4 of each step's columns);
-// lane 0 of warp 8 issues the copies; lane 0 of warp 9 issues the MMAs.  Per chunk:
+// lane 0 of warp 8 issues the copies; lane 0 of warp 9 issues the MMAs but P D, which
+// lane 0 of warp 10 issues (a tcgen05.mma blocks its thread while the tensor pipe's
+// queue is full, and P D must not hold up the MMAs the chunk waits for).  Per chunk:
 //   MMA: X's hi.(hi, lo) terms from the state as it stands, while the epilogue
 //   writes the state's lo part (in two halves); MMA: X's lo.hi terms, then the
 //   chunk before's P D -> epilogue: U', then e^gamma_last S in place -> MMA: D ->
@@ -42,9 +44,9 @@
 namespace gdn {
 namespace {
 
-constexpr int TM_THREADS = 320;
+constexpr int TM_THREADS = 352;
 constexpr int kEpiWarps = 8;
-constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr int kProducerWarp = 8, kMmaWarp = 9, kOWarp = 10;
 constexpr uint32_t TMEM_COLS = 512;
 
 // tensor-memory columns
@@ -67,8 +69,8 @@ constexpr uint32_t OFF_BAR = 221696;  // mbarriers, then the tensor-memory addre
 constexpr uint32_t SCAN_SMEM = OFF_BAR + 256;
 enum {
     B_KQ0, B_KQ1, B_P0, B_P1, B_VG0, B_VG1, B_TP, B_KT,  // copies landed
-    B_MX0, B_MX1, B_MD, B_MS, B_MO, B_FIN,               // MMA groups done (tcgen05.commit)
-    B_ESA, B_ESB, B_EU, B_ED, B_EDO, B_EO,               // epilogue steps done (one arrival per epilogue warp)
+    B_MX0, B_MX1, B_MD, B_MS, B_MO, B_FIN, B_FINO,       // MMA groups done (tcgen05.commit)
+    B_ESA, B_ESB, B_EU, B_ED, B_EDO0, B_EDO1, B_EO,      // epilogue steps done (one arrival per epilogue warp)
     B_VF0, B_VF1,                                        // v / gates buffer read for the last time (the same)
     NBAR
 };
@@ -89,7 +91,19 @@ struct TmemShared {
 // Waits for the phase of `bar` with the given parity.  Returns false when the
 // wait gives up (poll limit: the abort word is set and the status reported) or
 // when another role already gave up.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 __device__ __forceinline__ bool wait_ab(const TmemShared& sh, int b, uint32_t parity) {
+    if (mbar_test(&sh.bar[b], parity)) return true;  // the common case: no suspend
     for (uint32_t i = 0;; ++i) {
         if (mbar_try_wait(&sh.bar[b], parity)) return true;
         if ((i & 255u) == 255u) {
@@ -250,24 +264,6 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
             auto kq_b = [&](int c, int ks) {  // [K; Q] block of k step ks: 128 rows [hi; lo]
                 return kq_desc + static_cast<uint64_t>(((c & 1) * 65536 + (ks >> 2) * 16384 + (ks & 3) * 32) >> 4);
             };
-            // P D of chunk cc, once its D and O's accumulators are in place and its P has
-            // landed: per k step D hi . [P hi; P lo] (N = 64: hi.hi onto e^gamma X_Q, hi.lo
-            // onto the zeros) and D lo . P hi (N = 32, onto the second half)
-            auto issue_o = [&](int cc) {
-                if (!wait_ab(sh, B_EDO, static_cast<uint32_t>(cc & 1))) return false;
-                if (!wait_ab(sh, B_P0 + (cc & 1), static_cast<uint32_t>((cc >> 1) & 1))) return false;
-                tc_fence_after_sync();
-                const uint32_t tXc = tbase + TM_X + 128 * static_cast<uint32_t>(cc & 1);
-                const uint64_t pb = p_desc + static_cast<uint64_t>(((cc & 1) * TX_P) >> 4);
-#pragma unroll
-                for (int ks = 0; ks < C / 8; ++ks) {
-                    const uint64_t b = pb + static_cast<uint64_t>((ks * 32) >> 4);
-                    umma_tf32_ts(tXc, tXc + 64 + 8 * ks, b, IDESC_N64, true);
-                    umma_tf32_ts(tXc + 32, tXc + 96 + 8 * ks, b, IDESC_N32, true);
-                }
-                umma_commit(&bar[B_MO]);
-                return true;
-            };
             bool alive = true;
             for (int c = 0; c < nch && alive; ++c) {
                 const uint32_t pp = static_cast<uint32_t>(c & 1);
@@ -300,8 +296,6 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
                     umma_tf32_ts(tX + 64, tbase + TM_L + 8 * ks, kq_b(c, ks), IDESC_N64, true);
                 }
                 umma_commit(&bar[B_MX0 + (c & 1)]);
-                // the chunk before's P D fills the tensor pipe while the epilogue forms U'
-                if (c >= 1 && !issue_o(c - 1)) break;
                 // D^T = U'^T T'^T (K = 32 tokens): per k step U' hi . [T' hi; T' lo] (N = 64: hi.hi
                 // terms to columns 64-95 of L, hi.lo to 96-127) and U' lo . T' hi (N = 32, to 96-127)
                 if (!wait_ab(sh, B_TP, pp)) break;
@@ -332,10 +326,40 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
                 umma_commit(&bar[B_MS]);
                 alive = true;
             }
-            if (alive) issue_o(nch - 1);  // the last chunk's P D
+            (void)alive;
             // every MMA issued has completed before the tensor memory is freed
             umma_commit(&bar[B_FIN]);
             mbar_wait(&bar[B_FIN], 0);
+        }
+        __syncwarp();
+    } else if (warp == kOWarp) {
+        // ---------------- P D ----------------
+        // P D of chunk c, once its D and O's accumulators are in place and its P has landed,
+        // and (but for the last chunk) after chunk c+1's X product, so it fills the tensor
+        // pipe while the epilogue forms U': per k step D hi . [P hi; P lo] (N = 64: hi.hi
+        // onto e^gamma X_Q, hi.lo onto the zeros) and D lo . P hi (N = 32, onto the second
+        // half).  Every barrier awaited here is one of a pair used by alternate chunks, whose
+        // next phase needs this chunk's P D first.
+        if (lane == 0) {
+            const uint64_t p_desc = umma_desc_sw128(sm + OFF_P);
+            for (int c = 0; c < nch; ++c) {
+                const uint32_t par = static_cast<uint32_t>((c >> 1) & 1);
+                if (!wait_ab(sh, B_EDO0 + (c & 1), par)) break;
+                if (!wait_ab(sh, B_P0 + (c & 1), par)) break;
+                if (c + 1 < nch && !wait_ab(sh, B_MX0 + ((c + 1) & 1), static_cast<uint32_t>(((c + 1) >> 1) & 1))) break;
+                tc_fence_after_sync();
+                const uint32_t tXc = tbase + TM_X + 128 * static_cast<uint32_t>(c & 1);
+                const uint64_t pb = p_desc + static_cast<uint64_t>(((c & 1) * TX_P) >> 4);
+#pragma unroll
+                for (int ks = 0; ks < C / 8; ++ks) {
+                    const uint64_t b = pb + static_cast<uint64_t>((ks * 32) >> 4);
+                    umma_tf32_ts(tXc, tXc + 64 + 8 * ks, b, IDESC_N64, true);
+                    umma_tf32_ts(tXc + 32, tXc + 96 + 8 * ks, b, IDESC_N32, true);
+                }
+                umma_commit(&bar[B_MO]);
+            }
+            umma_commit(&bar[B_FINO]);
+            mbar_wait(&bar[B_FINO], 0);
         }
         __syncwarp();
     } else {
@@ -468,7 +492,7 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
                 split16(d, h, l);
                 tmem_st16(tX + 64 + 16 * hc, h);
                 tmem_st16(tX + 96 + 16 * hc, l);
-                epi_arrive(sh, B_EDO);
+                epi_arrive(sh, B_EDO0 + (c & 1));
             }
             // O of chunk c-1, while the tensor pipe runs the update
             if (c >= 1) {
