@@ -69,7 +69,8 @@ constexpr uint32_t OFF_BAR = 221696;  // mbarriers, then the tensor-memory addre
 constexpr uint32_t SCAN_SMEM = OFF_BAR + 256;
 enum {
     B_KQ0, B_KQ1, B_P0, B_P1, B_VG0, B_VG1, B_TP, B_KT,  // copies landed
-    B_MX0, B_MX1, B_MD, B_MS, B_MO, B_FIN, B_FINO,       // MMA groups done (tcgen05.commit)
+    B_MX0, B_MX1, B_MD, B_MS, B_MO, B_MO0, B_MO1,        // MMA groups done (tcgen05.commit; B_MO0 / B_MO1:
+    B_FIN, B_FINO,                                       //   P D again, per P buffer)
     B_ESA, B_ESB, B_EU, B_ED, B_EDO0, B_EDO1, B_EO,      // epilogue steps done (one arrival per epilogue warp)
     B_VF0, B_VF1,                                        // v / gates buffer read for the last time (the same)
     NBAR
@@ -222,16 +223,16 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
                             static_cast<int>(p.prep.t_begin + static_cast<int64_t>(c) * C));
                 bulk_load(sm + OFF_G + s * 256, ht + kTileEG, 2 * C * 4, &bar[B_VG0 + s]);
                 if (s) armed[B_VG1] = c; else armed[B_VG0] = c;
-                // P of chunk c: the buffer's chunk c-2 P D is done
-                if (c >= 2 && !wait_ab(sh, B_MO, static_cast<uint32_t>(c & 1))) break;
-                mbar_arrive_expect_tx(&bar[B_P0 + s], TX_P);
-                bulk_load(sm + OFF_P + s * TX_P, ht + kTilePH, TX_P, &bar[B_P0 + s]);
-                if (s) armed[B_P1] = c; else armed[B_P0] = c;
                 // [K; Q] of chunk c: the buffer's chunk c-2 X product is done
                 if (c >= 2 && !wait_ab(sh, B_MX0 + s, par2)) break;
                 mbar_arrive_expect_tx(&bar[B_KQ0 + s], TX_KQ);
                 bulk_load(sm + OFF_KQ + s * 65536, kt + kTileKQ, TX_KQ, &bar[B_KQ0 + s]);
                 if (s) armed[B_KQ1] = c; else armed[B_KQ0] = c;
+                // P of chunk c: the buffer's chunk c-2 P D is done
+                if (c >= 2 && !wait_ab(sh, B_MO0 + s, par2)) break;
+                mbar_arrive_expect_tx(&bar[B_P0 + s], TX_P);
+                bulk_load(sm + OFF_P + s * TX_P, ht + kTilePH, TX_P, &bar[B_P0 + s]);
+                if (s) armed[B_P1] = c; else armed[B_P0] = c;
                 // T' of chunk c: chunk c-1's D product is done
                 if (c >= 1 && !wait_ab(sh, B_MD, static_cast<uint32_t>((c - 1) & 1))) break;
                 mbar_arrive_expect_tx(&bar[B_TP], TX_TP);
@@ -269,10 +270,10 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
                 const uint32_t pp = static_cast<uint32_t>(c & 1);
                 const uint32_t tX = tbase + TM_X + 128 * pp;
                 alive = false;
-                // [K; Q] has landed and X's buffer is free (chunk c-2's O is out); then the
-                // state after chunk c-1 is final (chunk 0: the starting state is in place)
-                if (!wait_ab(sh, B_KQ0 + (c & 1), static_cast<uint32_t>((c >> 1) & 1))) break;
-                if (c >= 2 && !wait_ab(sh, B_EO, pp)) break;
+                // (for c >= 1 the checks that [K; Q] has landed and that X's buffer is free were
+                // made while chunk c-1's update ran, below); the state after chunk c-1 is final
+                // (chunk 0: the starting state is in place)
+                if (c == 0 && !wait_ab(sh, B_KQ0, 0)) break;
                 if (!wait_ab(sh, c == 0 ? B_ESB : B_MS, c == 0 ? 0u : pp ^ 1)) break;
                 tc_fence_after_sync();
                 // X = S0^T [K; Q]^T, N = 64 tokens (k then q), 16 k steps of 8 key dims:
@@ -324,6 +325,12 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
                     umma_tf32_ts(tbase + TM_S, tbase + TM_L + 64 + 8 * ks, kt_desc + static_cast<uint64_t>((ks * 32) >> 4),
                                  IDESC_N128, true);
                 umma_commit(&bar[B_MS]);
+                // while the update runs: chunk c+1's [K; Q] has landed and its X buffer is free
+                // (chunk c-1's O is out)
+                if (c + 1 < nch) {
+                    if (!wait_ab(sh, B_KQ0 + ((c + 1) & 1), static_cast<uint32_t>(((c + 1) >> 1) & 1))) break;
+                    if (c >= 1 && !wait_ab(sh, B_EO, pp ^ 1)) break;
+                }
                 alive = true;
             }
             (void)alive;
@@ -357,6 +364,7 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
                     umma_tf32_ts(tXc + 32, tXc + 96 + 8 * ks, b, IDESC_N32, true);
                 }
                 umma_commit(&bar[B_MO]);
+                umma_commit(&bar[B_MO0 + (c & 1)]);
             }
             umma_commit(&bar[B_FINO]);
             mbar_wait(&bar[B_FINO], 0);
@@ -372,11 +380,17 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
         float* state = p.state + static_cast<int64_t>(vh) * D * D;
         bool ok = true;
 
-        // O of chunk cc (its two accumulators) -> out
-        auto o_out = [&](int cc) {
+        // O of chunk cc (its two accumulators) -> out; with `arrive`, X's buffer is released
+        // (B_EO) as soon as the values are in registers, before the stores
+        auto o_out = [&](int cc, bool arrive) {
             const uint32_t tX = tl + TM_X + 128 * static_cast<uint32_t>(cc & 1);
             float a[16], b2[16];
             tmem_ld16x2(tX + 16 * hc, tX + 32 + 16 * hc, a, b2);
+            if (arrive) {
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar[B_EO]);
+            }
             const int nt = min(C, n_tokens - cc * C);
             float* o = p.out + ((p.prep.t_begin + static_cast<int64_t>(cc) * C) * n_vh + vh) * D + j;
 #pragma unroll
@@ -429,25 +443,28 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
             if (!(ok = warp_wait_ab(sh, B_MX0 + (c & 1), static_cast<uint32_t>((c >> 1) & 1)))) break;
             tc_fence_after_sync();
             {
-                float xk[16], xq[16], ck[16], cq[16], h[16], l[16];
-                tmem_ld16x2(tX + 16 * hc, tX + 32 + 16 * hc, xk, xq);
-                tmem_ld16x2(tX + 64 + 16 * hc, tX + 96 + 16 * hc, ck, cq);
+                float xk[16], ck[16], h[16], l[16];
+                tmem_ld16x2(tX + 16 * hc, tX + 64 + 16 * hc, xk, ck);
 #pragma unroll
                 for (int i = 0; i < 16; i += 2) {
                     const float2 k2 = make_float2(xk[i] + ck[i], xk[i + 1] + ck[i + 1]);
-                    const float2 q2 = make_float2(xq[i] + cq[i], xq[i + 1] + cq[i + 1]);
                     const float2 u = ffma2(make_float2(-ev[i], -ev[i + 1]), k2, make_float2(vv[i], vv[i + 1]));
                     xk[i] = u.x;
                     xk[i + 1] = u.y;
-                    const float2 o = fmul2(make_float2(ev[i], ev[i + 1]), q2);
-                    xq[i] = o.x;
-                    xq[i + 1] = o.y;
                 }
                 split16(xk, h, l);
                 tmem_st16(tl + TM_L + 16 * hc, h);
                 tmem_st16(tl + TM_L + 32 + 16 * hc, l);
                 epi_arrive(sh, B_EU);
-                // (O's accumulators are next needed by P D, after the D step below)
+                // O's accumulators (next needed by P D, after the D step below): e^gamma X_Q, zeros
+                float xq[16], cq[16];
+                tmem_ld16x2(tX + 32 + 16 * hc, tX + 96 + 16 * hc, xq, cq);
+#pragma unroll
+                for (int i = 0; i < 16; i += 2) {
+                    const float2 o = fmul2(make_float2(ev[i], ev[i + 1]), make_float2(xq[i] + cq[i], xq[i + 1] + cq[i + 1]));
+                    xq[i] = o.x;
+                    xq[i + 1] = o.y;
+                }
 #pragma unroll
                 for (int i = 0; i < 16; ++i) l[i] = 0.f;
                 tmem_st16(tX + 16 * hc, xq);
@@ -498,10 +515,7 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
             if (c >= 1) {
                 if (!(ok = warp_wait_ab(sh, B_MO, pp ^ 1))) break;
                 tc_fence_after_sync();
-                o_out(c - 1);
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bar[B_EO]);
+                o_out(c - 1, true);
             }
         }
         if (ok) {
@@ -521,7 +535,7 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
             }
             if (ok) {
                 tc_fence_after_sync();
-                o_out(nch - 1);
+                o_out(nch - 1, false);
             }
         }
         tc_fence_before_sync();
