@@ -546,7 +546,7 @@ def main():
     ap.add_argument("--skip-other-mode", action="store_true")
     ap.add_argument("--skip-extra", action="store_true",
                     help="skip the T=8192 (both modes) and 36-layer stack measurements")
-    ap.add_argument("--chunk-products", default="mma", choices=["mma", "fma", "tc", "tmem"],
+    ap.add_argument("--chunk-products", default="tmem", choices=["mma", "fma", "tc", "tmem"],
                     help="how the chunked form computes its products (library option chunk_products)")
     ap.add_argument("--norm-in-launch", action="store_true",
                     help="with --step-api fused: the norm inside the recurrence's launch (library option "
@@ -903,16 +903,24 @@ def main():
     per_call = (kern["launches"] / args.steps - 1) / ncalls  # the norm is one launch per step
     scan_kind = args.chunk_products
     products = {"fma": "products as packed FP32 FMAs",
-                "tc": "S0 products as split-TF32 tcgen05 MMAs"}.get(scan_kind, "products as split-TF32 mma.sync MMAs")
+                "tc": "S0 products as split-TF32 tcgen05 MMAs",
+                "mma": "products as split-TF32 mma.sync MMAs"}.get(
+                    scan_kind, "state in tensor memory, every product a split-TF32 tcgen05 MMA")
     one_launch = per_call < 1.5
-    chunk_label = (("gdn_chunk_fused_kernel (prep and scan in one launch) per 2048-token call" if one_launch
-                    else "gdn_chunk_prep_kernel + gdn_chunk_scan_kernel per 2048-token call") + ", " + products)
-    # the capture in profiles/dram_traffic.md is of the default one-launch kernel
-    chunk_traffic = captured_traffic("gdn_chunk.cu") if one_launch and scan_kind not in ("fma", "tc") else None
+    tmem = scan_kind == "tmem" and one_launch
+    if tmem:
+        chunk_label = "gdn_chunk_tmem_kernel (prep and one scan CTA per value head in one launch) per 2048-token call"
+    else:
+        chunk_label = ("gdn_chunk_fused_kernel (prep and scan in one launch) per 2048-token call" if one_launch
+                       else "gdn_chunk_prep_kernel + gdn_chunk_scan_kernel per 2048-token call")
+    chunk_label += ", " + products
+    # the captures in profiles/ are of the one-launch kernels (tensor-memory and warp-MMA forms)
+    chunk_src = "gdn_chunk_tmem.cu" if tmem else "gdn_chunk.cu"
+    chunk_traffic = captured_traffic(chunk_src) if one_launch and scan_kind in ("mma", "tmem") else None
     norm_gbs = BYTES_NORM * T / (kern["norm_ms"] * 1e-3) / 1e9
-    counts = captured_counts("gdn_chunk.cu" if args.mode == "chunked" else "gdn_seq.cu")
-    if args.mode == "chunked" and not (one_launch and scan_kind == "mma"):
-        counts = None  # the capture is of the default one-launch kernel
+    counts = captured_counts(chunk_src if args.mode == "chunked" else "gdn_seq.cu")
+    if args.mode == "chunked" and not (one_launch and scan_kind in ("mma", "tmem")):
+        counts = None  # the captures are of the one-launch kernels
     counted = None
     if counts is not None:
         call_s = kern["rec_call_ms"] * 1e-3

@@ -30,7 +30,9 @@
  * Ownership: every pointer is a DEVICE pointer owned by the caller, on the
  * current CUDA device.  The library allocates only (a) a 4-byte status word per
  * device, (b) the chunked mode's per-device scratch (one 2048-token super-block
- * of prep results, about 25.9 MB, plus 12 KB of hand-off flags) and (c) the
+ * of prep results: about 152 MB for 48 value heads with the default
+ * GDN_PRODUCTS_TMEM form, 25.9 MB with the others, plus 12 KB of hand-off
+ * flags) and (c) the
  * sequential mode's fused-norm scratch (about 100 KB for 16 key heads), each on
  * first use and kept until gdn_release_scratch() or process exit.  Calls on one
  * device share that scratch: enqueue them on one stream (or otherwise order
@@ -234,7 +236,8 @@ int gdn_recurrence_norm(const float* q, const float* k, const float* v,
  * each other's results: serialise them.  A bounded wait that gives up in these
  * kernels sets the status word, which gdn_device_status() reads and clears
  * (without allocating anything).  Results are bit-identical to gdn_recurrence's
- * chunked mode for the same inputs.
+ * chunked mode with GDN_OPT_CHUNK_PRODUCTS = GDN_PRODUCTS_MMA (whose kernels this
+ * entry point runs) and within the same 2e-6 bound of its default form.
  */
 int gdn_recurrence_chunked_noalloc(const float* q, const float* k, const float* v,
                                    const float* g, const float* beta,
@@ -250,18 +253,20 @@ int gdn_recurrence_chunked_noalloc(const float* q, const float* k, const float* 
  * are the production forms.  The pages have no counterpart to these options.
  */
 typedef enum gdn_option {
-    /* How GDN_CHUNKED computes the chunk's products: GDN_PRODUCTS_MMA (default,
-     * split-TF32 warp-level MMAs), GDN_PRODUCTS_FMA (packed FP32 FMAs),
-     * GDN_PRODUCTS_TCGEN05 (the state products as split-TF32 tcgen05 MMAs; always
-     * two launches per super-block) or GDN_PRODUCTS_TMEM (one CTA per value head
-     * keeps the state in tensor memory and every product is a split-TF32 tcgen05
-     * MMA; one cooperative launch per super-block with the prep beside it, when the
-     * value heads leave at least n_kh SMs, else the GDN_PRODUCTS_MMA form; its
-     * scratch is about 152 MB for 48 value heads).  All meet the same 2e-6 bound. */
+    /* How GDN_CHUNKED computes the chunk's products: GDN_PRODUCTS_TMEM (default:
+     * one CTA per value head keeps the state in tensor memory and every product is
+     * a split-TF32 tcgen05 MMA; one cooperative launch per super-block with the
+     * prep beside it, when the value heads leave at least n_kh SMs, else the
+     * GDN_PRODUCTS_MMA form; its scratch is about 152 MB for 48 value heads),
+     * GDN_PRODUCTS_MMA (split-TF32 warp-level MMAs), GDN_PRODUCTS_FMA (packed
+     * FP32 FMAs) or GDN_PRODUCTS_TCGEN05 (the state products as split-TF32 tcgen05
+     * MMAs, 16 value columns per CTA; always two launches per super-block).  All
+     * meet the same 2e-6 bound; they round differently, so their bits differ. */
     GDN_OPT_CHUNK_PRODUCTS = 1,
     /* 1 (default): the chunk prep runs beside the scan in one cooperative launch
      * when the device has SMs to spare for it; 0: a prep launch, then a scan
-     * launch.  Same bits either way. */
+     * launch (GDN_PRODUCTS_TMEM has no two-launch form: the GDN_PRODUCTS_MMA
+     * scan runs then).  Same bits either way for a given scan. */
     GDN_OPT_CHUNK_ONE_LAUNCH = 2,
     /* gdn_recurrence_norm: 0 (default) launches the norm after the recurrence
      * (after each super-block in GDN_CHUNKED; in GDN_SEQUENTIAL only when `out` is

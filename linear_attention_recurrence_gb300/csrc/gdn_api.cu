@@ -39,7 +39,7 @@ DeviceState g_dev[kMaxDevices];
 // when it starts.  Nothing is read from the environment.
 constexpr int kOptSlots = 8;
 // constant-initialised defaults, in slot order (see opt_slot)
-std::atomic<int> g_opt[kOptSlots] = {GDN_PRODUCTS_MMA, 1, 0, 16, -1, 0, 0, 0};
+std::atomic<int> g_opt[kOptSlots] = {GDN_PRODUCTS_TMEM, 1, 0, 16, -1, 0, 0, 0};
 int opt_slot(int option) {
     switch (option) {
         case GDN_OPT_CHUNK_PRODUCTS: return 0;

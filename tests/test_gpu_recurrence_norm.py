@@ -70,7 +70,8 @@ def test_norm_inside_the_one_launch_same_bits(T):
     if not _one_launch_available():
         pytest.skip("too few SMs for the one-launch form")
     t = to_dev(make_inputs(T, seed=25))
-    with gdn.options(norm_in_launch=1):
+    # the in-launch norm belongs to the warp-MMA one-launch kernel
+    with gdn.options(norm_in_launch=1, chunk_products="mma"):
         (o1, y1, s1), (o2, y2, s2), launches = _pair(t, T, "chunked")
     assert launches == (T + 2047) // 2048
     assert np.array_equal(_bits(o1), _bits(o2)) and np.array_equal(_bits(s1), _bits(s2))
@@ -94,9 +95,10 @@ def test_recurrence_norm_two_launch_form_same_bits():
     T = 4099
     t = to_dev(make_inputs(T, seed=23))
     st = t["S0"].clone()
-    o1, y1 = gdn.gdn_recurrence_norm(t["q"], t["k"], t["v"], t["g"], t["beta"], st, t["z"], t["w"], 1e-6)
+    with gdn.options(chunk_products="mma"):  # the form that has both a one- and a two-launch kernel
+        o1, y1 = gdn.gdn_recurrence_norm(t["q"], t["k"], t["v"], t["g"], t["beta"], st, t["z"], t["w"], 1e-6)
     torch.cuda.synchronize()
-    with gdn.options(chunk_one_launch=0):
+    with gdn.options(chunk_one_launch=0, chunk_products="mma"):
         st2 = t["S0"].clone()
         n0 = gdn.gdn_launch_count()
         o2, y2 = gdn.gdn_recurrence_norm(t["q"], t["k"], t["v"], t["g"], t["beta"], st2, t["z"], t["w"], 1e-6)

@@ -45,12 +45,38 @@ def _noalloc(lib, t, a, b, state, out):
 
 
 def _alloc(lib, t, a, b, state, out):
+    """The allocating entry point with the warp-MMA products, whose kernels the
+    non-allocating one runs."""
     T = b - a
     n_kh, n_vh = t["q"].shape[1], t["v"].shape[1]
-    rc = lib.gdn_recurrence(_p(t["q"][a:b]), _p(t["k"][a:b]), _p(t["v"][a:b]), _p(t["g"][a:b]),
-                            _p(t["beta"][a:b]), _p(state), _p(out[a:b]), T, n_kh, n_vh, 128, gdn.GDN_CHUNKED,
-                            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    with gdn.options(chunk_products="mma"):
+        rc = lib.gdn_recurrence(_p(t["q"][a:b]), _p(t["k"][a:b]), _p(t["v"][a:b]), _p(t["g"][a:b]),
+                                _p(t["beta"][a:b]), _p(state), _p(out[a:b]), T, n_kh, n_vh, 128, gdn.GDN_CHUNKED,
+                                ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert rc == gdn.GDN_OK, lib.gdn_last_error().decode()
+
+
+@pytest.mark.parametrize("n_kh,T1,T2", [(16, 1300, 777), (32, 513, 64)])
+def test_noalloc_within_tolerance_of_the_default_form(lib, n_kh, T1, T2):
+    """Against the allocating entry point's default (tensor-memory) form, which
+    rounds differently: within the 2e-6 bound of each other's scale."""
+    from gdn_testutil import TOL
+    x = make_inputs(T1 + T2, seed=21, n_kh=n_kh, n_vh=3 * n_kh, norm=False)
+    t = to_dev(x)
+    shape = (T1 + T2, 3 * n_kh, 128)
+    out_d = torch.full(shape, float("nan"), device="cuda")
+    out_n = torch.full(shape, float("nan"), device="cuda")
+    st_d = t["S0"].clone()
+    st_n = t["S0"].clone()
+    for a, b in ((0, T1), (T1, T1 + T2)):
+        gdn.gdn_recurrence(t["q"][a:b], t["k"][a:b], t["v"][a:b], t["g"][a:b], t["beta"][a:b], st_d,
+                           out=out_d[a:b], mode="chunked")
+        _noalloc(lib, t, a, b, st_n, out_n)
+        torch.cuda.synchronize()
+        scale = float(out_d[a:b].abs().max())
+        assert float((out_n[a:b] - out_d[a:b]).abs().max()) <= 2 * TOL * scale
+        assert float((st_n - st_d).abs().max()) <= 2 * TOL * float(st_d.abs().max())
+    assert gdn.gdn_device_status() == gdn.GDN_OK
 
 
 @pytest.mark.parametrize("n_kh,T1,T2", [(16, 1300, 777), (32, 513, 64)])
