@@ -306,8 +306,9 @@ int run_recurrence(const float* q, const float* k, const float* v, const float* 
     if (n_vh != kHeadsPerKey * n_kh) return fail(GDN_ERR_UNSUPPORTED, "only n_vh == 3 * n_kh is supported");
     if (T > INT32_MAX - 4096) return fail(GDN_ERR_UNSUPPORTED, "T too large for 32-bit TMA coordinates");
     if (T == 0) return GDN_OK;
-    // the fused sequential norm may leave the FP32 output unwritten
-    const bool out_optional = norm && mode == GDN_SEQUENTIAL;
+    // with the norm fused (the sequential scan's epilogue, or the tensor-memory chunked
+    // scan's) the FP32 output may be left unwritten; a form that cannot fuse it requires out
+    const bool out_optional = norm != nullptr;
     if (!q || !k || !v || !g || !beta || !state_inout || (!out && !out_optional))
         return fail(GDN_ERR_INVALID_ARG, "null pointer");
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || (out && !aligned(out, 16)) ||
@@ -423,7 +424,7 @@ int run_recurrence(const float* q, const float* k, const float* v, const float* 
     int n_prep_tm = 0;
     ChunkTmemParams tp;
     std::memset(&tp, 0, sizeof(tp));
-    if (chunk_scan_kind() == ScanKind::kTmem && opt(GDN_OPT_CHUNK_ONE_LAUNCH) != 0 && !(norm && fused_norm_enabled()))
+    if (chunk_scan_kind() == ScanKind::kTmem && opt(GDN_OPT_CHUNK_ONE_LAUNCH) != 0)
         n_prep_tm = chunk_tmem_prep_ctas(n_kh, n_vh, dev->sm_count);
     if (n_prep_tm > 0) {
         if ((rc = make_map(&tp.tm_v, v, static_cast<uint64_t>(n_vh) * d, T, d, kChunk, CU_TENSOR_MAP_SWIZZLE_NONE)))
@@ -435,7 +436,14 @@ int run_recurrence(const float* q, const float* k, const float* v, const float* 
         tp.sync = dev->sync;
         tp.n_prep = n_prep_tm;
         tp.withhold_task = withheld_prep_task();
+        if (norm) {  // the norm in the scan's epilogue (each CTA holds whole rows)
+            tp.z = norm->z;
+            tp.w = norm->w;
+            tp.y = norm->y;
+            tp.eps = norm->eps;
+        }
     }
+    if (n_prep_tm == 0 && !out) return fail(GDN_ERR_INVALID_ARG, "out is required when the norm cannot be fused");
     for (int64_t t0 = 0; t0 < T; t0 += kSuperBlock) {
         const int n = static_cast<int>((T - t0) < kSuperBlock ? (T - t0) : kSuperBlock);
         pp.t_begin = t0;
@@ -447,16 +455,11 @@ int run_recurrence(const float* q, const float* k, const float* v, const float* 
             cudaError_t e = launch_chunk_tmem(tp, s);
             if (e == cudaSuccess) {
                 g_launches.fetch_add(1);
-                if (norm) {  // the norm of this super-block's rows after it
-                    e = launch_out_norm(out + t0 * n_vh * d, norm->z + t0 * n_vh * d, norm->w, norm->eps,
-                                        norm->y + t0 * n_vh * d, static_cast<int64_t>(n) * n_vh, dev->sm_count, s);
-                    if (e != cudaSuccess) return cuda_fail(e, "output norm launch");
-                    g_launches.fetch_add(1);
-                }
                 continue;
             }
             if (e != cudaErrorCooperativeLaunchTooLarge) return cuda_fail(e, "chunk prep+scan (tensor memory) launch");
             cudaGetLastError();  // fewer SMs available than the device has: the forms below
+            if (!out) return fail(GDN_ERR_INVALID_ARG, "out is required when the norm cannot be fused");
             n_prep_tm = 0;
         }
         if (n_prep > 0) {

@@ -36,10 +36,16 @@
 //   chunk before's P D -> epilogue: U', then e^gamma_last S in place -> MMA: D ->
 //   epilogue: D', then D -> MMA: the state update, while the epilogue writes the
 //   chunk before's O to out.
+// For gdn_recurrence_norm a second instance of the kernel (NORM) also writes the
+// gated RMSNorm of the output to y: each CTA holds whole 128-column rows, so the
+// norm needs no other CTA.  The row's sum of squares is formed in the order of
+// gdn_out_norm's warp (so y has that kernel's bits), during the next chunk's X
+// product, when the epilogue warps are otherwise idle.
 // The CTAs before the scan CTAs run the prep of the same super-block (one task per
 // (chunk, key head), in chunk order) and publish a flag per task, as the one-launch
 // kernel of gdn_chunk.cu does; the cooperative launch keeps every CTA resident.
 #include "gdn_chunk_prep.cuh"
+#include "gdn_norm_row.cuh"
 
 namespace gdn {
 namespace {
@@ -67,12 +73,18 @@ constexpr uint32_t OFF_V = 188416;    // [2 buffers][32 tokens][128 columns] flo
 constexpr uint32_t OFF_G = 221184;    // [2 buffers][e^gamma 32 | e^(gamma_last - gamma) 32] floats
 constexpr uint32_t OFF_BAR = 221696;  // mbarriers, then the tensor-memory address and the abort word
 constexpr uint32_t SCAN_SMEM = OFF_BAR + 256;
+// (the instance without the norm stays at this size, so that a 128-thread CTA of the
+// norm kernel launched on another stream still fits on an SM beside its CTA)
+constexpr uint32_t OFF_NP = SCAN_SMEM;  // norm: [2 halves][16 tokens][32] partial sums of squares
+constexpr uint32_t OFF_NR = OFF_NP + 4096;  // norm: [2 halves][16 tokens] 1 / rms
+constexpr uint32_t SCAN_SMEM_NORM = OFF_NR + 128;
 enum {
     B_KQ0, B_KQ1, B_P0, B_P1, B_VG0, B_VG1, B_TP, B_KT,  // copies landed
     B_MX0, B_MX1, B_MD, B_MS, B_MO, B_MO0, B_MO1,        // MMA groups done (tcgen05.commit; B_MO0 / B_MO1:
     B_FIN, B_FINO,                                       //   P D again, per P buffer)
     B_ESA, B_ESB, B_EU, B_ED, B_EDO0, B_EDO1, B_EO,      // epilogue steps done (one arrival per epilogue warp)
     B_VF0, B_VF1,                                        // v / gates buffer read for the last time (the same)
+    B_NP0, B_NP1, B_NR0, B_NR1,                          // norm exchange, per half (one arrival per warp of it)
     NBAR
 };
 static_assert(NBAR * 8 + 8 <= 256, "barrier space");
@@ -165,6 +177,7 @@ __device__ __forceinline__ void state_lo32(const float (&s)[32], float (&lo)[32]
 }
 
 // ---- the scan of value head vh ----
+template <bool NORM>
 __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned char* sm, const int vh,
                                           const uint32_t gen) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -179,7 +192,8 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
 
     if (tid == 0) {
         for (int b = 0; b < B_ESA; ++b) mbar_init(&bar[b], 1);
-        for (int b = B_ESA; b < NBAR; ++b) mbar_init(&bar[b], kEpiWarps);
+        for (int b = B_ESA; b < B_NP0; ++b) mbar_init(&bar[b], kEpiWarps);
+        for (int b = B_NP0; b < NBAR; ++b) mbar_init(&bar[b], kEpiWarps / 2);
         *abort_flag = 0;
         mbar_init_fence();
     }
@@ -400,6 +414,88 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
             }
         };
 
+        // (NORM) the output's norm, in two steps:
+        float* NP = reinterpret_cast<float*>(sm + OFF_NP) + hc * (16 * 32);
+        float* NR = reinterpret_cast<float*>(sm + OFF_NR) + hc * 16;
+        const float wj = p.y ? __ldg(p.w + j) : 0.f;
+        // The output of chunk cc, in two steps.  o_read: O's two accumulators -> registers (with
+        // `arrive`, X's buffer is released at once, B_EO), the FP32 rows to out, and for the norm
+        // the z loads issued; o_norm, later (during the next chunk's X product, so the z loads
+        // are in by then): the gated RMSNorm of those rows -> y, with gdn_out_norm's arithmetic
+        // (norm lane l = j / 4 sums the squares of columns 4l .. 4l+3 in order, then the 32
+        // lanes' sums meet in an xor butterfly), so y has its bits.
+        float on[16], zn[16];  // the rows (tokens 16 hc .. +15) of column j awaiting their norm
+        int pend = -1;         // their chunk, or -1
+        auto o_read = [&](int cc, bool arrive) {
+            const uint32_t tX = tl + TM_X + 128 * static_cast<uint32_t>(cc & 1);
+            float b2[16];
+            tmem_ld16x2(tX + 16 * hc, tX + 32 + 16 * hc, on, b2);
+            if (arrive) {
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar[B_EO]);
+            }
+            const int nt = min(C, n_tokens - cc * C);
+            const int64_t row0 = (p.prep.t_begin + static_cast<int64_t>(cc) * C) * n_vh + vh;  // token 0's row
+#pragma unroll
+            for (int i = 0; i < 16; ++i) on[i] += b2[i];
+            if (p.out) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int t = 16 * hc + i;
+                    if (t < nt) p.out[(row0 + static_cast<int64_t>(t) * n_vh) * D + j] = on[i];
+                }
+            }
+            if (p.y) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int t = 16 * hc + i;
+                    zn[i] = (t < nt) ? __ldg(p.z + (row0 + static_cast<int64_t>(t) * n_vh) * D + j) : 0.f;
+                }
+                pend = cc;
+            }
+        };
+        // Returns false if a norm exchange wait gave up.
+        auto o_norm = [&]() {
+            const int cc = pend;
+            pend = -1;
+            const int nt = min(C, n_tokens - cc * C);
+            const int64_t row0 = (p.prep.t_begin + static_cast<int64_t>(cc) * C) * n_vh + vh;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float x1 = __shfl_down_sync(0xffffffffu, on[i], 1);
+                const float x2 = __shfl_down_sync(0xffffffffu, on[i], 2);
+                const float x3 = __shfl_down_sync(0xffffffffu, on[i], 3);
+                float ss = on[i] * on[i];
+                ss = fmaf(x1, x1, ss);
+                ss = fmaf(x2, x2, ss);
+                ss = fmaf(x3, x3, ss);
+                if ((lane & 3) == 0) NP[i * 32 + 8 * q + (lane >> 2)] = ss;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[B_NP0 + hc]);
+            if (!warp_wait_ab(sh, B_NP0 + hc, static_cast<uint32_t>(cc & 1))) return false;
+            // this warp's 4 of the 16 rows: the butterfly over the 32 norm lanes
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                float v = NP[(4 * q + u) * 32 + lane];
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+                if (lane == 0) NR[4 * q + u] = rsqrtf(fmaf(v, 1.0f / 128.0f, p.eps));
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[B_NR0 + hc]);
+            if (!warp_wait_ab(sh, B_NR0 + hc, static_cast<uint32_t>(cc & 1))) return false;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int t = 16 * hc + i;
+                if (t < nt)
+                    p.y[(row0 + static_cast<int64_t>(t) * n_vh) * D + j] =
+                        __half_as_ushort(__float2half_rn(on[i] * NR[i] * wj * norm_silu(zn[i])));
+            }
+            return true;
+        };
+
         // the starting state and its lo part (key dims 64 hc + 32 b .. +31)
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
@@ -429,6 +525,10 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
                     tmem_st32(tl + TM_L + 64 * hc + 32 * b, lo);
                     epi_arrive(sh, b ? B_ESB : B_ESA);
                 }
+            }
+            // (NORM) the norm of chunk c-2's rows while X runs
+            if constexpr (NORM) {
+                if (pend >= 0 && !(ok = o_norm())) break;
             }
             // U' = V - e^gamma X_K (tokens 16 hc .. +15), split -> U' hi / lo; e^gamma X_Q and
             // zeros, the start of O's two accumulators, in X's place
@@ -515,7 +615,10 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
             if (c >= 1) {
                 if (!(ok = warp_wait_ab(sh, B_MO, pp ^ 1))) break;
                 tc_fence_after_sync();
-                o_out(c - 1, true);
+                if constexpr (NORM)
+                    o_read(c - 1, true);
+                else
+                    o_out(c - 1, true);
             }
         }
         if (ok) {
@@ -535,7 +638,15 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
             }
             if (ok) {
                 tc_fence_after_sync();
-                o_out(nch - 1, false);
+                if constexpr (NORM) {
+                    if (pend >= 0) ok = o_norm();
+                    if (ok) {
+                        o_read(nch - 1, false);
+                        if (pend >= 0) ok = o_norm();
+                    }
+                } else {
+                    o_out(nch - 1, false);
+                }
             }
         }
         tc_fence_before_sync();
@@ -547,6 +658,7 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
     }
 }
 
+template <bool NORM>
 __global__ void __launch_bounds__(TM_THREADS, 1) gdn_chunk_tmem_kernel(const __grid_constant__ ChunkTmemParams p) {
     __shared__ uint32_t s_gen;
     const int tid = threadIdx.x;
@@ -577,7 +689,7 @@ __global__ void __launch_bounds__(TM_THREADS, 1) gdn_chunk_tmem_kernel(const __g
             }
         }
     } else {
-        tmem_scan(p, aligned_dynamic_smem<unsigned char, 1024>(), b - p.n_prep, gen);
+        tmem_scan<NORM>(p, aligned_dynamic_smem<unsigned char, 1024>(), b - p.n_prep, gen);
     }
     __syncthreads();
     if (tid == 0) {
@@ -589,9 +701,12 @@ __global__ void __launch_bounds__(TM_THREADS, 1) gdn_chunk_tmem_kernel(const __g
     }
 }
 
-constexpr size_t kTmemSmem =
-    (SCAN_SMEM > sizeof(PrepSmemT<2>) ? SCAN_SMEM : sizeof(PrepSmemT<2>)) + 1024;
-static_assert(kTmemSmem <= 227 * 1024, "tensor-memory kernel shared memory");
+template <bool NORM>
+constexpr size_t tmem_smem() {
+    constexpr size_t scan = NORM ? SCAN_SMEM_NORM : SCAN_SMEM;
+    return (scan > sizeof(PrepSmemT<2>) ? scan : sizeof(PrepSmemT<2>)) + 1024;
+}
+static_assert(tmem_smem<true>() <= 227 * 1024, "tensor-memory kernel shared memory");
 
 }  // namespace
 
@@ -601,23 +716,28 @@ int chunk_tmem_prep_ctas(int n_kh, int n_vh, int sm_count) {
 }
 
 cudaError_t preload_chunk_tmem() {
-    return set_smem_once(reinterpret_cast<const void*>(gdn_chunk_tmem_kernel), static_cast<int>(kTmemSmem));
+    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(gdn_chunk_tmem_kernel<false>),
+                                  static_cast<int>(tmem_smem<false>()));
+    if (e != cudaSuccess) return e;
+    return set_smem_once(reinterpret_cast<const void*>(gdn_chunk_tmem_kernel<true>), static_cast<int>(tmem_smem<true>()));
 }
 
 cudaError_t launch_chunk_tmem(const ChunkTmemParams& p, cudaStream_t s) {
     cudaError_t e = preload_chunk_tmem();
     if (e != cudaSuccess) return e;
+    const bool norm = p.y != nullptr;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.n_prep + p.prep.n_vh);
     cfg.blockDim = dim3(TM_THREADS);
-    cfg.dynamicSmemBytes = kTmemSmem;
+    cfg.dynamicSmemBytes = norm ? tmem_smem<true>() : tmem_smem<false>();
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gdn_chunk_tmem_kernel, p);
+    return norm ? cudaLaunchKernelEx(&cfg, gdn_chunk_tmem_kernel<true>, p)
+                : cudaLaunchKernelEx(&cfg, gdn_chunk_tmem_kernel<false>, p);
 }
 
 }  // namespace gdn

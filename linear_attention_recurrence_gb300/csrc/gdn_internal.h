@@ -197,6 +197,12 @@ struct ChunkTmemParams {
     uint32_t* sync;        // as ChunkFusedParams::sync
     int n_prep;
     int withhold_task;     // failure-path test: this prep task's flag is never published (-1: none)
+    // The gated RMSNorm of the output in the scan's epilogue, when y != nullptr (out may
+    // then be nullptr: the FP32 output is not stored).
+    const float* z;        // [T][n_vh][128], absolute token rows like out
+    const float* w;        // [128]
+    uint16_t* y;           // [T][n_vh][128] binary16 bits
+    float eps;
 };
 // Prep CTAs of the tensor-memory form on a device with sm_count SMs (one CTA per
 // SM: the scan CTAs hold all 512 tensor-memory columns), or 0 when fewer than

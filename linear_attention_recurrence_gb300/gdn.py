@@ -170,9 +170,9 @@ def gdn_recurrence_norm(q, k, v, g, beta, state, z, w, eps: float = 1e-6, out=No
     """gdn_recurrence and gdn_out_norm of its output in one call; returns (out, y).
 
     ``out`` ([T][n_vh][d] FP32) and ``y`` ([T][n_vh][d] float16) are allocated if
-    None.  In sequential mode the norm is fused into the scan (one launch), and
-    with ``store_out=False`` the FP32 output is not written at all (``out`` is
-    returned as None).
+    None.  With ``store_out=False`` the FP32 output is not written at all (``out``
+    is returned as None): the norm is then fused into the scan (sequential mode,
+    and chunked mode's tensor-memory form, which always norms in its epilogue).
     """
     T, n_kh, d = q.shape
     n_vh = v.shape[1]
