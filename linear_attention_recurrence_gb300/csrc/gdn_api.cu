@@ -306,9 +306,8 @@ int run_recurrence(const float* q, const float* k, const float* v, const float* 
     if (n_vh != kHeadsPerKey * n_kh) return fail(GDN_ERR_UNSUPPORTED, "only n_vh == 3 * n_kh is supported");
     if (T > INT32_MAX - 4096) return fail(GDN_ERR_UNSUPPORTED, "T too large for 32-bit TMA coordinates");
     if (T == 0) return GDN_OK;
-    // with the norm fused (the sequential scan's epilogue, or the tensor-memory chunked
-    // scan's) the FP32 output may be left unwritten; a form that cannot fuse it requires out
-    const bool out_optional = norm != nullptr;
+    // the fused sequential norm may leave the FP32 output unwritten
+    const bool out_optional = norm && mode == GDN_SEQUENTIAL;
     if (!q || !k || !v || !g || !beta || !state_inout || (!out && !out_optional))
         return fail(GDN_ERR_INVALID_ARG, "null pointer");
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || (out && !aligned(out, 16)) ||
@@ -436,14 +435,15 @@ int run_recurrence(const float* q, const float* k, const float* v, const float* 
         tp.sync = dev->sync;
         tp.n_prep = n_prep_tm;
         tp.withhold_task = withheld_prep_task();
-        if (norm) {  // the norm in the scan's epilogue (each CTA holds whole rows)
+        if (norm) {  // the norm inside the launch, on the prep SMs once their tasks are done
             tp.z = norm->z;
             tp.w = norm->w;
             tp.y = norm->y;
             tp.eps = norm->eps;
+            tp.out_flags = dev->out_flags;
         }
     }
-    if (n_prep_tm == 0 && !out) return fail(GDN_ERR_INVALID_ARG, "out is required when the norm cannot be fused");
+    if (!out) return fail(GDN_ERR_INVALID_ARG, "out is required in chunked mode");
     for (int64_t t0 = 0; t0 < T; t0 += kSuperBlock) {
         const int n = static_cast<int>((T - t0) < kSuperBlock ? (T - t0) : kSuperBlock);
         pp.t_begin = t0;
@@ -459,7 +459,6 @@ int run_recurrence(const float* q, const float* k, const float* v, const float* 
             }
             if (e != cudaErrorCooperativeLaunchTooLarge) return cuda_fail(e, "chunk prep+scan (tensor memory) launch");
             cudaGetLastError();  // fewer SMs available than the device has: the forms below
-            if (!out) return fail(GDN_ERR_INVALID_ARG, "out is required when the norm cannot be fused");
             n_prep_tm = 0;
         }
         if (n_prep > 0) {

@@ -37,10 +37,11 @@
 //   epilogue: D', then D -> MMA: the state update, while the epilogue writes the
 //   chunk before's O to out.
 // For gdn_recurrence_norm a second instance of the kernel (NORM) also writes the
-// gated RMSNorm of the output to y: each CTA holds whole 128-column rows, so the
-// norm needs no other CTA.  The row's sum of squares is formed in the order of
-// gdn_out_norm's warp (so y has that kernel's bits), during the next chunk's X
-// product, when the epilogue warps are otherwise idle.
+// gated RMSNorm of the output to y, inside the same launch: once a scan CTA has
+// stored a chunk's rows, its P D warp publishes a flag for (chunk, value head), and
+// the prep CTAs, whose tasks end long before the scan does, norm those rows (read
+// back while they are still in L2) with gdn_out_norm's row function, so y has that
+// kernel's bits.  The scan's own warps do no more work than without the norm.
 // The CTAs before the scan CTAs run the prep of the same super-block (one task per
 // (chunk, key head), in chunk order) and publish a flag per task, as the one-launch
 // kernel of gdn_chunk.cu does; the cooperative launch keeps every CTA resident.
@@ -73,18 +74,15 @@ constexpr uint32_t OFF_V = 188416;    // [2 buffers][32 tokens][128 columns] flo
 constexpr uint32_t OFF_G = 221184;    // [2 buffers][e^gamma 32 | e^(gamma_last - gamma) 32] floats
 constexpr uint32_t OFF_BAR = 221696;  // mbarriers, then the tensor-memory address and the abort word
 constexpr uint32_t SCAN_SMEM = OFF_BAR + 256;
-// (the instance without the norm stays at this size, so that a 128-thread CTA of the
-// norm kernel launched on another stream still fits on an SM beside its CTA)
-constexpr uint32_t OFF_NP = SCAN_SMEM;  // norm: [2 halves][16 tokens][32] partial sums of squares
-constexpr uint32_t OFF_NR = OFF_NP + 4096;  // norm: [2 halves][16 tokens] 1 / rms
-constexpr uint32_t SCAN_SMEM_NORM = OFF_NR + 128;
+// (kept at about 218 KB, so that a 128-thread CTA of the norm kernel launched on another
+// stream still fits on an SM beside this kernel's CTA)
 enum {
     B_KQ0, B_KQ1, B_P0, B_P1, B_VG0, B_VG1, B_TP, B_KT,  // copies landed
     B_MX0, B_MX1, B_MD, B_MS, B_MO, B_MO0, B_MO1,        // MMA groups done (tcgen05.commit; B_MO0 / B_MO1:
     B_FIN, B_FINO,                                       //   P D again, per P buffer)
     B_ESA, B_ESB, B_EU, B_ED, B_EDO0, B_EDO1, B_EO,      // epilogue steps done (one arrival per epilogue warp)
     B_VF0, B_VF1,                                        // v / gates buffer read for the last time (the same)
-    B_NP0, B_NP1, B_NR0, B_NR1,                          // norm exchange, per half (one arrival per warp of it)
+    B_OS,                                                // (NORM) a chunk's rows are stored (the same)
     NBAR
 };
 static_assert(NBAR * 8 + 8 <= 256, "barrier space");
@@ -192,8 +190,7 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
 
     if (tid == 0) {
         for (int b = 0; b < B_ESA; ++b) mbar_init(&bar[b], 1);
-        for (int b = B_ESA; b < B_NP0; ++b) mbar_init(&bar[b], kEpiWarps);
-        for (int b = B_NP0; b < NBAR; ++b) mbar_init(&bar[b], kEpiWarps / 2);
+        for (int b = B_ESA; b < NBAR; ++b) mbar_init(&bar[b], kEpiWarps);
         *abort_flag = 0;
         mbar_init_fence();
     }
@@ -363,6 +360,16 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
         // next phase needs this chunk's P D first.
         if (lane == 0) {
             const uint64_t p_desc = umma_desc_sw128(sm + OFF_P);
+            // (NORM) once the epilogue warps have stored chunk cc's rows (B_OS; its next phase
+            // needs this warp's next P D first), a GPU-scope release of this launch's generation
+            // in the chunk's output flag; the stores of the other warps are ordered before it
+            // by the barrier and the fence
+            auto publish_rows = [&](int cc) {
+                if (!wait_ab(sh, B_OS, static_cast<uint32_t>(cc & 1))) return false;
+                __threadfence();
+                st_release_gpu(p.out_flags + cc * n_vh + vh, gen);
+                return true;
+            };
             for (int c = 0; c < nch; ++c) {
                 const uint32_t par = static_cast<uint32_t>((c >> 1) & 1);
                 if (!wait_ab(sh, B_EDO0 + (c & 1), par)) break;
@@ -379,6 +386,13 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
                 }
                 umma_commit(&bar[B_MO]);
                 umma_commit(&bar[B_MO0 + (c & 1)]);
+                // (NORM) chunk c-1's rows are stored: publish them for the norm
+                if constexpr (NORM) {
+                    if (c >= 1 && !publish_rows(c - 1)) break;
+                }
+            }
+            if constexpr (NORM) {
+                if (!*abort_flag) publish_rows(nch - 1);
             }
             umma_commit(&bar[B_FINO]);
             mbar_wait(&bar[B_FINO], 0);
@@ -412,88 +426,10 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
                 const int t = 16 * hc + i;
                 if (t < nt) o[static_cast<int64_t>(t) * n_vh * D] = a[i] + b2[i];
             }
-        };
-
-        // (NORM) the output's norm, in two steps:
-        float* NP = reinterpret_cast<float*>(sm + OFF_NP) + hc * (16 * 32);
-        float* NR = reinterpret_cast<float*>(sm + OFF_NR) + hc * 16;
-        const float wj = p.y ? __ldg(p.w + j) : 0.f;
-        // The output of chunk cc, in two steps.  o_read: O's two accumulators -> registers (with
-        // `arrive`, X's buffer is released at once, B_EO), the FP32 rows to out, and for the norm
-        // the z loads issued; o_norm, later (during the next chunk's X product, so the z loads
-        // are in by then): the gated RMSNorm of those rows -> y, with gdn_out_norm's arithmetic
-        // (norm lane l = j / 4 sums the squares of columns 4l .. 4l+3 in order, then the 32
-        // lanes' sums meet in an xor butterfly), so y has its bits.
-        float on[16], zn[16];  // the rows (tokens 16 hc .. +15) of column j awaiting their norm
-        int pend = -1;         // their chunk, or -1
-        auto o_read = [&](int cc, bool arrive) {
-            const uint32_t tX = tl + TM_X + 128 * static_cast<uint32_t>(cc & 1);
-            float b2[16];
-            tmem_ld16x2(tX + 16 * hc, tX + 32 + 16 * hc, on, b2);
-            if (arrive) {
-                tc_fence_before_sync();
+            if constexpr (NORM) {  // the rows are stored: the P D warp publishes them
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bar[B_EO]);
+                if (lane == 0) mbar_arrive(&bar[B_OS]);
             }
-            const int nt = min(C, n_tokens - cc * C);
-            const int64_t row0 = (p.prep.t_begin + static_cast<int64_t>(cc) * C) * n_vh + vh;  // token 0's row
-#pragma unroll
-            for (int i = 0; i < 16; ++i) on[i] += b2[i];
-            if (p.out) {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int t = 16 * hc + i;
-                    if (t < nt) p.out[(row0 + static_cast<int64_t>(t) * n_vh) * D + j] = on[i];
-                }
-            }
-            if (p.y) {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int t = 16 * hc + i;
-                    zn[i] = (t < nt) ? __ldg(p.z + (row0 + static_cast<int64_t>(t) * n_vh) * D + j) : 0.f;
-                }
-                pend = cc;
-            }
-        };
-        // Returns false if a norm exchange wait gave up.
-        auto o_norm = [&]() {
-            const int cc = pend;
-            pend = -1;
-            const int nt = min(C, n_tokens - cc * C);
-            const int64_t row0 = (p.prep.t_begin + static_cast<int64_t>(cc) * C) * n_vh + vh;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const float x1 = __shfl_down_sync(0xffffffffu, on[i], 1);
-                const float x2 = __shfl_down_sync(0xffffffffu, on[i], 2);
-                const float x3 = __shfl_down_sync(0xffffffffu, on[i], 3);
-                float ss = on[i] * on[i];
-                ss = fmaf(x1, x1, ss);
-                ss = fmaf(x2, x2, ss);
-                ss = fmaf(x3, x3, ss);
-                if ((lane & 3) == 0) NP[i * 32 + 8 * q + (lane >> 2)] = ss;
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar[B_NP0 + hc]);
-            if (!warp_wait_ab(sh, B_NP0 + hc, static_cast<uint32_t>(cc & 1))) return false;
-            // this warp's 4 of the 16 rows: the butterfly over the 32 norm lanes
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                float v = NP[(4 * q + u) * 32 + lane];
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-                if (lane == 0) NR[4 * q + u] = rsqrtf(fmaf(v, 1.0f / 128.0f, p.eps));
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar[B_NR0 + hc]);
-            if (!warp_wait_ab(sh, B_NR0 + hc, static_cast<uint32_t>(cc & 1))) return false;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int t = 16 * hc + i;
-                if (t < nt)
-                    p.y[(row0 + static_cast<int64_t>(t) * n_vh) * D + j] =
-                        __half_as_ushort(__float2half_rn(on[i] * NR[i] * wj * norm_silu(zn[i])));
-            }
-            return true;
         };
 
         // the starting state and its lo part (key dims 64 hc + 32 b .. +31)
@@ -526,10 +462,7 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
                     epi_arrive(sh, b ? B_ESB : B_ESA);
                 }
             }
-            // (NORM) the norm of chunk c-2's rows while X runs
-            if constexpr (NORM) {
-                if (pend >= 0 && !(ok = o_norm())) break;
-            }
+
             // U' = V - e^gamma X_K (tokens 16 hc .. +15), split -> U' hi / lo; e^gamma X_Q and
             // zeros, the start of O's two accumulators, in X's place
             if (!(ok = warp_wait_ab(sh, B_VG0 + (c & 1), static_cast<uint32_t>((c >> 1) & 1)))) break;
@@ -615,10 +548,7 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
             if (c >= 1) {
                 if (!(ok = warp_wait_ab(sh, B_MO, pp ^ 1))) break;
                 tc_fence_after_sync();
-                if constexpr (NORM)
-                    o_read(c - 1, true);
-                else
-                    o_out(c - 1, true);
+                o_out(c - 1, true);
             }
         }
         if (ok) {
@@ -638,15 +568,7 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
             }
             if (ok) {
                 tc_fence_after_sync();
-                if constexpr (NORM) {
-                    if (pend >= 0) ok = o_norm();
-                    if (ok) {
-                        o_read(nch - 1, false);
-                        if (pend >= 0) ok = o_norm();
-                    }
-                } else {
-                    o_out(nch - 1, false);
-                }
+                o_out(nch - 1, false);
             }
         }
         tc_fence_before_sync();
@@ -655,6 +577,57 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
     if (warp == kMmaWarp) {
         tc_fence_after_sync();
         tmem_dealloc(tbase, TMEM_COLS);
+    }
+}
+
+// 16-byte load through L2 only: the rows were written by another CTA of this launch.
+__device__ __forceinline__ float4 ld_cg4(const float* ptr) {
+    float4 r;
+    asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w) : "l"(ptr));
+    return r;
+}
+
+// (NORM) The gated RMSNorm of the super-block's outputs by one prep CTA (threads
+// 0..255): units (chunk c, value head vh) = b, b + n_prep, ... in chunk order; a unit
+// waits until the scan CTA of vh has published chunk c (bounded), then norms its
+// (up to) 32 token rows, one warp per row, with gdn_out_norm's row function.
+__device__ __forceinline__ void tmem_norm_units(const ChunkTmemParams& p, const int b, const uint32_t gen) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int n_vh = p.prep.n_vh;
+    const int n_tokens = p.prep.n_tokens;
+    const int nch = (n_tokens + C - 1) / C;
+    const float4 w4 = __ldg(reinterpret_cast<const float4*>(p.w) + lane);
+    for (int u = b; u < nch * n_vh; u += p.n_prep) {
+        const int c = u / n_vh, vh = u % n_vh;
+        if (tid == 0) {
+            uint32_t seen = 0;
+            if (!wait_flag(p.out_flags + u, gen, &seen)) {
+                report_error(p.status, kDevErrFlagTimeout);
+                p.sync[2] = 0x80000000u | static_cast<uint32_t>(u);
+                p.sync[3] = seen;
+                p.sync[4] = gen;
+            }
+        }
+        PrepSyncNamed::sync();  // the acquire above orders the scan CTA's stores before every warp's loads
+        const int nt = min(C, n_tokens - c * C);
+        const int64_t row0 = (p.prep.t_begin + static_cast<int64_t>(c) * C) * n_vh + vh;
+        constexpr int R = C / (PREP_THREADS / 32);  // rows per warp, all loaded before any is normed
+        float4 o[R], z[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int t = warp + (PREP_THREADS / 32) * r;
+            const int64_t row = row0 + static_cast<int64_t>(t < nt ? t : 0) * n_vh;
+            o[r] = ld_cg4(p.out + row * D + 4 * lane);
+            z[r] = __ldg(reinterpret_cast<const float4*>(p.z + row * D) + lane);
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int t = warp + (PREP_THREADS / 32) * r;
+            if (t < nt) {
+                const int64_t row = row0 + static_cast<int64_t>(t) * n_vh;
+                __stcs(reinterpret_cast<uint2*>(p.y) + row * (D / 4) + lane, norm_row_lane(o[r], z[r], w4, p.eps));
+            }
+        }
     }
 }
 
@@ -687,6 +660,7 @@ __global__ void __launch_bounds__(TM_THREADS, 1) gdn_chunk_tmem_kernel(const __g
                 PrepSyncNamed::sync();
                 if (tid == 0 && task != p.withhold_task) st_release_gpu(p.flags + task, gen);
             }
+            if constexpr (NORM) tmem_norm_units(p, static_cast<int>(blockIdx.x), gen);
         }
     } else {
         tmem_scan<NORM>(p, aligned_dynamic_smem<unsigned char, 1024>(), b - p.n_prep, gen);
@@ -703,8 +677,7 @@ __global__ void __launch_bounds__(TM_THREADS, 1) gdn_chunk_tmem_kernel(const __g
 
 template <bool NORM>
 constexpr size_t tmem_smem() {
-    constexpr size_t scan = NORM ? SCAN_SMEM_NORM : SCAN_SMEM;
-    return (scan > sizeof(PrepSmemT<2>) ? scan : sizeof(PrepSmemT<2>)) + 1024;
+    return (SCAN_SMEM > sizeof(PrepSmemT<2>) ? SCAN_SMEM : sizeof(PrepSmemT<2>)) + 1024;
 }
 static_assert(tmem_smem<true>() <= 227 * 1024, "tensor-memory kernel shared memory");
 

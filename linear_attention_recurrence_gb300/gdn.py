@@ -170,9 +170,10 @@ def gdn_recurrence_norm(q, k, v, g, beta, state, z, w, eps: float = 1e-6, out=No
     """gdn_recurrence and gdn_out_norm of its output in one call; returns (out, y).
 
     ``out`` ([T][n_vh][d] FP32) and ``y`` ([T][n_vh][d] float16) are allocated if
-    None.  With ``store_out=False`` the FP32 output is not written at all (``out``
-    is returned as None): the norm is then fused into the scan (sequential mode,
-    and chunked mode's tensor-memory form, which always norms in its epilogue).
+    None.  In sequential mode the norm can be fused into the scan: with
+    ``store_out=False`` the FP32 output is then not written at all (``out`` is
+    returned as None).  Chunked mode needs the FP32 output (its in-launch norm
+    reads the stored rows back).
     """
     T, n_kh, d = q.shape
     n_vh = v.shape[1]

@@ -221,38 +221,30 @@ def _sequential_fused_graph_case():
         assert np.array_equal(_bits(st), s_ref)
 
 
-@pytest.mark.parametrize("T", [1, 33, 2048, 4099])
-def test_chunked_epilogue_norm_without_fp32_output(T):
-    """The tensor-memory chunked scan norms in its epilogue, so the FP32 output need
-    not be stored: y has the bits of the call that stores it (and so of gdn_out_norm
-    of that output), the state too, and y is within 1 ulp of the FP64 norm of the
-    oracle's output plus what the output tolerance can move."""
+def test_chunked_norm_needs_the_fp32_output():
+    """Chunked mode's in-launch norm reads the stored FP32 rows back: out is required."""
+    t = to_dev(make_inputs(40, seed=27))
+    with pytest.raises(gdn.GDNError) as e:
+        gdn.gdn_recurrence_norm(t["q"], t["k"], t["v"], t["g"], t["beta"], t["S0"].clone(), t["z"], t["w"],
+                                1e-6, store_out=False, mode="chunked")
+    assert e.value.status == gdn.GDN_ERR_INVALID_ARG
+    assert gdn.gdn_device_status() == gdn.GDN_OK
+
+
+@pytest.mark.parametrize("T", [33, 2048, 4099])
+def test_chunked_norm_inside_the_launch_within_one_ulp_of_fp64(T):
+    """The tensor-memory form norms inside its launch (the prep CTAs, once each
+    (chunk, value head) is published): one launch per super-block, y within 1 ulp of
+    the FP64 norm of the same FP32 output."""
     if not _one_launch_available():
         pytest.skip("too few SMs for the one-launch form")
     x = make_inputs(T, seed=26)
     t = to_dev(x)
-    st1 = t["S0"].clone()
+    st = t["S0"].clone()
     n0 = gdn.gdn_launch_count()
-    o1, y1 = gdn.gdn_recurrence_norm(t["q"], t["k"], t["v"], t["g"], t["beta"], st1, t["z"], t["w"], 1e-6,
-                                     store_out=False)
-    launches = gdn.gdn_launch_count() - n0
-    assert o1 is None
-    st2 = t["S0"].clone()
-    o2, y2 = gdn.gdn_recurrence_norm(t["q"], t["k"], t["v"], t["g"], t["beta"], st2, t["z"], t["w"], 1e-6)
+    out, y = gdn.gdn_recurrence_norm(t["q"], t["k"], t["v"], t["g"], t["beta"], st, t["z"], t["w"], 1e-6)
     torch.cuda.synchronize()
+    assert gdn.gdn_launch_count() - n0 == (T + 2047) // 2048
     assert gdn.gdn_device_status() == gdn.GDN_OK
-    assert launches == (T + 2047) // 2048
-    assert np.array_equal(_bits(y1), _bits(y2)) and np.array_equal(_bits(st1), _bits(st2))
-    y_iso = oracle.out_norm(o2.double().cpu().numpy(), x["z"], x["w"], 1e-6)
-    assert int(fp16_ulp_distance(_bits(y1), y_iso).max()) <= 1
-
-
-def test_chunked_epilogue_norm_with_the_other_forms_needs_out():
-    """Forms that cannot norm in the scan's epilogue still need the FP32 output."""
-    t = to_dev(make_inputs(40, seed=27))
-    with gdn.options(chunk_products="mma"):
-        with pytest.raises(gdn.GDNError) as e:
-            gdn.gdn_recurrence_norm(t["q"], t["k"], t["v"], t["g"], t["beta"], t["S0"].clone(), t["z"], t["w"],
-                                    1e-6, store_out=False, mode="chunked")
-    assert e.value.status == gdn.GDN_ERR_INVALID_ARG
-    assert gdn.gdn_device_status() == gdn.GDN_OK
+    y_iso = oracle.out_norm(out.double().cpu().numpy(), x["z"], x["w"], 1e-6)
+    assert int(fp16_ulp_distance(_bits(y), y_iso).max()) <= 1
