@@ -548,6 +548,9 @@ def main():
                     help="skip the T=8192 (both modes) and 36-layer stack measurements")
     ap.add_argument("--chunk-products", default="tmem", choices=["mma", "fma", "tc", "tmem"],
                     help="how the chunked form computes its products (library option chunk_products)")
+    ap.add_argument("--prep-ctas", type=int, default=0,
+                    help="tensor-memory chunked form: CTAs running the prep beside the scan (library option "
+                         "chunk_prep_ctas; 0 = the library's choice)")
     ap.add_argument("--norm-in-launch", action="store_true",
                     help="with --step-api fused: the norm inside the recurrence's launch (library option "
                          "norm_in_launch; sequential mode: the scan's fused epilogue)")
@@ -590,6 +593,7 @@ def main():
         dist.barrier()
     gdn.load_library()
     gdn.gdn_set_option("chunk_products", args.chunk_products)
+    gdn.gdn_set_option("chunk_prep_ctas", args.prep_ctas)
     gdn.gdn_set_option("norm_in_launch", 1 if args.norm_in_launch else 0)
 
     T, CT = args.tokens, args.call_tokens

@@ -276,6 +276,11 @@ typedef enum gdn_option {
     GDN_OPT_NORM_IN_LAUNCH = 3,
     /* GDN_SEQUENTIAL: state rows per thread, 16 (default) or 8.  Same bits. */
     GDN_OPT_SEQ_ROWS_PER_THREAD = 4,
+    /* GDN_PRODUCTS_TMEM: CTAs that run the chunk prep beside the scan (0, the
+     * default: 4 n_kh for gdn_recurrence, every SM the scan leaves for
+     * gdn_recurrence_norm; else this many), capped by the SMs the scan leaves and at
+     * least n_kh.  Same bits either way. */
+    GDN_OPT_CHUNK_PREP_CTAS = 5,
     /* Failure-path test hook: the prep task (chunk * n_kh + key head, in every
      * super-block) whose hand-off flag the one-launch chunked kernel never
      * publishes, so the scan CTAs waiting for it give up their bounded wait and

@@ -34,6 +34,7 @@ GDN_OPT_CHUNK_PRODUCTS = 1
 GDN_OPT_CHUNK_ONE_LAUNCH = 2
 GDN_OPT_NORM_IN_LAUNCH = 3
 GDN_OPT_SEQ_ROWS_PER_THREAD = 4
+GDN_OPT_CHUNK_PREP_CTAS = 5
 GDN_OPT_TEST_WITHHOLD_PREP_TASK = 101
 GDN_OPT_TEST_FAIL_SCRATCH_ALLOC = 102
 GDN_PRODUCTS_MMA = 0
@@ -42,6 +43,7 @@ GDN_PRODUCTS_TCGEN05 = 2
 GDN_PRODUCTS_TMEM = 3
 _OPTIONS = {"chunk_products": GDN_OPT_CHUNK_PRODUCTS, "chunk_one_launch": GDN_OPT_CHUNK_ONE_LAUNCH,
             "norm_in_launch": GDN_OPT_NORM_IN_LAUNCH, "seq_rows_per_thread": GDN_OPT_SEQ_ROWS_PER_THREAD,
+            "chunk_prep_ctas": GDN_OPT_CHUNK_PREP_CTAS,
             "test_withhold_prep_task": GDN_OPT_TEST_WITHHOLD_PREP_TASK,
             "test_fail_scratch_alloc": GDN_OPT_TEST_FAIL_SCRATCH_ALLOC}
 _PRODUCTS = {"mma": GDN_PRODUCTS_MMA, "fma": GDN_PRODUCTS_FMA, "tc": GDN_PRODUCTS_TCGEN05,

@@ -169,3 +169,27 @@ def test_chunked_reruns_at_engine_shapes_with_poisoned_scratch():
             o, s = _run(t, "chunked", [T])
             assert np.array_equal(o.view(np.uint32), o_ref.view(np.uint32)), (T, i)
             assert np.array_equal(s.view(np.uint32), s_ref.view(np.uint32)), (T, i)
+
+
+@pytest.mark.parametrize("T", [130, 4099])
+def test_tensor_memory_form_same_bits_for_any_prep_cta_count(T):
+    """The tensor-memory form's prep CTA count (option chunk_prep_ctas) only changes
+    how far the prep runs ahead of the scan: the same bits for 16, 48 and every SM
+    the scan leaves, with and without the norm inside the launch."""
+    x = make_inputs(T, seed=17)
+    t = to_dev(x)
+    ref = None
+    for n in (0, 16, 48, 4096):
+        with gdn.options(chunk_products="tmem", chunk_prep_ctas=n):
+            o, s = _run(t, "chunked", [T])
+            st = t["S0"].clone()
+            out, y = gdn.gdn_recurrence_norm(t["q"], t["k"], t["v"], t["g"], t["beta"], st, t["z"], t["w"], 1e-6)
+            torch.cuda.synchronize()
+            assert gdn.gdn_device_status() == gdn.GDN_OK
+        bits = (o.view(np.uint32), s.view(np.uint32), out.cpu().numpy().view(np.uint32),
+                y.cpu().numpy().view(np.uint16))
+        if ref is None:
+            ref = bits
+        else:
+            for a, b in zip(ref, bits):
+                assert np.array_equal(a, b), n
