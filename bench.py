@@ -105,7 +105,8 @@ def captured_counts(source_file: str):
     """Instruction counts of one launch from profiles/flop_counts.md for the kernel
     whose source is `source_file` (None when that file changed since the capture):
     {"fp32_flop": FFMA x 2 + FFMA2 x 4 + FADD + FADD2 x 2 + FMUL + FMUL2 x 2 (thread
-    instructions), "tensor_flop": mma.sync m16n8k8 warp instructions x 2048}."""
+    instructions), "tensor_flop": mma.sync m16n8k8 warp instructions x 2048 + tcgen05.mma
+    kind::tf32 math ops (two per multiply-add)}."""
     import hashlib
     import re
 
@@ -116,12 +117,12 @@ def captured_counts(source_file: str):
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     for line in open(table):
         cells = [c.strip() for c in line.strip().strip("|").split("|")]
-        if len(cells) >= 10 and cells[1] == "csrc/" + source_file and re.fullmatch(r"[0-9a-f]{16}", cells[2]):
+        if len(cells) >= 11 and cells[1] == "csrc/" + source_file and re.fullmatch(r"[0-9a-f]{16}", cells[2]):
             if cells[2] != sha:
                 return None
-            ffma, ffma2, fadd, fadd2, fmul, fmul2, hmma = (int(c) for c in cells[3:10])
+            ffma, ffma2, fadd, fadd2, fmul, fmul2, hmma, umma = (int(c) for c in cells[3:11])
             return {"fp32_flop": 2 * ffma + 4 * ffma2 + fadd + 2 * fadd2 + fmul + 2 * fmul2,
-                    "tensor_flop": hmma * 2048}
+                    "tensor_flop": hmma * 2048 + umma}
     return None
 
 
