@@ -295,6 +295,7 @@ def run_sweep(args):
     from linear_attention_recurrence_gb300.inputs import make_inputs
 
     build.build()
+    gdn.gdn_set_option("chunk_products", args.chunk_products)
     dev = torch.device("cuda", torch.cuda.current_device())
     Ts = [1, 8, 16, 32, 64, 96, 128, 192, 256, 512, 1024, 2048, 8192, 32768]
     x = make_inputs(max(Ts), seed=0, norm=False)
@@ -327,7 +328,8 @@ def run_sweep(args):
                 samples.append(e0.elapsed_time(e1) * 1e3 / reps)
             res[T][mode] = statistics.median(samples)
     line = {"metric": "GDN recurrence GPU time per call (µs) by mode and T", "unit": "µs", "data": "synthetic",
-            "config": {"n_kh": N_KH, "n_vh": N_VH, "d": D, "state": "carried, non-zero", "timing": "CUDA graph replay"},
+            "config": {"n_kh": N_KH, "n_vh": N_VH, "d": D, "state": "carried, non-zero", "timing": "CUDA graph replay",
+                       "chunk_products": args.chunk_products},
             "sweep": {str(T): v for T, v in res.items()}}
     print(json.dumps(line), flush=True)
     return 0
