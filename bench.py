@@ -554,6 +554,9 @@ def main():
     ap.add_argument("--prep-ctas", type=int, default=0,
                     help="tensor-memory chunked form: CTAs running the prep beside the scan (library option "
                          "chunk_prep_ctas; 0 = the library's choice)")
+    ap.add_argument("--no-fp32-out", action="store_true",
+                    help="with --step-api fused: the FP32 output is not stored (the norm in the scan's epilogue: "
+                         "sequential mode, and the tensor-memory chunked form)")
     ap.add_argument("--norm-in-launch", action="store_true",
                     help="with --step-api fused: the norm inside the recurrence's launch (library option "
                          "norm_in_launch; sequential mode: the scan's fused epilogue)")
@@ -636,7 +639,8 @@ def main():
         for i in range(ncalls):
             a, b = i * CT, (i + 1) * CT
             gdn.gdn_recurrence_norm(t["q"][a:b], t["k"][a:b], t["v"][a:b], t["g"][a:b], t["beta"][a:b], state,
-                                    t["z"][a:b], t["w"], 1e-6, out=out[a:b], y=y[a:b], mode=mode, stream=stream)
+                                    t["z"][a:b], t["w"], 1e-6, out=out[a:b], y=y[a:b], mode=mode, stream=stream,
+                                    store_out=not args.no_fp32_out)
 
     def step(mode, ev=None):
         if ev is None and args.step_api == "fused":
@@ -946,7 +950,8 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": _config(args),
         "tokens_per_s": T * ws / (main_res["ms_per_step"] * 1e-3),
-        "step_schedule": {"fused": "16 gdn_recurrence_norm calls (recurrence + norm of the call's rows)",
+        "step_schedule": {"fused": "16 gdn_recurrence_norm calls (recurrence + norm of the call's rows"
+                                   + (", no FP32 output)" if args.no_fp32_out else ")"),
                           "overlap": "16 recurrence calls on one stream; each call's rows normed on a second "
                                      "stream once that call is done",
                           "plain": "16 recurrence calls, then the norm"}[args.step_api],

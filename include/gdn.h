@@ -185,12 +185,20 @@ int gdn_out_norm(const float* out, const float* z, const float* w, float eps,
  * GB300 take less time (the scan is ALU-bound; the fused form saves the FP32
  * output's HBM traffic, not time).  The fused form needs the 8 n_kh CTAs
  * resident at once (n_kh <= SMs / 8); beyond that `out` is required.
- * GDN_CHUNKED: the norm of each 2048-token super-block is launched after its
- * recurrence.  With the option GDN_OPT_NORM_IN_LAUNCH set to 1 and the one-launch
- * chunked form, the norm instead runs inside that launch, on the SMs that
- * prepare the chunks, as the scan finishes each (chunk, key head), reading the
- * output back from L2 (same bits; on GB300 slower, those SMs cannot stream the
- * norm's traffic as fast as the scan produces it).
+ * GDN_CHUNKED with the tensor-memory form (GDN_PRODUCTS_TMEM, the default): the
+ * norm is in the scan's output epilogue.  Each scan CTA holds whole 128-column
+ * rows of its value head, so it forms every row's sum of squares itself, in
+ * gdn_out_norm's order, and writes y from the outputs while they are on chip;
+ * with `out` NULL the FP32 output is never written.  One launch per 2048-token
+ * super-block.  If that launch cannot be resident on the SMs available, the call
+ * takes the forms below and then needs `out`.
+ * GDN_CHUNKED with the other product forms: the norm of each super-block is
+ * launched after its recurrence (`out` required).  With the option
+ * GDN_OPT_NORM_IN_LAUNCH set to 1 and the one-launch warp-MMA form, the norm
+ * instead runs inside that launch, on the SMs that prepare the chunks, as the
+ * scan finishes each (chunk, key head), reading the output back from L2 (same
+ * bits; on GB300 slower, those SMs cannot stream the norm's traffic as fast as
+ * the scan produces it).
  *
  * Arguments as the two calls'; z, w and y_fp16 16-byte aligned; y_fp16 may
  * overlap no other argument.

@@ -307,8 +307,9 @@ int run_recurrence(const float* q, const float* k, const float* v, const float* 
     if (n_vh != kHeadsPerKey * n_kh) return fail(GDN_ERR_UNSUPPORTED, "only n_vh == 3 * n_kh is supported");
     if (T > INT32_MAX - 4096) return fail(GDN_ERR_UNSUPPORTED, "T too large for 32-bit TMA coordinates");
     if (T == 0) return GDN_OK;
-    // the fused sequential norm may leave the FP32 output unwritten
-    const bool out_optional = norm && mode == GDN_SEQUENTIAL;
+    // the fused norms (sequential, and the tensor-memory chunked form) may leave the FP32
+    // output unwritten; the chunked forms that need it are checked below
+    const bool out_optional = norm != nullptr;
     if (!q || !k || !v || !g || !beta || !state_inout || (!out && !out_optional))
         return fail(GDN_ERR_INVALID_ARG, "null pointer");
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || (out && !aligned(out, 16)) ||
@@ -424,16 +425,15 @@ int run_recurrence(const float* q, const float* k, const float* v, const float* 
     int n_prep_tm = 0;
     ChunkTmemParams tp;
     std::memset(&tp, 0, sizeof(tp));
-    // Prep CTAs: with the norm, every SM the scan leaves (they norm the rows once their
-    // tasks are done); without it 4 n_kh by default, about twice the prep rate the scan
-    // consumes, so that the prep stays a few chunks ahead (its tiles are then read back
-    // from L2) and the other SMs are free for work on other streams (measured, 48 value
-    // heads: 182.4 us per 2048-token call with 64 prep CTAs, 186.3 with 104, 206.8 with 40).
+    // Prep CTAs: 4 n_kh by default, about twice the prep rate the scan consumes, so that
+    // the prep stays a few chunks ahead (its tiles are then read back from L2) and the
+    // other SMs are free for work on other streams (measured, 48 value heads: 182.4 us
+    // per 2048-token call with 64 prep CTAs, 186.3 with 104, 206.8 with 40).
     if (chunk_scan_kind() == ScanKind::kTmem && opt(GDN_OPT_CHUNK_ONE_LAUNCH) != 0) {
         n_prep_tm = chunk_tmem_prep_ctas(n_kh, n_vh, dev->sm_count);
         int want = opt(GDN_OPT_CHUNK_PREP_CTAS);
-        if (want == 0 && !norm) want = 4 * n_kh;
-        if (n_prep_tm > 0 && want > 0) n_prep_tm = want < n_kh ? n_kh : (want < n_prep_tm ? want : n_prep_tm);
+        if (want == 0) want = 4 * n_kh;
+        if (n_prep_tm > 0) n_prep_tm = want < n_kh ? n_kh : (want < n_prep_tm ? want : n_prep_tm);
     }
     if (n_prep_tm > 0) {
         if ((rc = make_map(&tp.tm_v, v, static_cast<uint64_t>(n_vh) * d, T, d, kChunk, CU_TENSOR_MAP_SWIZZLE_NONE)))
@@ -445,15 +445,17 @@ int run_recurrence(const float* q, const float* k, const float* v, const float* 
         tp.sync = dev->sync;
         tp.n_prep = n_prep_tm;
         tp.withhold_task = withheld_prep_task();
-        if (norm) {  // the norm inside the launch, on the prep SMs once their tasks are done
-            tp.z = norm->z;
+        if (norm) {  // the norm in the scan's output epilogue
+            if ((rc = make_map(&tp.tm_z, norm->z, static_cast<uint64_t>(n_vh) * d, T, d, kChunk,
+                               CU_TENSOR_MAP_SWIZZLE_NONE)))
+                return rc;
             tp.w = norm->w;
             tp.y = norm->y;
             tp.eps = norm->eps;
-            tp.out_flags = dev->out_flags;
         }
     }
-    if (!out) return fail(GDN_ERR_INVALID_ARG, "out is required in chunked mode");
+    if (!out && n_prep_tm == 0)
+        return fail(GDN_ERR_INVALID_ARG, "out is required in chunked mode unless the tensor-memory form runs");
     for (int64_t t0 = 0; t0 < T; t0 += kSuperBlock) {
         const int n = static_cast<int>((T - t0) < kSuperBlock ? (T - t0) : kSuperBlock);
         pp.t_begin = t0;
@@ -470,6 +472,8 @@ int run_recurrence(const float* q, const float* k, const float* v, const float* 
             if (e != cudaErrorCooperativeLaunchTooLarge) return cuda_fail(e, "chunk prep+scan (tensor memory) launch");
             cudaGetLastError();  // fewer SMs available than the device has: the forms below
             n_prep_tm = 0;
+            if (!out)
+                return fail(GDN_ERR_INVALID_ARG, "out is required: the tensor-memory launch does not fit the SMs available");
         }
         if (n_prep > 0) {
             ChunkFusedParams fp;

@@ -37,11 +37,12 @@
 //   epilogue: D', then D -> MMA: the state update, while the epilogue writes the
 //   chunk before's O to out.
 // For gdn_recurrence_norm a second instance of the kernel (NORM) also writes the
-// gated RMSNorm of the output to y, inside the same launch: once a scan CTA has
-// stored a chunk's rows, its P D warp publishes a flag for (chunk, value head), and
-// the prep CTAs, whose tasks end long before the scan does, norm those rows (read
-// back while they are still in L2) with gdn_out_norm's row function, so y has that
-// kernel's bits.  The scan's own warps do no more work than without the norm.
+// gated RMSNorm of the output to y from the output epilogue: a scan CTA holds whole
+// 128-column rows of its value head, so each row's sum of squares is formed inside
+// the CTA, in the order of gdn_out_norm's warp (norm lane l = j / 4 sums the squares
+// of columns 4l .. 4l+3 in turn, then the 32 lanes' sums meet in an xor butterfly),
+// and y has that kernel's bits; z arrives by TMA like v.  The FP32 output is then
+// optional.  To make room for z, that instance keeps v in one buffer.
 // The CTAs before the scan CTAs run the prep of the same super-block (one task per
 // (chunk, key head), in chunk order) and publish a flag per task, as the one-launch
 // kernel of gdn_chunk.cu does; the cooperative launch keeps every CTA resident.
@@ -65,29 +66,39 @@ constexpr uint32_t TM_X = 256;  // chunk parity p: 128 columns at TM_X + 128 p: 
                                 // (k tokens, then q) and cross terms [64,128); then O's accumulators,
                                 // e^gamma X_Q [0,32) and zeros [32,64), and D hi [64,96), D lo [96,128)
 
-// shared memory (bytes from a 1024-aligned base)
-constexpr uint32_t OFF_KQ = 0;        // [2 buffers][4 key-dim blocks][128 rows: hi 64, lo 64][128 B]
-constexpr uint32_t OFF_KT = 131072;   // K^T hi 16 KB | lo 16 KB: [128 key dims][128 B]
-constexpr uint32_t OFF_TP = 163840;   // T' hi 4 KB | lo 4 KB: [32 rows][128 B] (one 64-row operand [hi; lo])
-constexpr uint32_t OFF_P = 172032;    // [2 buffers][P hi 4 KB | lo 4 KB], the same
-constexpr uint32_t OFF_V = 188416;    // [2 buffers][32 tokens][128 columns] floats (TMA)
-constexpr uint32_t OFF_G = 221184;    // [2 buffers][e^gamma 32 | e^(gamma_last - gamma) 32] floats
-constexpr uint32_t OFF_BAR = 221696;  // mbarriers, then the tensor-memory address and the abort word
-constexpr uint32_t SCAN_SMEM = OFF_BAR + 256;
-// (kept at about 218 KB, so that a 128-thread CTA of the norm kernel launched on another
-// stream still fits on an SM beside this kernel's CTA)
+// shared memory (bytes from a 1024-aligned base); the instance with the norm keeps v
+// in one buffer and adds z's buffer and the norm's exchange space
+template <bool NORM>
+struct Smem {
+    static constexpr uint32_t KQ = 0;          // [2 buffers][4 key-dim blocks][128 rows: hi 64, lo 64][128 B]
+    static constexpr uint32_t KT = 131072;     // K^T hi 16 KB | lo 16 KB: [128 key dims][128 B]
+    static constexpr uint32_t TP = 163840;     // T' hi 4 KB | lo 4 KB: [32 rows][128 B] (one 64-row operand [hi; lo])
+    static constexpr uint32_t P = 172032;      // [2 buffers][P hi 4 KB | lo 4 KB], the same
+    static constexpr uint32_t V = 188416;      // [2 buffers (NORM: 1)][32 tokens][128 columns] floats (TMA)
+    static constexpr uint32_t Z = V + 16384;   // (NORM) [32 tokens][128 columns] floats of z (TMA)
+    static constexpr uint32_t G = V + 32768;   // [2 buffers][e^gamma 32 | e^(gamma_last - gamma) 32] floats
+    static constexpr uint32_t NP = G + 512;    // (NORM) [2 halves][16 tokens][32 norm lanes] sums of squares
+    static constexpr uint32_t NR = NP + (NORM ? 4096 : 0);   // (NORM) [2 halves][16 tokens] 1 / rms
+    static constexpr uint32_t BAR = NR + (NORM ? 128 : 0);   // mbarriers, the tensor-memory address, the abort word
+    static constexpr uint32_t TOTAL = BAR + (NORM ? 512 : 256);
+};
+// (the instance without the norm is kept at about 218 KB, so that a 128-thread CTA of
+// the norm kernel launched on another stream still fits on an SM beside its CTA)
 enum {
     B_KQ0, B_KQ1, B_P0, B_P1, B_VG0, B_VG1, B_TP, B_KT,  // copies landed
     B_MX0, B_MX1, B_MD, B_MS, B_MO, B_MO0, B_MO1,        // MMA groups done (tcgen05.commit; B_MO0 / B_MO1:
     B_FIN, B_FINO,                                       //   P D again, per P buffer)
     B_ESA, B_ESB, B_EU, B_ED, B_EDO0, B_EDO1, B_EO,      // epilogue steps done (one arrival per epilogue warp)
     B_VF0, B_VF1,                                        // v / gates buffer read for the last time (the same)
-    B_OS,                                                // (NORM) a chunk's rows are stored (the same)
-    NBAR
+    NBAR_PLAIN,
+    B_Z = NBAR_PLAIN,                                    // (NORM) z copy landed
+    B_ZF,                                                // (NORM) z read (one arrival per epilogue warp)
+    B_NP0, B_NP1, B_NR0, B_NR1,                          // (NORM) norm exchange, per half (one arrival per warp of it)
+    NBAR_NORM
 };
-static_assert(NBAR * 8 + 8 <= 256, "barrier space");
+static_assert(NBAR_PLAIN * 8 + 8 <= 256 && NBAR_NORM * 8 + 8 <= 512, "barrier space");
 constexpr uint32_t TX_KQ = 2 * 2 * C * D * 4, TX_TP = 2 * C * C * 4, TX_P = 2 * C * C * 4, TX_KT = 2 * D * C * 4;
-constexpr uint32_t TX_VG = C * D * 4 + 2 * C * 4;
+constexpr uint32_t TX_VG = C * D * 4 + 2 * C * 4, TX_Z = C * D * 4;
 
 constexpr uint32_t IDESC_N32 = umma_idesc_tf32(128, 32);
 constexpr uint32_t IDESC_N64 = umma_idesc_tf32(128, 64);
@@ -183,14 +194,21 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
     const int kh = vh % n_kh;
     const int n_tokens = p.prep.n_tokens;
     const int nch = (n_tokens + C - 1) / C;
-    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + NBAR * 8);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + OFF_BAR + NBAR * 8 + 4);
+    using L = Smem<NORM>;
+    constexpr int NBAR = NORM ? NBAR_NORM : NBAR_PLAIN;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::BAR);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::BAR + NBAR * 8);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::BAR + NBAR * 8 + 4);
     const TmemShared sh{bar, abort_flag, p.status};
 
     if (tid == 0) {
         for (int b = 0; b < B_ESA; ++b) mbar_init(&bar[b], 1);
-        for (int b = B_ESA; b < NBAR; ++b) mbar_init(&bar[b], kEpiWarps);
+        for (int b = B_ESA; b < NBAR_PLAIN; ++b) mbar_init(&bar[b], kEpiWarps);
+        if constexpr (NORM) {
+            mbar_init(&bar[B_Z], 1);
+            mbar_init(&bar[B_ZF], kEpiWarps);
+            for (int b = B_NP0; b <= B_NR1; ++b) mbar_init(&bar[b], kEpiWarps / 2);
+        }
         *abort_flag = 0;
         mbar_init_fence();
     }
@@ -205,11 +223,12 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
         // Each buffer is refilled once the MMA group or epilogue step that last reads it
         // has finished.  The order below also keeps every wait at most one phase behind
         // its barrier: the phase after the awaited one depends on a copy issued later in
-        // the same iteration.
+        // the same iteration (or, for z, in the next one).
         if (lane == 0) {
             int armed[B_KT + 1];  // last chunk whose copies each load barrier was armed for (-1: none)
 #pragma unroll
             for (int b = 0; b <= B_KT; ++b) armed[b] = -1;
+            int armed_z = -1;     // (NORM) the same for z
             float* tiles = p.prep.prep;
             for (int c = 0; c < nch && !*abort_flag; ++c) {
                 // the prep task of (c, kh) has published its tiles
@@ -227,33 +246,64 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
                 const float* ht = head_tiles(tiles, n_kh, n_vh, c, vh);
                 const int s = c & 1;
                 const uint32_t par2 = static_cast<uint32_t>(((c - 2) >> 1) & 1);
-                // v and the gates of chunk c: the buffer's chunk c-2 has been read for the last time
-                if (c >= 2 && !wait_ab(sh, B_VF0 + s, par2)) break;
-                mbar_arrive_expect_tx(&bar[B_VG0 + s], TX_VG);
-                tma_load_2d(sm + OFF_V + s * (C * D * 4), &p.tm_v, &bar[B_VG0 + s], vh * D,
-                            static_cast<int>(p.prep.t_begin + static_cast<int64_t>(c) * C));
-                bulk_load(sm + OFF_G + s * 256, ht + kTileEG, 2 * C * 4, &bar[B_VG0 + s]);
-                if (s) armed[B_VG1] = c; else armed[B_VG0] = c;
+                const int row = static_cast<int>(p.prep.t_begin + static_cast<int64_t>(c) * C);
+                // v and the gates of chunk c (v: slot s of two, or the one buffer)
+                auto copy_vg = [&]() {
+                    mbar_arrive_expect_tx(&bar[B_VG0 + s], TX_VG);
+                    tma_load_2d(sm + L::V + (NORM ? 0 : s * (C * D * 4)), &p.tm_v, &bar[B_VG0 + s], vh * D, row);
+                    bulk_load(sm + L::G + s * 256, ht + kTileEG, 2 * C * 4, &bar[B_VG0 + s]);
+                    if (s) armed[B_VG1] = c; else armed[B_VG0] = c;
+                };
+                if constexpr (!NORM) {
+                    // the buffer's chunk c-2 has been read for the last time
+                    if (c >= 2 && !wait_ab(sh, B_VF0 + s, par2)) break;
+                    copy_vg();
+                }
                 // [K; Q] of chunk c: the buffer's chunk c-2 X product is done
                 if (c >= 2 && !wait_ab(sh, B_MX0 + s, par2)) break;
                 mbar_arrive_expect_tx(&bar[B_KQ0 + s], TX_KQ);
-                bulk_load(sm + OFF_KQ + s * 65536, kt + kTileKQ, TX_KQ, &bar[B_KQ0 + s]);
+                bulk_load(sm + L::KQ + s * 65536, kt + kTileKQ, TX_KQ, &bar[B_KQ0 + s]);
                 if (s) armed[B_KQ1] = c; else armed[B_KQ0] = c;
                 // P of chunk c: the buffer's chunk c-2 P D is done
                 if (c >= 2 && !wait_ab(sh, B_MO0 + s, par2)) break;
                 mbar_arrive_expect_tx(&bar[B_P0 + s], TX_P);
-                bulk_load(sm + OFF_P + s * TX_P, ht + kTilePH, TX_P, &bar[B_P0 + s]);
+                bulk_load(sm + L::P + s * TX_P, ht + kTilePH, TX_P, &bar[B_P0 + s]);
                 if (s) armed[B_P1] = c; else armed[B_P0] = c;
+                if constexpr (NORM) {
+                    // one v buffer: chunk c-1's v and gates have been read for the last time
+                    // (after [K; Q] and P, which the next MMAs wait for sooner)
+                    if (c >= 1 && !wait_ab(sh, B_VF0 + (s ^ 1), static_cast<uint32_t>(((c - 1) >> 1) & 1))) break;
+                    copy_vg();
+                }
                 // T' of chunk c: chunk c-1's D product is done
                 if (c >= 1 && !wait_ab(sh, B_MD, static_cast<uint32_t>((c - 1) & 1))) break;
                 mbar_arrive_expect_tx(&bar[B_TP], TX_TP);
-                bulk_load(sm + OFF_TP, ht + kTileTPH, TX_TP, &bar[B_TP]);
+                bulk_load(sm + L::TP, ht + kTileTPH, TX_TP, &bar[B_TP]);
                 armed[B_TP] = c;
                 // K^T of chunk c: chunk c-1's update is done
                 if (c >= 1 && !wait_ab(sh, B_MS, static_cast<uint32_t>((c - 1) & 1))) break;
                 mbar_arrive_expect_tx(&bar[B_KT], TX_KT);
-                bulk_load(sm + OFF_KT, kt + kTileKTH, TX_KT, &bar[B_KT]);
+                bulk_load(sm + L::KT, kt + kTileKTH, TX_KT, &bar[B_KT]);
                 armed[B_KT] = c;
+                if constexpr (NORM) {
+                    // z of chunk c-1 (one buffer, needed a chunk later): chunk c-2's z has been read
+                    if (c >= 1) {
+                        if (c >= 2 && !wait_ab(sh, B_ZF, static_cast<uint32_t>((c - 2) & 1))) break;
+                        mbar_arrive_expect_tx(&bar[B_Z], TX_Z);
+                        tma_load_2d(sm + L::Z, &p.tm_z, &bar[B_Z], vh * D, row - C);
+                        armed_z = c - 1;
+                    }
+                }
+            }
+            if constexpr (NORM) {
+                // z of the last chunk
+                if (!*abort_flag && armed_z == nch - 2 &&
+                    (nch < 2 || wait_ab(sh, B_ZF, static_cast<uint32_t>((nch - 2) & 1)))) {
+                    mbar_arrive_expect_tx(&bar[B_Z], TX_Z);
+                    tma_load_2d(sm + L::Z, &p.tm_z, &bar[B_Z], vh * D,
+                                static_cast<int>(p.prep.t_begin + static_cast<int64_t>(nch - 1) * C));
+                    armed_z = nch - 1;
+                }
             }
             // before the CTA ends: every copy issued has landed (bounded waits; normally
             // these phases completed long ago and the waits return at once)
@@ -263,15 +313,16 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
                 const bool two = b < B_TP;  // double-buffered: one phase per two chunks
                 mbar_wait(&bar[b], static_cast<uint32_t>((two ? armed[b] >> 1 : armed[b]) & 1));
             }
+            if (armed_z >= 0) mbar_wait(&bar[B_Z], static_cast<uint32_t>(armed_z & 1));
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
         // ---------------- MMAs ----------------
         if (lane == 0) {
-            const uint64_t kq_desc = umma_desc_sw128(sm + OFF_KQ);
-            const uint64_t kt_desc = umma_desc_sw128(sm + OFF_KT);
-            const uint64_t tp_desc = umma_desc_sw128(sm + OFF_TP);
-            const uint64_t p_desc = umma_desc_sw128(sm + OFF_P);
+            const uint64_t kq_desc = umma_desc_sw128(sm + L::KQ);
+            const uint64_t kt_desc = umma_desc_sw128(sm + L::KT);
+            const uint64_t tp_desc = umma_desc_sw128(sm + L::TP);
+            const uint64_t p_desc = umma_desc_sw128(sm + L::P);
             // descriptor start addresses count 16-byte units: +2 per 8-float k step
             auto kq_b = [&](int c, int ks) {  // [K; Q] block of k step ks: 128 rows [hi; lo]
                 return kq_desc + static_cast<uint64_t>(((c & 1) * 65536 + (ks >> 2) * 16384 + (ks & 3) * 32) >> 4);
@@ -359,17 +410,7 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
         // half).  Every barrier awaited here is one of a pair used by alternate chunks, whose
         // next phase needs this chunk's P D first.
         if (lane == 0) {
-            const uint64_t p_desc = umma_desc_sw128(sm + OFF_P);
-            // (NORM) once the epilogue warps have stored chunk cc's rows (B_OS; its next phase
-            // needs this warp's next P D first), a GPU-scope release of this launch's generation
-            // in the chunk's output flag; the stores of the other warps are ordered before it
-            // by the barrier and the fence
-            auto publish_rows = [&](int cc) {
-                if (!wait_ab(sh, B_OS, static_cast<uint32_t>(cc & 1))) return false;
-                __threadfence();
-                st_release_gpu(p.out_flags + cc * n_vh + vh, gen);
-                return true;
-            };
+            const uint64_t p_desc = umma_desc_sw128(sm + L::P);
             for (int c = 0; c < nch; ++c) {
                 const uint32_t par = static_cast<uint32_t>((c >> 1) & 1);
                 if (!wait_ab(sh, B_EDO0 + (c & 1), par)) break;
@@ -386,13 +427,6 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
                 }
                 umma_commit(&bar[B_MO]);
                 umma_commit(&bar[B_MO0 + (c & 1)]);
-                // (NORM) chunk c-1's rows are stored: publish them for the norm
-                if constexpr (NORM) {
-                    if (c >= 1 && !publish_rows(c - 1)) break;
-                }
-            }
-            if constexpr (NORM) {
-                if (!*abort_flag) publish_rows(nch - 1);
             }
             umma_commit(&bar[B_FINO]);
             mbar_wait(&bar[B_FINO], 0);
@@ -403,13 +437,22 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
         const int q = warp & 3, hc = warp >> 2;
         const int j = 32 * q + lane;                        // value column = tensor-memory lane
         const uint32_t tl = tbase + (static_cast<uint32_t>(32 * q) << 16);  // this warp's lanes
-        const float* Vb = reinterpret_cast<const float*>(sm + OFF_V);
-        const float* Gb = reinterpret_cast<const float*>(sm + OFF_G);
+        const float* Vb = reinterpret_cast<const float*>(sm + L::V);
+        const float* Gb = reinterpret_cast<const float*>(sm + L::G);
         float* state = p.state + static_cast<int64_t>(vh) * D * D;
         bool ok = true;
+        // (NORM) the exchange space of this warp's half, z and w of column j
+        float* NP = reinterpret_cast<float*>(sm + L::NP) + hc * (16 * 32);
+        float* NR = reinterpret_cast<float*>(sm + L::NR) + hc * 16;
+        const float* Zs = reinterpret_cast<const float*>(sm + L::Z);
+        const float wj = NORM ? __ldg(p.w + j) : 0.f;
 
-        // O of chunk cc (its two accumulators) -> out; with `arrive`, X's buffer is released
-        // (B_EO) as soon as the values are in registers, before the stores
+        // O of chunk cc (its two accumulators) -> out (if given); with `arrive`, X's buffer is
+        // released (B_EO) as soon as the values are in registers.  (NORM) Then the gated
+        // RMSNorm of those rows -> y, with gdn_out_norm's arithmetic: norm lane l = j / 4
+        // sums the squares of columns 4l .. 4l+3 in turn (lanes 4l .. 4l+3 of this warp),
+        // the 32 norm lanes' sums of a row meet in an xor butterfly (16, 8, 4, 2, 1) over
+        // shared memory, and y = fp16(o r w silu(z)).  Returns false if a wait gave up.
         auto o_out = [&](int cc, bool arrive) {
             const uint32_t tX = tl + TM_X + 128 * static_cast<uint32_t>(cc & 1);
             float a[16], b2[16];
@@ -426,10 +469,130 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
                 const int t = 16 * hc + i;
                 if (t < nt) o[static_cast<int64_t>(t) * n_vh * D] = a[i] + b2[i];
             }
-            if constexpr (NORM) {  // the rows are stored: the P D warp publishes them
+        };
+        // (NORM) The same in two steps.  o_read: O of chunk cc -> a (and out, if given);
+        // o_norm, once the next chunk's state split is out of the way: the gated RMSNorm of
+        // those rows -> y, with gdn_out_norm's arithmetic: norm lane l = j / 4 sums the
+        // squares of columns 4l .. 4l+3 in turn (lanes 4l .. 4l+3 of this warp), the 32 norm
+        // lanes' sums of a row meet in an xor butterfly (16, 8, 4, 2, 1) over shared memory,
+        // and y = fp16(o r w silu(z)).  o_norm returns false if a wait gave up.
+        auto o_read = [&](int cc, bool arrive, float (&a)[16]) {
+            const uint32_t tX = tl + TM_X + 128 * static_cast<uint32_t>(cc & 1);
+            float b2[16];
+            tmem_ld16x2(tX + 16 * hc, tX + 32 + 16 * hc, a, b2);
+            if (arrive) {
+                tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bar[B_OS]);
+                if (lane == 0) mbar_arrive(&bar[B_EO]);
             }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) a[i] += b2[i];
+            if (p.out) {
+                const int nt = min(C, n_tokens - cc * C);
+                float* o = p.out + ((p.prep.t_begin + static_cast<int64_t>(cc) * C) * n_vh + vh) * D + j;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int t = 16 * hc + i;
+                    if (t < nt) o[static_cast<int64_t>(t) * n_vh * D] = a[i];
+                }
+            }
+        };
+        // silu(z) of this lane's 16 rows of chunk cc (waits for z; its buffer is then free)
+        auto z_silu = [&](int cc, float (&sz)[16]) {
+            if (!warp_wait_ab(sh, B_Z, static_cast<uint32_t>(cc & 1))) return false;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) sz[i] = Zs[(16 * hc + i) * D + j];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[B_ZF]);  // z of chunk cc is read
+#pragma unroll
+            for (int i = 0; i < 16; ++i) sz[i] = norm_silu(sz[i]);
+            return true;
+        };
+        auto o_norm = [&](int cc, const float (&a)[16], const float (&sz)[16]) {
+            const uint32_t par = static_cast<uint32_t>(cc & 1);
+            const int nt = min(C, n_tokens - cc * C);
+            // Each quad of lanes holds one norm lane's four columns.  Per group of 4 rows the
+            // quad transposes its 4 x 4 values (lane k of the quad gathers the four columns of
+            // row 4g + k), so each lane sums the squares of one row in column order.
+            const int k = lane & 3, quad = lane & ~3;
+            auto pick = [](int i, float v0, float v1, float v2, float v3) {  // v_i, branch-free
+                const float lo = (i & 1) ? v1 : v0, hi = (i & 1) ? v3 : v2;
+                return (i & 2) ? hi : lo;
+            };
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const float v0 = a[4 * g], v1 = a[4 * g + 1], v2 = a[4 * g + 2], v3 = a[4 * g + 3];
+                float x[4];  // x[r]: column (k + r) & 3 of row 4g + k
+                x[0] = pick(k, v0, v1, v2, v3);
+#pragma unroll
+                for (int r = 1; r < 4; ++r)
+                    x[r] = __shfl_sync(0xffffffffu, pick((k - r) & 3, v0, v1, v2, v3), quad | ((k + r) & 3));
+                const float c0 = pick((0 - k) & 3, x[0], x[1], x[2], x[3]);
+                const float c1 = pick((1 - k) & 3, x[0], x[1], x[2], x[3]);
+                const float c2 = pick((2 - k) & 3, x[0], x[1], x[2], x[3]);
+                const float c3 = pick((3 - k) & 3, x[0], x[1], x[2], x[3]);
+                float ss = c0 * c0;
+                ss = fmaf(c1, c1, ss);
+                ss = fmaf(c2, c2, ss);
+                ss = fmaf(c3, c3, ss);
+                NP[(4 * g + k) * 32 + 8 * q + (lane >> 2)] = ss;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[B_NP0 + hc]);
+            if (!warp_wait_ab(sh, B_NP0 + hc, par)) return false;
+            // this warp's 4 of the half's 16 rows, one per lane 0-3: the 32 norm lanes' sums
+            // added in the xor butterfly's order (16, 8, 4, 2, 1)
+            if (lane < 4) {
+                const int row = 4 * q + lane;
+                float v[32];
+#pragma unroll
+                for (int l4 = 0; l4 < 8; ++l4) {
+                    const float4 f = *reinterpret_cast<const float4*>(&NP[row * 32 + 4 * l4]);
+                    v[4 * l4] = f.x;
+                    v[4 * l4 + 1] = f.y;
+                    v[4 * l4 + 2] = f.z;
+                    v[4 * l4 + 3] = f.w;
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+                    for (int l = 0; l < off; ++l) v[l] += v[l + off];
+                NR[row] = rsqrtf(fmaf(v[0], 1.0f / 128.0f, p.eps));
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[B_NR0 + hc]);
+            if (!warp_wait_ab(sh, B_NR0 + hc, par)) return false;
+            float r[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) r[i] = NR[i];
+            unsigned short yv[16];
+#pragma unroll
+            for (int i = 0; i < 16; i += 2) {  // two rows per conversion (each rounded to nearest)
+                const __half2 h2 = __floats2half2_rn(a[i] * r[i] * wj * sz[i], a[i + 1] * r[i + 1] * wj * sz[i + 1]);
+                yv[i] = __half_as_ushort(__low2half(h2));
+                yv[i + 1] = __half_as_ushort(__high2half(h2));
+            }
+            uint16_t* yo = p.y + ((p.prep.t_begin + static_cast<int64_t>(cc) * C) * n_vh + vh) * D + j;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int t = 16 * hc + i;
+                if (t < nt) yo[static_cast<int64_t>(t) * n_vh * D] = yv[i];
+            }
+            return true;
+        };
+        // the lo part of the state after chunk cc (cc >= 0), in two halves
+        auto split_state = [&](int cc) {
+            if (!warp_wait_ab(sh, B_MS, static_cast<uint32_t>(cc & 1))) return false;
+            tc_fence_after_sync();
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                float s[32], lo[32];
+                tmem_ld32(tl + TM_S + 64 * hc + 32 * b, s);
+                state_lo32(s, lo);
+                tmem_st32(tl + TM_L + 64 * hc + 32 * b, lo);
+                epi_arrive(sh, b ? B_ESB : B_ESA);
+            }
+            return true;
         };
 
         // the starting state and its lo part (key dims 64 hc + 32 b .. +31)
@@ -446,10 +609,10 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
         for (int c = 0; c < nch && ok; ++c) {
             const uint32_t pp = static_cast<uint32_t>(c & 1);
             const uint32_t tX = tl + TM_X + 128 * pp;
-            const float* V = Vb + (c & 1) * (C * D);
+            const float* V = Vb + (NORM ? 0 : (c & 1) * (C * D));
             const float* eg = Gb + (c & 1) * 64;
             const float* er = eg + C;
-            if (c >= 1) {
+            if (!NORM && c >= 1) {
                 // the lo part of the state after chunk c-1, in two halves
                 if (!(ok = warp_wait_ab(sh, B_MS, pp ^ 1))) break;
                 tc_fence_after_sync();
@@ -545,10 +708,25 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
                 epi_arrive(sh, B_EDO0 + (c & 1));
             }
             // O of chunk c-1, while the tensor pipe runs the update
-            if (c >= 1) {
-                if (!(ok = warp_wait_ab(sh, B_MO, pp ^ 1))) break;
-                tc_fence_after_sync();
-                o_out(c - 1, true);
+            if constexpr (!NORM) {
+                if (c >= 1) {
+                    if (!(ok = warp_wait_ab(sh, B_MO, pp ^ 1))) break;
+                    tc_fence_after_sync();
+                    o_out(c - 1, true);
+                }
+            } else {
+                // (NORM) O of chunk c-1 into registers while the update runs, then the next
+                // chunk's state split (the X product waits for it), then the norm of those
+                // rows while X runs
+                float a[16], sz[16];
+                if (c >= 1) {
+                    if (!(ok = warp_wait_ab(sh, B_MO, pp ^ 1))) break;
+                    tc_fence_after_sync();
+                    o_read(c - 1, true, a);
+                    if (!(ok = z_silu(c - 1, sz))) break;
+                }
+                if (c + 1 < nch && !(ok = split_state(c))) break;
+                if (c >= 1 && !(ok = o_norm(c - 1, a, sz))) break;
             }
         }
         if (ok) {
@@ -568,7 +746,13 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
             }
             if (ok) {
                 tc_fence_after_sync();
-                o_out(nch - 1, false);
+                if constexpr (NORM) {
+                    float a[16], sz[16];
+                    o_read(nch - 1, false, a);
+                    ok = z_silu(nch - 1, sz) && o_norm(nch - 1, a, sz);
+                } else {
+                    o_out(nch - 1, false);
+                }
             }
         }
         tc_fence_before_sync();
@@ -577,57 +761,6 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
     if (warp == kMmaWarp) {
         tc_fence_after_sync();
         tmem_dealloc(tbase, TMEM_COLS);
-    }
-}
-
-// 16-byte load through L2 only: the rows were written by another CTA of this launch.
-__device__ __forceinline__ float4 ld_cg4(const float* ptr) {
-    float4 r;
-    asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w) : "l"(ptr));
-    return r;
-}
-
-// (NORM) The gated RMSNorm of the super-block's outputs by one prep CTA (threads
-// 0..255): units (chunk c, value head vh) = b, b + n_prep, ... in chunk order; a unit
-// waits until the scan CTA of vh has published chunk c (bounded), then norms its
-// (up to) 32 token rows, one warp per row, with gdn_out_norm's row function.
-__device__ __forceinline__ void tmem_norm_units(const ChunkTmemParams& p, const int b, const uint32_t gen) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int n_vh = p.prep.n_vh;
-    const int n_tokens = p.prep.n_tokens;
-    const int nch = (n_tokens + C - 1) / C;
-    const float4 w4 = __ldg(reinterpret_cast<const float4*>(p.w) + lane);
-    for (int u = b; u < nch * n_vh; u += p.n_prep) {
-        const int c = u / n_vh, vh = u % n_vh;
-        if (tid == 0) {
-            uint32_t seen = 0;
-            if (!wait_flag(p.out_flags + u, gen, &seen)) {
-                report_error(p.status, kDevErrFlagTimeout);
-                p.sync[2] = 0x80000000u | static_cast<uint32_t>(u);
-                p.sync[3] = seen;
-                p.sync[4] = gen;
-            }
-        }
-        PrepSyncNamed::sync();  // the acquire above orders the scan CTA's stores before every warp's loads
-        const int nt = min(C, n_tokens - c * C);
-        const int64_t row0 = (p.prep.t_begin + static_cast<int64_t>(c) * C) * n_vh + vh;
-        constexpr int R = C / (PREP_THREADS / 32);  // rows per warp, all loaded before any is normed
-        float4 o[R], z[R];
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const int t = warp + (PREP_THREADS / 32) * r;
-            const int64_t row = row0 + static_cast<int64_t>(t < nt ? t : 0) * n_vh;
-            o[r] = ld_cg4(p.out + row * D + 4 * lane);
-            z[r] = __ldg(reinterpret_cast<const float4*>(p.z + row * D) + lane);
-        }
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const int t = warp + (PREP_THREADS / 32) * r;
-            if (t < nt) {
-                const int64_t row = row0 + static_cast<int64_t>(t) * n_vh;
-                __stcs(reinterpret_cast<uint2*>(p.y) + row * (D / 4) + lane, norm_row_lane(o[r], z[r], w4, p.eps));
-            }
-        }
     }
 }
 
@@ -660,7 +793,6 @@ __global__ void __launch_bounds__(TM_THREADS, 1) gdn_chunk_tmem_kernel(const __g
                 PrepSyncNamed::sync();
                 if (tid == 0 && task != p.withhold_task) st_release_gpu(p.flags + task, gen);
             }
-            if constexpr (NORM) tmem_norm_units(p, static_cast<int>(blockIdx.x), gen);
         }
     } else {
         tmem_scan<NORM>(p, aligned_dynamic_smem<unsigned char, 1024>(), b - p.n_prep, gen);
@@ -677,9 +809,10 @@ __global__ void __launch_bounds__(TM_THREADS, 1) gdn_chunk_tmem_kernel(const __g
 
 template <bool NORM>
 constexpr size_t tmem_smem() {
-    return (SCAN_SMEM > sizeof(PrepSmemT<2>) ? SCAN_SMEM : sizeof(PrepSmemT<2>)) + 1024;
+    return (Smem<NORM>::TOTAL > sizeof(PrepSmemT<2>) ? Smem<NORM>::TOTAL : sizeof(PrepSmemT<2>)) + 1024;
 }
 static_assert(tmem_smem<true>() <= 227 * 1024, "tensor-memory kernel shared memory");
+static_assert(tmem_smem<false>() == 221952 + 1024, "the instance without the norm keeps its size");
 
 }  // namespace
 

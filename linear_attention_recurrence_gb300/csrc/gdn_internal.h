@@ -197,13 +197,12 @@ struct ChunkTmemParams {
     uint32_t* sync;        // as ChunkFusedParams::sync
     int n_prep;
     int withhold_task;     // failure-path test: this prep task's flag is never published (-1: none)
-    // The gated RMSNorm of the output inside the launch, when y != nullptr: the prep
-    // CTAs norm each (chunk, value head)'s rows once its scan CTA has published them.
-    const float* z;        // [T][n_vh][128], absolute token rows like out
+    // The gated RMSNorm of the output in the scan's epilogue, when y != nullptr (out
+    // may then be nullptr: the FP32 output is not written).
+    CUtensorMap tm_z;      // z viewed as [T][n_vh*128], box {128, 32}, no swizzle
     const float* w;        // [128]
     uint16_t* y;           // [T][n_vh][128] binary16 bits
     float eps;
-    uint32_t* out_flags;   // [kChunksPerSuperBlock][n_vh]: generation of each published (chunk, value head)
 };
 // Prep CTAs of the tensor-memory form on a device with sm_count SMs (one CTA per
 // SM: the scan CTAs hold all 512 tensor-memory columns), or 0 when fewer than

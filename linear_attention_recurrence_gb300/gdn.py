@@ -172,10 +172,10 @@ def gdn_recurrence_norm(q, k, v, g, beta, state, z, w, eps: float = 1e-6, out=No
     """gdn_recurrence and gdn_out_norm of its output in one call; returns (out, y).
 
     ``out`` ([T][n_vh][d] FP32) and ``y`` ([T][n_vh][d] float16) are allocated if
-    None.  In sequential mode the norm can be fused into the scan: with
-    ``store_out=False`` the FP32 output is then not written at all (``out`` is
-    returned as None).  Chunked mode needs the FP32 output (its in-launch norm
-    reads the stored rows back).
+    None.  With ``store_out=False`` the FP32 output is not written at all (``out``
+    is returned as None): the norm is then fused into the scan, in sequential mode
+    and in chunked mode's tensor-memory form (the default); chunked mode's other
+    product forms need the FP32 output.
     """
     T, n_kh, d = q.shape
     n_vh = v.shape[1]

@@ -1,10 +1,12 @@
 """gdn_recurrence_norm: the recurrence and the gated RMSNorm of its output in one
 call.  Its FP32 output must be the bits gdn_recurrence gives, and its FP16 output
 the bits gdn_out_norm gives for that output, whichever way the call runs the norm
-(inside the one-launch chunked kernel, on the SMs that prepare the chunks, or as
-a launch after the recurrence); and the FP16 output within 1 ulp of the FP64 norm
-of the same FP32 output ("#413 prefill: DeltaNet recurrence with the three value
-heads of a key head in one thread", section "What changes")."""
+(in the output epilogue of the tensor-memory chunked scan or of the sequential
+scan, inside the warp-MMA one-launch kernel on the SMs that prepare the chunks,
+or as a launch after the recurrence), also when the FP32 output is not stored;
+and the FP16 output within 1 ulp of the FP64 norm of the same FP32 output ("#413
+prefill: DeltaNet recurrence with the three value heads of a key head in one
+thread", section "What changes")."""
 import numpy as np
 import pytest
 import torch
@@ -221,21 +223,97 @@ def _sequential_fused_graph_case():
         assert np.array_equal(_bits(st), s_ref)
 
 
-def test_chunked_norm_needs_the_fp32_output():
-    """Chunked mode's in-launch norm reads the stored FP32 rows back: out is required."""
+def test_chunked_norm_warp_mma_form_needs_the_fp32_output():
+    """The warp-MMA chunked form norms the stored FP32 rows (after the scan, or read
+    back inside its launch): out is required there."""
     t = to_dev(make_inputs(40, seed=27))
-    with pytest.raises(gdn.GDNError) as e:
-        gdn.gdn_recurrence_norm(t["q"], t["k"], t["v"], t["g"], t["beta"], t["S0"].clone(), t["z"], t["w"],
-                                1e-6, store_out=False, mode="chunked")
+    with gdn.options(chunk_products="mma"):
+        with pytest.raises(gdn.GDNError) as e:
+            gdn.gdn_recurrence_norm(t["q"], t["k"], t["v"], t["g"], t["beta"], t["S0"].clone(), t["z"], t["w"],
+                                    1e-6, store_out=False, mode="chunked")
     assert e.value.status == gdn.GDN_ERR_INVALID_ARG
     assert gdn.gdn_device_status() == gdn.GDN_OK
 
 
+@pytest.mark.parametrize("T,splits", [(1, [1]), (40, [40]), (2048, [2048]), (4099, [4099]), (4099, [1000, 3099]),
+                                      (2100, [31, 2069])])
+def test_chunked_norm_in_the_epilogue_without_fp32_output(T, splits):
+    """The tensor-memory form norms in its output epilogue, so the FP32 output is
+    optional: without it, y and the state have the bits of gdn_recurrence +
+    gdn_out_norm (also over split calls, ragged chunks and super-blocks), one launch
+    per super-block."""
+    if not _one_launch_available():
+        pytest.skip("too few SMs for the one-launch form")
+    t = to_dev(make_inputs(T, seed=28))
+    st_ref = t["S0"].clone()
+    out_ref = gdn.gdn_recurrence(t["q"], t["k"], t["v"], t["g"], t["beta"], st_ref, mode="chunked")
+    y_ref = gdn.gdn_out_norm(out_ref, t["z"], t["w"], 1e-6)
+    st = t["S0"].clone()
+    y = torch.full((T, 48, 128), float("nan"), device="cuda", dtype=torch.float16)
+    n0 = gdn.gdn_launch_count()
+    t0 = 0
+    for n in splits:
+        sl = slice(t0, t0 + n)
+        out, _ = gdn.gdn_recurrence_norm(t["q"][sl], t["k"][sl], t["v"][sl], t["g"][sl], t["beta"][sl], st,
+                                         t["z"][sl], t["w"], 1e-6, y=y[sl], mode="chunked", store_out=False)
+        assert out is None
+        t0 += n
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_status() == gdn.GDN_OK
+    assert gdn.gdn_launch_count() - n0 == sum((n + 2047) // 2048 for n in splits)
+    if len(splits) == 1:
+        assert np.array_equal(_bits(st), _bits(st_ref))
+        assert np.array_equal(_bits(y), _bits(y_ref))
+    else:
+        # a split changes the chunk boundaries, so compare each call's y with the two
+        # calls made on the same split
+        st2 = t["S0"].clone()
+        t0 = 0
+        for n in splits:
+            sl = slice(t0, t0 + n)
+            o2 = gdn.gdn_recurrence(t["q"][sl], t["k"][sl], t["v"][sl], t["g"][sl], t["beta"][sl], st2, mode="chunked")
+            assert np.array_equal(_bits(y[sl]), _bits(gdn.gdn_out_norm(o2, t["z"][sl], t["w"], 1e-6)))
+            t0 += n
+        torch.cuda.synchronize()
+        assert np.array_equal(_bits(st), _bits(st2))
+
+
+def test_chunked_norm_in_the_epilogue_graph_replay_without_fp32_output():
+    """Captured once without the FP32 output, replayed with y poisoned and the
+    scratch poisoned in between: every replay gives the eager bits."""
+    if not _one_launch_available():
+        pytest.skip("too few SMs for the one-launch form")
+    T = 4099
+    t = to_dev(make_inputs(T, seed=29))
+    st = t["S0"].clone()
+    _, y_ref = gdn.gdn_recurrence_norm(t["q"], t["k"], t["v"], t["g"], t["beta"], st, t["z"], t["w"], 1e-6,
+                                       store_out=False)
+    torch.cuda.synchronize()
+    y_ref, s_ref = _bits(y_ref), _bits(st)
+    st = t["S0"].clone()
+    y = torch.empty((T, 48, 128), device="cuda", dtype=torch.float16)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            gdn.gdn_recurrence_norm(t["q"], t["k"], t["v"], t["g"], t["beta"], st, t["z"], t["w"], 1e-6, y=y,
+                                    store_out=False)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        st.copy_(t["S0"])
+        y.fill_(float("nan"))
+        gdn.gdn_poison_scratch(0x7FC00000)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert gdn.gdn_device_status() == gdn.GDN_OK
+        assert np.array_equal(_bits(y), y_ref) and np.array_equal(_bits(st), s_ref)
+
+
 @pytest.mark.parametrize("T", [33, 2048, 4099])
 def test_chunked_norm_inside_the_launch_within_one_ulp_of_fp64(T):
-    """The tensor-memory form norms inside its launch (the prep CTAs, once each
-    (chunk, value head) is published): one launch per super-block, y within 1 ulp of
-    the FP64 norm of the same FP32 output."""
+    """The tensor-memory form norms in its output epilogue: one launch per
+    super-block, y within 1 ulp of the FP64 norm of the same FP32 output."""
     if not _one_launch_available():
         pytest.skip("too few SMs for the one-launch form")
     x = make_inputs(T, seed=26)
