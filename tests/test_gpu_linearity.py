@@ -46,8 +46,8 @@ def _run(t, v, s0, mode, kind):
     return out.cpu().numpy(), st.cpu().numpy()
 
 
-@pytest.mark.parametrize("mode,kind", [("sequential", None), ("chunked", None), ("chunked", "fma"),
-                                       ("chunked", "tc")])
+@pytest.mark.parametrize("mode,kind", [("sequential", None), ("chunked", "tmem"), ("chunked", None),
+                                       ("chunked", "fma"), ("chunked", "tc")])
 @pytest.mark.parametrize("e", [-20, 12])
 def test_power_of_two_scaling_is_exact(mode, kind, e):
     T = 2100  # a full super-block, a second one of 52 tokens, a ragged last chunk
@@ -60,7 +60,8 @@ def test_power_of_two_scaling_is_exact(mode, kind, e):
     assert np.array_equal((s1 * f).view(np.uint32), s2.view(np.uint32))
 
 
-@pytest.mark.parametrize("mode,kind", [("sequential", None), ("chunked", None), ("chunked", "fma")])
+@pytest.mark.parametrize("mode,kind", [("sequential", None), ("chunked", "tmem"), ("chunked", None),
+                                       ("chunked", "fma")])
 def test_heads_do_not_mix(mode, kind):
     """Value head h reads only its own v, g, beta and state and key head h % n_kh:
     changing value head 7's inputs, or key head 3's q and k, leaves every other
