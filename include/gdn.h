@@ -276,17 +276,18 @@ typedef enum gdn_option {
      * launch (GDN_PRODUCTS_TMEM has no two-launch form: the GDN_PRODUCTS_MMA
      * scan runs then).  Same bits either way for a given scan. */
     GDN_OPT_CHUNK_ONE_LAUNCH = 2,
-    /* gdn_recurrence_norm: 0 (default) launches the norm after the recurrence
-     * (after each super-block in GDN_CHUNKED; in GDN_SEQUENTIAL only when `out` is
-     * given); 1 norms inside the recurrence's launch (GDN_CHUNKED: on the prep
-     * SMs of the one-launch form; GDN_SEQUENTIAL: in the scan's epilogue).  Same
-     * bits either way. */
+    /* gdn_recurrence_norm with the sequential scan or the warp-MMA chunked form:
+     * 0 (default) launches the norm after the recurrence (after each super-block
+     * in GDN_CHUNKED; in GDN_SEQUENTIAL only when `out` is given); 1 norms inside
+     * the recurrence's launch (GDN_CHUNKED: on the prep SMs of the warp-MMA
+     * one-launch form; GDN_SEQUENTIAL: in the scan's epilogue).  The
+     * tensor-memory chunked form always norms in its epilogue.  Same bits either
+     * way. */
     GDN_OPT_NORM_IN_LAUNCH = 3,
     /* GDN_SEQUENTIAL: state rows per thread, 16 (default) or 8.  Same bits. */
     GDN_OPT_SEQ_ROWS_PER_THREAD = 4,
     /* GDN_PRODUCTS_TMEM: CTAs that run the chunk prep beside the scan (0, the
-     * default: 4 n_kh for gdn_recurrence, every SM the scan leaves for
-     * gdn_recurrence_norm; else this many), capped by the SMs the scan leaves and at
+     * default: 4 n_kh; else this many), capped by the SMs the scan leaves and at
      * least n_kh.  Same bits either way. */
     GDN_OPT_CHUNK_PREP_CTAS = 5,
     /* Failure-path test hook: the prep task (chunk * n_kh + key head, in every
