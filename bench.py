@@ -226,27 +226,37 @@ def cpu_baseline(tokens_target_s: float = 10.0, seed: int = 0):
                       f"{nt} OpenMP threads, {dt:.1f} s"}
 
 
-def oracle_t8192(seed: int = 0):
+def oracle_t8192(seed: int = 0, with_t32768: bool = True):
     """The FP64 oracle (unchanged) at the T = 8192 configuration (recurrence + norm,
-    one layer): single-thread and all-core wall times.  The all-core run is the
-    cpu_baseline of the headline line."""
+    one layer): single-thread and all-core wall times; and, all cores, the whole
+    T = 32768 headline workload (its 16 calls of 2048 carry the state, which the
+    oracle's one pass over the 32768 tokens does likewise).  The all-core T = 8192
+    run is the cpu_baseline of the headline line."""
     import oracle
     from linear_attention_recurrence_gb300.inputs import make_inputs
 
     T = 8192
     nt = oracle.max_threads()
-    x = make_inputs(T, seed=seed)
-    res = {}
-    for threads in (nt, 1):
+    x = make_inputs(32768 if with_t32768 else T, seed=seed)
+
+    def run(n, threads):
         t0 = time.perf_counter()
-        o, _ = oracle.recurrence(x["q"], x["k"], x["v"], x["g"], x["beta"], x["S0"], nthreads=threads)
-        oracle.out_norm(o, x["z"], x["w"], 1e-6, nthreads=threads)
-        res[threads] = time.perf_counter() - t0
-    return {"value": res[nt] / T * 1e6, "unit": "µs/token/layer", "cores": nt, "kind": "oracle",
+        o, _ = oracle.recurrence(x["q"][:n], x["k"][:n], x["v"][:n], x["g"][:n], x["beta"][:n], x["S0"],
+                                 nthreads=threads)
+        oracle.out_norm(o, x["z"][:n], x["w"], 1e-6, nthreads=threads)
+        return time.perf_counter() - t0
+
+    res = {threads: run(T, threads) for threads in (nt, 1)}
+    line = {"value": res[nt] / T * 1e6, "unit": "µs/token/layer", "cores": nt, "kind": "oracle",
             "sample": f"T=8192 (the first 8192 tokens of the workload), 48 value heads, FP64 recurrence + norm, "
                       f"{nt} OpenMP threads: {res[nt]:.2f} s; 1 thread: {res[1]:.2f} s",
             "t8192_all_cores_s": res[nt], "t8192_one_thread_s": res[1],
             "one_thread_us_per_token_layer": res[1] / T * 1e6}
+    if with_t32768:
+        t = run(32768, nt)
+        line["t32768_all_cores_s"] = t
+        line["t32768_all_cores_us_per_token_layer"] = t / 32768 * 1e6
+    return line
 
 
 def _stack_layer_inputs(layer: int):
