@@ -164,9 +164,11 @@ def test_superblock_edges(mode, T):
 
 
 @pytest.mark.parametrize("mode", MODES)
-@pytest.mark.parametrize("n_kh", [1, 5, 32])
+@pytest.mark.parametrize("n_kh", [1, 5, 32, 48])
 def test_other_head_counts(mode, n_kh):
-    """Any number of key heads with three value heads each."""
+    """Any number of key heads with three value heads each (with 48 key heads the
+    tensor-memory and one-launch forms do not fit a GB300's SMs: the call takes the
+    two-launch form)."""
     T = 97
     x = make_inputs(T, seed=4, n_kh=n_kh, n_vh=3 * n_kh, norm=False)
     o_ref, s_ref = oracle.recurrence(x["q"], x["k"], x["v"], x["g"], x["beta"], x["S0"])

@@ -223,6 +223,21 @@ def _sequential_fused_graph_case():
         assert np.array_equal(_bits(st), s_ref)
 
 
+def test_chunked_norm_without_fp32_output_needs_the_tensor_memory_launch():
+    """With 48 key heads (144 value heads) the tensor-memory launch does not fit the
+    SMs, so the chunked call takes a form that norms the stored FP32 rows: without
+    out it is refused, with out it gives the two calls' bits."""
+    T, n_kh = 70, 48
+    t = to_dev(make_inputs(T, seed=30, n_kh=n_kh, n_vh=3 * n_kh))
+    with pytest.raises(gdn.GDNError) as e:
+        gdn.gdn_recurrence_norm(t["q"], t["k"], t["v"], t["g"], t["beta"], t["S0"].clone(), t["z"], t["w"],
+                                1e-6, store_out=False, mode="chunked")
+    assert e.value.status == gdn.GDN_ERR_INVALID_ARG
+    (o1, y1, s1), (o2, y2, s2), _ = _pair(t, T, "chunked")
+    assert np.array_equal(_bits(o1), _bits(o2)) and np.array_equal(_bits(s1), _bits(s2))
+    assert np.array_equal(_bits(y1), _bits(y2))
+
+
 def test_chunked_norm_warp_mma_form_needs_the_fp32_output():
     """The warp-MMA chunked form norms the stored FP32 rows (after the scan, or read
     back inside its launch): out is required there."""
