@@ -42,7 +42,9 @@
 // the CTA, in the order of gdn_out_norm's warp (norm lane l = j / 4 sums the squares
 // of columns 4l .. 4l+3 in turn, then the 32 lanes' sums meet in an xor butterfly),
 // and y has that kernel's bits; z arrives by TMA like v.  The FP32 output is then
-// optional.  To make room for z, that instance keeps v in one buffer.
+// optional.  To make room for z, that instance keeps v in one buffer, and its
+// epilogue loop is rotated: a chunk's O is read during the update, the next chunk's
+// state split follows, and the norm of those rows runs while the X product does.
 // The CTAs before the scan CTAs run the prep of the same super-block (one task per
 // (chunk, key head), in chunk order) and publish a flag per task, as the one-launch
 // kernel of gdn_chunk.cu does; the cooperative launch keeps every CTA resident.
@@ -447,12 +449,8 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
         const float* Zs = reinterpret_cast<const float*>(sm + L::Z);
         const float wj = NORM ? __ldg(p.w + j) : 0.f;
 
-        // O of chunk cc (its two accumulators) -> out (if given); with `arrive`, X's buffer is
-        // released (B_EO) as soon as the values are in registers.  (NORM) Then the gated
-        // RMSNorm of those rows -> y, with gdn_out_norm's arithmetic: norm lane l = j / 4
-        // sums the squares of columns 4l .. 4l+3 in turn (lanes 4l .. 4l+3 of this warp),
-        // the 32 norm lanes' sums of a row meet in an xor butterfly (16, 8, 4, 2, 1) over
-        // shared memory, and y = fp16(o r w silu(z)).  Returns false if a wait gave up.
+        // O of chunk cc (its two accumulators) -> out; with `arrive`, X's buffer is released
+        // (B_EO) as soon as the values are in registers, before the stores
         auto o_out = [&](int cc, bool arrive) {
             const uint32_t tX = tl + TM_X + 128 * static_cast<uint32_t>(cc & 1);
             float a[16], b2[16];
