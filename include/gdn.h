@@ -185,13 +185,16 @@ int gdn_out_norm(const float* out, const float* z, const float* w, float eps,
  * GB300 take less time (the scan is ALU-bound; the fused form saves the FP32
  * output's HBM traffic, not time).  The fused form needs the 8 n_kh CTAs
  * resident at once (n_kh <= SMs / 8); beyond that `out` is required.
- * GDN_CHUNKED with the tensor-memory form (GDN_PRODUCTS_TMEM, the default): the
- * norm is in the scan's output epilogue.  Each scan CTA holds whole 128-column
- * rows of its value head, so it forms every row's sum of squares itself, in
- * gdn_out_norm's order, and writes y from the outputs while they are on chip;
- * with `out` NULL the FP32 output is never written.  One launch per 2048-token
- * super-block.  If that launch cannot be resident on the SMs available, the call
- * takes the forms below and then needs `out`.
+ * GDN_CHUNKED with the tensor-memory form (GDN_PRODUCTS_TMEM, the default): with
+ * `out` NULL (or the option GDN_OPT_NORM_IN_LAUNCH set to 1) the norm is in the
+ * scan's output epilogue.  Each scan CTA holds whole 128-column rows of its value
+ * head, so it forms every row's sum of squares itself, in gdn_out_norm's order,
+ * and writes y from the outputs while they are on chip; with `out` NULL the FP32
+ * output is never written.  One launch per 2048-token super-block.  Otherwise
+ * the recurrence, then the norm's own launch, per super-block (with the FP32
+ * output stored this takes less time on GB300).  If the tensor-memory launch
+ * cannot be resident on the SMs available, the call takes the forms below and
+ * then needs `out`.
  * GDN_CHUNKED with the other product forms: the norm of each super-block is
  * launched after its recurrence (`out` required).  With the option
  * GDN_OPT_NORM_IN_LAUNCH set to 1 and the one-launch warp-MMA form, the norm
@@ -276,13 +279,12 @@ typedef enum gdn_option {
      * launch (GDN_PRODUCTS_TMEM has no two-launch form: the GDN_PRODUCTS_MMA
      * scan runs then).  Same bits either way for a given scan. */
     GDN_OPT_CHUNK_ONE_LAUNCH = 2,
-    /* gdn_recurrence_norm with the sequential scan or the warp-MMA chunked form:
-     * 0 (default) launches the norm after the recurrence (after each super-block
-     * in GDN_CHUNKED; in GDN_SEQUENTIAL only when `out` is given); 1 norms inside
-     * the recurrence's launch (GDN_CHUNKED: on the prep SMs of the warp-MMA
-     * one-launch form; GDN_SEQUENTIAL: in the scan's epilogue).  The
-     * tensor-memory chunked form always norms in its epilogue.  Same bits either
-     * way. */
+    /* gdn_recurrence_norm: 0 (default) launches the norm after the recurrence
+     * when `out` is given (after each super-block in GDN_CHUNKED); 1 norms inside
+     * the recurrence's launch (GDN_CHUNKED: in the tensor-memory scan's epilogue,
+     * or on the prep SMs of the warp-MMA one-launch form; GDN_SEQUENTIAL: in the
+     * scan's epilogue).  Without `out` the fused forms run either way.  Same bits
+     * either way. */
     GDN_OPT_NORM_IN_LAUNCH = 3,
     /* GDN_SEQUENTIAL: state rows per thread, 16 (default) or 8.  Same bits. */
     GDN_OPT_SEQ_ROWS_PER_THREAD = 4,
