@@ -79,8 +79,8 @@ struct Smem {
     static constexpr uint32_t V = 188416;      // [2 buffers (NORM: 1)][32 tokens][128 columns] floats (TMA)
     static constexpr uint32_t Z = V + 16384;   // (NORM) [32 tokens][128 columns] floats of z (TMA)
     static constexpr uint32_t G = V + 32768;   // [2 buffers][e^gamma 32 | e^(gamma_last - gamma) 32] floats
-    static constexpr uint32_t NP = G + 512;    // (NORM) [2 halves][16 tokens][32 norm lanes] sums of squares
-    static constexpr uint32_t NR = NP + (NORM ? 4096 : 0);   // (NORM) [2 halves][16 tokens] 1 / rms
+    static constexpr uint32_t NP = G + 512;    // (NORM) [2 halves][16 tokens][32 norm lanes, row stride 40]
+    static constexpr uint32_t NR = NP + (NORM ? 5120 : 0);   // (NORM) [2 halves][16 tokens] 1 / rms
     static constexpr uint32_t BAR = NR + (NORM ? 128 : 0);   // mbarriers, the tensor-memory address, the abort word
     static constexpr uint32_t TOTAL = BAR + (NORM ? 512 : 256);
 };
@@ -444,7 +444,8 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
         float* state = p.state + static_cast<int64_t>(vh) * D * D;
         bool ok = true;
         // (NORM) the exchange space of this warp's half, z and w of column j
-        float* NP = reinterpret_cast<float*>(sm + L::NP) + hc * (16 * 32);
+        constexpr int NPS = 40;  // row stride of NP (floats): the row sums' loads hit 32 banks
+        float* NP = reinterpret_cast<float*>(sm + L::NP) + hc * (16 * NPS);
         float* NR = reinterpret_cast<float*>(sm + L::NR) + hc * 16;
         const float* Zs = reinterpret_cast<const float*>(sm + L::Z);
         const float wj = NORM ? __ldg(p.w + j) : 0.f;
@@ -533,29 +534,22 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
                 ss = fmaf(c1, c1, ss);
                 ss = fmaf(c2, c2, ss);
                 ss = fmaf(c3, c3, ss);
-                NP[(4 * g + k) * 32 + 8 * q + (lane >> 2)] = ss;
+                NP[(4 * g + k) * NPS + 8 * q + (lane >> 2)] = ss;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar[B_NP0 + hc]);
             if (!warp_wait_ab(sh, B_NP0 + hc, par)) return false;
-            // this warp's 4 of the half's 16 rows, one per lane 0-3: the 32 norm lanes' sums
-            // added in the xor butterfly's order (16, 8, 4, 2, 1)
-            if (lane < 4) {
-                const int row = 4 * q + lane;
-                float v[32];
-#pragma unroll
-                for (int l4 = 0; l4 < 8; ++l4) {
-                    const float4 f = *reinterpret_cast<const float4*>(&NP[row * 32 + 4 * l4]);
-                    v[4 * l4] = f.x;
-                    v[4 * l4 + 1] = f.y;
-                    v[4 * l4 + 2] = f.z;
-                    v[4 * l4 + 3] = f.w;
-                }
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-                    for (int l = 0; l < off; ++l) v[l] += v[l + off];
-                NR[row] = rsqrtf(fmaf(v[0], 1.0f / 128.0f, p.eps));
+            // this warp's 4 of the half's 16 rows, 8 lanes a row: lane 8u + m adds norm lanes
+            // m, m + 16 and m + 8, m + 24 of row 4q + u, then those two sums, as the xor
+            // butterfly's levels 16 and 8 do; levels 4, 2, 1 are shuffles among the 8 lanes
+            {
+                const int m = lane & 7, row = 4 * q + (lane >> 3);
+                const float* src = NP + row * NPS;
+                float v = (src[m] + src[m + 16]) + (src[m + 8] + src[m + 24]);
+                v += __shfl_xor_sync(0xffffffffu, v, 4);
+                v += __shfl_xor_sync(0xffffffffu, v, 2);
+                v += __shfl_xor_sync(0xffffffffu, v, 1);
+                if (m == 0) NR[row] = rsqrtf(fmaf(v, 1.0f / 128.0f, p.eps));
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar[B_NR0 + hc]);
