@@ -29,10 +29,9 @@
  *
  * Ownership: every pointer is a DEVICE pointer owned by the caller, on the
  * current CUDA device.  The library allocates only (a) a 4-byte status word per
- * device, (b) the chunked mode's per-device scratch (one 2048-token super-block
- * of prep results: about 152 MB for 48 value heads with the default
- * GDN_PRODUCTS_TMEM form, 25.9 MB with the others, plus 12 KB of hand-off
- * flags) and (c) the
+ * device, (b) the chunked mode's per-device scratch (prep results: 25.9 MB for
+ * 48 value heads, which also holds the default GDN_PRODUCTS_TMEM form's ring of
+ * operand tiles for 8 chunks, plus 15 KB of hand-off flags) and (c) the
  * sequential mode's fused-norm scratch (about 100 KB for 16 key heads), each on
  * first use and kept until gdn_release_scratch() or process exit.  Calls on one
  * device share that scratch: enqueue them on one stream (or otherwise order
@@ -268,7 +267,7 @@ typedef enum gdn_option {
      * one CTA per value head keeps the state in tensor memory and every product is
      * a split-TF32 tcgen05 MMA; one cooperative launch per super-block with the
      * prep beside it, when the value heads leave at least n_kh SMs, else the
-     * GDN_PRODUCTS_MMA form; its scratch is about 152 MB for 48 value heads),
+     * GDN_PRODUCTS_MMA form),
      * GDN_PRODUCTS_MMA (split-TF32 warp-level MMAs), GDN_PRODUCTS_FMA (packed
      * FP32 FMAs) or GDN_PRODUCTS_TCGEN05 (the state products as split-TF32 tcgen05
      * MMAs, 16 value columns per CTA; always two launches per super-block).  All

@@ -29,6 +29,7 @@ struct DeviceState {
     uint32_t* flags = nullptr; // one-launch chunked form: per-(chunk, key head) flags, then 2 sync words
     uint32_t* sync = nullptr;
     uint32_t* out_flags = nullptr;
+    unsigned long long* ring = nullptr;  // tensor-memory form: the tile ring's slot flags
     void* seqnorm = nullptr;   // the sequential scan's fused norm: exchange buffer, counters, generation
     int seqnorm_n_kh = 0;
 };
@@ -167,12 +168,19 @@ int ensure_seqnorm(DeviceState* d, int n_kh) {
 size_t flag_words_for(int n_vh) { return static_cast<size_t>(gdn::kChunksPerSuperBlock) * n_vh; }
 // Output flags of the one-launch form with the norm: [chunk][key head][8 scan CTAs] (n_kh <= n_vh).
 size_t out_flag_words_for(int n_vh) { return static_cast<size_t>(gdn::kChunksPerSuperBlock) * n_vh * 8; }
+// The 32-bit flag words (rounded up to an even count, so the 64-bit ring flags that
+// follow are 8-byte aligned), then the ring flags [kTileRing][n_vh].
+size_t u32_flag_words_for(int n_vh) {
+    return (flag_words_for(n_vh) + out_flag_words_for(n_vh) + gdn::kSyncWords + 1) & ~static_cast<size_t>(1);
+}
+size_t ring_flags_for(int n_vh) { return static_cast<size_t>(gdn::kTileRing) * n_vh; }
 
 void free_scratch(DeviceState* d) {
     cudaFree(d->scratch);
     cudaFree(d->flags);
     d->scratch = nullptr;
     d->flags = d->sync = d->out_flags = nullptr;
+    d->ring = nullptr;
     d->scratch_bytes = 0;
 }
 
@@ -190,7 +198,7 @@ int ensure_scratch(DeviceState* d, int n_vh) {
     }
     void* p = nullptr;
     void* f = nullptr;
-    const size_t flag_bytes = (flag_words_for(n_vh) + out_flag_words_for(n_vh) + gdn::kSyncWords) * sizeof(uint32_t);
+    const size_t flag_bytes = u32_flag_words_for(n_vh) * sizeof(uint32_t) + ring_flags_for(n_vh) * sizeof(unsigned long long);
     cudaError_t e = cudaMalloc(&p, need);
     if (e == cudaSuccess) {
         e = cudaMalloc(&f, flag_bytes);
@@ -206,6 +214,7 @@ int ensure_scratch(DeviceState* d, int n_vh) {
     d->flags = static_cast<uint32_t*>(f);
     d->out_flags = d->flags + flag_words_for(n_vh);
     d->sync = d->out_flags + out_flag_words_for(n_vh);
+    d->ring = reinterpret_cast<unsigned long long*>(d->flags + u32_flag_words_for(n_vh));
     // zero flags and generation before any stream (blocking or not) can use them
     e = cudaMemset(f, 0, flag_bytes);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -448,6 +457,7 @@ int run_recurrence(const float* q, const float* k, const float* v, const float* 
         tp.status = dev->status;
         tp.flags = dev->flags;
         tp.sync = dev->sync;
+        tp.ring = dev->ring;
         tp.n_prep = n_prep_tm;
         tp.withhold_task = withheld_prep_task();
         if (tm_epi_norm) {  // the norm in the scan's output epilogue
@@ -727,6 +737,7 @@ int gdn_release_scratch(int device) {
     cudaSetDevice(cur);
     d.scratch = nullptr;
     d.flags = d.sync = d.out_flags = nullptr;
+    d.ring = nullptr;
     d.scratch_bytes = 0;
     if (e != cudaSuccess) return cuda_fail(e, "cudaFree");
     if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFree");

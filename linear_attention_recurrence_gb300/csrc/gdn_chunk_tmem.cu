@@ -429,6 +429,13 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
                 }
                 umma_commit(&bar[B_MO]);
                 umma_commit(&bar[B_MO0 + (c & 1)]);
+                // every copy of chunk c has landed: P (awaited above), V and the gates (U' read
+                // them before D's epilogue), T' (the D product), [K; Q] and K^T (chunk c+1's X
+                // product follows chunk c's update, which follows chunk c's X): the chunk's ring
+                // slot is free as far as this value head goes (the last chunk's is not needed)
+                if (c + 1 < nch)
+                    st_release_gpu_u64(p.ring + (c % kTileRing) * n_vh + vh,
+                                       (static_cast<unsigned long long>(gen) << 32) | static_cast<uint32_t>(c));
             }
             umma_commit(&bar[B_FINO]);
             mbar_wait(&bar[B_FINO], 0);
@@ -756,6 +763,17 @@ __device__ __forceinline__ void tmem_scan(const ChunkTmemParams& p, unsigned cha
     }
 }
 
+// Waits until *flag >= value, polling at a slow rate (the prep runs ahead of the scan,
+// so this wait is never on the critical path, and slow polls leave L2 to the scan's
+// copies).  Returns false if the poll limit (about 0.1 s) ran out.
+__device__ __forceinline__ bool wait_ring(const unsigned long long* flag, unsigned long long value) {
+    for (uint32_t i = 0; i < kFlagPolls / 4; ++i) {
+        if (ld_acquire_gpu_u64(flag) >= value) return true;
+        __nanosleep(400);
+    }
+    return false;
+}
+
 template <bool NORM>
 __global__ void __launch_bounds__(TM_THREADS, 1) gdn_chunk_tmem_kernel(const __grid_constant__ ChunkTmemParams p) {
     __shared__ uint32_t s_gen;
@@ -771,6 +789,7 @@ __global__ void __launch_bounds__(TM_THREADS, 1) gdn_chunk_tmem_kernel(const __g
             const int n_kh = p.prep.n_kh;
             const int tasks = ((p.prep.n_tokens + C - 1) / C) * n_kh;
             if (b < tasks) prep_load(p.prep, sm, 0, b / n_kh, b % n_kh);
+            bool ring_gave_up = false;
             for (int task = b, i = 0; task < tasks; task += p.n_prep, ++i) {
                 const int next = task + p.n_prep;
                 if (next < tasks) {
@@ -778,6 +797,19 @@ __global__ void __launch_bounds__(TM_THREADS, 1) gdn_chunk_tmem_kernel(const __g
                     cp_async_wait<1>();
                 } else {
                     cp_async_wait<0>();
+                }
+                // the ring slot of chunk ci: the three value heads' scan CTAs have copied out the
+                // tiles of chunk ci - kTileRing (bounded; once a wait gives up, the CTA waits no
+                // more)
+                const int ci = task / n_kh, kh = task % n_kh;
+                if (tid == 0 && ci >= kTileRing && !ring_gave_up) {
+                    const unsigned long long want =
+                        (static_cast<unsigned long long>(gen) << 32) | static_cast<uint32_t>(ci - kTileRing);
+                    for (int m = 0; m < kHeadsPerKey && !ring_gave_up; ++m)
+                        if (!wait_ring(p.ring + ((ci - kTileRing) % kTileRing) * p.prep.n_vh + kh + m * n_kh, want)) {
+                            ring_gave_up = true;
+                            report_error(p.status, kDevErrFlagTimeout);
+                        }
                 }
                 PrepSyncNamed::sync();
                 prep_task<PrepOut::kTiles, PrepSyncNamed>(p.prep, sm, i & 1, task / n_kh, task % n_kh);

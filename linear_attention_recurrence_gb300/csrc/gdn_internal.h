@@ -35,18 +35,22 @@ constexpr int kTileKQ = 0, kTileKQLoRow = 64, kTileKTH = 16384, kTileKTL = 20480
 // [32 rows t][32 columns s], then e^gamma_t [32] and e^(gamma_last - gamma_t) [32].
 constexpr int kTileTPH = 0, kTileTPL = 1024, kTilePH = 2048, kTilePL = 3072, kTileEG = 4096, kTileER = 4128;
 constexpr int kHeadTileFloats = 4160;
-// One super-block's tiles: key tiles [kChunksPerSuperBlock][n_kh], then head tiles
-// [kChunksPerSuperBlock][n_vh].
+// The tiles live in a ring of kTileRing chunk slots (chunk ci in slot ci % kTileRing,
+// 19 MB for 16 key heads and 48 value heads): key tiles [kTileRing][n_kh], then head
+// tiles [kTileRing][n_vh].  The prep writes a slot again only once the scan CTAs of the
+// chunk that last used it have copied it (ChunkTmemParams::ring), so the ring stays in
+// L2 rather than streaming a whole super-block's tiles through HBM.
+constexpr int kTileRing = 8;
 inline size_t tile_scratch_floats(int n_kh, int n_vh) {
-    return static_cast<size_t>(kChunksPerSuperBlock) *
+    return static_cast<size_t>(kTileRing) *
            (static_cast<size_t>(n_kh) * kKeyTileFloats + static_cast<size_t>(n_vh) * kHeadTileFloats);
 }
 __host__ __device__ inline float* key_tiles(float* base, int n_kh, int ci, int kh) {
-    return base + (static_cast<int64_t>(ci) * n_kh + kh) * kKeyTileFloats;
+    return base + (static_cast<int64_t>(ci % kTileRing) * n_kh + kh) * kKeyTileFloats;
 }
 __host__ __device__ inline float* head_tiles(float* base, int n_kh, int n_vh, int ci, int vh) {
-    return base + static_cast<int64_t>(kChunksPerSuperBlock) * n_kh * kKeyTileFloats +
-           (static_cast<int64_t>(ci) * n_vh + vh) * kHeadTileFloats;
+    return base + static_cast<int64_t>(kTileRing) * n_kh * kKeyTileFloats +
+           (static_cast<int64_t>(ci % kTileRing) * n_vh + vh) * kHeadTileFloats;
 }
 
 // ---- sequential scan ----
@@ -195,6 +199,9 @@ struct ChunkTmemParams {
     int* status;
     uint32_t* flags;       // as ChunkFusedParams::flags
     uint32_t* sync;        // as ChunkFusedParams::sync
+    // [kTileRing][n_vh]: (generation << 32) | chunk, once the scan CTA of value head vh has
+    // copied that chunk's tiles out of the ring slot
+    unsigned long long* ring;
     int n_prep;
     int withhold_task;     // failure-path test: this prep task's flag is never published (-1: none)
     // The gated RMSNorm of the output in the scan's epilogue, when y != nullptr (out

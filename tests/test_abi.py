@@ -88,13 +88,16 @@ def test_overlap_rejected(lib):
 
 
 def test_scratch_size_and_counters(lib):
-    # the default (tensor-memory) form's tiles per 2048-token super-block: per chunk and key
-    # head [K; Q] and K^T as TF32 hi / lo (24576 floats), per chunk and value head T', P as
-    # hi / lo and the two gate vectors (4160 floats)
-    assert lib.gdn_chunked_scratch_bytes(48) == 64 * (16 * 24576 + 48 * 4160) * 4
-    # the other forms' records: T'^T, P^T, e^gamma, e^(gamma_last - gamma) per chunk and value head
+    # the other forms' records per 2048-token super-block: T'^T, P^T, e^gamma,
+    # e^(gamma_last - gamma) per chunk and value head
+    records = 64 * 48 * (2 * 32 * 32 + 2 * 32) * 4
     with gdn.options(chunk_products="mma"):
-        assert lib.gdn_chunked_scratch_bytes(48) == 64 * 48 * (2 * 32 * 32 + 2 * 32) * 4
+        assert lib.gdn_chunked_scratch_bytes(48) == records
+    # the default (tensor-memory) form's tile ring of 8 chunk slots: per slot and key head
+    # [K; Q] and K^T as TF32 hi / lo (24576 floats), per slot and value head T', P as hi / lo
+    # and the two gate vectors (4160 floats); the scratch holds the larger of the two
+    ring = 8 * (16 * 24576 + 48 * 4160) * 4
+    assert lib.gdn_chunked_scratch_bytes(48) == max(ring, records)
     assert lib.gdn_chunked_scratch_bytes(0) == 0
     assert lib.gdn_release_scratch(0) == 0
     assert lib.gdn_release_scratch(-1) != 0

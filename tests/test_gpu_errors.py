@@ -81,11 +81,14 @@ def test_launch_counter_counts_kernels():
     torch.cuda.synchronize()
 
 
-def test_bounded_flag_wait_runs_out_and_reports():
+@pytest.mark.parametrize("T", [64, 1000])
+def test_bounded_flag_wait_runs_out_and_reports(T):
     """A prep flag that nothing sets (the test hook withholds one task's flag): the
     scan CTAs waiting for it give up after their bounded wait, the kernel ends, and
     gdn_device_status() reports GDN_ERR_TIMEOUT naming the flag; the context stays
-    usable and the next call is correct."""
+    usable and the next call is correct.  At 1000 tokens (32 chunks) the prep tasks
+    of that key head's later chunks also wait, bounded, for ring slots that the
+    stopped scan CTAs never hand back."""
     import time
 
     import numpy as np
@@ -95,7 +98,7 @@ def test_bounded_flag_wait_runs_out_and_reports():
 
     if torch.cuda.get_device_properties(0).multi_processor_count < 9 * 16:
         pytest.skip("too few SMs for the one-launch form")
-    x = make_inputs(64, seed=31, norm=False)
+    x = make_inputs(T, seed=31, norm=False)
     t = to_dev(x)
     st = t["S0"].clone()
     with gdn.options(test_withhold_prep_task=5):  # chunk 0, key head 5
