@@ -711,6 +711,7 @@ int gdn_device_status(void* cuda_stream) {
     std::string msg = "a kernel gave up a bounded wait (status word " + std::to_string(word | na_word) + ")";
     if (na_word != 0) msg += " in gdn_recurrence_chunked_noalloc";
     if (word & gdn::kDevErrNormTimeout) msg += " (the fused sequential norm's exchange between CTAs)";
+    if (word & gdn::kDevErrRingTimeout) msg += " (a chunk prep's wait for a free slot of the tile ring)";
     uint32_t diag[3] = {0, 0, 0};
     if ((word & gdn::kDevErrFlagTimeout) && d && d->sync &&
         cudaMemcpy(diag, d->sync + 2, sizeof(diag), cudaMemcpyDeviceToHost) == cudaSuccess)

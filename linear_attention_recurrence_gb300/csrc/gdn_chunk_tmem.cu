@@ -808,7 +808,7 @@ __global__ void __launch_bounds__(TM_THREADS, 1) gdn_chunk_tmem_kernel(const __g
                     for (int m = 0; m < kHeadsPerKey && !ring_gave_up; ++m)
                         if (!wait_ring(p.ring + ((ci - kTileRing) % kTileRing) * p.prep.n_vh + kh + m * n_kh, want)) {
                             ring_gave_up = true;
-                            report_error(p.status, kDevErrFlagTimeout);
+                            report_error(p.status, kDevErrRingTimeout);
                         }
                 }
                 PrepSyncNamed::sync();

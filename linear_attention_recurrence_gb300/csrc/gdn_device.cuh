@@ -13,6 +13,7 @@ namespace gdn {
 constexpr int kDevErrTimeout = 1;      // a wait for an asynchronous copy gave up
 constexpr int kDevErrFlagTimeout = 2;  // a wait for another CTA's flag gave up (chunked prep hand-off)
 constexpr int kDevErrNormTimeout = 4;  // a wait for another CTA's sums of squares gave up (fused sequential norm)
+constexpr int kDevErrRingTimeout = 8;  // a chunk prep's wait for a free slot of the tile ring gave up
 
 // A wait gives up after this many unsuccessful mbarrier.try_wait polls (each
 // poll may itself suspend the thread for a hardware-chosen interval).  Legit

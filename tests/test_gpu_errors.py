@@ -109,6 +109,8 @@ def test_bounded_flag_wait_runs_out_and_reports(T):
     assert rc == gdn.GDN_ERR_TIMEOUT
     msg = gdn.gdn_last_error()
     assert "prep flag 5" in msg, msg
+    if T > 8 * 32 and torch.cuda.get_device_properties(0).multi_processor_count >= 48 + 16:
+        assert "tile ring" in msg, msg  # the tensor-memory form's prep also gave up on its ring
     assert elapsed < 30.0
     # the context is usable and the next call is right
     st = t["S0"].clone()
